@@ -1,0 +1,254 @@
+"""Seeded synthetic inputs for the EntropyCache decode-and-gate step and the
+selective-recompute attention.
+
+This module only draws random numbers and lays them out in the shapes the
+library takes.  It holds none of the method's arithmetic: no softmax, entropy,
+ranking, gate or index-set logic lives here.  The CUDA path (through the
+binding) and the CPU oracle both consume exactly the arrays built here, so the
+two sides see bit-identical inputs.
+
+Recipe (one seeded ``numpy.random.Generator`` per call, PCG64):
+
+* Logits.  Spiked rows: ``x = z * T`` with ``z ~ N(0, 1)`` and ``T``
+  log-uniform in [0.1, 3], plus ``s ~ U[0, 15]`` added to one uniformly chosen
+  token.  Near-uniform rows (a fixed fraction, chosen by a seeded permutation):
+  ``x = z / T`` with ``T`` log-uniform in [5, 20], no spike.  bf16 logits are the
+  round-to-nearest-even bf16 of the float32 draw.
+* Decode state.  Positions ``[0, prompt)`` are prompt (unmasked, never decoded).
+  The generated region is split into blocks of ``block`` positions decoded one
+  after the other; every block before the active one is fully decoded, in a
+  seeded random order, ``n_unmask`` tokens per denoising step.  The active block
+  and everything after it is masked (token id = vocab, the [MASK] id).
+* Attention operands.  Q, the pre-step K/V caches and the freshly projected
+  K/V rows are i.i.d. ``N(0, std^2)``.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+# dtype codes shared by the C ABI and the oracle's typed loaders.
+F32 = 0
+BF16 = 1
+F64 = 2
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic configuration of the decode step and its attention."""
+
+    name: str
+    batch: int
+    seq_len: int
+    prompt_len: int
+    block: int
+    active_block: int
+    vocab: int
+    logits_dtype: int
+    near_uniform_frac: float
+    n_unmask: int
+    k: int
+    tau: float
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    attn_dtype: int
+    qkv_std: float
+    n_layers: int = 0
+    n_steps: int = 0
+
+    @property
+    def rows_per_seq(self) -> int:
+        return self.block
+
+    @property
+    def n_rows(self) -> int:
+        return self.batch * self.block
+
+    @property
+    def r_max(self) -> int:
+        """Recompute rows per sequence before this step's unmasking: the
+        masked block plus the k most recently decoded positions."""
+        decoded = self.active_block * self.block
+        return self.block + min(self.k, decoded)
+
+
+_INV_SQRT_128 = 1.0 / math.sqrt(128.0)
+
+WORKLOADS = {
+    # N=32 masked rows, V=1024 fp32 logits; attention L=64, H=2, d=64 fp32 N(0,1).
+    "tiny": Workload("tiny", batch=1, seq_len=64, prompt_len=0, block=32, active_block=1,
+                     vocab=1024, logits_dtype=F32, near_uniform_frac=0.0, n_unmask=4, k=4,
+                     tau=1.0, n_heads=2, n_kv_heads=2, head_dim=64, attn_dtype=F32,
+                     qkv_std=1.0),
+    # One sequence, L=1024 (512 prompt + 512 generated, block 32), V=126464 bf16;
+    # attention 48 rows x 1024 keys, H=32, d=128, N(0, 1/sqrt(d)).
+    "single_seq": Workload("single_seq", batch=1, seq_len=1024, prompt_len=512, block=32,
+                           active_block=8, vocab=126464, logits_dtype=BF16,
+                           near_uniform_frac=0.0, n_unmask=2, k=16, tau=0.5, n_heads=32,
+                           n_kv_heads=32, head_dim=128, attn_dtype=BF16,
+                           qkv_std=_INV_SQRT_128),
+    # 8 sequences, L=2048, 64 masked each (512 rows), V=152064 bf16, 30% near-uniform;
+    # attention GQA 28/4 heads, d=128, 96 rows per sequence.
+    "batched": Workload("batched", batch=8, seq_len=2048, prompt_len=1024, block=64,
+                        active_block=8, vocab=152064, logits_dtype=BF16,
+                        near_uniform_frac=0.3, n_unmask=4, k=32, tau=0.8, n_heads=28,
+                        n_kv_heads=4, head_dim=128, attn_dtype=BF16,
+                        qkv_std=_INV_SQRT_128),
+    # One sequence, L=8192, 256 masked, V=126464 bf16; attention 288 rows x 8192 keys.
+    "long_ctx": Workload("long_ctx", batch=1, seq_len=8192, prompt_len=4096, block=256,
+                         active_block=8, vocab=126464, logits_dtype=BF16,
+                         near_uniform_frac=0.0, n_unmask=8, k=32, tau=0.5, n_heads=32,
+                         n_kv_heads=32, head_dim=128, attn_dtype=BF16,
+                         qkv_std=_INV_SQRT_128),
+    # 128 denoising steps on L=1024 (768 prompt + 256 generated in blocks of 32),
+    # 2 tokens per step, 32 synthetic layers, V=126464 bf16.
+    "trajectory": Workload("trajectory", batch=1, seq_len=1024, prompt_len=768, block=32,
+                           active_block=0, vocab=126464, logits_dtype=BF16,
+                           near_uniform_frac=0.0, n_unmask=2, k=16, tau=0.6, n_heads=32,
+                           n_kv_heads=32, head_dim=128, attn_dtype=BF16,
+                           qkv_std=_INV_SQRT_128, n_layers=32, n_steps=128),
+}
+
+
+def scaled(w: Workload, **changes) -> Workload:
+    """A copy of ``w`` with some fields replaced (smaller parity cases)."""
+    return dataclasses.replace(w, **changes)
+
+
+# ---------------------------------------------------------------------------
+# element types
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to the nearest bf16 (ties to even); returns uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = ((u >> 16) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((u + bias) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bits to float32."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _as_dtype(x32: np.ndarray, dtype: int) -> np.ndarray:
+    if dtype == BF16:
+        return f32_to_bf16_bits(x32)
+    if dtype == F32:
+        return np.ascontiguousarray(x32, dtype=np.float32)
+    raise ValueError(f"unsupported dtype code {dtype}")
+
+
+# ---------------------------------------------------------------------------
+# logits
+
+
+def make_logits(rng: np.random.Generator, n_rows: int, vocab: int, dtype: int,
+                near_uniform_frac: float = 0.0) -> np.ndarray:
+    """``[n_rows, vocab]`` logits of the temperature + spike recipe above."""
+    x = rng.standard_normal((n_rows, vocab), dtype=np.float32)
+    n_near = int(round(near_uniform_frac * n_rows))
+    order = rng.permutation(n_rows)
+    near = np.zeros(n_rows, dtype=bool)
+    near[order[:n_near]] = True
+    t_spiked = np.exp(rng.uniform(math.log(0.1), math.log(3.0), size=n_rows)).astype(np.float32)
+    t_near = np.exp(rng.uniform(math.log(5.0), math.log(20.0), size=n_rows)).astype(np.float32)
+    spike = rng.uniform(0.0, 15.0, size=n_rows).astype(np.float32)
+    spike_at = rng.integers(0, vocab, size=n_rows)
+    for i in range(n_rows):
+        if near[i]:
+            x[i] /= t_near[i]
+        else:
+            x[i] *= t_spiked[i]
+            x[i, spike_at[i]] += spike[i]
+    return _as_dtype(x, dtype)
+
+
+# ---------------------------------------------------------------------------
+# decode state
+
+
+@dataclasses.dataclass
+class DecodeState:
+    is_masked: np.ndarray    # uint8 [B, L]
+    tokens: np.ndarray       # int32 [B, L]
+    decode_step: np.ndarray  # int32 [B, L], -1 = never decoded
+    step: int                # index of the denoising step about to run
+    block_lo: int            # active block [block_lo, block_hi)
+    block_hi: int
+    row_pos: np.ndarray      # int32 [N]: position of each logits row
+    seq_row_offsets: np.ndarray  # int32 [B + 1]
+
+
+def make_state(rng: np.random.Generator, w: Workload) -> DecodeState:
+    B, L, n = w.batch, w.seq_len, w.n_unmask
+    gen0 = w.prompt_len
+    lo = gen0 + w.active_block * w.block
+    hi = lo + w.block
+    if hi > L:
+        raise ValueError("active block runs past the sequence")
+    is_masked = np.zeros((B, L), np.uint8)
+    tokens = rng.integers(0, w.vocab, size=(B, L)).astype(np.int32)
+    decode_step = np.full((B, L), -1, np.int32)
+    is_masked[:, lo:] = 1
+    tokens[:, lo:] = w.vocab
+    n_prev = lo - gen0
+    for b in range(B):
+        order = np.concatenate([gen0 + i * w.block + rng.permutation(w.block)
+                                for i in range(w.active_block)]) if n_prev else np.zeros(0, int)
+        decode_step[b, order] = (np.arange(n_prev) // n).astype(np.int32)
+    step = (n_prev + n - 1) // n
+    row_pos = np.concatenate([np.arange(lo, hi, dtype=np.int32) for _ in range(B)])
+    offsets = (np.arange(B + 1, dtype=np.int32) * w.block).astype(np.int32)
+    return DecodeState(is_masked, tokens, decode_step, step, lo, hi, row_pos, offsets)
+
+
+# ---------------------------------------------------------------------------
+# attention operands
+
+
+@dataclasses.dataclass
+class AttentionInputs:
+    q: np.ndarray        # [B, r_max, H, d]
+    k_new: np.ndarray    # [B, r_max, Hkv, d]
+    v_new: np.ndarray
+    k_cache: np.ndarray  # [B, L, Hkv, d] (pre-step)
+    v_cache: np.ndarray
+    dtype: int
+
+
+def make_attention(rng: np.random.Generator, w: Workload, r_max: int,
+                   std: float | None = None) -> AttentionInputs:
+    s = w.qkv_std if std is None else std
+    B, L, H, Hkv, d = w.batch, w.seq_len, w.n_heads, w.n_kv_heads, w.head_dim
+
+    def draw(*shape):
+        x = rng.standard_normal(shape, dtype=np.float32)
+        x *= np.float32(s)
+        return _as_dtype(x, w.attn_dtype)
+
+    q = draw(B, r_max, H, d)
+    k_new = draw(B, r_max, Hkv, d)
+    v_new = draw(B, r_max, Hkv, d)
+    k_cache = draw(B, L, Hkv, d)
+    v_cache = draw(B, L, Hkv, d)
+    return AttentionInputs(q, k_new, v_new, k_cache, v_cache, w.attn_dtype)
+
+
+def random_index_set(rng: np.random.Generator, batch: int, seq_len: int,
+                     counts: np.ndarray, stride: int) -> np.ndarray:
+    """``[batch, stride]`` int32: row b holds ``counts[b]`` distinct positions in
+    ascending order, the rest -1 (a generic recompute set for attention-only cases)."""
+    idx = np.full((batch, stride), -1, np.int32)
+    for b in range(batch):
+        c = int(counts[b])
+        idx[b, :c] = np.sort(rng.choice(seq_len, size=c, replace=False)).astype(np.int32)
+    return idx
+
+
+def step_rng(seed: int, step: int) -> np.random.Generator:
+    """Independent generator for the logits of one trajectory step."""
+    return np.random.default_rng(np.random.SeedSequence([seed, step]))

@@ -1,0 +1,161 @@
+"""ctypes wrapper of the float64 CPU oracle (``oracle.c``).
+
+TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` import this module.  The CUDA library and its
+Python binding never do, and this module never imports them.
+
+Every function takes numpy arrays (host memory) and returns numpy arrays; the
+arithmetic is all in ``oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "oracle.c")
+LIBRARY = os.path.join(_HERE, "liboracle.so")
+
+F32, BF16, F64 = 0, 1, 2
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` with plain ``-O2`` (no fast-math) if stale."""
+    if force or not os.path.exists(LIBRARY) or os.path.getmtime(LIBRARY) < os.path.getmtime(SOURCE):
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-Wall", "-fPIC", "-shared",
+                               "-o", LIBRARY, SOURCE, "-lm"])
+    return LIBRARY
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(LIBRARY)
+        vp, i32, i64, f32, f64 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                  ctypes.c_float, ctypes.c_double)
+        L.orc_row_stats.argtypes = [vp, ctypes.c_int, i64, i32, i32, vp, vp, vp]
+        L.orc_unmask_gate.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, i32,
+                                      vp, vp, vp, vp, vp, vp]
+        L.orc_recompute_set.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
+        L.orc_scatter_kv.argtypes = [vp, vp, ctypes.c_int, vp, i64, vp, vp, vp,
+                                     i32, i32, i32, i32, i32]
+        L.orc_attention.argtypes = [vp, vp, vp, ctypes.c_int, vp, i32, i32, i32, i32, i32, i32,
+                                    f64, vp, i64, vp]
+        for fn in (L.orc_row_stats, L.orc_unmask_gate, L.orc_recompute_set,
+                   L.orc_scatter_kv, L.orc_attention):
+            fn.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed with code {rc}")
+
+
+def _dtype_of(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    if a.dtype == np.float64:
+        return F64
+    raise TypeError(f"oracle takes float32, bf16 bits (uint16) or float64, got {a.dtype}")
+
+
+def row_stats(logits: np.ndarray):
+    """(entropy f64[N], conf f64[N], token i32[N]) of each row of ``[N, V]`` logits."""
+    x = np.ascontiguousarray(logits)
+    n, v = x.shape
+    h = np.empty(n, np.float64)
+    c = np.empty(n, np.float64)
+    t = np.empty(n, np.int32)
+    _check(lib().orc_row_stats(_p(x), _dtype_of(x), v, n, v, _p(h), _p(c), _p(t)), "row_stats")
+    return h, c, t
+
+
+def unmask_gate(conf, entropy, token, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step,
+                is_masked, tokens, decode_step):
+    """Unmask, max entropy and gate for one step.  The three state arrays are
+    copied, updated and returned; the inputs are left unchanged."""
+    conf = np.ascontiguousarray(conf, np.float64)
+    entropy = np.ascontiguousarray(entropy, np.float64)
+    token = np.ascontiguousarray(token, np.int32)
+    off = np.ascontiguousarray(seq_row_offsets, np.int32)
+    pos = np.ascontiguousarray(row_pos, np.int32)
+    batch = off.shape[0] - 1
+    im = np.array(is_masked, np.uint8, copy=True, order="C")
+    tk = np.array(tokens, np.int32, copy=True, order="C")
+    ds = np.array(decode_step, np.int32, copy=True, order="C")
+    unmask = np.empty(batch * n_unmask, np.int32)
+    e = np.empty(batch, np.float64)
+    refresh = np.empty(batch, np.uint8)
+    _check(lib().orc_unmask_gate(_p(conf), _p(entropy), _p(token), _p(off), _p(pos), batch,
+                                 seq_len, n_unmask, float(np.float32(tau)), step, _p(unmask),
+                                 _p(e), _p(refresh), _p(im), _p(tk), _p(ds)), "unmask_gate")
+    return dict(unmask_rows=unmask.reshape(batch, n_unmask), max_entropy=e, refresh=refresh,
+                is_masked=im, tokens=tk, decode_step=ds)
+
+
+def recompute_set(is_masked, decode_step, refresh, block_lo, block_hi, k):
+    """(idx i32[B, L] ascending and -1 padded, count i32[B])."""
+    im = np.ascontiguousarray(is_masked, np.uint8)
+    ds = np.ascontiguousarray(decode_step, np.int32)
+    rf = np.ascontiguousarray(refresh, np.uint8)
+    batch, seq_len = im.shape
+    idx = np.empty((batch, seq_len), np.int32)
+    cnt = np.empty(batch, np.int32)
+    _check(lib().orc_recompute_set(_p(im), _p(ds), _p(rf), batch, seq_len, block_lo, block_hi,
+                                   k, _p(idx), _p(cnt)), "recompute_set")
+    return idx, cnt
+
+
+def scatter_kv(k_new, v_new, idx, count, k_cache, v_cache):
+    """Copies of the caches with the fresh rows written at ``idx``."""
+    kn = np.ascontiguousarray(k_new)
+    vn = np.ascontiguousarray(v_new)
+    kc = np.array(k_cache, copy=True, order="C")
+    vc = np.array(v_cache, copy=True, order="C")
+    ix = np.ascontiguousarray(idx, np.int32)
+    cnt = np.ascontiguousarray(count, np.int32)
+    batch, seq_len, hkv, d = kc.shape
+    r_max = kn.shape[1]
+    dt = _dtype_of(kc)
+    if not (_dtype_of(kn) == _dtype_of(vn) == _dtype_of(vc) == dt):
+        raise TypeError("mixed dtypes")
+    _check(lib().orc_scatter_kv(_p(kn), _p(vn), dt, _p(ix), ix.shape[-1], _p(cnt), _p(kc),
+                                _p(vc), batch, seq_len, r_max, hkv, d), "scatter_kv")
+    return kc, vc
+
+
+def attention(q, k_cache, v_cache, count, scale, samples=None):
+    """float64 attention outputs.  ``samples`` None: ``[B, r_max, H, d]`` with rows
+    past ``count`` set to NaN; else an ``[S, 3]`` array of (b, r, h) and the result
+    is ``[S, d]``."""
+    qq = np.ascontiguousarray(q)
+    kc = np.ascontiguousarray(k_cache)
+    vc = np.ascontiguousarray(v_cache)
+    cnt = np.ascontiguousarray(count, np.int32)
+    batch, r_max, h, d = qq.shape
+    seq_len, hkv = kc.shape[1], kc.shape[2]
+    dt = _dtype_of(qq)
+    if samples is None:
+        out = np.full((batch, r_max, h, d), np.nan, np.float64)
+        sp, ns = None, 0
+    else:
+        sp = np.ascontiguousarray(samples, np.int32).reshape(-1, 3)
+        ns = sp.shape[0]
+        out = np.empty((ns, d), np.float64)
+    _check(lib().orc_attention(_p(qq), _p(kc), _p(vc), dt, _p(cnt), batch, seq_len, r_max, h,
+                               hkv, d, float(scale), _p(sp), ns, _p(out)), "attention")
+    return out

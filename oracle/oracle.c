@@ -1,0 +1,396 @@
+/*
+ * Oracle for the EntropyCache per-step hot path: a plain, slow, float64 CPU
+ * implementation written from the method's definitions.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark load this library.  It shares no code, header
+ * or table with the CUDA library, and the CUDA library never calls it.
+ *
+ * Sources (cited by page title and section):
+ *   [EC-it]  "EntropyCache: Decoded Token Entropy Guided KV Caching for Diffusion
+ *            Language Models", Italian summary (gist.science/it/paper/2603.18489),
+ *            section "2. Metodologia", subsection "Algoritmo di Funzionamento".
+ *   [EC-ar]  the same paper, Arabic technical summary
+ *            (gist.science/ar/paper/2603.18489), section "2. Methodology",
+ *            subsection "Algorithm workflow" and its equation for E_{t+1}.
+ *
+ * Readings taken where the pages are silent (all listed in the design notes):
+ *   - "log" in the entropy is the natural logarithm (nats);
+ *   - decoding a row is greedy: token = argmax of the logits (lowest index on a
+ *     tie), confidence = the softmax probability of that token;
+ *   - unmasking takes, per sequence, the n rows of highest confidence (ties:
+ *     lower position first);
+ *   - the gate is the strict comparison E > tau, E the maximum entropy over the
+ *     rows unmasked this step (E = -inf when none is);
+ *   - "currently masked" means the masked positions of the active block, and the
+ *     k most recently decoded positions are those with the largest decode step
+ *     (ties: lower position first);
+ *   - attention is bidirectional softmax(q K^T * scale) V over all L keys of the
+ *     cache after the fresh K/V rows were written into it.
+ *
+ * Element types: 0 = float32, 1 = bfloat16 (raw uint16 bits), 2 = float64.
+ * Every value is widened exactly to double before any arithmetic.
+ * Return codes: 0 = ok, -2 = bad shape/argument, -3 = bad dtype, -9 = out of memory.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_BAD_ARG (-2)
+#define ORC_BAD_DTYPE (-3)
+#define ORC_NOMEM (-9)
+
+static int dtype_ok(int dtype) { return dtype == 0 || dtype == 1 || dtype == 2; }
+
+static size_t dtype_size(int dtype) { return dtype == 0 ? 4 : (dtype == 1 ? 2 : 8); }
+
+/* Exact widening of element i of a typed array to double. */
+static double load(const void *base, int dtype, int64_t i)
+{
+    if (dtype == 0)
+        return (double)((const float *)base)[i];
+    if (dtype == 1) {
+        uint32_t bits = ((uint32_t)((const uint16_t *)base)[i]) << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return ((const double *)base)[i];
+}
+
+/*
+ * Per-row decode statistics.  [EC-it] step 1 ("decode new tokens and compute
+ * the entropy of their distributions"); [EC-ar] phase 2, the inner sum of the
+ * E_{t+1} equation: H_i = -sum_j p_ij log p_ij with p_i = softmax(x_i).
+ *
+ * For each of n_rows rows (row i starts at element i * row_stride):
+ *   token[i]   = smallest j with x_ij = max_j x_ij
+ *   conf[i]    = p_{i, token[i]}
+ *   entropy[i] = -sum_j p_ij ln p_ij   (terms with p_ij = 0 contribute 0)
+ */
+int orc_row_stats(const void *logits, int dtype, int64_t row_stride, int32_t n_rows,
+                  int32_t vocab, double *entropy, double *conf, int32_t *token)
+{
+    if (!dtype_ok(dtype))
+        return ORC_BAD_DTYPE;
+    if (n_rows < 0 || vocab <= 0 || row_stride < vocab)
+        return ORC_BAD_ARG;
+    double *x = (double *)malloc((size_t)vocab * sizeof(double));
+    double *p = (double *)malloc((size_t)vocab * sizeof(double));
+    if (!x || !p) {
+        free(x);
+        free(p);
+        return ORC_NOMEM;
+    }
+    for (int32_t i = 0; i < n_rows; ++i) {
+        const int64_t base = (int64_t)i * row_stride;
+        for (int32_t j = 0; j < vocab; ++j)
+            x[j] = load(logits, dtype, base + j);
+
+        /* greedy decode: the first index holding the maximum */
+        double m = x[0];
+        int32_t a = 0;
+        for (int32_t j = 1; j < vocab; ++j)
+            if (x[j] > m) {
+                m = x[j];
+                a = j;
+            }
+
+        /* softmax, shifted by the maximum for range */
+        double z = 0.0;
+        for (int32_t j = 0; j < vocab; ++j) {
+            p[j] = exp(x[j] - m);
+            z += p[j];
+        }
+        for (int32_t j = 0; j < vocab; ++j)
+            p[j] /= z;
+
+        /* Shannon entropy in nats */
+        double h = 0.0;
+        for (int32_t j = 0; j < vocab; ++j)
+            if (p[j] > 0.0)
+                h -= p[j] * log(p[j]);
+
+        entropy[i] = h;
+        conf[i] = p[a];
+        token[i] = a;
+    }
+    free(x);
+    free(p);
+    return ORC_OK;
+}
+
+/* ---- confidence-ranked unmasking, max entropy, gate, state update ---- */
+
+typedef struct {
+    double conf;
+    int32_t pos;
+    int32_t row;
+} ranked_row;
+
+/* higher confidence first; on equal confidence the lower position first */
+static int by_conf_then_pos(const void *pa, const void *pb)
+{
+    const ranked_row *a = (const ranked_row *)pa, *b = (const ranked_row *)pb;
+    if (a->conf > b->conf)
+        return -1;
+    if (a->conf < b->conf)
+        return 1;
+    if (a->pos < b->pos)
+        return -1;
+    if (a->pos > b->pos)
+        return 1;
+    return (a->row > b->row) - (a->row < b->row);
+}
+
+/*
+ * One decode step for every sequence b.  [EC-it] steps 1-2; [EC-ar] phases 2-3.
+ *
+ *   rows of sequence b: [seq_row_offsets[b], seq_row_offsets[b+1]), row r at
+ *   position row_pos[r] of that sequence.
+ *   unmask:   the min(n_unmask, #rows) rows ranked first by (conf desc, pos asc),
+ *             written in rank order to unmask_rows[b*n_unmask ...], rest -1.
+ *   E_b:      max of entropy[r] over the unmasked rows ([EC-ar] E_{t+1}), -inf if none.
+ *   refresh:  E_b > tau, compared in double against the float32 threshold
+ *             ([EC-it] step 2: E > tau -> full forward; E <= tau -> partial).
+ *   state:    for each unmasked row: is_masked[b,pos] = 0, tokens[b,pos] = token[r],
+ *             decode_step[b,pos] = step (the decode-time log of [EC-ar] phase 3).
+ */
+int orc_unmask_gate(const double *conf, const double *entropy, const int32_t *token,
+                    const int32_t *seq_row_offsets, const int32_t *row_pos, int32_t batch,
+                    int32_t seq_len, int32_t n_unmask, float tau, int32_t step,
+                    int32_t *unmask_rows, double *max_entropy, uint8_t *refresh,
+                    uint8_t *is_masked, int32_t *tokens, int32_t *decode_step)
+{
+    if (batch < 0 || seq_len <= 0 || n_unmask <= 0)
+        return ORC_BAD_ARG;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int32_t r0 = seq_row_offsets[b], r1 = seq_row_offsets[b + 1];
+        if (r1 < r0)
+            return ORC_BAD_ARG;
+        const int32_t cnt = r1 - r0;
+        ranked_row *rows = (ranked_row *)malloc((size_t)(cnt > 0 ? cnt : 1) * sizeof(ranked_row));
+        if (!rows)
+            return ORC_NOMEM;
+        for (int32_t i = 0; i < cnt; ++i) {
+            rows[i].conf = conf[r0 + i];
+            rows[i].pos = row_pos[r0 + i];
+            rows[i].row = r0 + i;
+            if (rows[i].pos < 0 || rows[i].pos >= seq_len) {
+                free(rows);
+                return ORC_BAD_ARG;
+            }
+        }
+        qsort(rows, (size_t)cnt, sizeof(ranked_row), by_conf_then_pos);
+        const int32_t take = cnt < n_unmask ? cnt : n_unmask;
+        double e = -INFINITY;
+        for (int32_t s = 0; s < n_unmask; ++s)
+            unmask_rows[(int64_t)b * n_unmask + s] = s < take ? rows[s].row : -1;
+        for (int32_t s = 0; s < take; ++s) {
+            const int32_t r = rows[s].row;
+            const int64_t at = (int64_t)b * seq_len + rows[s].pos;
+            if (entropy[r] > e)
+                e = entropy[r];
+            is_masked[at] = 0;
+            tokens[at] = token[r];
+            decode_step[at] = step;
+        }
+        max_entropy[b] = e;
+        refresh[b] = (uint8_t)(e > (double)tau);
+        free(rows);
+    }
+    return ORC_OK;
+}
+
+/* ---- recompute index set ---- */
+
+typedef struct {
+    int32_t step;
+    int32_t pos;
+} decoded_pos;
+
+/* latest decode step first; on equal step the lower position first */
+static int by_recency(const void *pa, const void *pb)
+{
+    const decoded_pos *a = (const decoded_pos *)pa, *b = (const decoded_pos *)pb;
+    if (a->step > b->step)
+        return -1;
+    if (a->step < b->step)
+        return 1;
+    return (a->pos > b->pos) - (a->pos < b->pos);
+}
+
+/*
+ * Positions whose K/V the next forward recomputes.  [EC-it] step 2, second
+ * bullet list; [EC-ar] phase 1 and phase 3 ("token selection").
+ *
+ *   refresh[b] set:  every position 0..L-1 (full forward).
+ *   otherwise:       M_b = masked positions in the active block [block_lo, block_hi)
+ *                    R_b = the min(k, #decoded) decoded, unmasked positions with
+ *                          the largest decode_step (ties: lower position first)
+ *                    idx[b, 0..count[b]) = M_b u R_b in ascending order.
+ *   Entries idx[b, count[b]..L) are set to -1.
+ */
+int orc_recompute_set(const uint8_t *is_masked, const int32_t *decode_step,
+                      const uint8_t *refresh, int32_t batch, int32_t seq_len, int32_t block_lo,
+                      int32_t block_hi, int32_t k, int32_t *idx, int32_t *count)
+{
+    if (batch < 0 || seq_len <= 0 || k < 0 || block_lo < 0 || block_hi < block_lo ||
+        block_hi > seq_len)
+        return ORC_BAD_ARG;
+    uint8_t *take = (uint8_t *)malloc((size_t)seq_len);
+    decoded_pos *dec = (decoded_pos *)malloc((size_t)seq_len * sizeof(decoded_pos));
+    if (!take || !dec) {
+        free(take);
+        free(dec);
+        return ORC_NOMEM;
+    }
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t row = (int64_t)b * seq_len;
+        if (refresh[b]) {
+            for (int32_t p = 0; p < seq_len; ++p)
+                take[p] = 1;
+        } else {
+            memset(take, 0, (size_t)seq_len);
+            for (int32_t p = block_lo; p < block_hi; ++p)
+                if (is_masked[row + p])
+                    take[p] = 1;
+            int32_t nd = 0;
+            for (int32_t p = 0; p < seq_len; ++p)
+                if (decode_step[row + p] >= 0 && !is_masked[row + p]) {
+                    dec[nd].step = decode_step[row + p];
+                    dec[nd].pos = p;
+                    ++nd;
+                }
+            qsort(dec, (size_t)nd, sizeof(decoded_pos), by_recency);
+            const int32_t keep = nd < k ? nd : k;
+            for (int32_t s = 0; s < keep; ++s)
+                take[dec[s].pos] = 1;
+        }
+        int32_t c = 0;
+        for (int32_t p = 0; p < seq_len; ++p)
+            if (take[p])
+                idx[row + c++] = p;
+        for (int32_t s = c; s < seq_len; ++s)
+            idx[row + s] = -1;
+        count[b] = c;
+    }
+    free(take);
+    free(dec);
+    return ORC_OK;
+}
+
+/*
+ * KV write-back of the recomputed rows: for r < count[b],
+ *   cache[b, idx[b*idx_stride + r], :, :] = fresh[b, r, :, :]
+ * ([EC-it] step 2: the partial forward recomputes K/V of the selected tokens and
+ * reuses the cache for the rest; [EC-ar] phase 1).  Layouts: fresh
+ * [batch, r_max, Hkv, d], cache [batch, L, Hkv, d]; a bitwise copy.
+ */
+int orc_scatter_kv(const void *k_new, const void *v_new, int dtype, const int32_t *idx,
+                   int64_t idx_stride, const int32_t *count, void *k_cache, void *v_cache,
+                   int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_kv_heads,
+                   int32_t head_dim)
+{
+    if (!dtype_ok(dtype))
+        return ORC_BAD_DTYPE;
+    const size_t row_bytes = (size_t)n_kv_heads * (size_t)head_dim * dtype_size(dtype);
+    for (int32_t b = 0; b < batch; ++b) {
+        if (count[b] < 0 || count[b] > r_max)
+            return ORC_BAD_ARG;
+        for (int32_t r = 0; r < count[b]; ++r) {
+            const int32_t p = idx[(int64_t)b * idx_stride + r];
+            if (p < 0 || p >= seq_len)
+                return ORC_BAD_ARG;
+            const size_t src = ((size_t)b * r_max + r) * row_bytes;
+            const size_t dst = ((size_t)b * seq_len + p) * row_bytes;
+            memcpy((char *)k_cache + dst, (const char *)k_new + src, row_bytes);
+            memcpy((char *)v_cache + dst, (const char *)v_new + src, row_bytes);
+        }
+    }
+    return ORC_OK;
+}
+
+/*
+ * Bidirectional attention of the recomputed query rows over every cached key
+ * ([EC-it] section 1: dLLM attention is non-causal, every position attends to all
+ * others; [EC-it] step 2 and [EC-ar] phase 1: only the selected rows are
+ * recomputed, all other K/V come from the cache).
+ *
+ * For a query row (b, r, h), r < count[b], with kv head g = h / (H / Hkv):
+ *   s_j = scale * sum_e q[b,r,h,e] * K[b,j,g,e]        for every key j < L
+ *   w_j = exp(s_j - max_j s_j)
+ *   o_e = sum_j w_j V[b,j,g,e] / sum_j w_j
+ *
+ * samples == NULL: every valid row is written to out[b, r, h, :] (rows
+ * r >= count[b] are left untouched).  Otherwise samples holds n_samples triples
+ * (b, r, h) and out[s, :] receives the output of triple s.
+ */
+int orc_attention(const void *q, const void *k_cache, const void *v_cache, int dtype,
+                  const int32_t *count, int32_t batch, int32_t seq_len, int32_t r_max,
+                  int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, double scale,
+                  const int32_t *samples, int64_t n_samples, double *out)
+{
+    if (!dtype_ok(dtype))
+        return ORC_BAD_DTYPE;
+    if (batch < 0 || seq_len <= 0 || r_max < 0 || n_heads <= 0 || n_kv_heads <= 0 ||
+        head_dim <= 0 || n_heads % n_kv_heads != 0)
+        return ORC_BAD_ARG;
+    const int32_t group = n_heads / n_kv_heads;
+    double *s = (double *)malloc((size_t)seq_len * sizeof(double));
+    if (!s)
+        return ORC_NOMEM;
+
+    const int64_t total = samples ? n_samples : (int64_t)batch * r_max * n_heads;
+    for (int64_t t = 0; t < total; ++t) {
+        int32_t b, r, h;
+        double *o;
+        if (samples) {
+            b = samples[3 * t];
+            r = samples[3 * t + 1];
+            h = samples[3 * t + 2];
+            o = out + t * head_dim;
+            if (b < 0 || b >= batch || r < 0 || r >= r_max || h < 0 || h >= n_heads) {
+                free(s);
+                return ORC_BAD_ARG;
+            }
+        } else {
+            b = (int32_t)(t / ((int64_t)r_max * n_heads));
+            r = (int32_t)((t / n_heads) % r_max);
+            h = (int32_t)(t % n_heads);
+            if (r >= count[b])
+                continue;
+            o = out + t * head_dim;
+        }
+        const int32_t g = h / group;
+        const int64_t qoff = (((int64_t)b * r_max + r) * n_heads + h) * head_dim;
+
+        double m = -INFINITY;
+        for (int32_t j = 0; j < seq_len; ++j) {
+            const int64_t koff = (((int64_t)b * seq_len + j) * n_kv_heads + g) * head_dim;
+            double dot = 0.0;
+            for (int32_t e = 0; e < head_dim; ++e)
+                dot += load(q, dtype, qoff + e) * load(k_cache, dtype, koff + e);
+            s[j] = scale * dot;
+            if (s[j] > m)
+                m = s[j];
+        }
+        double z = 0.0;
+        for (int32_t j = 0; j < seq_len; ++j) {
+            s[j] = exp(s[j] - m);
+            z += s[j];
+        }
+        for (int32_t e = 0; e < head_dim; ++e)
+            o[e] = 0.0;
+        for (int32_t j = 0; j < seq_len; ++j) {
+            const int64_t voff = (((int64_t)b * seq_len + j) * n_kv_heads + g) * head_dim;
+            const double w = s[j] / z;
+            for (int32_t e = 0; e < head_dim; ++e)
+                o[e] += w * load(v_cache, dtype, voff + e);
+        }
+    }
+    free(s);
+    return ORC_OK;
+}
