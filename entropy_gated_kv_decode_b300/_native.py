@@ -1,0 +1,226 @@
+"""Thin ctypes binding of ``libec.so`` (declared in ``include/ec.h``).
+
+Argument marshalling only: every function checks that the tensors it is given
+are CUDA tensors of the expected dtype and layout, passes their device
+pointers, sizes and the current CUDA stream to the C function of the same
+name, and raises ``ECError`` on a non-zero status.  All arithmetic runs in the
+library's kernels; there is no other code path.  If the library has not been
+built, every call raises ``NativeLibraryMissing``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIBRARY = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libec.so")
+
+EC_F32, EC_BF16 = 0, 1
+WORKSPACE_ALIGN = 256
+
+DEV_BAD_OFFSETS = 0x1
+DEV_BAD_ROW_POS = 0x2
+DEV_BAD_COUNT = 0x4
+DEV_BAD_INDEX = 0x8
+DEV_TIMEOUT = 0x10
+
+EXPORTED = ("ec_status_str", "ec_abi_version", "ec_workspace_init", "ec_read_device_status",
+            "ec_decode_workspace_size", "ec_decode_step", "ec_build_recompute_set",
+            "ec_attention_workspace_size", "ec_selective_attention")
+
+
+class NativeLibraryMissing(RuntimeError):
+    pass
+
+
+class ECError(RuntimeError):
+    def __init__(self, code: int, fn: str):
+        self.code = code
+        super().__init__(f"{fn}: {status_str(code)} ({code})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIBRARY):
+            raise NativeLibraryMissing(
+                f"{LIBRARY} is missing; build it with `python -m entropy_gated_kv_decode_b300.build`")
+        L = ctypes.CDLL(LIBRARY)
+        vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                                 ctypes.c_size_t)
+        L.ec_status_str.argtypes = [ctypes.c_int]
+        L.ec_status_str.restype = ctypes.c_char_p
+        L.ec_abi_version.argtypes = []
+        L.ec_abi_version.restype = ctypes.c_int
+        L.ec_workspace_init.argtypes = [vp, sz, vp]
+        L.ec_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+        L.ec_decode_workspace_size.argtypes = [i32, i32]
+        L.ec_decode_workspace_size.restype = sz
+        L.ec_decode_step.argtypes = [vp, ctypes.c_int, i64, i32, i32, vp, vp, i32, i32, i32, f32,
+                                     i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.ec_build_recompute_set.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+        L.ec_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        L.ec_attention_workspace_size.restype = sz
+        L.ec_selective_attention.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, ctypes.c_int,
+                                             i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
+        for name in ("ec_workspace_init", "ec_read_device_status", "ec_decode_step",
+                     "ec_build_recompute_set", "ec_selective_attention"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_str(code: int) -> str:
+    return lib().ec_status_str(code).decode()
+
+
+def _check(rc: int, fn: str):
+    if rc != 0:
+        raise ECError(rc, fn)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cuda(name, t, dtype=None, contiguous=True):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _float_code(t):
+    if t.dtype == torch.bfloat16:
+        return EC_BF16
+    if t.dtype == torch.float32:
+        return EC_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: float32 or bfloat16")
+
+
+def _numel(t, n, name):
+    if t.numel() != n:
+        raise ValueError(f"{name} must hold {n} elements, has {t.numel()}")
+
+
+# ---------------------------------------------------------------------------
+
+
+def ec_abi_version() -> int:
+    return lib().ec_abi_version()
+
+
+def ec_decode_workspace_size(n_rows: int, batch: int) -> int:
+    return lib().ec_decode_workspace_size(n_rows, batch)
+
+
+def ec_attention_workspace_size(batch, seq_len, r_max, n_heads, head_dim) -> int:
+    return lib().ec_attention_workspace_size(batch, seq_len, r_max, n_heads, head_dim)
+
+
+def new_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A zeroed device workspace (torch's allocator returns 512-byte aligned blocks)."""
+    ws = torch.zeros(max(int(nbytes), WORKSPACE_ALIGN), dtype=torch.uint8, device=device)
+    if ws.data_ptr() % WORKSPACE_ALIGN:
+        raise RuntimeError("workspace allocation is not 256-byte aligned")
+    return ws
+
+
+def ec_workspace_init(workspace: torch.Tensor, stream=None):
+    _cuda("workspace", workspace, torch.uint8)
+    _check(lib().ec_workspace_init(_p(workspace), workspace.numel(), _stream(stream)),
+           "ec_workspace_init")
+
+
+def ec_read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    _cuda("workspace", workspace, torch.uint8)
+    bits = ctypes.c_uint32(0)
+    _check(lib().ec_read_device_status(_p(workspace), ctypes.byref(bits), _stream(stream)),
+           "ec_read_device_status")
+    return bits.value
+
+
+def ec_decode_step(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step,
+                   token_out, conf_out, entropy_out, unmask_rows, max_entropy, refresh,
+                   is_masked, seq_tokens, decode_step, workspace, stream=None):
+    """logits [N, V] (row stride may exceed V); see ``ec_decode_step`` in ec.h."""
+    _cuda("logits", logits, contiguous=False)
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be [N, V] with unit stride along V")
+    n_rows, vocab = logits.shape
+    batch = seq_row_offsets.numel() - 1
+    _cuda("seq_row_offsets", seq_row_offsets, torch.int32)
+    _cuda("row_pos", row_pos, torch.int32)
+    for name, t, dt, n in (("token_out", token_out, torch.int32, n_rows),
+                           ("conf_out", conf_out, torch.float32, n_rows),
+                           ("entropy_out", entropy_out, torch.float32, n_rows),
+                           ("unmask_rows", unmask_rows, torch.int32, batch * n_unmask),
+                           ("max_entropy", max_entropy, torch.float32, batch),
+                           ("refresh", refresh, torch.uint8, batch),
+                           ("is_masked", is_masked, torch.uint8, batch * seq_len),
+                           ("seq_tokens", seq_tokens, torch.int32, batch * seq_len),
+                           ("decode_step", decode_step, torch.int32, batch * seq_len)):
+        _cuda(name, t, dt)
+        _numel(t, n, name)
+    _numel(row_pos, n_rows, "row_pos")
+    _cuda("workspace", workspace, torch.uint8)
+    rc = lib().ec_decode_step(
+        _p(logits), _float_code(logits), logits.stride(0) if n_rows > 0 else vocab, n_rows, vocab,
+        _p(seq_row_offsets), _p(row_pos), batch, seq_len, n_unmask, float(tau), int(step),
+        _p(token_out), _p(conf_out), _p(entropy_out), _p(unmask_rows), _p(max_entropy),
+        _p(refresh), _p(is_masked), _p(seq_tokens), _p(decode_step), _p(workspace),
+        workspace.numel(), _stream(stream))
+    _check(rc, "ec_decode_step")
+
+
+def ec_build_recompute_set(is_masked, decode_step, refresh, block_lo, block_hi, k, idx, count,
+                           stream=None):
+    """is_masked / decode_step [B, L]; idx [B, L] and count [B] are written."""
+    _cuda("is_masked", is_masked, torch.uint8)
+    _cuda("decode_step", decode_step, torch.int32)
+    _cuda("refresh", refresh, torch.uint8)
+    _cuda("idx", idx, torch.int32)
+    _cuda("count", count, torch.int32)
+    batch, seq_len = is_masked.shape
+    for name, t, n in (("decode_step", decode_step, batch * seq_len), ("refresh", refresh, batch),
+                       ("idx", idx, batch * seq_len), ("count", count, batch)):
+        _numel(t, n, name)
+    _check(lib().ec_build_recompute_set(_p(is_masked), _p(decode_step), _p(refresh), batch, seq_len,
+                                        block_lo, block_hi, k, _p(idx), _p(count), _stream(stream)),
+           "ec_build_recompute_set")
+
+
+def ec_selective_attention(q, k_new, v_new, idx, count, k_cache, v_cache, out, scale, workspace,
+                           stream=None):
+    """q/out [B, R, H, d]; k_new/v_new [B, R, Hkv, d]; caches [B, L, Hkv, d];
+    idx [B, >= R] int32 (row stride = its second dimension); count [B]."""
+    for name, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache),
+                    ("v_cache", v_cache), ("out", out)):
+        _cuda(name, t, q.dtype)
+    _cuda("idx", idx, torch.int32)
+    _cuda("count", count, torch.int32)
+    _cuda("workspace", workspace, torch.uint8)
+    batch, r_max, n_heads, head_dim = q.shape
+    seq_len, n_kv = k_cache.shape[1], k_cache.shape[2]
+    if (k_new.shape != (batch, r_max, n_kv, head_dim) or v_new.shape != k_new.shape
+            or k_cache.shape != (batch, seq_len, n_kv, head_dim) or v_cache.shape != k_cache.shape
+            or out.shape != q.shape or idx.dim() != 2 or idx.shape[0] != batch
+            or count.numel() != batch):
+        raise ValueError("inconsistent attention shapes")
+    rc = lib().ec_selective_attention(
+        _p(q), _p(k_new), _p(v_new), _p(idx), idx.shape[1], _p(count), _p(k_cache), _p(v_cache),
+        _p(out), _float_code(q), batch, seq_len, r_max, n_heads, n_kv, head_dim, float(scale),
+        _p(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "ec_selective_attention")

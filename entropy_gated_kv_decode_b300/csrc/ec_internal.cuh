@@ -1,0 +1,79 @@
+// Internal declarations shared by the CUDA sources of libec (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ec.h"
+
+namespace ec {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Every workspace starts with a 256-byte header; its first word is the device
+// status word (EC_DEV_* bits).
+constexpr size_t kWsHeader = 256;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__device__ __forceinline__ void flag_status(uint32_t *status, uint32_t bits)
+{
+    if (status) atomicOr(status, bits);
+}
+
+// 2^x on the SFU (ex2.approx, flushes subnormal results to zero).
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Streaming 16-byte load that does not allocate in L1.
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+int device_sm_count();  // SM count of the current device (cached per device)
+
+// ---- launchers (each returns cudaSuccess or the launch error) ----
+
+// decode_gate.cu
+size_t decode_workspace_bytes(int32_t n_rows, int32_t batch);
+int decode_splits(int32_t n_rows, int32_t vocab, int elem_bytes);
+cudaError_t launch_decode_gate(const void *logits, int dtype, int64_t row_stride, int32_t n_rows,
+                               int32_t vocab, const int32_t *seq_row_offsets,
+                               const int32_t *row_pos, int32_t batch, int32_t seq_len,
+                               int32_t n_unmask, float tau, int32_t step, int32_t *token_out,
+                               float *conf_out, float *entropy_out, int32_t *unmask_rows,
+                               float *max_entropy, uint8_t *refresh, uint8_t *is_masked,
+                               int32_t *seq_tokens, int32_t *decode_step, void *workspace,
+                               cudaStream_t stream);
+
+// recompute_set.cu
+cudaError_t launch_recompute_set(const uint8_t *is_masked, const int32_t *decode_step,
+                                 const uint8_t *refresh, int32_t batch, int32_t seq_len,
+                                 int32_t block_lo, int32_t block_hi, int32_t k, int32_t *idx,
+                                 int32_t *count, cudaStream_t stream);
+
+// attention_simt.cu
+size_t attention_workspace_bytes(int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
+                                 int32_t head_dim);
+cudaError_t launch_scatter_kv(const void *k_new, const void *v_new, const int32_t *idx,
+                              int64_t idx_stride, const int32_t *count, void *k_cache,
+                              void *v_cache, int dtype, int32_t batch, int32_t seq_len,
+                              int32_t r_max, int32_t n_kv_heads, int32_t head_dim,
+                              uint32_t *status, cudaStream_t stream);
+cudaError_t launch_attention_simt(const void *q, const void *k_cache, const void *v_cache,
+                                  void *out, const int32_t *count, int dtype, int32_t batch,
+                                  int32_t seq_len, int32_t r_max, int32_t n_heads,
+                                  int32_t n_kv_heads, int32_t head_dim, float scale,
+                                  uint32_t *status, cudaStream_t stream);
+
+}  // namespace ec

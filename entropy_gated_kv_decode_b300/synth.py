@@ -252,3 +252,13 @@ def random_index_set(rng: np.random.Generator, batch: int, seq_len: int,
 def step_rng(seed: int, step: int) -> np.random.Generator:
     """Independent generator for the logits of one trajectory step."""
     return np.random.default_rng(np.random.SeedSequence([seed, step]))
+
+
+def random_state(rng: np.random.Generator, batch: int, seq_len: int, p_masked: float = 0.3,
+                 max_step: int = 40):
+    """Unstructured decode state for edge-case tests: each position masked with
+    probability p_masked, otherwise prompt (-1) or decoded at a step in [0, max_step)."""
+    is_masked = (rng.uniform(size=(batch, seq_len)) < p_masked).astype(np.uint8)
+    steps = rng.integers(-1, max_step, size=(batch, seq_len)).astype(np.int32)
+    decode_step = np.where(is_masked == 1, -1, steps).astype(np.int32)
+    return is_masked, decode_step

@@ -1,0 +1,196 @@
+/*
+ * ec.h — C ABI of the EntropyCache per-step hot path on one B300 (sm_103a).
+ *
+ * The method: "EntropyCache: Decoded Token Entropy Guided KV Caching for
+ * Diffusion Language Models".  Passages cited below by page and section:
+ *   [EC-it] Italian summary (gist.science/it/paper/2603.18489), section
+ *           "2. Metodologia", subsection "Algoritmo di Funzionamento", steps 1-3;
+ *           section "1. Il Problema" for the bidirectional attention.
+ *   [EC-ar] Arabic technical summary (gist.science/ar/paper/2603.18489), section
+ *           "2. Methodology", subsection "Algorithm workflow", phases 1-3 and the
+ *           equation E_{t+1} = max_{i in D_{t+1}} ( -sum_j p_ij log p_ij ).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named "device" are CUDA device pointers; every buffer is owned by
+ *     the caller, the library allocates nothing and keeps no host-side state.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and runs asynchronously; nothing synchronises the host except
+ *     ec_read_device_status().
+ *   - Argument errors (null pointers, shapes, dtypes, alignment, workspace size)
+ *     are detected on the host and returned before anything is launched.  A
+ *     failed launch returns EC_ERR_CUDA.  Inconsistent device-resident indices
+ *     (a row position outside [0, L), a count above its bound, an unsorted index
+ *     set) cannot be seen from the host: the kernels keep every access in bounds,
+ *     skip the offending item and set a bit in the workspace's status word, which
+ *     ec_read_device_status() returns.
+ *   - Floating-point work is float32 on float32 or bfloat16 inputs; NaN inputs
+ *     are outside the contract.
+ */
+#ifndef ENTROPY_GATED_KV_DECODE_EC_H
+#define ENTROPY_GATED_KV_DECODE_EC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st *ec_stream_t;
+
+typedef enum {
+    EC_OK = 0,
+    EC_ERR_NULL = -1,        /* a required pointer is NULL */
+    EC_ERR_SHAPE = -2,       /* a size or scalar argument is out of range */
+    EC_ERR_DTYPE = -3,       /* unsupported element type */
+    EC_ERR_ALIGN = -4,       /* a pointer or row stride breaks the 16-byte rule */
+    EC_ERR_WORKSPACE = -5,   /* workspace missing, misaligned or too small */
+    EC_ERR_CUDA = -6,        /* a CUDA runtime call or launch failed */
+    EC_ERR_UNSUPPORTED = -7  /* valid request this build does not implement */
+} ec_status;
+
+typedef enum { EC_F32 = 0, EC_BF16 = 1 } ec_dtype;
+
+/* Bits of the device status word (first 4 bytes of every workspace). */
+#define EC_DEV_BAD_OFFSETS 0x1u  /* seq_row_offsets not 0 .. n_rows non-decreasing */
+#define EC_DEV_BAD_ROW_POS 0x2u  /* a row position outside [0, seq_len) */
+#define EC_DEV_BAD_COUNT 0x4u    /* a recompute count above r_max or seq_len */
+#define EC_DEV_BAD_INDEX 0x8u    /* an index outside [0, seq_len) or not ascending */
+#define EC_DEV_TIMEOUT 0x10u     /* a bounded wait inside a kernel gave up */
+
+/* Human-readable name of a status code (static string). */
+const char *ec_status_str(int status);
+
+/* ABI revision of this header; bumped on any incompatible change. */
+#define EC_ABI_VERSION 1
+int ec_abi_version(void);
+
+/* Alignment, in bytes, that every workspace pointer must have. */
+#define EC_WORKSPACE_ALIGN 256
+
+/*
+ * Zero a workspace (cudaMemsetAsync).  Every workspace must be zeroed once
+ * before its first use; the kernels leave their counters at zero on exit, so
+ * later calls need no further reset.  Returns EC_ERR_CUDA if the memset fails.
+ */
+ec_status ec_workspace_init(void *workspace, size_t workspace_bytes, ec_stream_t stream);
+
+/*
+ * Read, and clear, the device status word of `workspace`.  Synchronises
+ * `stream` first.  *bits receives the EC_DEV_* flags set since the last read.
+ */
+ec_status ec_read_device_status(void *workspace, uint32_t *bits, ec_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* (a) decode and gate                                                        */
+/* ------------------------------------------------------------------------- */
+
+/* Bytes of device workspace ec_decode_step needs for this many rows/sequences. */
+size_t ec_decode_workspace_size(int32_t n_rows, int32_t batch);
+
+/*
+ * One denoising step's decode and gate ([EC-it] steps 1-2; [EC-ar] phases 2-3).
+ *
+ * Inputs
+ *   logits        device, [n_rows, vocab] row-major with `row_stride` elements
+ *                 between rows, `dtype` EC_F32 or EC_BF16.  The base pointer must be
+ *                 16-byte aligned and row_stride * element size a multiple of 16.
+ *                 Each row holds the logits of one currently masked position.
+ *   seq_row_offsets device int32 [batch + 1]: the rows of sequence b are
+ *                 [seq_row_offsets[b], seq_row_offsets[b+1]); offsets[0] = 0,
+ *                 non-decreasing, offsets[batch] = n_rows.
+ *   row_pos       device int32 [n_rows]: position in [0, seq_len) of each row
+ *                 (distinct within a sequence).
+ *   n_unmask      tokens unmasked per sequence this step (1 .. 1024).
+ *   tau           entropy threshold in nats (finite).
+ *   step          index of this denoising step, written to the decode-time log.
+ * Outputs (device)
+ *   token_out, conf_out, entropy_out  [n_rows]: greedy token (first index of the
+ *                 maximum logit), its softmax probability, and the Shannon entropy
+ *                 -sum_j p_j ln p_j of the row's softmax, in nats.
+ *   unmask_rows   int32 [batch, n_unmask]: per sequence, the rows unmasked this
+ *                 step in rank order (confidence descending, position ascending
+ *                 on ties), at most the sequence's row count; the rest -1.
+ *   max_entropy   float [batch]: E = max entropy over the rows unmasked this
+ *                 step ([EC-ar] E_{t+1}); -inf for a sequence with no rows.
+ *   refresh       uint8 [batch]: 1 when E > tau (strict), i.e. the next forward
+ *                 must recompute the whole KV cache; 0 when E <= tau.
+ * State (device, in/out, [batch, seq_len] each)
+ *   is_masked     uint8: cleared at every unmasked position.
+ *   seq_tokens    int32: receives the decoded token at every unmasked position.
+ *   decode_step   int32: receives `step` at every unmasked position (the
+ *                 decode-time log of [EC-ar] phase 3; -1 = never decoded).
+ * Workspace: device, EC_WORKSPACE_ALIGN-aligned, at least
+ *   ec_decode_workspace_size(n_rows, batch) bytes, zeroed before first use.
+ * Calls on the same workspace must not overlap in time.
+ */
+ec_status ec_decode_step(const void *logits, ec_dtype dtype, int64_t row_stride,
+                         int32_t n_rows, int32_t vocab, const int32_t *seq_row_offsets,
+                         const int32_t *row_pos, int32_t batch, int32_t seq_len,
+                         int32_t n_unmask, float tau, int32_t step, int32_t *token_out,
+                         float *conf_out, float *entropy_out, int32_t *unmask_rows,
+                         float *max_entropy, uint8_t *refresh, uint8_t *is_masked,
+                         int32_t *seq_tokens, int32_t *decode_step, void *workspace,
+                         size_t workspace_bytes, ec_stream_t stream);
+
+/*
+ * Recompute index set of the next forward ([EC-it] step 2; [EC-ar] phase 1 and
+ * phase 3 "token selection").
+ *
+ *   refresh[b] != 0: idx[b, :] = 0 .. seq_len-1, count[b] = seq_len (full forward).
+ *   otherwise:       the masked positions of the active block [block_lo, block_hi)
+ *                    together with the min(k, #decoded) decoded positions of largest
+ *                    decode_step (ties: lower position first), ascending.
+ * Inputs: is_masked uint8 / decode_step int32 device [batch, seq_len] (state
+ * after ec_decode_step), refresh uint8 device [batch].  0 <= block_lo <= block_hi
+ * <= seq_len, k >= 0.
+ * Outputs: idx int32 device [batch, seq_len] (ascending, the unused tail -1),
+ * count int32 device [batch].  No workspace.
+ */
+ec_status ec_build_recompute_set(const uint8_t *is_masked, const int32_t *decode_step,
+                                 const uint8_t *refresh, int32_t batch, int32_t seq_len,
+                                 int32_t block_lo, int32_t block_hi, int32_t k, int32_t *idx,
+                                 int32_t *count, ec_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* (b) selective-recompute attention                                          */
+/* ------------------------------------------------------------------------- */
+
+/* Bytes of device workspace ec_selective_attention needs. */
+size_t ec_attention_workspace_size(int32_t batch, int32_t seq_len, int32_t r_max,
+                                   int32_t n_heads, int32_t head_dim);
+
+/*
+ * Write the freshly projected K/V rows into the caches and run bidirectional
+ * attention of the recomputed query rows over every cached key ([EC-it] step 2:
+ * recompute only the selected tokens, reuse the cache for the others; [EC-it]
+ * section 1 and [EC-ar] section 1: dLLM attention is non-causal).
+ *
+ *   for b, r < count[b]:  K[b, idx[b*idx_stride + r]] = k_new[b, r]  (same for V)
+ *   then for every such r and head h (kv head g = h / (n_heads / n_kv_heads)):
+ *     out[b, r, h, :] = softmax_j( scale * q[b,r,h,:] . K[b,j,g,:] ) V[b,j,g,:]
+ *   over all j < seq_len.
+ *
+ * Layouts (contiguous, `dtype` elements): q and out [batch, r_max, n_heads, head_dim];
+ * k_new, v_new [batch, r_max, n_kv_heads, head_dim]; k_cache, v_cache (in/out)
+ * [batch, seq_len, n_kv_heads, head_dim].  idx int32 device with row stride
+ * idx_stride >= r_max; the first count[b] entries of row b are distinct positions in
+ * [0, seq_len), strictly ascending (the output of ec_build_recompute_set).
+ * count int32 device [batch], 0 <= count[b] <= r_max.  Rows r >= count[b] of
+ * `out` are left unchanged.  head_dim 64 or 128; n_heads % n_kv_heads == 0;
+ * 16-byte aligned pointers.  Workspace: ec_attention_workspace_size bytes, zeroed
+ * before first use.  Calls on the same workspace or caches must not overlap.
+ */
+ec_status ec_selective_attention(const void *q, const void *k_new, const void *v_new,
+                                 const int32_t *idx, int64_t idx_stride, const int32_t *count,
+                                 void *k_cache, void *v_cache, void *out, ec_dtype dtype,
+                                 int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
+                                 int32_t n_kv_heads, int32_t head_dim, float scale,
+                                 void *workspace, size_t workspace_bytes, ec_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENTROPY_GATED_KV_DECODE_EC_H */
