@@ -203,26 +203,20 @@ class GpuStep:
         torch.cuda.synchronize(device)
         got = self.count.cpu().numpy()
         assert (got == w.r_max).all(), f"recompute set size {got} != {w.r_max}"
-
-    def attention(self):
-        self.nat.ec_selective_attention(self.q, self.k_new, self.v_new, self.idx, self.count,
-                                        self.k_cache, self.v_cache, self.out, self.scale,
-                                        self.ws_att)
-
-    def decode(self):
-        w = self.w
-        self.nat.ec_decode_step(self.logits, self.offsets, self.row_pos, w.seq_len, w.n_unmask,
-                                w.tau, self.step_index, self.token, self.conf, self.entropy,
-                                self.unmask, self.emax, self.refresh, self.is_masked, self.tokens,
-                                self.decode_step, self.ws_dec)
-
-    def recompute(self):
-        self.nat.ec_build_recompute_set(self.is_masked, self.decode_step, self.refresh,
-                                        self.block[0], self.block[1], self.w.k, self.idx_next,
-                                        self.count_next)
+        # the three calls of a step, validated and marshalled once
+        self.attention = nat.prepare_selective_attention(
+            self.q, self.k_new, self.v_new, self.idx, self.count, self.k_cache, self.v_cache,
+            self.out, self.scale, self.ws_att)
+        self.decode = nat.prepare_decode_step(
+            self.logits, self.offsets, self.row_pos, w.seq_len, w.n_unmask, w.tau,
+            self.step_index, self.token, self.conf, self.entropy, self.unmask, self.emax,
+            self.refresh, self.is_masked, self.tokens, self.decode_step, self.ws_dec)
+        self.recompute = nat.prepare_build_recompute_set(
+            self.is_masked, self.decode_step, self.refresh, self.block[0], self.block[1], w.k,
+            self.idx_next, self.count_next)
 
 
-KERNELS_PER_STEP = {"attention": 2, "decode": 1, "recompute": 1}
+KERNELS_PER_STEP = {"attention": 1, "decode": 1, "recompute": 1}  # bf16: write-back fused
 
 
 def dist_setup(args):

@@ -157,7 +157,7 @@ def ec_decode_step(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, ste
                    is_masked, seq_tokens, decode_step, workspace, stream=None):
     """logits [N, V] (row stride may exceed V); see ``ec_decode_step`` in ec.h."""
     _cuda("logits", logits, contiguous=False)
-    if logits.dim() != 2 or logits.stride(1) != 1:
+    if logits.dim() != 2 or (logits.shape[0] > 0 and logits.stride(1) != 1):
         raise ValueError("logits must be [N, V] with unit stride along V")
     n_rows, vocab = logits.shape
     batch = seq_row_offsets.numel() - 1
@@ -224,3 +224,80 @@ def ec_selective_attention(q, k_new, v_new, idx, count, k_cache, v_cache, out, s
         _p(out), _float_code(q), batch, seq_len, r_max, n_heads, n_kv, head_dim, float(scale),
         _p(workspace), workspace.numel(), _stream(stream))
     _check(rc, "ec_selective_attention")
+
+
+# ---------------------------------------------------------------------------
+# Prepared calls: validate and marshal once, then invoke with ~no host cost.
+# The buffers bound at preparation must stay alive and keep their addresses.
+
+
+class Prepared:
+    """A C-ABI call with its arguments already validated and converted."""
+
+    def __init__(self, name, args, stream_slot):
+        self.name = name
+        self.fn = getattr(lib(), name)
+        # pre-convert every argument to its ctypes type so a call converts nothing
+        self.args = [a if (a is None or isinstance(a, t)) else t(a)
+                     for a, t in zip(args, self.fn.argtypes)]
+        self.stream_slot = stream_slot
+
+    def set_arg(self, i, value):
+        self.args[i] = value
+
+    def __call__(self, stream=None):
+        if stream is not None:
+            self.args[self.stream_slot] = _stream(stream)
+        rc = self.fn(*self.args)
+        if rc != 0:
+            raise ECError(rc, self.name)
+
+
+def _capture_args(fn_name, call, *a, **k):
+    """Run the validating wrapper `call` with a recording library, returning the
+    converted argument list it would have passed to `fn_name`."""
+    captured = {}
+
+    class _Rec:
+        def __getattr__(self, n):
+            real = getattr(lib(), n)
+            if n != fn_name:
+                return real
+
+            def rec(*args):
+                captured["args"] = args
+                return 0
+            return rec
+
+    global _lib
+    saved = _lib
+    _lib = _Rec()
+    try:
+        call(*a, **k)
+    finally:
+        _lib = saved
+    return list(captured["args"])
+
+
+def prepare_decode_step(*args, stream=None, **kwargs):
+    """Same arguments as ec_decode_step; returns a Prepared call.  The step index
+    can be changed with ``.set_step(t)``."""
+    lib()
+    conv = _capture_args("ec_decode_step", ec_decode_step, *args, stream=stream, **kwargs)
+    p = Prepared("ec_decode_step", conv, len(conv) - 1)
+    p.set_step = lambda t: p.set_arg(11, ctypes.c_int32(int(t)))
+    return p
+
+
+def prepare_build_recompute_set(*args, stream=None, **kwargs):
+    lib()
+    conv = _capture_args("ec_build_recompute_set", ec_build_recompute_set, *args, stream=stream,
+                         **kwargs)
+    return Prepared("ec_build_recompute_set", conv, len(conv) - 1)
+
+
+def prepare_selective_attention(*args, stream=None, **kwargs):
+    lib()
+    conv = _capture_args("ec_selective_attention", ec_selective_attention, *args, stream=stream,
+                         **kwargs)
+    return Prepared("ec_selective_attention", conv, len(conv) - 1)

@@ -9,7 +9,7 @@
 // 16-byte non-allocating loads and fold it into an online softmax state
 //     m = max x,   a = first index of m,
 //     S = sum 2^{y},  T = sum 2^{y} y,   y = (x - m) log2(e)
-// so that for the whole row  H = ln S - ln2 * T / S  and  conf = p_a = 1 / S.
+// so that for the whole row  H = ln S - ln2 * T / S  and  conf = p_a = 2^{y_a} / S.
 // The state merges associatively (rescaling by 2^{(m' - m) log2 e}), so a row
 // can be split across CTAs; warps merge with shuffles, the CTA through smem.
 // Phase 2 (the last CTA of a row to finish, found with an atomic ticket — no
@@ -64,7 +64,10 @@ __device__ __forceinline__ void merge(Partial &a, const Partial &b)
     const bool b_wins = b.m > a.m || (b.m == a.m && b.idx < a.idx);
     const Partial hi = b_wins ? b : a;
     const Partial lo = b_wins ? a : b;
-    const float d = (lo.m - hi.m) * kLog2e;  // <= 0
+    // The sums of a partial are relative to mb = fl(m * log2 e), the rounded value
+    // its fold used; shifting between partials uses the same rounded values so the
+    // merged sums stay exactly consistent with one reference point.
+    const float d = lo.m * kLog2e - hi.m * kLog2e;  // <= 0
     const float f = ex2(d);
     a.m = hi.m;
     a.idx = hi.idx;
@@ -142,7 +145,7 @@ __device__ __forceinline__ void fold(const float (&x)[N], IndexOf index_of, floa
             if (x[i] == cm) first = index_of(i);
         const float s = s0 + s1;
         if (s > 0.f) {
-            const float d = (m - cm) * kLog2e;
+            const float d = m * kLog2e - cm * kLog2e;
             const float f = ex2(d);
             const float t = t0 + t1;
             t0 = f * fmaf(d, s, t);
@@ -396,10 +399,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
     }
 
     if (tid == 0) {
+        // Sums are relative to mb = fl(m log2 e); for any reference point
+        // H = ln S - ln2 * T / S, and the argmax's own term is 2^{m log2 e - mb}.
         const float S = p.s;
         const float H = logf(S) - kLn2 * (p.t / S);
+        const float top = ex2(fmaf(p.m, kLog2e, -(p.m * kLog2e)));
         A.entropy_out[row] = fmaxf(H, 0.f);
-        A.conf_out[row] = 1.f / S;
+        A.conf_out[row] = top / S;
         A.token_out[row] = p.idx;
         const int pos = __ldg(A.row_pos + row);
         if (pos < 0 || pos >= A.seq_len) flag_status(A.status, EC_DEV_BAD_ROW_POS);

@@ -144,6 +144,10 @@ ec_status ec_selective_attention(const void *q, const void *k_new, const void *v
         return EC_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint32_t *status = static_cast<uint32_t *>(workspace);
+    if (ec::attention_tc_supported(dtype, seq_len, head_dim))  // one launch, write-back fused
+        return launched(ec::launch_attention_tc(q, k_new, v_new, idx, idx_stride, count, k_cache,
+                                                v_cache, out, batch, seq_len, r_max, n_heads,
+                                                n_kv_heads, head_dim, scale, status, s));
     cudaError_t e = ec::launch_scatter_kv(k_new, v_new, idx, idx_stride, count, k_cache, v_cache,
                                           dtype, batch, seq_len, r_max, n_kv_heads, head_dim,
                                           status, s);
