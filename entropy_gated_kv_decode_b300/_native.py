@@ -152,10 +152,9 @@ def ec_read_device_status(workspace: torch.Tensor, stream=None) -> int:
     return bits.value
 
 
-def ec_decode_step(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step,
-                   token_out, conf_out, entropy_out, unmask_rows, max_entropy, refresh,
-                   is_masked, seq_tokens, decode_step, workspace, stream=None):
-    """logits [N, V] (row stride may exceed V); see ``ec_decode_step`` in ec.h."""
+def _decode_args(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step, token_out,
+                 conf_out, entropy_out, unmask_rows, max_entropy, refresh, is_masked, seq_tokens,
+                 decode_step, workspace):
     _cuda("logits", logits, contiguous=False)
     if logits.dim() != 2 or (logits.shape[0] > 0 and logits.stride(1) != 1):
         raise ValueError("logits must be [N, V] with unit stride along V")
@@ -176,18 +175,24 @@ def ec_decode_step(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, ste
         _numel(t, n, name)
     _numel(row_pos, n_rows, "row_pos")
     _cuda("workspace", workspace, torch.uint8)
-    rc = lib().ec_decode_step(
-        _p(logits), _float_code(logits), logits.stride(0) if n_rows > 0 else vocab, n_rows, vocab,
-        _p(seq_row_offsets), _p(row_pos), batch, seq_len, n_unmask, float(tau), int(step),
-        _p(token_out), _p(conf_out), _p(entropy_out), _p(unmask_rows), _p(max_entropy),
-        _p(refresh), _p(is_masked), _p(seq_tokens), _p(decode_step), _p(workspace),
-        workspace.numel(), _stream(stream))
-    _check(rc, "ec_decode_step")
+    return [_p(logits), _float_code(logits), logits.stride(0) if n_rows > 0 else vocab, n_rows,
+            vocab, _p(seq_row_offsets), _p(row_pos), batch, seq_len, n_unmask, float(tau),
+            int(step), _p(token_out), _p(conf_out), _p(entropy_out), _p(unmask_rows),
+            _p(max_entropy), _p(refresh), _p(is_masked), _p(seq_tokens), _p(decode_step),
+            _p(workspace), workspace.numel()]
 
 
-def ec_build_recompute_set(is_masked, decode_step, refresh, block_lo, block_hi, k, idx, count,
-                           stream=None):
-    """is_masked / decode_step [B, L]; idx [B, L] and count [B] are written."""
+def ec_decode_step(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step,
+                   token_out, conf_out, entropy_out, unmask_rows, max_entropy, refresh,
+                   is_masked, seq_tokens, decode_step, workspace, stream=None):
+    """logits [N, V] (row stride may exceed V); see ``ec_decode_step`` in ec.h."""
+    args = _decode_args(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step,
+                        token_out, conf_out, entropy_out, unmask_rows, max_entropy, refresh,
+                        is_masked, seq_tokens, decode_step, workspace)
+    _check(lib().ec_decode_step(*args, _stream(stream)), "ec_decode_step")
+
+
+def _recompute_args(is_masked, decode_step, refresh, block_lo, block_hi, k, idx, count):
     _cuda("is_masked", is_masked, torch.uint8)
     _cuda("decode_step", decode_step, torch.int32)
     _cuda("refresh", refresh, torch.uint8)
@@ -197,15 +202,18 @@ def ec_build_recompute_set(is_masked, decode_step, refresh, block_lo, block_hi, 
     for name, t, n in (("decode_step", decode_step, batch * seq_len), ("refresh", refresh, batch),
                        ("idx", idx, batch * seq_len), ("count", count, batch)):
         _numel(t, n, name)
-    _check(lib().ec_build_recompute_set(_p(is_masked), _p(decode_step), _p(refresh), batch, seq_len,
-                                        block_lo, block_hi, k, _p(idx), _p(count), _stream(stream)),
-           "ec_build_recompute_set")
+    return [_p(is_masked), _p(decode_step), _p(refresh), batch, seq_len, block_lo, block_hi, k,
+            _p(idx), _p(count)]
 
 
-def ec_selective_attention(q, k_new, v_new, idx, count, k_cache, v_cache, out, scale, workspace,
+def ec_build_recompute_set(is_masked, decode_step, refresh, block_lo, block_hi, k, idx, count,
                            stream=None):
-    """q/out [B, R, H, d]; k_new/v_new [B, R, Hkv, d]; caches [B, L, Hkv, d];
-    idx [B, >= R] int32 (row stride = its second dimension); count [B]."""
+    """is_masked / decode_step [B, L]; idx [B, L] and count [B] are written."""
+    args = _recompute_args(is_masked, decode_step, refresh, block_lo, block_hi, k, idx, count)
+    _check(lib().ec_build_recompute_set(*args, _stream(stream)), "ec_build_recompute_set")
+
+
+def _attention_args(q, k_new, v_new, idx, count, k_cache, v_cache, out, scale, workspace):
     for name, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache),
                     ("v_cache", v_cache), ("out", out)):
         _cuda(name, t, q.dtype)
@@ -219,85 +227,55 @@ def ec_selective_attention(q, k_new, v_new, idx, count, k_cache, v_cache, out, s
             or out.shape != q.shape or idx.dim() != 2 or idx.shape[0] != batch
             or count.numel() != batch):
         raise ValueError("inconsistent attention shapes")
-    rc = lib().ec_selective_attention(
-        _p(q), _p(k_new), _p(v_new), _p(idx), idx.shape[1], _p(count), _p(k_cache), _p(v_cache),
-        _p(out), _float_code(q), batch, seq_len, r_max, n_heads, n_kv, head_dim, float(scale),
-        _p(workspace), workspace.numel(), _stream(stream))
-    _check(rc, "ec_selective_attention")
+    return [_p(q), _p(k_new), _p(v_new), _p(idx), idx.shape[1], _p(count), _p(k_cache),
+            _p(v_cache), _p(out), _float_code(q), batch, seq_len, r_max, n_heads, n_kv, head_dim,
+            float(scale), _p(workspace), workspace.numel()]
+
+
+def ec_selective_attention(q, k_new, v_new, idx, count, k_cache, v_cache, out, scale, workspace,
+                           stream=None):
+    """q/out [B, R, H, d]; k_new/v_new [B, R, Hkv, d]; caches [B, L, Hkv, d];
+    idx [B, >= R] int32 (row stride = its second dimension); count [B]."""
+    args = _attention_args(q, k_new, v_new, idx, count, k_cache, v_cache, out, scale, workspace)
+    _check(lib().ec_selective_attention(*args, _stream(stream)), "ec_selective_attention")
 
 
 # ---------------------------------------------------------------------------
-# Prepared calls: validate and marshal once, then invoke with ~no host cost.
-# The buffers bound at preparation must stay alive and keep their addresses.
+# Prepared calls: validate and marshal once, then invoke with almost no host
+# cost.  The tensors bound at preparation must stay alive and in place.
 
 
 class Prepared:
-    """A C-ABI call with its arguments already validated and converted."""
+    """A C-ABI call whose arguments are already validated and converted."""
 
-    def __init__(self, name, args, stream_slot):
+    def __init__(self, name, args, stream):
         self.name = name
         self.fn = getattr(lib(), name)
+        args = list(args) + [_stream(stream)]
         # pre-convert every argument to its ctypes type so a call converts nothing
         self.args = [a if (a is None or isinstance(a, t)) else t(a)
                      for a, t in zip(args, self.fn.argtypes)]
-        self.stream_slot = stream_slot
 
     def set_arg(self, i, value):
-        self.args[i] = value
+        t = self.fn.argtypes[i]
+        self.args[i] = value if isinstance(value, t) else t(value)
 
-    def __call__(self, stream=None):
-        if stream is not None:
-            self.args[self.stream_slot] = _stream(stream)
+    def __call__(self):
         rc = self.fn(*self.args)
         if rc != 0:
             raise ECError(rc, self.name)
 
 
-def _capture_args(fn_name, call, *a, **k):
-    """Run the validating wrapper `call` with a recording library, returning the
-    converted argument list it would have passed to `fn_name`."""
-    captured = {}
-
-    class _Rec:
-        def __getattr__(self, n):
-            real = getattr(lib(), n)
-            if n != fn_name:
-                return real
-
-            def rec(*args):
-                captured["args"] = args
-                return 0
-            return rec
-
-    global _lib
-    saved = _lib
-    _lib = _Rec()
-    try:
-        call(*a, **k)
-    finally:
-        _lib = saved
-    return list(captured["args"])
-
-
 def prepare_decode_step(*args, stream=None, **kwargs):
-    """Same arguments as ec_decode_step; returns a Prepared call.  The step index
-    can be changed with ``.set_step(t)``."""
-    lib()
-    conv = _capture_args("ec_decode_step", ec_decode_step, *args, stream=stream, **kwargs)
-    p = Prepared("ec_decode_step", conv, len(conv) - 1)
-    p.set_step = lambda t: p.set_arg(11, ctypes.c_int32(int(t)))
+    """ec_decode_step bound to fixed buffers; ``.set_step(t)`` changes the step index."""
+    p = Prepared("ec_decode_step", _decode_args(*args, **kwargs), stream)
+    p.set_step = lambda t: p.set_arg(11, int(t))
     return p
 
 
 def prepare_build_recompute_set(*args, stream=None, **kwargs):
-    lib()
-    conv = _capture_args("ec_build_recompute_set", ec_build_recompute_set, *args, stream=stream,
-                         **kwargs)
-    return Prepared("ec_build_recompute_set", conv, len(conv) - 1)
+    return Prepared("ec_build_recompute_set", _recompute_args(*args, **kwargs), stream)
 
 
 def prepare_selective_attention(*args, stream=None, **kwargs):
-    lib()
-    conv = _capture_args("ec_selective_attention", ec_selective_attention, *args, stream=stream,
-                         **kwargs)
-    return Prepared("ec_selective_attention", conv, len(conv) - 1)
+    return Prepared("ec_selective_attention", _attention_args(*args, **kwargs), stream)
