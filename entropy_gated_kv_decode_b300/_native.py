@@ -26,8 +26,8 @@ DEV_BAD_INDEX = 0x8
 DEV_TIMEOUT = 0x10
 
 EXPORTED = ("ec_status_str", "ec_abi_version", "ec_workspace_init", "ec_read_device_status",
-            "ec_decode_workspace_size", "ec_decode_step", "ec_build_recompute_set",
-            "ec_attention_workspace_size", "ec_selective_attention")
+            "ec_decode_workspace_size", "ec_decode_step", "ec_decode_step_noalloc",
+            "ec_build_recompute_set", "ec_attention_workspace_size", "ec_selective_attention")
 
 
 class NativeLibraryMissing(RuntimeError):
@@ -62,13 +62,15 @@ def lib() -> ctypes.CDLL:
         L.ec_decode_workspace_size.restype = sz
         L.ec_decode_step.argtypes = [vp, ctypes.c_int, i64, i32, i32, vp, vp, i32, i32, i32, f32,
                                      i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.ec_decode_step_noalloc.argtypes = [vp, ctypes.c_int, i64, i32, i32, vp, vp, i32, i32, i32,
+                                             f32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.ec_build_recompute_set.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
         L.ec_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         L.ec_attention_workspace_size.restype = sz
         L.ec_selective_attention.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, ctypes.c_int,
                                              i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
         for name in ("ec_workspace_init", "ec_read_device_status", "ec_decode_step",
-                     "ec_build_recompute_set", "ec_selective_attention"):
+                     "ec_decode_step_noalloc", "ec_build_recompute_set", "ec_selective_attention"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -190,6 +192,18 @@ def ec_decode_step(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, ste
                         token_out, conf_out, entropy_out, unmask_rows, max_entropy, refresh,
                         is_masked, seq_tokens, decode_step, workspace)
     _check(lib().ec_decode_step(*args, _stream(stream)), "ec_decode_step")
+
+
+def ec_decode_step_noalloc(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step,
+                           token_out, conf_out, entropy_out, unmask_rows, max_entropy, refresh,
+                           is_masked, seq_tokens, decode_step, stream=None):
+    """ec_decode_step without a workspace, for callers that cannot allocate device
+    memory: the scratch is a fixed 2 MiB array inside the library (see ec.h)."""
+    dummy = torch.empty(0, dtype=torch.uint8, device=logits.device)
+    args = _decode_args(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step,
+                        token_out, conf_out, entropy_out, unmask_rows, max_entropy, refresh,
+                        is_masked, seq_tokens, decode_step, dummy)[:-2]
+    _check(lib().ec_decode_step_noalloc(*args, _stream(stream)), "ec_decode_step_noalloc")
 
 
 def _recompute_args(is_masked, decode_step, refresh, block_lo, block_hi, k, idx, count):

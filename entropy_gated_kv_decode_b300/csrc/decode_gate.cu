@@ -500,3 +500,77 @@ cudaError_t launch_decode_gate(const void *logits, int dtype, int64_t row_stride
 }
 
 }  // namespace ec
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of ec_decode_step.
+//
+// For callers that cannot allocate device memory themselves (their device
+// memory belongs to a host framework or a fixed pool, or a cudaMalloc, which
+// may synchronise the device, is not acceptable in their decode loop).  The
+// scratch that ec_decode_step takes as a workspace lives here in a fixed
+// device array instead; every device that loads the library holds it until
+// the process exits.
+
+namespace ec {
+
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;  // 2 MiB
+
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+// Device address of g_decode_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+static cudaError_t decode_scratch_address(void **out)
+{
+    static void *addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace ec
+
+extern "C" ec_status ec_decode_step_noalloc(
+    const void *logits, ec_dtype dtype, int64_t row_stride, int32_t n_rows, int32_t vocab,
+    const int32_t *seq_row_offsets, const int32_t *row_pos, int32_t batch, int32_t seq_len,
+    int32_t n_unmask, float tau, int32_t step, int32_t *token_out, float *conf_out,
+    float *entropy_out, int32_t *unmask_rows, float *max_entropy, uint8_t *refresh,
+    uint8_t *is_masked, int32_t *seq_tokens, int32_t *decode_step, ec_stream_t stream)
+{
+    if (dtype != EC_F32 && dtype != EC_BF16) return EC_ERR_DTYPE;
+    if (n_rows < 0 || vocab < 1 || batch < 1 || seq_len < 1 || n_unmask < 1 ||
+        n_unmask > ec::kMaxUnmask || row_stride < vocab || !isfinite(tau))
+        return EC_ERR_SHAPE;
+    if (!seq_row_offsets || !unmask_rows || !max_entropy || !refresh || !is_masked ||
+        !seq_tokens || !decode_step)
+        return EC_ERR_NULL;
+    if (n_rows > 0 && (!logits || !row_pos || !token_out || !conf_out || !entropy_out))
+        return EC_ERR_NULL;
+    const int elem = dtype == EC_BF16 ? 2 : 4;
+    if (n_rows > 0 && ((reinterpret_cast<uintptr_t>(logits) & 15) != 0 ||
+                       (row_stride * elem) % 16 != 0))
+        return EC_ERR_ALIGN;
+    const size_t need = ec::decode_workspace_bytes(n_rows, batch);
+    if (need > ec::kNoAllocScratchBytes) return EC_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    if (ec::decode_scratch_address(&scratch) != cudaSuccess) return EC_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // The array keeps the previous call's contents: clear the status word and the
+    // tickets, which must start at zero (the per-slice partials need no clearing).
+    const size_t zeroed = need - static_cast<size_t>(n_rows) * ec::kMaxSplits * sizeof(ec::Partial);
+    if (cudaMemsetAsync(scratch, 0, zeroed, s) != cudaSuccess) return EC_ERR_CUDA;
+    const cudaError_t e = ec::launch_decode_gate(
+        logits, dtype, row_stride, n_rows, vocab, seq_row_offsets, row_pos, batch, seq_len,
+        n_unmask, tau, step, token_out, conf_out, entropy_out, unmask_rows, max_entropy, refresh,
+        is_masked, seq_tokens, decode_step, scratch, s);
+    return e == cudaSuccess ? EC_OK : EC_ERR_CUDA;
+}

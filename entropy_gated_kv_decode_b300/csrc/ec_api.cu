@@ -42,6 +42,8 @@ const char *ec_status_str(int s)
     case EC_ERR_WORKSPACE: return "EC_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case EC_ERR_CUDA: return "EC_ERR_CUDA: a CUDA call or kernel launch failed";
     case EC_ERR_UNSUPPORTED: return "EC_ERR_UNSUPPORTED: not implemented for these arguments";
+    case EC_ERR_SCRATCH_LIMIT:
+        return "EC_ERR_SCRATCH_LIMIT: request exceeds the fixed scratch of the allocation-free entry point";
     default: return "unknown ec_status";
     }
 }

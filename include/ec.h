@@ -12,7 +12,9 @@
  *
  * Conventions shared by every entry point
  *   - Pointers named "device" are CUDA device pointers; every buffer is owned by
- *     the caller, the library allocates nothing and keeps no host-side state.
+ *     the caller, the library allocates nothing and keeps no host-side state
+ *     (beyond per-device lookups it caches, such as the address of the fixed
+ *     scratch array of ec_decode_step_noalloc).
  *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  *     stream) and runs asynchronously; nothing synchronises the host except
  *     ec_read_device_status().
@@ -47,7 +49,8 @@ typedef enum {
     EC_ERR_ALIGN = -4,       /* a pointer or row stride breaks the 16-byte rule */
     EC_ERR_WORKSPACE = -5,   /* workspace missing, misaligned or too small */
     EC_ERR_CUDA = -6,        /* a CUDA runtime call or launch failed */
-    EC_ERR_UNSUPPORTED = -7  /* valid request this build does not implement */
+    EC_ERR_UNSUPPORTED = -7, /* valid request this build does not implement */
+    EC_ERR_SCRATCH_LIMIT = -8 /* request needs more than the fixed built-in scratch */
 } ec_status;
 
 typedef enum { EC_F32 = 0, EC_BF16 = 1 } ec_dtype;
@@ -133,6 +136,38 @@ ec_status ec_decode_step(const void *logits, ec_dtype dtype, int64_t row_stride,
                          float *max_entropy, uint8_t *refresh, uint8_t *is_masked,
                          int32_t *seq_tokens, int32_t *decode_step, void *workspace,
                          size_t workspace_bytes, ec_stream_t stream);
+
+/*
+ * ec_decode_step without a caller-provided workspace: it allocates nothing.
+ *
+ * The paper has no counterpart; this is a deployment convenience.  Some callers
+ * cannot allocate device memory on their own: their device memory is owned by a
+ * host framework or a fixed-size pool that hands out only the tensors of the
+ * model, or they run in a latency-critical decode loop where a cudaMalloc (which
+ * may synchronise the device) is not acceptable.  This entry point takes the same
+ * inputs, outputs and state as ec_decode_step and keeps its scratch (counters and
+ * per-slice partial results) in a fixed array compiled into the library.
+ *
+ *   - Limit: ec_decode_workspace_size(n_rows, batch) must not exceed 2 MiB
+ *     (about 2000 logits rows); larger requests return EC_ERR_SCRATCH_LIMIT
+ *     before anything is enqueued.
+ *   - Every device that loads the library holds those 2 MiB until the process exits.
+ *   - The first call on a device looks the array's device address up (with that
+ *     device current); make that first call before any stream capture.
+ *   - All calls share the one array: each call first clears the part that must
+ *     start at zero, on `stream`.  Calls whose kernels can overlap on the GPU
+ *     (different streams, no ordering between them) race on the array and give
+ *     undefined results; serialise them.
+ *   - Device-side index checks still keep every access in bounds, but their status
+ *     bits are not reported by this entry point.
+ */
+ec_status ec_decode_step_noalloc(const void *logits, ec_dtype dtype, int64_t row_stride,
+                                 int32_t n_rows, int32_t vocab, const int32_t *seq_row_offsets,
+                                 const int32_t *row_pos, int32_t batch, int32_t seq_len,
+                                 int32_t n_unmask, float tau, int32_t step, int32_t *token_out,
+                                 float *conf_out, float *entropy_out, int32_t *unmask_rows,
+                                 float *max_entropy, uint8_t *refresh, uint8_t *is_masked,
+                                 int32_t *seq_tokens, int32_t *decode_step, ec_stream_t stream);
 
 /*
  * Recompute index set of the next forward ([EC-it] step 2; [EC-ar] phase 1 and
