@@ -56,6 +56,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=300)
+    p.add_argument("--eager", action="store_true", help="time eager launches, not graph replays")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU time budget of the oracle baseline sample")
     return p.parse_args(argv)
@@ -159,10 +160,11 @@ class GpuStep:
     """Device-resident inputs, outputs and workspaces of one step, and the three
     C-ABI calls that make it up."""
 
-    def __init__(self, nat, w: synth.Workload, st, logits, att, device):
+    def __init__(self, nat, w: synth.Workload, st, logits, att, device, stream):
         import torch
         self.nat, self.w, self.torch = nat, w, torch
         self.dev = device
+        self.stream = stream
 
         def up(a):
             if a.dtype == np.uint16:
@@ -190,7 +192,8 @@ class GpuStep:
         self.k_cache, self.v_cache = up(att.k_cache), up(att.v_cache)
         self.out = torch.zeros_like(self.q)
         self.ws_att = nat.new_workspace(
-            nat.ec_attention_workspace_size(B, L, w.r_max, w.n_heads, w.head_dim), device)
+            nat.ec_attention_workspace_size(B, L, w.r_max, w.n_heads, w.n_kv_heads,
+                                           w.head_dim), device)
         # this step's recompute set: built once from the initial state
         self.idx = torch.empty((B, L), dtype=i32, device=device)
         self.count = torch.empty(B, dtype=i32, device=device)
@@ -206,17 +209,27 @@ class GpuStep:
         # the three calls of a step, validated and marshalled once
         self.attention = nat.prepare_selective_attention(
             self.q, self.k_new, self.v_new, self.idx, self.count, self.k_cache, self.v_cache,
-            self.out, self.scale, self.ws_att)
+            self.out, self.scale, self.ws_att, stream=stream)
         self.decode = nat.prepare_decode_step(
             self.logits, self.offsets, self.row_pos, w.seq_len, w.n_unmask, w.tau,
             self.step_index, self.token, self.conf, self.entropy, self.unmask, self.emax,
-            self.refresh, self.is_masked, self.tokens, self.decode_step, self.ws_dec)
+            self.refresh, self.is_masked, self.tokens, self.decode_step, self.ws_dec,
+            stream=stream)
         self.recompute = nat.prepare_build_recompute_set(
             self.is_masked, self.decode_step, self.refresh, self.block[0], self.block[1], w.k,
-            self.idx_next, self.count_next)
+            self.idx_next, self.count_next, stream=stream)
+
+    def run(self):
+        self.attention()
+        self.decode()
+        self.recompute()
 
 
-KERNELS_PER_STEP = {"attention": 1, "decode": 1, "recompute": 1}  # bf16: write-back fused
+def kernels_per_step(w: synth.Workload):
+    """Launches of our kernels per step: bf16 attention is one tensor-core kernel
+    with the write-back fused; float32 attention is a write-back kernel plus the
+    SIMT kernel."""
+    return {"attention": 1 if w.attn_dtype == synth.BF16 else 2, "decode": 1, "recompute": 1}
 
 
 def dist_setup(args):
@@ -271,17 +284,50 @@ def run_ours(args):
     w = synth.WORKLOADS[args.workload]
     geo = workload_geometry(w)
     st, logits, att = host_inputs(w, args.seed)
-    step = GpuStep(nat, w, st, logits, att, device)
+    stream = torch.cuda.Stream(device)
+    torch.cuda.set_stream(stream)
+    step = GpuStep(nat, w, st, logits, att, device, stream)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     K, W = args.steps, args.warmup
 
     for _ in range(W):
         flush.zero_()
-        step.attention()
-        step.decode()
-        step.recompute()
+        step.run()
     torch.cuda.synchronize(device)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    # One step = one replay of a CUDA graph holding the three calls with timing
+    # events between them, so host launch cost stays out of the device timings.
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+    graph, mode = None, "cuda-graph replay per step"
+    if args.eager:
+        mode = "eager launches"
+    else:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                ev[0].record()
+                step.attention()
+                ev[1].record()
+                step.decode()
+                ev[2].record()
+                step.recompute()
+                ev[3].record()
+            graph.replay()
+            torch.cuda.synchronize(device)
+        except Exception as exc:  # capture not possible: time eager launches instead
+            graph, mode = None, f"eager launches (graph capture failed: {type(exc).__name__})"
+
+    def one_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            ev[0].record()
+            step.attention()
+            ev[1].record()
+            step.decode()
+            ev[2].record()
+            step.recompute()
+            ev[3].record()
+
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(device).uuid)
@@ -293,23 +339,18 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize(device)
     t_wall = time.perf_counter()
-    for i in range(K):
+    t_att = t_dec = t_rec = 0.0
+    for _ in range(K):
         flush.zero_()
-        e = ev[i]
-        e[0].record()
-        step.attention()
-        e[1].record()
-        step.decode()
-        e[2].record()
-        step.recompute()
-        e[3].record()
+        one_step()
+        ev[3].synchronize()
+        t_att += ev[0].elapsed_time(ev[1]) / 1e3
+        t_dec += ev[1].elapsed_time(ev[2]) / 1e3
+        t_rec += ev[2].elapsed_time(ev[3]) / 1e3
     torch.cuda.synchronize(device)
     barrier(world)
     wall = time.perf_counter() - t_wall
     clocks = sampler.stop()
-    t_att = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
-    t_dec = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3
-    t_rec = sum(e[2].elapsed_time(e[3]) for e in ev) / 1e3
     t_step = t_att + t_dec + t_rec
     t_step_max = reduce_max(t_step, world)
     status = nat.ec_read_device_status(step.ws_dec) | nat.ec_read_device_status(step.ws_att)
@@ -329,7 +370,7 @@ def run_ours(args):
         "attention": {"us": us(t_att), "tflops": att_tflops, "frac_tensor_peak": att_tflops / tc,
                       "gbs": att_gbs, "frac_hbm": att_gbs / hbm,
                       "frac_attainable": att_tflops / att_roof, "intensity_flop_per_byte": att_ai,
-                      "launches": KERNELS_PER_STEP["attention"]},
+                      "launches": kernels_per_step(w)["attention"]},
         "decode_gate": {"us": us(t_dec), "gbs": geo["logits_bytes"] * K / t_dec / 1e9,
                         "frac_hbm": geo["logits_bytes"] * K / t_dec / 1e9 / hbm, "launches": 1},
         "recompute_set": {"us": us(t_rec), "launches": 1},
@@ -365,10 +406,10 @@ def run_ours(args):
                    "n_rows": w.n_rows, "recompute_rows": w.r_max, "n_heads": w.n_heads,
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "n_unmask": w.n_unmask,
                    "k": w.k, "tau": w.tau, "accumulate": "f32",
-                   "l2": "flushed between steps (256 MiB write, untimed)",
+                   "l2": "flushed between steps (256 MiB write, untimed)", "launch": mode,
                    "parallelism": f"replicas x{world}"},
         "parts": parts, "roofline": roof, "clocks": clocks, "e2e": e2e,
-        "gpu_launches": sum(KERNELS_PER_STEP.values()) * K,
+        "gpu_launches": sum(kernels_per_step(w).values()) * K,
         "cpu_baseline": cpu, "device_status": status, "wall_s_timed_region": wall,
     }
     if rank == 0:
@@ -401,9 +442,7 @@ def run_e2e(step: GpuStep, geo, w, logits, att, K, world):
     def one():
         for h, d in h_in:
             d.copy_(h, non_blocking=True)
-        step.attention()
-        step.decode()
-        step.recompute()
+        step.run()
         for d, h in zip(d_out, h_out):
             h.copy_(d, non_blocking=True)
 

@@ -65,7 +65,7 @@ def lib() -> ctypes.CDLL:
         L.ec_decode_step_noalloc.argtypes = [vp, ctypes.c_int, i64, i32, i32, vp, vp, i32, i32, i32,
                                              f32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.ec_build_recompute_set.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
-        L.ec_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        L.ec_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         L.ec_attention_workspace_size.restype = sz
         L.ec_selective_attention.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, ctypes.c_int,
                                              i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
@@ -128,8 +128,8 @@ def ec_decode_workspace_size(n_rows: int, batch: int) -> int:
     return lib().ec_decode_workspace_size(n_rows, batch)
 
 
-def ec_attention_workspace_size(batch, seq_len, r_max, n_heads, head_dim) -> int:
-    return lib().ec_attention_workspace_size(batch, seq_len, r_max, n_heads, head_dim)
+def ec_attention_workspace_size(batch, seq_len, r_max, n_heads, n_kv_heads, head_dim) -> int:
+    return lib().ec_attention_workspace_size(batch, seq_len, r_max, n_heads, n_kv_heads, head_dim)
 
 
 def new_workspace(nbytes: int, device="cuda") -> torch.Tensor:

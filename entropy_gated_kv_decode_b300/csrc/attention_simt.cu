@@ -13,6 +13,8 @@
 // softmax in the log2 domain, and the output is normalised at the end.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "ec_internal.cuh"
 
 namespace ec {
@@ -149,7 +151,14 @@ cudaError_t launch_simt_typed(const void *q, const void *kc, const void *vc, voi
 
 }  // namespace
 
-size_t attention_workspace_bytes(int32_t, int32_t, int32_t, int32_t, int32_t) { return kWsHeader; }
+size_t attention_workspace_bytes(int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
+                                 int32_t n_kv_heads, int32_t head_dim)
+{
+    // the SIMT path needs only the status header; the tensor-core path also keeps
+    // split-KV partials and its grid-barrier words
+    return std::max(kWsHeader, attention_tc_workspace_bytes(batch, seq_len, r_max, n_heads,
+                                                            n_kv_heads, head_dim));
+}
 
 cudaError_t launch_scatter_kv(const void *k_new, const void *v_new, const int32_t *idx,
                               int64_t idx_stride, const int32_t *count, void *k_cache,

@@ -119,9 +119,9 @@ ec_status ec_build_recompute_set(const uint8_t *is_masked, const int32_t *decode
 }
 
 size_t ec_attention_workspace_size(int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
-                                   int32_t head_dim)
+                                   int32_t n_kv_heads, int32_t head_dim)
 {
-    return ec::attention_workspace_bytes(batch, seq_len, r_max, n_heads, head_dim);
+    return ec::attention_workspace_bytes(batch, seq_len, r_max, n_heads, n_kv_heads, head_dim);
 }
 
 ec_status ec_selective_attention(const void *q, const void *k_new, const void *v_new,
@@ -142,14 +142,15 @@ ec_status ec_selective_attention(const void *q, const void *k_new, const void *v
     for (const void *p : ptrs)
         if (p && !aligned(p, 16)) return EC_ERR_ALIGN;
     if (!aligned(workspace, EC_WORKSPACE_ALIGN) ||
-        workspace_bytes < ec::attention_workspace_bytes(batch, seq_len, r_max, n_heads, head_dim))
+        workspace_bytes <
+            ec::attention_workspace_bytes(batch, seq_len, r_max, n_heads, n_kv_heads, head_dim))
         return EC_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint32_t *status = static_cast<uint32_t *>(workspace);
     if (ec::attention_tc_supported(dtype, seq_len, head_dim))  // one launch, write-back fused
         return launched(ec::launch_attention_tc(q, k_new, v_new, idx, idx_stride, count, k_cache,
                                                 v_cache, out, batch, seq_len, r_max, n_heads,
-                                                n_kv_heads, head_dim, scale, status, s));
+                                                n_kv_heads, head_dim, scale, workspace, s));
     cudaError_t e = ec::launch_scatter_kv(k_new, v_new, idx, idx_stride, count, k_cache, v_cache,
                                           dtype, batch, seq_len, r_max, n_kv_heads, head_dim,
                                           status, s);

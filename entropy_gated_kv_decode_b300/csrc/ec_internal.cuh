@@ -64,7 +64,7 @@ cudaError_t launch_recompute_set(const uint8_t *is_masked, const int32_t *decode
 
 // attention_simt.cu
 size_t attention_workspace_bytes(int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
-                                 int32_t head_dim);
+                                 int32_t n_kv_heads, int32_t head_dim);
 cudaError_t launch_scatter_kv(const void *k_new, const void *v_new, const int32_t *idx,
                               int64_t idx_stride, const int32_t *count, void *k_cache,
                               void *v_cache, int dtype, int32_t batch, int32_t seq_len,
@@ -78,11 +78,13 @@ cudaError_t launch_attention_simt(const void *q, const void *k_cache, const void
 
 // attention_tc.cu
 bool attention_tc_supported(int dtype, int32_t seq_len, int32_t head_dim);
+size_t attention_tc_workspace_bytes(int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
+                                    int32_t n_kv_heads, int32_t head_dim);
 cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_new,
                                 const int32_t *idx, int64_t idx_stride, const int32_t *count,
                                 void *k_cache, void *v_cache, void *out, int32_t batch,
                                 int32_t seq_len, int32_t r_max, int32_t n_heads,
                                 int32_t n_kv_heads, int32_t head_dim, float scale,
-                                uint32_t *status, cudaStream_t stream);
+                                void *workspace, cudaStream_t stream);
 
 }  // namespace ec

@@ -192,9 +192,11 @@ ec_status ec_build_recompute_set(const uint8_t *is_masked, const int32_t *decode
 /* (b) selective-recompute attention                                          */
 /* ------------------------------------------------------------------------- */
 
-/* Bytes of device workspace ec_selective_attention needs. */
+/* Bytes of device workspace ec_selective_attention needs on the current device
+ * (the split of the keys across CTAs, hence the partial-result storage, depends
+ * on its SM count). */
 size_t ec_attention_workspace_size(int32_t batch, int32_t seq_len, int32_t r_max,
-                                   int32_t n_heads, int32_t head_dim);
+                                   int32_t n_heads, int32_t n_kv_heads, int32_t head_dim);
 
 /*
  * Write the freshly projected K/V rows into the caches and run bidirectional

@@ -43,7 +43,7 @@ def test_workspace_sizes(L):
     small = L.ec_decode_workspace_size(32, 1)
     big = L.ec_decode_workspace_size(512, 8)
     assert small >= 256 and big > small and big % 16 == 0
-    assert L.ec_attention_workspace_size(8, 2048, 96, 28, 128) >= 256
+    assert L.ec_attention_workspace_size(8, 2048, 96, 28, 4, 128) >= 256
 
 
 def _decode(L, **over):

@@ -23,6 +23,7 @@ def run_case(orc, w, idx, cnt, r_max, std=None, n_samples=None, seed=0):
     q, kn, vn, kc, vc = (dev(x) for x in (a.q, a.k_new, a.v_new, a.k_cache, a.v_cache))
     out = torch.zeros_like(q)
     ws = nat.new_workspace(nat.ec_attention_workspace_size(w.batch, w.seq_len, r_max, w.n_heads,
+                                                           w.n_kv_heads,
                                                            w.head_dim))
     nat.ec_selective_attention(q, kn, vn, dev(idx), dev(cnt), kc, vc, out, scale, ws)
     assert nat.ec_read_device_status(ws) == 0

@@ -37,7 +37,7 @@ def test_prepared_calls_match_direct_calls():
         q, kn, vn, kc, vc = (dev(x) for x in (att.q, att.k_new, att.v_new, att.k_cache,
                                               att.v_cache))
         out = torch.zeros_like(q)
-        wsa = nat.new_workspace(nat.ec_attention_workspace_size(B, L, w.r_max, w.n_heads,
+        wsa = nat.new_workspace(nat.ec_attention_workspace_size(B, L, w.r_max, w.n_heads, w.n_kv_heads,
                                                                 w.head_dim))
         aargs = (q, kn, vn, idx, cnt, kc, vc, out, 1 / math.sqrt(w.head_dim), wsa)
         if prepared:
