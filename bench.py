@@ -567,10 +567,124 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# the multi-step trajectory workload
+
+
+def trajectory_bytes(w):
+    rows = synth.trajectory_rows_per_step(w)
+    return sum(rows) * w.vocab * 2
+
+
+def time_projection(nat, tr, rows, reps=20):
+    """Mean device time (s) of one full-shape Q/K/V projection launch, on the
+    trajectory's stream with its own buffers (the launch the forward makes)."""
+    import torch
+    calls = tr.forward_full if rows == tr.w.seq_len else tr.forward_sel
+    proj = calls[1]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(tr.stream):
+        proj()
+        e0.record()
+        for _ in range(reps):
+            proj()
+        e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / reps
+
+
+def run_trajectory(args):
+    import torch
+    rank, world, local = dist_setup(args)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from entropy_gated_kv_decode_b300 import _native as nat
+    from entropy_gated_kv_decode_b300.trajectory import Trajectory
+    nat.lib()
+    w = synth.WORKLOADS["trajectory"]
+    stream = torch.cuda.Stream(device)
+    torch.cuda.set_stream(stream)
+    tr = Trajectory(w, seed=args.seed, device=device, stream=stream)
+    tr.warm_up()
+    K, W = max(1, args.steps), max(3, args.warmup)
+    for _ in range(W):
+        tr.run()
+    sampler = ClockSampler(None)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    recs_all, walls = [], []
+    for _ in range(K):
+        t0 = time.perf_counter()
+        recs_all.append(tr.run())
+        walls.append(time.perf_counter() - t0)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    clocks = sampler.stop()
+    recs = recs_all[-1]
+    fwd = sum(r.forward_ms for rr in recs_all for r in rr) / 1e3
+    dec = sum(r.decode_ms for rr in recs_all for r in rr) / 1e3
+    device_s = fwd + dec
+    wall = sum(walls)
+    t_max = reduce_max(wall, world)
+    n_steps = w.n_steps * K
+    full = [r for r in recs if r.full]
+    sel = [r for r in recs if not r.full]
+    t_proj_full = time_projection(nat, tr, w.seq_len)
+    t_proj_sel = time_projection(nat, tr, tr.r_sel)
+    peaks, peak_kind = load_peaks()
+    tc = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hid = w.n_heads * w.head_dim
+    flops_full = 2.0 * w.seq_len * hid * 3 * hid
+    proj_tflops = flops_full / t_proj_full / 1e12
+    wbytes = 3 * hid * hid * 2
+    value = aggregate(trajectory_bytes(w) * K, world, t_max) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": t_max / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "trajectory", "seq_len": w.seq_len, "vocab": w.vocab,
+                   "denoising_steps": w.n_steps, "layers": w.n_layers, "n_heads": w.n_heads,
+                   "head_dim": w.head_dim, "hidden": hid, "n_unmask": w.n_unmask, "k": w.k,
+                   "tau": w.tau, "step": "one whole 128-step trajectory",
+                   "l2": "inputs (3.2 GB of weights per step) exceed L2",
+                   "parallelism": f"replicas x{world}"},
+        "parts": {
+            "denoising_steps_per_s": n_steps / wall,
+            "refresh_fraction": sum(r.refresh for r in recs) / len(recs),
+            "full_forward_steps": len(full), "partial_forward_steps": len(sel),
+            "mean_rows": float(np.mean([r.rows for r in recs])),
+            "full_forward_ms": float(np.mean([r.forward_ms for r in full])) if full else None,
+            "partial_forward_ms": float(np.mean([r.forward_ms for r in sel])) if sel else None,
+            "decode_and_sets_ms": float(np.mean([r.decode_ms for r in recs])),
+            "gate_share_of_device_time": dec / device_s,
+            "host_overhead_share": max(0.0, 1 - device_s / wall),
+            "projection_full_us": t_proj_full * 1e6, "projection_full_tflops": proj_tflops,
+            "projection_partial_us": t_proj_sel * 1e6,
+            "projection_partial_weight_gbs": wbytes / t_proj_sel / 1e9,
+        },
+        "roofline": {"bound": "tensor", "achieved": proj_tflops, "peak": tc, "unit": "TFLOP/s",
+                     "frac": proj_tflops / tc, "traffic": None,
+                     "kernel": "qkv_gemm_kernel (full-refresh shape 1024 x 12288 x 4096)",
+                     "peak_source": f"{peak_kind} sustained (MEASURED_PEAKS.json)"},
+        "clocks": clocks,
+        "gpu_launches": sum(1 + 2 * w.n_layers + 3 for _ in recs) * K,
+        "e2e": None, "cpu_baseline": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "trajectory":
+        run_trajectory(args)
     else:
         run_ours(args)
 

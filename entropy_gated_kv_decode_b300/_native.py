@@ -27,7 +27,8 @@ DEV_TIMEOUT = 0x10
 
 EXPORTED = ("ec_status_str", "ec_abi_version", "ec_workspace_init", "ec_read_device_status",
             "ec_decode_workspace_size", "ec_decode_step", "ec_decode_step_noalloc",
-            "ec_build_recompute_set", "ec_attention_workspace_size", "ec_selective_attention")
+            "ec_build_recompute_set", "ec_attention_workspace_size", "ec_selective_attention",
+            "ec_embed_rows", "ec_qkv_projection")
 
 
 class NativeLibraryMissing(RuntimeError):
@@ -69,8 +70,12 @@ def lib() -> ctypes.CDLL:
         L.ec_attention_workspace_size.restype = sz
         L.ec_selective_attention.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, ctypes.c_int,
                                              i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
+        L.ec_embed_rows.argtypes = [vp, i64, i32, vp, i64, vp, vp, vp, i32, i32, i32, i32, vp, vp,
+                                    sz, vp]
+        L.ec_qkv_projection.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, sz, vp]
         for name in ("ec_workspace_init", "ec_read_device_status", "ec_decode_step",
-                     "ec_decode_step_noalloc", "ec_build_recompute_set", "ec_selective_attention"):
+                     "ec_decode_step_noalloc", "ec_build_recompute_set", "ec_selective_attention",
+                     "ec_embed_rows", "ec_qkv_projection"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -254,6 +259,57 @@ def ec_selective_attention(q, k_new, v_new, idx, count, k_cache, v_cache, out, s
     _check(lib().ec_selective_attention(*args, _stream(stream)), "ec_selective_attention")
 
 
+def _embed_args(table, idx, count, seq_tokens, is_masked, mask_id, x, workspace):
+    _cuda("table", table, torch.bfloat16)
+    _cuda("idx", idx, torch.int32)
+    _cuda("count", count, torch.int32)
+    _cuda("seq_tokens", seq_tokens, torch.int32)
+    _cuda("is_masked", is_masked, torch.uint8)
+    _cuda("x", x, torch.bfloat16)
+    _cuda("workspace", workspace, torch.uint8)
+    batch, seq_len = seq_tokens.shape
+    r_max, hidden = x.shape[-2], x.shape[-1]
+    if (table.dim() != 2 or table.shape[1] != hidden or x.numel() != batch * r_max * hidden
+            or idx.dim() != 2 or idx.shape[0] != batch or count.numel() != batch
+            or is_masked.shape != seq_tokens.shape):
+        raise ValueError("inconsistent embedding shapes")
+    return [_p(table), table.shape[0], hidden, _p(idx), idx.shape[1], _p(count), _p(seq_tokens),
+            _p(is_masked), int(mask_id), batch, seq_len, r_max, _p(x), _p(workspace),
+            workspace.numel()]
+
+
+def ec_embed_rows(table, idx, count, seq_tokens, is_masked, mask_id, x, workspace, stream=None):
+    """x [B, r_max, hidden] <- table rows of the tokens at idx (mask_id while masked)."""
+    args = _embed_args(table, idx, count, seq_tokens, is_masked, mask_id, x, workspace)
+    _check(lib().ec_embed_rows(*args, _stream(stream)), "ec_embed_rows")
+
+
+def _projection_args(x, count, w_qkv, q, k, v, workspace):
+    for name, t in (("x", x), ("w_qkv", w_qkv), ("q", q), ("k", k), ("v", v)):
+        _cuda(name, t, torch.bfloat16)
+    _cuda("workspace", workspace, torch.uint8)
+    if count is not None:
+        _cuda("count", count, torch.int32)
+    if x.dim() != 3:
+        raise ValueError("x must be [batch, r_max, hidden]")
+    batch, r_max, hidden = x.shape
+    if w_qkv.dim() != 2 or w_qkv.shape[1] != hidden or w_qkv.shape[0] % 3:
+        raise ValueError("w_qkv must be [3 * width, hidden]")
+    width = w_qkv.shape[0] // 3
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _numel(t, batch * r_max * width, name)
+    if count is not None:
+        _numel(count, batch, "count")
+    return [_p(x), _p(count), batch, r_max, hidden, _p(w_qkv), width, _p(q), _p(k), _p(v),
+            _p(workspace), workspace.numel()]
+
+
+def ec_qkv_projection(x, count, w_qkv, q, k, v, workspace, stream=None):
+    """q/k/v [B, r_max, width] <- x [B, r_max, hidden] @ w_qkv[3 width, hidden]^T, rows < count."""
+    args = _projection_args(x, count, w_qkv, q, k, v, workspace)
+    _check(lib().ec_qkv_projection(*args, _stream(stream)), "ec_qkv_projection")
+
+
 # ---------------------------------------------------------------------------
 # Prepared calls: validate and marshal once, then invoke with almost no host
 # cost.  The tensors bound at preparation must stay alive and in place.
@@ -293,3 +349,11 @@ def prepare_build_recompute_set(*args, stream=None, **kwargs):
 
 def prepare_selective_attention(*args, stream=None, **kwargs):
     return Prepared("ec_selective_attention", _attention_args(*args, **kwargs), stream)
+
+
+def prepare_embed_rows(*args, stream=None, **kwargs):
+    return Prepared("ec_embed_rows", _embed_args(*args, **kwargs), stream)
+
+
+def prepare_qkv_projection(*args, stream=None, **kwargs):
+    return Prepared("ec_qkv_projection", _projection_args(*args, **kwargs), stream)

@@ -47,7 +47,6 @@ constexpr int kBlockM = 128;   // query rows per unit = TMEM lanes
 constexpr int kBlockN = 128;   // keys per tile
 constexpr int kThreads = 224;  // 7 warps
 constexpr int kMaxSplit = 32;
-constexpr long long kWaitCycles = 4000000000LL;  // ~2 s: a wait this long is a fault
 
 template <int D>
 struct Cfg {
@@ -128,38 +127,6 @@ __device__ __forceinline__ bool item_active(const Params &P, const Item &it)
 {
     return it.mt * P.tok_per_tile < it.cnt && it.t1 > it.t0;
 }
-
-struct Sync {
-    uint32_t bars;
-    volatile int *abort_flag;
-    uint32_t *status;
-    __device__ uint32_t bar(int i) const { return bars + 8u * static_cast<uint32_t>(i); }
-    // Bounded wait: gives up (and raises the abort flag) after ~2 s.
-    __device__ bool wait(int i, uint32_t parity) const
-    {
-        const uint32_t b = bar(i);
-        if (mbar_try_wait(b, parity)) return true;
-        const long long t0 = clock64();
-        for (uint32_t it = 1;; ++it) {
-            if (mbar_try_wait(b, parity)) return true;
-            if ((it & 127u) == 0u) {
-                if (*abort_flag) return false;
-                if (clock64() - t0 > kWaitCycles) {
-                    *abort_flag = 1;
-                    flag_status(status, EC_DEV_TIMEOUT);
-                    return false;
-                }
-            }
-        }
-    }
-    __device__ bool drain(int i, uint32_t parity) const
-    {
-        const long long t0 = clock64();
-        while (!mbar_try_wait(bar(i), parity))
-            if (clock64() - t0 > kWaitCycles / 4) return false;
-        return true;
-    }
-};
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p)
 {

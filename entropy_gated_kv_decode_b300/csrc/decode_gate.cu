@@ -5,36 +5,62 @@
 // Arabic technical summary, "Algorithm workflow" phases 2-3 with the equation
 // E_{t+1} = max_{i in D_{t+1}} ( -sum_j p_ij log p_ij ).
 //
-// Phase 1 (every CTA): stream one slice of one logits row once from HBM with
-// 16-byte non-allocating loads and fold it into an online softmax state
+// One pass over the logits folds every row into an online softmax state
 //     m = max x,   a = first index of m,
 //     S = sum 2^{y},  T = sum 2^{y} y,   y = (x - m) log2(e)
 // so that for the whole row  H = ln S - ln2 * T / S  and  conf = p_a = 2^{y_a} / S.
-// The state merges associatively (rescaling by 2^{(m' - m) log2 e}), so a row
-// can be split across CTAs; warps merge with shuffles, the CTA through smem.
-// Phase 2 (the last CTA of a row to finish, found with an atomic ticket — no
-// CTA ever waits on another): merge the row's slices in a fixed order and write
-// token / conf / entropy.
-// Phase 3 (the last row of a sequence to finish): rank the sequence's rows by
-// (confidence desc, position asc), take the first n_unmask, write them in rank
-// order, E = max entropy over them, refresh = E > tau, and update the
-// is_masked / token / decode-step state at their positions.
+// The state merges associatively (rescaling by 2^{(m' - m) log2 e}).
+//
+// Work split: the rows' 16-byte vectors (plus, per row, one "tail" unit holding
+// the vocab % 8 (bf16) or % 4 (fp32) last elements) are laid end to end and cut
+// into one contiguous, equal range per CTA of a persistent grid, so every CTA
+// streams the same number of bytes whatever the row count.  A range covers
+// pieces of one or more rows.
+//   producer warp   one thread streams the range's bytes into a ring of
+//                   shared-memory stages with bulk asynchronous copies (TMA,
+//                   evict-first in L2), completing on mbarriers;
+//   8 consumer warps fold each stage from shared memory, one 16-byte vector per
+//                   thread at a time, and reduce a row piece to one partial
+//                   state (warp shuffles, then shared memory);
+//   row merge       each partial goes to the workspace slot (row, CTA); the last
+//                   CTA of a row to finish (an atomic ticket — no CTA waits on
+//                   another) merges the row's partials in slot order and writes
+//                   token / conf / entropy;
+//   sequence        the last row of a sequence to finish ranks the sequence's
+//                   rows by (confidence desc, position asc), takes the first
+//                   n_unmask, writes them in rank order, E = max entropy over
+//                   them, refresh = E > tau, and updates the is_masked / token /
+//                   decode-step state at their positions.
+// Every wait is bounded (~2 s); a timeout sets EC_DEV_TIMEOUT and unwinds.
 #include <float.h>
 #include <limits.h>
 #include <math.h>
 
+#include <algorithm>
+
 #include "ec_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace ec {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 4;          // 16-byte vectors per thread per batch of loads
-constexpr int kCtasPerSm = 4;       // resident CTAs per SM the grid is sized for
-constexpr int kMaxSplits = 64;      // CTAs per row at most
-constexpr int kMaxStagedRows = 2048;  // selection keys kept in smem up to this many rows
+using ptx::Sync;
+
+constexpr int kConsumers = 256;              // 8 folding warps
+constexpr int kConsumerWarps = kConsumers / 32;
+constexpr int kThreads = kConsumers + 32;    // + 1 producer warp
+constexpr int kCtasPerSm = 2;
+constexpr uint32_t kChunk = 16384;           // bytes per ring stage
+constexpr int kStages = 6;
+constexpr int kVecPerChunk = kChunk / 16;
+constexpr int kVecPerThread = kVecPerChunk / kConsumers;  // 4
+constexpr int kMaxSplits = 64;               // partial slots per row
+constexpr int kMaxStagedRows = 1024;         // selection keys kept in smem up to this many rows
 constexpr int kMaxUnmask = 1024;
+constexpr uint32_t kSmemDyn = kStages * kChunk + 1024 + 128;  // ring + align slack + barriers
+constexpr int kBarConsumers = 1;             // named barrier id of the consumer warps
+
+enum : int { D_FULL = 0, D_EMPTY = kStages, D_COUNT = 2 * kStages };
 
 struct __align__(16) Partial {
     float m;  // running maximum logit
@@ -129,53 +155,78 @@ struct Elem<uint16_t> {
     }
 };
 
-// Fold elements x[0..N) into (m, s0/s1, t0/t1, a); index_of(i) is the row index
-// of x[i] (increasing in i), evaluated only when the maximum moves.
-template <int N, typename IndexOf>
-__device__ __forceinline__ void fold(const float (&x)[N], IndexOf index_of, float &m, float &s0,
-                                     float &s1, float &t0, float &t1, int &a)
-{
-    float cm = x[0];
-#pragma unroll
-    for (int i = 1; i < N; ++i) cm = fmaxf(cm, x[i]);
-    if (cm > m) {  // rare after the first batch: new maximum, rescale the sums
-        int first = INT_MAX;
-#pragma unroll
-        for (int i = N - 1; i >= 0; --i)
-            if (x[i] == cm) first = index_of(i);
-        const float s = s0 + s1;
-        if (s > 0.f) {
-            const float d = m * kLog2e - cm * kLog2e;
-            const float f = ex2(d);
-            const float t = t0 + t1;
-            t0 = f * fmaf(d, s, t);
-            t1 = 0.f;
-            s0 = f * s;
-            s1 = 0.f;
-        }
-        m = cm;
-        a = first;
+// Running fold state of one thread.
+struct Fold {
+    float m, s0, s1, t0, t1;
+    int a;
+    __device__ void reset()
+    {
+        m = -INFINITY;
+        s0 = s1 = t0 = t1 = 0.f;
+        a = INT_MAX;
     }
-    const float mb = m * kLog2e;
+    // Fold elements x[0..N) with row indices index_of(i) (increasing in i;
+    // evaluated only when the maximum moves).  Elements equal to -inf get weight 0.
+    template <int N, typename IndexOf>
+    __device__ __forceinline__ void add(const float (&x)[N], IndexOf index_of)
+    {
+        float cm = x[0];
 #pragma unroll
-    for (int i = 0; i < N; i += 2) {
-        const float y0 = fmaxf(fmaf(x[i], kLog2e, -mb), -1e30f);  // -inf logits -> weight 0
-        const float e0 = ex2(y0);
-        s0 += e0;
-        t0 = fmaf(e0, y0, t0);
-        if (i + 1 < N) {
-            const float y1 = fmaxf(fmaf(x[i + 1], kLog2e, -mb), -1e30f);
-            const float e1 = ex2(y1);
-            s1 += e1;
-            t1 = fmaf(e1, y1, t1);
+        for (int i = 1; i < N; ++i) cm = fmaxf(cm, x[i]);
+        if (cm > m) {  // rare after the first elements: new maximum, rescale the sums
+            int first = INT_MAX;
+#pragma unroll
+            for (int i = N - 1; i >= 0; --i)
+                if (x[i] == cm) first = index_of(i);
+            const float s = s0 + s1;
+            if (s > 0.f) {
+                const float d = m * kLog2e - cm * kLog2e;
+                const float f = ex2(d);
+                const float t = t0 + t1;
+                t0 = f * fmaf(d, s, t);
+                t1 = 0.f;
+                s0 = f * s;
+                s1 = 0.f;
+            }
+            m = cm;
+            a = first;
+        }
+        const float mb = m * kLog2e;
+#pragma unroll
+        for (int i = 0; i < N; i += 2) {
+            const float y0 = fmaxf(fmaf(x[i], kLog2e, -mb), -1e30f);
+            const float e0 = ex2(y0);
+            s0 += e0;
+            t0 = fmaf(e0, y0, t0);
+            if (i + 1 < N) {
+                const float y1 = fmaxf(fmaf(x[i + 1], kLog2e, -mb), -1e30f);
+                const float e1 = ex2(y1);
+                s1 += e1;
+                t1 = fmaf(e1, y1, t1);
+            }
         }
     }
-}
+    __device__ Partial partial() const
+    {
+        Partial p;
+        p.m = m;
+        p.s = s0 + s1;
+        p.t = t0 + t1;
+        p.idx = a;
+        if (p.s == 0.f) p = empty_partial();
+        return p;
+    }
+};
 
 struct Args {
     const void *logits;
-    int64_t row_stride;
-    int n_rows, vocab, splits;
+    int64_t row_stride;  // elements
+    int n_rows, vocab;
+    int64_t nvec;        // whole 16-byte vectors per row
+    int tail;            // elements after them
+    int64_t units;       // per row: nvec + (tail > 0)
+    int64_t total;       // n_rows * units
+    int grid;
     const int32_t *offsets, *row_pos;
     int batch, seq_len, n_unmask;
     float tau;
@@ -191,6 +242,16 @@ struct Args {
     Partial *parts;
 };
 
+// First unit of CTA c's range, and the CTA whose range holds unit u.
+__device__ __forceinline__ int64_t range_begin(const Args &A, int c)
+{
+    return static_cast<int64_t>(c) * A.total / A.grid;
+}
+__device__ __forceinline__ int cta_of(const Args &A, int64_t u)
+{
+    return static_cast<int>(((u + 1) * A.grid - 1) / A.total);
+}
+
 __device__ __forceinline__ unsigned long long select_key(float conf, int pos)
 {
     // larger key = higher confidence, then lower position (conf > 0, so its bits order)
@@ -198,19 +259,40 @@ __device__ __forceinline__ unsigned long long select_key(float conf, int pos)
            static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(pos));
 }
 
-// Phase 3 for sequence b (whole CTA).
+__device__ __forceinline__ void consumers_sync() { ptx::named_bar_sync(kBarConsumers, kConsumers); }
+
+// The sequence holding row i (rows of a sequence are contiguous), or -1 when the
+// offsets do not place it in a well-formed range.
+__device__ int sequence_of(const Args &A, int i, int &lo, int &cnt)
+{
+    int a = 0, z = A.batch;  // find the last b with offsets[b] <= i
+    while (z - a > 1) {
+        const int mid = (a + z) >> 1;
+        if (__ldg(A.offsets + mid) <= i)
+            a = mid;
+        else
+            z = mid;
+    }
+    const int o0 = __ldg(A.offsets + a), o1 = __ldg(A.offsets + a + 1);
+    if (o0 < 0 || o1 > A.n_rows || o0 > i || i >= o1) return -1;
+    lo = o0;
+    cnt = o1 - o0;
+    return a;
+}
+
+// Rank, gate and state update for sequence b (consumer threads).
 __device__ void finish_sequence(const Args &A, int b, int r0, int cnt)
 {
     __shared__ unsigned long long s_key[kMaxStagedRows];
     __shared__ int s_sel[kMaxUnmask];
     __shared__ int s_nsel;
-    __shared__ float s_wmax[kWarps];
+    __shared__ float s_wmax[kConsumerWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const bool staged = cnt <= kMaxStagedRows;
     if (staged)
-        for (int i = tid; i < cnt; i += kThreads)
+        for (int i = tid; i < cnt; i += kConsumers)
             s_key[i] = select_key(__ldcg(A.conf_out + r0 + i), __ldg(A.row_pos + r0 + i));
-    __syncthreads();
+    consumers_sync();
 
     const int take = min(A.n_unmask, cnt);
     if (warp == 0) {
@@ -244,11 +326,11 @@ __device__ void finish_sequence(const Args &A, int b, int r0, int cnt)
         }
         if (lane == 0) s_nsel = nsel;
     }
-    __syncthreads();
+    consumers_sync();
 
     const int nsel = s_nsel;
     float h = -INFINITY;
-    for (int s = tid; s < A.n_unmask; s += kThreads) {
+    for (int s = tid; s < A.n_unmask; s += kConsumers) {
         int32_t *slot = A.unmask_rows + static_cast<int64_t>(b) * A.n_unmask + s;
         if (s < nsel) {
             const int r = r0 + s_sel[s];
@@ -269,26 +351,121 @@ __device__ void finish_sequence(const Args &A, int b, int r0, int cnt)
 #pragma unroll
     for (int off = 16; off; off >>= 1) h = fmaxf(h, __shfl_xor_sync(0xffffffffu, h, off));
     if (lane == 0) s_wmax[warp] = h;
-    __syncthreads();
+    consumers_sync();
     if (tid == 0) {
         float e = s_wmax[0];
-        for (int w = 1; w < kWarps; ++w) e = fmaxf(e, s_wmax[w]);
+        for (int w = 1; w < kConsumerWarps; ++w) e = fmaxf(e, s_wmax[w]);
         A.max_entropy[b] = e;
         A.refresh[b] = e > A.tau ? 1 : 0;
     }
+    consumers_sync();  // s_key / s_sel / s_wmax may be reused by a later call
+}
+
+// A finished piece of row i: publish its partial; the row's last contributor
+// merges all of them, and the sequence's last row ranks and gates.  Returns true
+// (in every consumer thread alike) when some consumer warp gave up a wait.
+__device__ bool finish_piece(const Args &A, int i, Partial p, bool failed)
+{
+    __shared__ Partial s_part[kConsumerWarps];
+    __shared__ int s_flag, s_seq, s_lo, s_cnt;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (ptx::named_bar_or(kBarConsumers, kConsumers, failed)) return true;
+    warp_merge(p);
+    if (lane == 0) s_part[warp] = p;
+    consumers_sync();
+    const int c0 = cta_of(A, static_cast<int64_t>(i) * A.units);
+    const int c1 = cta_of(A, static_cast<int64_t>(i) * A.units + A.units - 1);
+    const int n_contrib = c1 - c0 + 1;
+    if (warp == 0) {
+        p = lane < kConsumerWarps ? s_part[lane] : empty_partial();
+        warp_merge(p);
+        if (lane == 0) {
+            int last = 1;
+            if (n_contrib > 1) {
+                const int slot = static_cast<int>(blockIdx.x) - c0;
+                __stcg(reinterpret_cast<float4 *>(A.parts + static_cast<int64_t>(i) * kMaxSplits + slot),
+                       make_float4(p.m, p.s, p.t, __int_as_float(p.idx)));
+                __threadfence();
+                const unsigned ticket = atomicInc(A.row_ctr + i, static_cast<unsigned>(n_contrib - 1));
+                last = ticket == static_cast<unsigned>(n_contrib - 1);
+            }
+            s_flag = last;
+        }
+        __syncwarp();
+        // the last contributor merges every slot in order
+        if (n_contrib > 1 && s_flag) {
+            __threadfence();
+            p = empty_partial();
+            for (int k = lane; k < n_contrib; k += 32) {
+                const float4 q4 = __ldcg(
+                    reinterpret_cast<const float4 *>(A.parts + static_cast<int64_t>(i) * kMaxSplits + k));
+                Partial q;
+                q.m = q4.x;
+                q.s = q4.y;
+                q.t = q4.z;
+                q.idx = __float_as_int(q4.w);
+                merge(p, q);
+            }
+            warp_merge(p);
+        }
+        if (lane == 0 && s_flag) {
+            // Sums are relative to mb = fl(m log2 e); for any reference point
+            // H = ln S - ln2 * T / S, and the argmax's own term is 2^{m log2 e - mb}.
+            const float S = p.s;
+            const float H = logf(S) - kLn2 * (p.t / S);
+            const float top = ex2(fmaf(p.m, kLog2e, -(p.m * kLog2e)));
+            A.entropy_out[i] = fmaxf(H, 0.f);
+            A.conf_out[i] = top / S;
+            A.token_out[i] = p.idx;
+            const int pos = __ldg(A.row_pos + i);
+            if (pos < 0 || pos >= A.seq_len) flag_status(A.status, EC_DEV_BAD_ROW_POS);
+            int lo = 0, cnt = 0, last_row = 0;
+            const int b = sequence_of(A, i, lo, cnt);
+            if (b < 0) {
+                flag_status(A.status, EC_DEV_BAD_OFFSETS);
+            } else {
+                __threadfence();
+                const unsigned ticket = atomicInc(A.seq_ctr + b, static_cast<unsigned>(cnt - 1));
+                last_row = ticket == static_cast<unsigned>(cnt - 1);
+            }
+            s_seq = last_row ? b : -1;
+            s_lo = lo;
+            s_cnt = cnt;
+        }
+    }
+    consumers_sync();
+    const int b = s_flag ? s_seq : -1;
+    if (b >= 0) {
+        __threadfence();
+        finish_sequence(A, b, s_lo, s_cnt);
+    }
+    consumers_sync();
+    return false;
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const Args A)
 {
     constexpr int E = Elem<T>::kPerVec;
-    __shared__ Partial s_part[kWarps];
-    __shared__ int s_seq, s_seq_lo, s_seq_cnt, s_row_last, s_seq_last;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t ring_u32 = ptx::smem_u32(ring);
+    __shared__ int s_abort;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    Sync S{ring_u32 + kStages * kChunk, reinterpret_cast<volatile int *>(&s_abort), A.status};
+
+    if (tid == 0) {
+        s_abort = 0;
+        for (int i = 0; i < D_COUNT; ++i)
+            ptx::mbar_init(S.bar(i), i >= D_EMPTY ? static_cast<uint32_t>(kConsumerWarps) : 1u);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
 
     // CTA 0 checks the offsets and finishes sequences that have no rows.
-    if (blockIdx.x == 0) {
-        for (int b = tid; b <= A.batch; b += kThreads) {
+    if (blockIdx.x == 0 && warp < kConsumerWarps) {
+        for (int b = tid; b <= A.batch; b += kConsumers) {
             const int o = __ldg(A.offsets + b);
             bool bad = (b == 0 && o != 0) || (b == A.batch && o != A.n_rows);
             if (b < A.batch) {
@@ -304,127 +481,81 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
             if (bad) flag_status(A.status, EC_DEV_BAD_OFFSETS);
         }
     }
-    if (A.n_rows == 0) return;
+    if (A.total == 0) return;
 
-    const int row = blockIdx.x / A.splits;
-    const int split = blockIdx.x - row * A.splits;
+    const int64_t u_begin = range_begin(A, blockIdx.x);
+    const int64_t u_end = range_begin(A, blockIdx.x + 1);
+    if (u_begin >= u_end) return;
+    const int row_first = static_cast<int>(u_begin / A.units);
+    const int row_last = static_cast<int>((u_end - 1) / A.units);
 
-    // Which sequence owns this row (rows of a sequence are contiguous).
-    if (tid == 0) s_seq = -1;
-    __syncthreads();
-    for (int b = tid; b < A.batch; b += kThreads) {
-        const int o0 = __ldg(A.offsets + b), o1 = __ldg(A.offsets + b + 1);
-        // only a well-formed range is trusted (keeps phase 3 inside [0, n_rows))
-        if (o0 >= 0 && o1 <= A.n_rows && o0 <= row && row < o1) {
-            atomicMax(&s_seq, b);
-            s_seq_lo = o0;  // benign: only one b matches valid offsets
-            s_seq_cnt = o1 - o0;
-        }
-    }
-
-    // ---- phase 1: stream this CTA's slice of the row ----
-    const T *row_ptr = static_cast<const T *>(A.logits) + static_cast<int64_t>(row) * A.row_stride;
-    const int64_t nvec = A.vocab / E;
-    const int64_t per = (nvec + A.splits - 1) / A.splits;
-    const int64_t v0 = min(nvec, static_cast<int64_t>(split) * per);
-    const int64_t v1 = min(nvec, v0 + per);
-    const uint4 *vp = reinterpret_cast<const uint4 *>(row_ptr);
-
-    float m = -INFINITY, s0 = 0.f, s1 = 0.f, t0 = 0.f, t1 = 0.f;
-    int a = INT_MAX;
-    for (int64_t base = v0 + tid; base < v1; base += kThreads * kUnroll) {
-        uint4 raw[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t v = base + static_cast<int64_t>(u) * kThreads;
-            const uint32_t w = Elem<T>::kNegInfWord;
-            raw[u] = v < v1 ? ld_stream_v4(vp + v) : make_uint4(w, w, w, w);
-        }
-        float x[kUnroll * E];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) Elem<T>::unpack(raw[u], x + u * E);
-        const int vb = static_cast<int>(base);
-        fold(x, [vb](int i) { return (vb + (i / E) * kThreads) * E + (i % E); }, m, s0, s1, t0, t1, a);
-    }
-    // ragged tail (vocab % E elements) belongs to the last slice
-    if (split == A.splits - 1) {
-        const int tail0 = static_cast<int>(nvec * E);
-        const int j = tail0 + tid;
-        if (j < A.vocab) {
-            float x[1] = {Elem<T>::scalar(row_ptr + j)};
-            fold(x, [j](int) { return j; }, m, s0, s1, t0, t1, a);
-        }
-    }
-
-    Partial p;
-    p.m = m;
-    p.s = s0 + s1;
-    p.t = t0 + t1;
-    p.idx = a;
-    if (p.s == 0.f) p = empty_partial();
-    warp_merge(p);
-    if (lane == 0) s_part[warp] = p;
-    __syncthreads();
-    if (warp == 0) {
-        p = lane < kWarps ? s_part[lane] : empty_partial();
-        warp_merge(p);
-    }
-
-    // ---- phase 2: the last slice of the row to finish merges the slices ----
-    if (A.splits > 1) {
-        if (tid == 0) {
-            __stcg(reinterpret_cast<float4 *>(A.parts + static_cast<int64_t>(row) * kMaxSplits + split),
-                   make_float4(p.m, p.s, p.t, __int_as_float(p.idx)));
-            __threadfence();
-            const unsigned ticket = atomicInc(A.row_ctr + row, static_cast<unsigned>(A.splits - 1));
-            s_row_last = ticket == static_cast<unsigned>(A.splits - 1);
-        }
-        __syncthreads();
-        if (!s_row_last) return;
-        __threadfence();
-        if (warp == 0) {
-            p = empty_partial();
-            for (int i = lane; i < A.splits; i += 32) {
-                const float4 q4 =
-                    __ldcg(reinterpret_cast<const float4 *>(A.parts + static_cast<int64_t>(row) * kMaxSplits + i));
-                Partial q;
-                q.m = q4.x;
-                q.s = q4.y;
-                q.t = q4.z;
-                q.idx = __float_as_int(q4.w);
-                merge(p, q);
+    if (warp == kConsumerWarps) {
+        // ---- producer: one thread streams the vector part of every row piece ----
+        if ((tid & 31) == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int i = row_first; i <= row_last && ok; ++i) {
+                const int64_t base = static_cast<int64_t>(i) * A.units;
+                const int64_t va = max(u_begin, base) - base;
+                const int64_t vb = min(min(u_end, base + A.units) - base, A.nvec);
+                const char *row =
+                    static_cast<const char *>(A.logits) + static_cast<int64_t>(i) * A.row_stride * sizeof(T);
+                for (int64_t v = va; v < vb && ok; v += kVecPerChunk, ++it) {
+                    const int s = it % kStages;
+                    if (it >= static_cast<uint32_t>(kStages)) ok = S.wait(D_EMPTY + s, ((it / kStages) - 1) & 1);
+                    if (!ok) break;
+                    const uint32_t bytes = static_cast<uint32_t>(std::min<int64_t>(kVecPerChunk, vb - v) * 16);
+                    ptx::mbar_expect_tx(S.bar(D_FULL + s), bytes);
+                    ptx::bulk_load_stream(ring_u32 + s * kChunk, row + v * 16, bytes, S.bar(D_FULL + s));
+                }
             }
-            warp_merge(p);
+            if (!ok)  // let every copy already started land before the CTA exits
+                for (uint32_t u = (it > kStages ? it - kStages : 0); u < it; ++u)
+                    S.drain(D_FULL + u % kStages, (u / kStages) & 1);
         }
+        return;
     }
 
-    if (tid == 0) {
-        // Sums are relative to mb = fl(m log2 e); for any reference point
-        // H = ln S - ln2 * T / S, and the argmax's own term is 2^{m log2 e - mb}.
-        const float S = p.s;
-        const float H = logf(S) - kLn2 * (p.t / S);
-        const float top = ex2(fmaf(p.m, kLog2e, -(p.m * kLog2e)));
-        A.entropy_out[row] = fmaxf(H, 0.f);
-        A.conf_out[row] = top / S;
-        A.token_out[row] = p.idx;
-        const int pos = __ldg(A.row_pos + row);
-        if (pos < 0 || pos >= A.seq_len) flag_status(A.status, EC_DEV_BAD_ROW_POS);
-        // ---- phase 3 ticket: is this the last row of its sequence? ----
-        int last = 0;
-        const int b = s_seq;
-        if (b < 0) {
-            flag_status(A.status, EC_DEV_BAD_OFFSETS);
-        } else {
-            __threadfence();
-            const unsigned ticket = atomicInc(A.seq_ctr + b, static_cast<unsigned>(s_seq_cnt - 1));
-            last = ticket == static_cast<unsigned>(s_seq_cnt - 1);
+    // ---- consumers ----
+    uint32_t it = 0;
+    bool failed = false;  // warp-uniform: a wait of this warp gave up
+    for (int i = row_first; i <= row_last; ++i) {
+        const int64_t base = static_cast<int64_t>(i) * A.units;
+        const int64_t ua = max(u_begin, base) - base;
+        const int64_t ub = min(u_end, base + A.units) - base;
+        const int64_t vb = min(ub, A.nvec);
+        Fold f;
+        f.reset();
+        for (int64_t v = ua; v < vb && !failed; v += kVecPerChunk, ++it) {
+            const int s = it % kStages;
+            failed = !__all_sync(0xffffffffu, S.wait(D_FULL + s, (it / kStages) & 1));
+            if (failed) break;
+            const int nv = static_cast<int>(std::min<int64_t>(kVecPerChunk, vb - v));
+            const uint4 *src = reinterpret_cast<const uint4 *>(ring + s * kChunk);
+            uint4 raw[kVecPerThread];
+#pragma unroll
+            for (int u = 0; u < kVecPerThread; ++u) {
+                const int j = tid + u * kConsumers;
+                const uint32_t ni = Elem<T>::kNegInfWord;
+                raw[u] = j < nv ? src[j] : make_uint4(ni, ni, ni, ni);
+            }
+            __syncwarp();
+            if ((tid & 31) == 0) ptx::mbar_arrive(S.bar(D_EMPTY + s));
+            float x[kVecPerThread * E];
+#pragma unroll
+            for (int u = 0; u < kVecPerThread; ++u) Elem<T>::unpack(raw[u], x + u * E);
+            const int vb0 = static_cast<int>(v) + tid;
+            f.add(x, [vb0](int k) { return (vb0 + (k / E) * kConsumers) * E + (k % E); });
         }
-        s_seq_last = last;
+        // the tail unit (vocab % E last elements) belongs to the range holding it
+        if (A.tail > 0 && ub == A.units && tid < A.tail) {
+            const int j = static_cast<int>(A.nvec * E) + tid;
+            const T *row = static_cast<const T *>(A.logits) + static_cast<int64_t>(i) * A.row_stride;
+            float x[1] = {Elem<T>::scalar(row + j)};
+            f.add(x, [j](int) { return j; });
+        }
+        if (finish_piece(A, i, f.partial(), failed)) break;  // aborted (same answer in every thread)
     }
-    __syncthreads();
-    if (!s_seq_last) return;
-    __threadfence();
-    finish_sequence(A, s_seq, s_seq_lo, s_seq_cnt);
 }
 
 }  // namespace
@@ -439,15 +570,16 @@ size_t decode_workspace_bytes(int32_t n_rows, int32_t batch)
     return off + rows * kMaxSplits * sizeof(Partial);
 }
 
-int decode_splits(int32_t n_rows, int32_t vocab, int elem_bytes)
+// CTAs of the persistent grid: kCtasPerSm per SM, fewer when there are fewer
+// units than that, and few enough that a row is split over at most
+// kMaxSplits - 2 ranges (its partial slots).
+int decode_grid(int32_t n_rows, int64_t units)
 {
     if (n_rows <= 0) return 1;
-    const int64_t nvec = vocab / (16 / elem_bytes);
-    const int slots = device_sm_count() * kCtasPerSm;
-    int64_t s = slots / n_rows;
-    s = std::min<int64_t>(s, nvec / (2 * kThreads));  // >= 2 vectors per thread per slice
-    s = std::max<int64_t>(1, std::min<int64_t>(s, kMaxSplits));
-    return static_cast<int>(s);
+    int64_t g = static_cast<int64_t>(device_sm_count()) * kCtasPerSm;
+    g = std::min<int64_t>(g, static_cast<int64_t>(n_rows) * (kMaxSplits - 2));
+    g = std::min<int64_t>(g, static_cast<int64_t>(n_rows) * units);
+    return static_cast<int>(std::max<int64_t>(1, g));
 }
 
 cudaError_t launch_decode_gate(const void *logits, int dtype, int64_t row_stride, int32_t n_rows,
@@ -460,12 +592,17 @@ cudaError_t launch_decode_gate(const void *logits, int dtype, int64_t row_stride
                                cudaStream_t stream)
 {
     const int elem = dtype == EC_BF16 ? 2 : 4;
+    const int per_vec = 16 / elem;
     Args A;
     A.logits = logits;
     A.row_stride = row_stride;
     A.n_rows = n_rows;
     A.vocab = vocab;
-    A.splits = decode_splits(n_rows, vocab, elem);
+    A.nvec = vocab / per_vec;
+    A.tail = vocab - static_cast<int>(A.nvec) * per_vec;
+    A.units = A.nvec + (A.tail > 0 ? 1 : 0);
+    A.total = static_cast<int64_t>(n_rows) * A.units;
+    A.grid = decode_grid(n_rows, A.units);
     A.offsets = seq_row_offsets;
     A.row_pos = row_pos;
     A.batch = batch;
@@ -491,11 +628,23 @@ cudaError_t launch_decode_gate(const void *logits, int dtype, int64_t row_stride
     off = align_up(off + static_cast<size_t>(batch) * sizeof(unsigned), 256);
     A.parts = reinterpret_cast<Partial *>(ws + off);
 
-    const unsigned grid = n_rows > 0 ? static_cast<unsigned>(n_rows) * A.splits : 1u;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(decode_gate_kernel<uint16_t>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDyn);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_gate_kernel<float>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDyn);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = 1;
+    }
+    const unsigned grid = static_cast<unsigned>(A.grid);
     if (dtype == EC_BF16)
-        decode_gate_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(A);
+        decode_gate_kernel<uint16_t><<<grid, kThreads, kSmemDyn, stream>>>(A);
     else
-        decode_gate_kernel<float><<<grid, kThreads, 0, stream>>>(A);
+        decode_gate_kernel<float><<<grid, kThreads, kSmemDyn, stream>>>(A);
     return cudaGetLastError();
 }
 

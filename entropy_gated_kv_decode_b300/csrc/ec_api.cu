@@ -160,4 +160,41 @@ ec_status ec_selective_attention(const void *q, const void *k_new, const void *v
                                               scale, status, s));
 }
 
+ec_status ec_qkv_projection(const void *x, const int32_t *count, int32_t batch, int32_t r_max,
+                            int32_t hidden, const void *w_qkv, int32_t width, void *q, void *k,
+                            void *v, void *workspace, size_t workspace_bytes, ec_stream_t stream)
+{
+    if (batch < 1 || r_max < 0 || !ec::qkv_shape_ok(hidden, width)) return EC_ERR_SHAPE;
+    if (!workspace) return EC_ERR_NULL;
+    if (r_max > 0 && (!x || !w_qkv || !q || !k || !v)) return EC_ERR_NULL;
+    const void *ptrs[] = {x, w_qkv, q, k, v};
+    for (const void *p : ptrs)
+        if (p && !aligned(p, 16)) return EC_ERR_ALIGN;
+    if (!aligned(workspace, EC_WORKSPACE_ALIGN) || workspace_bytes < ec::kWsHeader)
+        return EC_ERR_WORKSPACE;
+    return launched(ec::launch_qkv_projection(x, count, batch, r_max, hidden, w_qkv, width, q, k,
+                                              v, static_cast<uint32_t *>(workspace),
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ec_status ec_embed_rows(const void *table, int64_t table_rows, int32_t hidden, const int32_t *idx,
+                        int64_t idx_stride, const int32_t *count, const int32_t *seq_tokens,
+                        const uint8_t *is_masked, int32_t mask_id, int32_t batch,
+                        int32_t seq_len, int32_t r_max, void *x, void *workspace,
+                        size_t workspace_bytes, ec_stream_t stream)
+{
+    if (batch < 1 || seq_len < 1 || r_max < 0 || table_rows < 1 || hidden < 8 || hidden % 8 ||
+        idx_stride < r_max || mask_id < 0 || mask_id >= table_rows)
+        return EC_ERR_SHAPE;
+    if (!count || !workspace) return EC_ERR_NULL;
+    if (r_max > 0 && (!table || !idx || !seq_tokens || !is_masked || !x)) return EC_ERR_NULL;
+    if ((table && !aligned(table, 16)) || (x && !aligned(x, 16))) return EC_ERR_ALIGN;
+    if (!aligned(workspace, EC_WORKSPACE_ALIGN) || workspace_bytes < ec::kWsHeader)
+        return EC_ERR_WORKSPACE;
+    return launched(ec::launch_embed_rows(table, table_rows, hidden, idx, idx_stride, count,
+                                          seq_tokens, is_masked, mask_id, batch, seq_len, r_max, x,
+                                          static_cast<uint32_t *>(workspace),
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

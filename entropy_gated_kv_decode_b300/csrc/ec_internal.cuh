@@ -46,7 +46,6 @@ int device_sm_count();  // SM count of the current device (cached per device)
 
 // decode_gate.cu
 size_t decode_workspace_bytes(int32_t n_rows, int32_t batch);
-int decode_splits(int32_t n_rows, int32_t vocab, int elem_bytes);
 cudaError_t launch_decode_gate(const void *logits, int dtype, int64_t row_stride, int32_t n_rows,
                                int32_t vocab, const int32_t *seq_row_offsets,
                                const int32_t *row_pos, int32_t batch, int32_t seq_len,
@@ -86,5 +85,16 @@ cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_
                                 int32_t seq_len, int32_t r_max, int32_t n_heads,
                                 int32_t n_kv_heads, int32_t head_dim, float scale,
                                 void *workspace, cudaStream_t stream);
+
+// qkv_gemm.cu
+bool qkv_shape_ok(int32_t hidden, int32_t width);
+cudaError_t launch_qkv_projection(const void *x, const int32_t *count, int32_t batch,
+                                  int32_t r_max, int32_t hidden, const void *w_qkv, int32_t width,
+                                  void *q, void *k, void *v, uint32_t *status, cudaStream_t stream);
+cudaError_t launch_embed_rows(const void *table, int64_t table_rows, int32_t hidden,
+                              const int32_t *idx, int64_t idx_stride, const int32_t *count,
+                              const int32_t *seq_tokens, const uint8_t *is_masked, int32_t mask_id,
+                              int32_t batch, int32_t seq_len, int32_t r_max, void *x,
+                              uint32_t *status, cudaStream_t stream);
 
 }  // namespace ec

@@ -16,6 +16,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include "ec_internal.cuh"
+
 namespace ec {
 namespace ptx {
 
@@ -67,6 +69,20 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// bar.red.or on a named barrier: true in every participating thread when any of
+// them passed true.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t threads, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
 // ---- TMA ----
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
 {
@@ -79,6 +95,40 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+// Untiled bulk copy global -> shared (16-byte aligned addresses, size a multiple
+// of 16), completing on an mbarrier; the L2 policy marks the lines evict-first
+// (data read exactly once).
+__device__ __forceinline__ void bulk_load_stream(uint32_t dst, const void *src, uint32_t bytes,
+                                                 uint32_t bar)
+{
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\t"
+        "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], pol;\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
         : "memory");
 }
 
@@ -205,6 +255,44 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk16, uint32_t 
     return static_cast<uint32_t>(col) * col_bytes + static_cast<uint32_t>(row) * 128u +
            (static_cast<uint32_t>(c ^ (row & 7)) << 4);
 }
+
+// ---- bounded waits on a CTA's array of mbarriers ----
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s: a wait this long is a fault
+
+// mbarrier i lives at bars + 8 i.  wait() gives up after ~2 s (or as soon as
+// another role of the CTA gave up): it raises the CTA's abort flag, sets
+// EC_DEV_TIMEOUT in the status word and returns false, so every role unwinds.
+struct Sync {
+    uint32_t bars;
+    volatile int *abort_flag;
+    uint32_t *status;
+    __device__ uint32_t bar(int i) const { return bars + 8u * static_cast<uint32_t>(i); }
+    __device__ bool wait(int i, uint32_t parity) const
+    {
+        const uint32_t b = bar(i);
+        if (mbar_try_wait(b, parity)) return true;
+        const long long t0 = clock64();
+        for (uint32_t it = 1;; ++it) {
+            if (mbar_try_wait(b, parity)) return true;
+            if ((it & 127u) == 0u) {
+                if (*abort_flag) return false;
+                if (clock64() - t0 > kWaitCycles) {
+                    *abort_flag = 1;
+                    flag_status(status, EC_DEV_TIMEOUT);
+                    return false;
+                }
+            }
+        }
+    }
+    // Used after an abort, to let copies already in flight land (bounded too).
+    __device__ bool drain(int i, uint32_t parity) const
+    {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar(i), parity))
+            if (clock64() - t0 > kWaitCycles / 4) return false;
+        return true;
+    }
+};
 
 }  // namespace ptx
 }  // namespace ec

@@ -262,3 +262,62 @@ def random_state(rng: np.random.Generator, batch: int, seq_len: int, p_masked: f
     steps = rng.integers(-1, max_step, size=(batch, seq_len)).astype(np.int32)
     decode_step = np.where(is_masked == 1, -1, steps).astype(np.int32)
     return is_masked, decode_step
+
+
+# ---------------------------------------------------------------------------
+# multi-step trajectory (synthetic layers)
+
+
+def trajectory_rows_per_step(w: Workload) -> list[int]:
+    """Masked rows of the active block at every step: each block starts fully
+    masked and loses ``n_unmask`` positions per step."""
+    per_block = -(-w.block // w.n_unmask)
+    rows = []
+    for t in range(w.n_steps):
+        j = t % per_block
+        rows.append(max(0, w.block - j * w.n_unmask))
+    return rows
+
+
+def trajectory_block(w: Workload, step: int) -> tuple[int, int]:
+    """Active block [lo, hi) at a step (blocks are decoded left to right)."""
+    per_block = -(-w.block // w.n_unmask)
+    j = min(step // per_block, (w.seq_len - w.prompt_len) // w.block - 1)
+    lo = w.prompt_len + j * w.block
+    return lo, lo + w.block
+
+
+@dataclasses.dataclass
+class TrajectoryStart:
+    is_masked: np.ndarray    # uint8 [1, L]: the generated region is masked
+    tokens: np.ndarray       # int32 [1, L]: prompt tokens, then the [MASK] id (= vocab)
+    decode_step: np.ndarray  # int32 [1, L]: -1 everywhere
+
+
+def trajectory_start(seed: int, w: Workload) -> TrajectoryStart:
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0x7A]))
+    L = w.seq_len
+    tokens = np.full((1, L), w.vocab, np.int32)
+    tokens[0, :w.prompt_len] = rng.integers(0, w.vocab, size=w.prompt_len)
+    is_masked = np.zeros((1, L), np.uint8)
+    is_masked[0, w.prompt_len:] = 1
+    return TrajectoryStart(is_masked, tokens, np.full((1, L), -1, np.int32))
+
+
+def trajectory_embedding(seed: int, vocab: int, hidden: int) -> np.ndarray:
+    """bf16 ``[vocab + 1, hidden]`` N(0, 1) table; row ``vocab`` is the [MASK] input."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0xE3]))
+    return f32_to_bf16_bits(rng.standard_normal((vocab + 1, hidden), dtype=np.float32))
+
+
+def trajectory_weights(seed: int, layer: int, hidden: int, width: int) -> np.ndarray:
+    """bf16 ``[3 width, hidden]`` N(0, 1/hidden) weights [W_q; W_k; W_v] of one layer."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0x3E, layer]))
+    x = rng.standard_normal((3 * width, hidden), dtype=np.float32)
+    x *= np.float32(1.0 / math.sqrt(hidden))
+    return f32_to_bf16_bits(x)
+
+
+def trajectory_logits(seed: int, step: int, n_rows: int, vocab: int) -> np.ndarray:
+    """bf16 logits of one step's masked rows (the temperature + spike recipe)."""
+    return make_logits(step_rng(seed, step), n_rows, vocab, BF16)

@@ -226,6 +226,57 @@ ec_status ec_selective_attention(const void *q, const void *k_new, const void *v
                                  int32_t n_kv_heads, int32_t head_dim, float scale,
                                  void *workspace, size_t workspace_bytes, ec_stream_t stream);
 
+/* ------------------------------------------------------------------------- */
+/* the forward that produces the recomputed rows' queries, keys and values    */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Rows of the first layer's input for the recomputed positions ([EC-it] step 2:
+ * the partial forward runs only the selected tokens; [EC-it] section 1: a
+ * masked diffusion model starts every position as [MASK] and replaces it by
+ * the decoded token).
+ *
+ *   for b, r < count[b], p = idx[b*idx_stride + r]:
+ *     x[b, r, :] = table[is_masked[b, p] ? mask_id : seq_tokens[b, p], :]
+ *
+ * table bf16 device [table_rows, hidden] (hidden a multiple of 8, 16-byte
+ * aligned); idx / count as produced by ec_build_recompute_set; seq_tokens int32
+ * and is_masked uint8 device [batch, seq_len]; x bf16 device [batch, r_max,
+ * hidden].  Rows r >= count[b] of x are left unchanged.  An index outside
+ * [0, seq_len) or a token outside [0, table_rows) skips the row and sets
+ * EC_DEV_BAD_INDEX.  Workspace: at least EC_WORKSPACE_ALIGN bytes (the status
+ * word), aligned, zeroed once.
+ */
+ec_status ec_embed_rows(const void *table, int64_t table_rows, int32_t hidden, const int32_t *idx,
+                        int64_t idx_stride, const int32_t *count, const int32_t *seq_tokens,
+                        const uint8_t *is_masked, int32_t mask_id, int32_t batch,
+                        int32_t seq_len, int32_t r_max, void *x, void *workspace,
+                        size_t workspace_bytes, ec_stream_t stream);
+
+/*
+ * Query, key and value projection of the recomputed rows ([EC-it] step 2: the
+ * partial forward recomputes Q/K/V of the selected tokens only; a full forward
+ * does it for all of them).  bf16 operands, float32 accumulation on the tensor
+ * cores, bf16 results:
+ *
+ *   for b, r < count[b], j < width:
+ *     q[b, r, j] = sum_e x[b, r, e] * w_qkv[j, e]
+ *     k[b, r, j] = sum_e x[b, r, e] * w_qkv[width + j, e]
+ *     v[b, r, j] = sum_e x[b, r, e] * w_qkv[2 width + j, e]
+ *
+ * x bf16 device [batch, r_max, hidden]; w_qkv bf16 device [3 width, hidden]
+ * (each output feature's weights contiguous, as a linear layer stores them);
+ * q, k, v bf16 device [batch, r_max, width] each (with width = heads x head_dim
+ * they are the [batch, r_max, heads, head_dim] operands of
+ * ec_selective_attention).  count int32 device [batch] or NULL (every one of the
+ * r_max rows); rows r >= count[b] are left unchanged.  hidden and width are
+ * multiples of 64; pointers 16-byte aligned.  Workspace: at least
+ * EC_WORKSPACE_ALIGN bytes (the status word), aligned, zeroed once.
+ */
+ec_status ec_qkv_projection(const void *x, const int32_t *count, int32_t batch, int32_t r_max,
+                            int32_t hidden, const void *w_qkv, int32_t width, void *q, void *k,
+                            void *v, void *workspace, size_t workspace_bytes, ec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

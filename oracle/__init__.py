@@ -51,8 +51,11 @@ def lib():
                                      i32, i32, i32, i32, i32]
         L.orc_attention.argtypes = [vp, vp, vp, ctypes.c_int, vp, i32, i32, i32, i32, i32, i32,
                                     f64, vp, i64, vp]
+        L.orc_embed_rows.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, i32, i32,
+                                     i32, i32, vp]
+        L.orc_projection.argtypes = [vp, vp, ctypes.c_int, i64, i32, i32, vp, i64, vp]
         for fn in (L.orc_row_stats, L.orc_unmask_gate, L.orc_recompute_set,
-                   L.orc_scatter_kv, L.orc_attention):
+                   L.orc_scatter_kv, L.orc_attention, L.orc_embed_rows, L.orc_projection):
             fn.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -159,3 +162,43 @@ def attention(q, k_cache, v_cache, count, scale, samples=None):
     _check(lib().orc_attention(_p(qq), _p(kc), _p(vc), dt, _p(cnt), batch, seq_len, r_max, h,
                                hkv, d, float(scale), _p(sp), ns, _p(out)), "attention")
     return out
+
+
+def embed_rows(table, idx, count, tokens, is_masked, mask_id, r_max):
+    """``[B, r_max, hidden]`` rows of ``table`` for the recomputed positions; rows
+    past ``count`` are zero."""
+    tb = np.ascontiguousarray(table)
+    ix = np.ascontiguousarray(idx, np.int32)
+    cnt = np.ascontiguousarray(count, np.int32)
+    tk = np.ascontiguousarray(tokens, np.int32)
+    im = np.ascontiguousarray(is_masked, np.uint8)
+    batch, seq_len = tk.shape
+    rows, hidden = tb.shape
+    x = np.zeros((batch, r_max, hidden), tb.dtype)
+    _check(lib().orc_embed_rows(_p(tb), _dtype_of(tb), rows, hidden, _p(ix), ix.shape[-1], _p(cnt),
+                                _p(tk), _p(im), int(mask_id), batch, seq_len, r_max, _p(x)),
+           "embed_rows")
+    return x
+
+
+def projection(x, w, rows=None):
+    """float64 ``x @ w.T`` for ``x [n, hidden]``, ``w [n_out, hidden]`` (same element
+    type); with ``rows`` only those rows of x, in that order."""
+    xx = np.ascontiguousarray(x)
+    ww = np.ascontiguousarray(w)
+    if _dtype_of(xx) != _dtype_of(ww):
+        raise TypeError("mixed dtypes")
+    n, hidden = xx.shape
+    n_out = ww.shape[0]
+    if ww.shape[1] != hidden:
+        raise ValueError("inner dimensions differ")
+    if rows is None:
+        sel, ns = None, 0
+        y = np.empty((n, n_out), np.float64)
+    else:
+        sel = np.ascontiguousarray(rows, np.int64)
+        ns = sel.shape[0]
+        y = np.empty((ns, n_out), np.float64)
+    _check(lib().orc_projection(_p(xx), _p(ww), _dtype_of(xx), n, hidden, n_out, _p(sel), ns,
+                                _p(y)), "projection")
+    return y

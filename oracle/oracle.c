@@ -394,3 +394,77 @@ int orc_attention(const void *q, const void *k_cache, const void *v_cache, int d
     free(s);
     return ORC_OK;
 }
+
+/*
+ * Input rows of the first layer for the recomputed positions ([EC-it] step 2:
+ * only the selected tokens go through the partial forward; [EC-it] section 1:
+ * a position holds [MASK] until its token is decoded).  For b, r < count[b],
+ * p = idx[b*idx_stride + r]:
+ *   x[b, r, :] = table[is_masked[b, p] ? mask_id : tokens[b, p], :]
+ * A bitwise row copy; x rows r >= count[b] are left untouched.
+ */
+int orc_embed_rows(const void *table, int dtype, int64_t table_rows, int32_t hidden,
+                   const int32_t *idx, int64_t idx_stride, const int32_t *count,
+                   const int32_t *tokens, const uint8_t *is_masked, int32_t mask_id,
+                   int32_t batch, int32_t seq_len, int32_t r_max, void *x)
+{
+    if (!dtype_ok(dtype))
+        return ORC_BAD_DTYPE;
+    if (batch < 0 || seq_len <= 0 || r_max < 0 || hidden <= 0 || table_rows <= 0)
+        return ORC_BAD_ARG;
+    const size_t row_bytes = (size_t)hidden * dtype_size(dtype);
+    for (int32_t b = 0; b < batch; ++b) {
+        if (count[b] < 0 || count[b] > r_max)
+            return ORC_BAD_ARG;
+        for (int32_t r = 0; r < count[b]; ++r) {
+            const int32_t p = idx[(int64_t)b * idx_stride + r];
+            if (p < 0 || p >= seq_len)
+                return ORC_BAD_ARG;
+            const int64_t at = (int64_t)b * seq_len + p;
+            const int64_t tok = is_masked[at] ? mask_id : tokens[at];
+            if (tok < 0 || tok >= table_rows)
+                return ORC_BAD_ARG;
+            memcpy((char *)x + ((size_t)b * r_max + r) * row_bytes,
+                   (const char *)table + (size_t)tok * row_bytes, row_bytes);
+        }
+    }
+    return ORC_OK;
+}
+
+/*
+ * Query, key and value projection of the recomputed rows ([EC-it] step 2: the
+ * partial forward recomputes Q/K/V of the selected tokens only), in float64:
+ *   y[row, j] = sum_e x[row, e] * w[j, e]       for j < n_out
+ * x [n_rows, hidden] and w [n_out, hidden] (typed), y double [n_rows, n_out].
+ * With rows != NULL only the n_sel listed rows of x are projected, and y is
+ * [n_sel, n_out].
+ */
+int orc_projection(const void *x, const void *w, int dtype, int64_t n_rows, int32_t hidden,
+                   int32_t n_out, const int64_t *rows, int64_t n_sel, double *y)
+{
+    if (!dtype_ok(dtype))
+        return ORC_BAD_DTYPE;
+    if (n_rows < 0 || hidden <= 0 || n_out <= 0)
+        return ORC_BAD_ARG;
+    double *xr = (double *)malloc((size_t)hidden * sizeof(double));
+    if (!xr)
+        return ORC_NOMEM;
+    const int64_t total = rows ? n_sel : n_rows;
+    for (int64_t s = 0; s < total; ++s) {
+        const int64_t row = rows ? rows[s] : s;
+        if (row < 0 || row >= n_rows) {
+            free(xr);
+            return ORC_BAD_ARG;
+        }
+        for (int32_t e = 0; e < hidden; ++e)
+            xr[e] = load(x, dtype, row * hidden + e);
+        for (int32_t j = 0; j < n_out; ++j) {
+            double acc = 0.0;
+            for (int32_t e = 0; e < hidden; ++e)
+                acc += xr[e] * load(w, dtype, (int64_t)j * hidden + e);
+            y[s * n_out + j] = acc;
+        }
+    }
+    free(xr);
+    return ORC_OK;
+}
