@@ -14,7 +14,8 @@ step (N * V * element size / step time).  The line also breaks the step into
 its parts (decode-and-gate GB/s and fraction of HBM, attention TFLOP/s and
 fraction of the tensor peak) and carries a roofline object for the dominant
 kernel, measured live with CUDA events on the launching stream.  L2 is flushed
-(a 256 MiB write) between timed steps, outside the timed intervals.
+(a 256 MiB write, then a 256 MiB read) between timed steps, outside the timed
+intervals.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -45,6 +46,21 @@ METRIC = "entropy/gate GB/s (% HBM peak); selective-recompute attention TFLOP/s 
 DEFAULT_WORKLOAD = "single_seq"
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+class L2Flush:
+    """Evicts L2 between timed steps: writes one 256 MiB buffer, then reads a
+    second one, so the next step starts with a cold L2 that holds no dirty
+    lines (whose write-back would otherwise be charged to the next kernel)."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.zeros(FLUSH_BYTES // 8, dtype=torch.int64, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
 
 
 def parse_args(argv=None):
@@ -287,11 +303,11 @@ def run_ours(args):
     stream = torch.cuda.Stream(device)
     torch.cuda.set_stream(stream)
     step = GpuStep(nat, w, st, logits, att, device, stream)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     K, W = args.steps, args.warmup
 
     for _ in range(W):
-        flush.zero_()
+        flush()
         step.run()
     torch.cuda.synchronize(device)
     # One step = one replay of a CUDA graph holding the three calls with timing
@@ -341,7 +357,7 @@ def run_ours(args):
     t_wall = time.perf_counter()
     t_att = t_dec = t_rec = 0.0
     for _ in range(K):
-        flush.zero_()
+        flush()
         one_step()
         ev[3].synchronize()
         t_att += ev[0].elapsed_time(ev[1]) / 1e3
@@ -406,7 +422,7 @@ def run_ours(args):
                    "n_rows": w.n_rows, "recompute_rows": w.r_max, "n_heads": w.n_heads,
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "n_unmask": w.n_unmask,
                    "k": w.k, "tau": w.tau, "accumulate": "f32",
-                   "l2": "flushed between steps (256 MiB write, untimed)", "launch": mode,
+                   "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)", "launch": mode,
                    "parallelism": f"replicas x{world}"},
         "parts": parts, "roofline": roof, "clocks": clocks, "e2e": e2e,
         "gpu_launches": sum(kernels_per_step(w).values()) * K,
@@ -437,7 +453,7 @@ def run_e2e(step: GpuStep, geo, w, logits, att, K, world):
     h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in d_out]
     bi = sum(h.numel() * h.element_size() for h, _ in h_in)
     bo = sum(h.numel() * h.element_size() for h in h_out)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def one():
         for h, d in h_in:
@@ -453,7 +469,7 @@ def run_e2e(step: GpuStep, geo, w, logits, att, K, world):
           for _ in range(K)]
     barrier(world)
     for i in range(K):
-        flush.zero_()
+        flush()
         ev[i][0].record()
         one()
         ev[i][1].record()

@@ -1,33 +1,39 @@
 // Selective-recompute bidirectional attention on the 5th-generation tensor
-// cores (tcgen05 + TMEM), fed by TMA, with the KV write-back fused into the
-// kernel's prologue.
+// cores (tcgen05 + TMEM), fed by TMA, with the KV write-back in the same call.
 //
 // "EntropyCache: Decoded Token Entropy Guided KV Caching for Diffusion Language
 // Models" — Italian summary, section "1. Il Problema" (dLLM attention is
 // bidirectional) and "Algoritmo di Funzionamento" step 2 (the partial forward
 // recomputes K/V only for the selected tokens; the cache supplies the rest).
 //
-// Persistent cooperative kernel, one CTA per SM:
-//   prologue   every CTA writes a share of the fresh K/V rows into the caches,
-//              then one bounded grid barrier; afterwards the caches hold the
-//              post-write-back state and every K/V tile is a plain TMA load.
-//   work items a unit is up to 128 query rows of one (sequence b, KV head g): the
-//              (recomputed row r, head h of g's group) pairs packed r-major, so a
-//              GQA group shares each K/V tile.  A unit's keys are split into
-//              `n_split` contiguous ranges of 128-key tiles; (unit, split) items
-//              are dealt round-robin to the CTAs.  A split's partial (O, m, l)
-//              goes to the workspace, and the last split of a unit to finish
-//              (an atomic ticket: no CTA waits on another) merges them.
-//   warp 0     producer of Q (one tile per item) and K tiles, warp 6 producer of
-//              V tiles: TMA loads with 128-byte swizzle into rings of stages; a K
-//              stage is released as soon as its QK product completes and a V
-//              stage when its PV product does, so K loads run well ahead;
+// Two launches, chained by programmatic dependent launch (PDL):
+//   write_back_kernel   copies every fresh K/V row into the caches and at once
+//                       lets the attention grid start;
+//   attention_tc_kernel allocates TMEM, sets up its barriers and loads its first
+//                       Q tile while the write-back runs, and waits for it
+//                       (griddepcontrol.wait) only before its first K/V load.
+//
+// Attention kernel: persistent, one CTA per SM.
+//   units      up to 128 query rows of one (sequence b, KV head g): the
+//              (recomputed row r, head h of g's group) pairs packed r-major, so
+//              a GQA group shares each K/V tile.
+//   pieces     the units' 128-key tiles are laid end to end and cut into one
+//              equal contiguous range per CTA (stream-K), so every CTA does the
+//              same number of tiles.  A range covers pieces of one or more
+//              units.  A piece that is a whole unit writes its output directly;
+//              otherwise it stores a partial (O, m, l) and the unit's last
+//              contributor (an acquire-release ticket; no CTA waits on another)
+//              merges the unit's partials.
+//   warp 0     producer of Q (one tile per piece) and K tiles, warp 6 producer
+//              of V tiles: TMA, 128-byte swizzle, rings of stages; a K stage is
+//              released when its QK product completes, a V stage when its PV
+//              product does;
 //   warp 1     TMEM allocation and tcgen05.mma issue: S = Q K^T into one of two
 //              TMEM S buffers, O += P V into the TMEM O accumulator;
-//   warps 2-5  one thread per query row: online softmax on S read by tcgen05.ld
-//              in the log2 domain (the reference maximum only moves when it grows
-//              by more than 8, rescaling O in TMEM when it does), P as bf16 into
-//              shared memory, and the epilogue.
+//   warps 2-5  one thread per query row: online softmax in the log2 domain on S
+//              read by tcgen05.ld (the reference maximum moves only when it
+//              grows by more than 8 in log2 units, rescaling O in TMEM when it
+//              does), P as bf16 into shared memory, and the epilogue.
 // Every wait is bounded (~2 s); a timeout sets EC_DEV_TIMEOUT and unwinds.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -46,7 +52,7 @@ using namespace ptx;
 constexpr int kBlockM = 128;   // query rows per unit = TMEM lanes
 constexpr int kBlockN = 128;   // keys per tile
 constexpr int kThreads = 224;  // 7 warps
-constexpr int kMaxSplit = 32;
+constexpr int kMaxContrib = 64;  // pieces a unit may be cut into
 
 template <int D>
 struct Cfg {
@@ -74,7 +80,7 @@ enum : int {
     B_VFULL = 8,    // [3] V tile landed
     B_VEMPTY = 11,  // [3] V stage consumed (its PV done)
     B_QFULL = 14,   // [2] Q tile landed
-    B_QEMPTY = 16,  // [2] Q tile consumed (last QK of its item done)
+    B_QEMPTY = 16,  // [2] Q tile consumed (last QK of its piece done)
     B_SFULL = 18,   // [2] S buffer written
     B_SFREE = 20,   // [2] S buffer read by the softmax warps
     B_PFULL = 22,   // P written, O corrected
@@ -82,9 +88,6 @@ enum : int {
     B_DRAIN = 24,
     B_COUNT = 25
 };
-
-// Workspace header words (the first 256 bytes of the workspace).
-constexpr int kHdrStatus = 0, kHdrBarCount = 2, kHdrBarGen = 3;
 
 struct Params {
     const __nv_bfloat16 *k_new, *v_new;
@@ -95,92 +98,96 @@ struct Params {
     int B, L, r_max, H, Hkv, G;
     int tok_per_tile;  // recomputed rows per unit: floor(128 / G)
     int n_mt;          // units per (b, g)
-    int n_units, n_split, n_items, n_tiles;
+    int n_units, n_tiles, grid;
+    int64_t total;     // n_units * n_tiles
+    int slots;         // partial slots per unit (most pieces a unit is cut into)
     float scale_log2;
-    uint32_t *hdr;      // workspace header
+    uint32_t *status;   // workspace status word
     unsigned *tickets;  // [n_units]
-    float2 *part_ml;    // [n_items][128] (m, l), log2 domain
-    float4 *part_o;     // [n_items][D / 4][128] unnormalised O
+    float2 *part_ml;    // [n_units][slots][128] (m, l), m in raw score units
+    float4 *part_o;     // [n_units][slots][D / 4][128] unnormalised O
 };
 
-struct Item {
-    int unit, split, b, g, mt, t0, t1, cnt;
+// A piece: tiles [t0, t1) of one unit, processed by this CTA.
+struct Piece {
+    int unit, b, g, mt, t0, t1, cnt, slot, n_contrib;
 };
 
-__device__ __forceinline__ Item decode_item(const Params &P, int i)
+__device__ __forceinline__ int64_t range_begin(const Params &P, int c)
 {
-    Item it;
-    it.unit = i % P.n_units;
-    it.split = i / P.n_units;
-    it.mt = it.unit % P.n_mt;
-    it.g = (it.unit / P.n_mt) % P.Hkv;
-    it.b = it.unit / (P.n_mt * P.Hkv);
-    it.t0 = static_cast<int>(static_cast<int64_t>(P.n_tiles) * it.split / P.n_split);
-    it.t1 = static_cast<int>(static_cast<int64_t>(P.n_tiles) * (it.split + 1) / P.n_split);
-    it.cnt = max(0, min(__ldg(P.count + it.b), P.r_max));
-    return it;
+    return static_cast<int64_t>(c) * P.total / P.grid;
+}
+__device__ __forceinline__ int cta_of(const Params &P, int64_t w)
+{
+    return static_cast<int>(((w + 1) * P.grid - 1) / P.total);
 }
 
-// Items with no recomputed rows (mt beyond the sequence's count) are skipped by
+// The pieces of CTA blockIdx.x, in order: units u_first .. u_last.
+struct Range {
+    int64_t w0, w1;
+    int u_first, u_last;
+};
+__device__ __forceinline__ Range my_range(const Params &P)
+{
+    Range r;
+    r.w0 = range_begin(P, blockIdx.x);
+    r.w1 = range_begin(P, blockIdx.x + 1);
+    r.u_first = static_cast<int>(r.w0 / P.n_tiles);
+    r.u_last = r.w1 > r.w0 ? static_cast<int>((r.w1 - 1) / P.n_tiles) : r.u_first - 1;
+    return r;
+}
+
+__device__ __forceinline__ Piece make_piece(const Params &P, const Range &r, int u)
+{
+    Piece p;
+    p.unit = u;
+    p.mt = u % P.n_mt;
+    p.g = (u / P.n_mt) % P.Hkv;
+    p.b = u / (P.n_mt * P.Hkv);
+    const int64_t base = static_cast<int64_t>(u) * P.n_tiles;
+    p.t0 = static_cast<int>(max(r.w0, base) - base);
+    p.t1 = static_cast<int>(min(r.w1, base + P.n_tiles) - base);
+    const int c0 = cta_of(P, base), c1 = cta_of(P, base + P.n_tiles - 1);
+    p.slot = static_cast<int>(blockIdx.x) - c0;
+    p.n_contrib = c1 - c0 + 1;
+    p.cnt = max(0, min(__ldg(P.count + p.b), P.r_max));
+    return p;
+}
+
+// Units with no recomputed rows (mt beyond the sequence's count) are skipped by
 // every role alike.
-__device__ __forceinline__ bool item_active(const Params &P, const Item &it)
+__device__ __forceinline__ bool piece_active(const Params &P, const Piece &p)
 {
-    return it.mt * P.tok_per_tile < it.cnt && it.t1 > it.t0;
+    return p.mt * P.tok_per_tile < p.cnt && p.t1 > p.t0;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p)
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents()
 {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Grid-wide barrier for a cooperative launch (all CTAs co-resident).  Sense
-// reversal on a generation word; bounded: returns false after ~2 s.
-__device__ bool grid_barrier(uint32_t *hdr, unsigned n_ctas, volatile int *abort_flag)
+__device__ __forceinline__ unsigned ticket(unsigned *ctr, unsigned last)
 {
-    __shared__ int s_ok;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t *count = hdr + kHdrBarCount;
-        uint32_t *gen = hdr + kHdrBarGen;
-        const uint32_t g0 = ld_acquire_u32(gen);
-        __threadfence();
-        const unsigned arrived = atomicAdd(count, 1u);
-        int ok = 1;
-        if (arrived == n_ctas - 1) {
-            atomicExch(count, 0u);
-            __threadfence();
-            atomicAdd(gen, 1u);
-        } else {
-            const long long t0 = clock64();
-            while (ld_acquire_u32(gen) == g0) {
-                if (clock64() - t0 > kWaitCycles) {
-                    flag_status(hdr + kHdrStatus, EC_DEV_TIMEOUT);
-                    ok = 0;
-                    break;
-                }
-            }
-        }
-        s_ok = ok;
-        if (!ok) *abort_flag = 1;
-    }
-    __syncthreads();
-    return s_ok != 0;
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(ctr), "r"(last)
+                 : "memory");
+    return old;
 }
 
-// Q and K producer (one thread): per item its Q tile, then its K tiles.
+// Q and K producer (one thread): per piece its Q tile, then its K tiles.
 template <int D>
 __device__ void producer_qk(const Params &P, const Sync &S, uint32_t sbase, const CUtensorMap *tm_q,
                             const CUtensorMap *tm_k)
 {
     using C = Cfg<D>;
     const uint32_t q_bytes = static_cast<uint32_t>(P.tok_per_tile * P.G) * D * 2;
+    const Range r = my_range(P);
     uint32_t T = 0, it = 0;
-    bool ok = true;
-    for (int i = blockIdx.x; i < P.n_items && ok; i += gridDim.x) {
-        const Item w = decode_item(P, i);
-        if (!item_active(P, w)) continue;
+    bool ok = true, waited = false;
+    for (int u = r.u_first; u <= r.u_last && ok; ++u) {
+        const Piece w = make_piece(P, r, u);
+        if (!piece_active(P, w)) continue;
         const int qb = it % C::kQBufs;
         if (it >= static_cast<uint32_t>(C::kQBufs))
             ok = S.wait(B_QEMPTY + qb, ((it / C::kQBufs) - 1) & 1);
@@ -191,6 +198,10 @@ __device__ void producer_qk(const Params &P, const Sync &S, uint32_t sbase, cons
             tma_load_4d(qdst + c * C::kCol, tm_q, S.bar(B_QFULL + qb), c * 64, w.g * P.G,
                         w.mt * P.tok_per_tile, w.b);
         ++it;
+        if (!waited) {  // the caches are read only after the write-back grid finished
+            pdl_wait();
+            waited = true;
+        }
         for (int t = w.t0; t < w.t1 && ok; ++t, ++T) {
             const int s = T % C::kKStages;
             if (T >= static_cast<uint32_t>(C::kKStages))
@@ -211,16 +222,18 @@ __device__ void producer_qk(const Params &P, const Sync &S, uint32_t sbase, cons
     }
 }
 
-// V producer (one thread): the V tiles of every item, in the same order.
+// V producer (one thread): the V tiles of every piece, in the same order.
 template <int D>
 __device__ void producer_v(const Params &P, const Sync &S, uint32_t sbase, const CUtensorMap *tm_v)
 {
     using C = Cfg<D>;
+    const Range r = my_range(P);
     uint32_t T = 0;
     bool ok = true;
-    for (int i = blockIdx.x; i < P.n_items && ok; i += gridDim.x) {
-        const Item w = decode_item(P, i);
-        if (!item_active(P, w)) continue;
+    pdl_wait();
+    for (int u = r.u_first; u <= r.u_last && ok; ++u) {
+        const Piece w = make_piece(P, r, u);
+        if (!piece_active(P, w)) continue;
         for (int t = w.t0; t < w.t1 && ok; ++t, ++T) {
             const int s = T % C::kVStages;
             if (T >= static_cast<uint32_t>(C::kVStages))
@@ -244,6 +257,7 @@ __device__ void mma_issuer(const Params &P, const Sync &S, uint32_t sbase, uint3
     using C = Cfg<D>;
     constexpr uint32_t kIdescQK = idesc_bf16(kBlockM, kBlockN, false, false);
     constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, false, true);
+    const Range r = my_range(P);
     uint32_t T = 0, it = 0;
     bool ok = true;
     // the PV product of the previous tile, issued after the next QK
@@ -266,9 +280,9 @@ __device__ void mma_issuer(const Params &P, const Sync &S, uint32_t sbase, uint3
         umma_commit(S.bar(B_PVDONE));
         pv_pending = false;
     };
-    for (int i = blockIdx.x; i < P.n_items && ok; i += gridDim.x) {
-        const Item w = decode_item(P, i);
-        if (!item_active(P, w)) continue;
+    for (int u = r.u_first; u <= r.u_last && ok; ++u) {
+        const Piece w = make_piece(P, r, u);
+        if (!piece_active(P, w)) continue;
         const int qb = it % C::kQBufs;
         ok = S.wait(B_QFULL + qb, (it / C::kQBufs) & 1);
         if (!ok) break;
@@ -303,6 +317,88 @@ __device__ void mma_issuer(const Params &P, const Sync &S, uint32_t sbase, uint3
     S.drain(B_DRAIN, 0);
 }
 
+__device__ __forceinline__ uint64_t f2x2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void x2f(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Merge of a unit's n partials (last contributor), by the 128 softmax threads:
+// work items (row, 32-column chunk); every load of an item is issued before use.
+template <int D>
+__device__ void merge_unit(const Params &P, const Piece &w, int ltid)
+{
+    constexpr int kChunks = D / 32;
+    const int n = w.n_contrib;
+    const int rows = min(kBlockM, P.tok_per_tile * P.G);
+    const float2 *ml = P.part_ml + static_cast<int64_t>(w.unit) * P.slots * kBlockM;
+    const float4 *po = P.part_o + static_cast<int64_t>(w.unit) * P.slots * (D / 4) * kBlockM;
+    for (int item = ltid; item < rows * kChunks; item += 128) {
+        const int row = item % rows, ch = item / rows;
+        const int tok = w.mt * P.tok_per_tile + row / P.G;
+        if (tok >= w.cnt) continue;
+        float m_all = -INFINITY;
+        for (int s = 0; s < n; ++s) m_all = fmaxf(m_all, __ldcg(ml + s * kBlockM + row).x);
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+        float l_tot = 0.f;
+        for (int s = 0; s < n; ++s) {
+            const float2 mls = __ldcg(ml + s * kBlockM + row);
+            const float f = ex2((mls.x - m_all) * P.scale_log2);
+            l_tot = fmaf(f, mls.y, l_tot);
+            const float4 *src = po + (static_cast<int64_t>(s) * (D / 4) + ch * 8) * kBlockM + row;
+            float4 x[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) x[q] = __ldcg(src + q * kBlockM);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                acc[4 * q] = fmaf(f, x[q].x, acc[4 * q]);
+                acc[4 * q + 1] = fmaf(f, x[q].y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(f, x[q].z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(f, x[q].w, acc[4 * q + 3]);
+            }
+        }
+        const float inv = 1.f / l_tot;
+        const int h = w.g * P.G + row % P.G;
+        __nv_bfloat16 *orow =
+            P.out + ((static_cast<int64_t>(w.b) * P.r_max + tok) * P.H + h) * D + ch * 32;
+        uint4 *dst = reinterpret_cast<uint4 *>(orow);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack_bf16x2(acc[8 * q] * inv, acc[8 * q + 1] * inv);
+            v.y = pack_bf16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv);
+            v.z = pack_bf16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv);
+            v.w = pack_bf16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv);
+            dst[q] = v;
+        }
+    }
+}
+
 template <int D>
 __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem)
 {
@@ -310,75 +406,104 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
+    const int ltid = (warp - 2) * 32 + lane;  // 0 .. 127 over the softmax warps
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float c = P.scale_log2;           // log2 units per raw score unit
+    const float move = 8.f / c;             // raw-score growth that moves the reference
+    const int kv_tail = P.L - (P.n_tiles - 1) * kBlockN;  // keys in the last tile
     __shared__ int s_last;
+    const Range r = my_range(P);
     uint32_t T = 0;
     bool ok = true;
-    for (int i = blockIdx.x; i < P.n_items && ok; i += gridDim.x) {
-        const Item w = decode_item(P, i);
-        if (!item_active(P, w)) continue;
-        float m_run = -INFINITY, l_run = 0.f;
+    // After a failed (timed-out) wait a warp skips all further work but keeps
+    // walking the same pieces, so the four softmax warps always meet at the same
+    // named barriers; every later wait returns at once (the abort flag is set).
+    for (int u = r.u_first; u <= r.u_last; ++u) {
+        const Piece w = make_piece(P, r, u);
+        if (!piece_active(P, w)) continue;
+        float m_run = -INFINITY, l_run = 0.f;  // m in raw score units
         for (int t = w.t0; t < w.t1; ++t, ++T) {
             const int sb = T & 1;
-            ok = S.wait(B_SFULL + sb, (T >> 1) & 1);
-            __syncwarp();  // reconverge before the warp-collective tcgen05.ld
-            if (!ok) break;
+            if (ok) ok = __all_sync(0xffffffffu, S.wait(B_SFULL + sb, (T >> 1) & 1));
+            if (!ok) continue;
             tc_fence_after();
             uint32_t sr[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                tmem_ld32(tmem + lane_off + C::kColS + sb * kBlockN + c * 32, sr[c]);
+            for (int cc = 0; cc < 4; ++cc)
+                tmem_ld32(tmem + lane_off + C::kColS + sb * kBlockN + cc * 32, sr[cc]);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
+            for (int cc = 0; cc < 4; ++cc) tmem_wait_ld(sr[cc]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(S.bar(B_SFREE + sb));
 
-            const int kv_valid = min(kBlockN, P.L - t * kBlockN);
-            float mx = -INFINITY;
+            if (t == P.n_tiles - 1 && kv_tail < kBlockN) {  // keys past L do not exist
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+                for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float s = __uint_as_float(sr[c][j]) * P.scale_log2;
-                    if (c * 32 + j >= kv_valid) s = -INFINITY;
-                    sr[c][j] = __float_as_uint(s);
-                    mx = fmaxf(mx, s);
+                    for (int j = 0; j < 32; ++j)
+                        if (cc * 32 + j >= kv_tail) sr[cc][j] = __float_as_uint(-INFINITY);
+            }
+            // row maximum of the raw scores (scale > 0 keeps the order)
+            float mx4[4];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float a = __uint_as_float(sr[cc][0]), b = __uint_as_float(sr[cc][1]);
+#pragma unroll
+                for (int j = 2; j < 32; j += 4) {
+                    a = fmax3(a, __uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1]));
+                    b = fmax3(b, __uint_as_float(sr[cc][j + 2]), __uint_as_float(sr[cc][j + 3]));
                 }
+                mx4[cc] = fmaxf(a, b);
+            }
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             float m_use = m_run, alpha = 1.f;
             bool rescale = false;
-            if (mx > m_run + 8.f) {  // move the reference only when p could exceed 2^8
+            if (mx > m_run + move) {  // p would exceed 2^8: move the reference
                 m_use = mx;
-                alpha = ex2(m_run - mx);
+                alpha = ex2((m_run - mx) * c);
                 rescale = t > w.t0;
             }
-            float rowsum = 0.f;
+            // p = 2^{(s - m) c}; two-wide FMA and adds, four partial sums
+            const uint64_t c2 = f2x2(c, c);
+            const float nmc = -m_use * c;
+            const uint64_t nmc2 = f2x2(nmc, nmc);
+            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
             uint32_t pk[64];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) {
-                    const float p0 = ex2(__uint_as_float(sr[c][j]) - m_use);
-                    const float p1 = ex2(__uint_as_float(sr[c][j + 1]) - m_use);
-                    rowsum += p0 + p1;
-                    pk[(c * 32 + j) >> 1] = pack_bf16x2(p0, p1);
+                    const uint64_t y2 = ffma2(f2x2(__uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1])),
+                                              c2, nmc2);
+                    float y0, y1;
+                    x2f(y2, y0, y1);
+                    const float p0 = ex2(y0), p1 = ex2(y1);
+                    const uint64_t p2 = f2x2(p0, p1);
+                    acc2[(j >> 1) & 3] = fadd2(acc2[(j >> 1) & 3], p2);
+                    pk[(cc * 32 + j) >> 1] = pack_bf16x2(p0, p1);
                 }
+            float rs0, rs1, rs2, rs3, rs4, rs5, rs6, rs7;
+            x2f(acc2[0], rs0, rs1);
+            x2f(acc2[1], rs2, rs3);
+            x2f(acc2[2], rs4, rs5);
+            x2f(acc2[3], rs6, rs7);
+            const float rowsum = ((rs0 + rs1) + (rs2 + rs3)) + ((rs4 + rs5) + (rs6 + rs7));
             l_run = l_run * alpha + rowsum;
             m_run = m_use;
 
-            // P buffer and O are free once the previous PV of this item completed
-            // (for an item's first tile the previous epilogue already waited).
+            // P buffer and O are free once the previous PV of this piece completed
+            // (for a piece's first tile the previous epilogue already waited).
             if (t > w.t0) {
-                ok = S.wait(B_PVDONE, (T - 1) & 1);
-                __syncwarp();
-                if (!ok) break;
+                ok = __all_sync(0xffffffffu, S.wait(B_PVDONE, (T - 1) & 1));
+                if (!ok) continue;
             }
             tc_fence_after();
             if (rescale) {
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
-                    const uint32_t ta = tmem + lane_off + C::kColO + c * 32;
+                    const uint32_t ta = tmem + lane_off + C::kColO + cc * 32;
                     tmem_ld32(ta, o);
                     tmem_wait_ld(o);
 #pragma unroll
@@ -396,26 +521,23 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase,
             __syncwarp();
             if (lane == 0) mbar_arrive(S.bar(B_PFULL));
         }
-        if (!ok) break;
-
-        // ---- epilogue of the item ----
-        ok = S.wait(B_PVDONE, (T - 1) & 1);
-        __syncwarp();
-        if (!ok) break;
+        // ---- epilogue of the piece ----
+        if (ok) ok = __all_sync(0xffffffffu, S.wait(B_PVDONE, (T - 1) & 1));
         tc_fence_after();
         const int tok = w.mt * P.tok_per_tile + row / P.G;
         const bool valid = row < P.tok_per_tile * P.G && tok < w.cnt;
         const int h = w.g * P.G + row % P.G;
         __nv_bfloat16 *orow = P.out + ((static_cast<int64_t>(w.b) * P.r_max + tok) * P.H + h) * D;
-        if (P.n_split == 1) {
+        if (w.n_contrib == 1) {
+            if (!ok) continue;
             const float inv = 1.f / l_run;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_off + C::kColO + c * 32, o);
+                tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
                 tmem_wait_ld(o);
                 if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint4 v;
@@ -430,86 +552,46 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase,
             tc_fence_before();
             continue;
         }
-        // split item: store the partial, then the last split of the unit merges
-        float4 *po = P.part_o + static_cast<int64_t>(i) * (D / 4) * kBlockM;
+        // part of a unit: store the partial, then the unit's last contributor merges
+        float4 *po = P.part_o + (static_cast<int64_t>(w.unit) * P.slots + w.slot) * (D / 4) * kBlockM;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int cc = 0; cc < D / 32; ++cc) {
+            if (!ok) break;
             uint32_t o[32];
-            tmem_ld32(tmem + lane_off + C::kColO + c * 32, o);
+            tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
             tmem_wait_ld(o);
             if (valid) {
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    __stcg(po + (c * 8 + q) * kBlockM + row,
+                    __stcg(po + (cc * 8 + q) * kBlockM + row,
                            make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
                                        __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3])));
             }
         }
         tc_fence_before();
-        if (valid) __stcg(P.part_ml + static_cast<int64_t>(i) * kBlockM + row, make_float2(m_run, l_run));
-        __threadfence();
+        if (ok && valid)
+            __stcg(P.part_ml + (static_cast<int64_t>(w.unit) * P.slots + w.slot) * kBlockM + row,
+                   make_float2(m_run, l_run));
+        // all four warps meet here whatever happened; a failure anywhere drops the piece
+        const bool failed = named_bar_or(1, 128, !ok);
+        if (!failed && ltid == 0)  // release: the partials above; acquire: the others'
+            s_last = ticket(P.tickets + w.unit, static_cast<unsigned>(w.n_contrib - 1)) ==
+                     static_cast<unsigned>(w.n_contrib - 1);
         named_bar_sync(1, 128);
-        if (warp == 2 && lane == 0) {
-            const unsigned ticket = atomicInc(P.tickets + w.unit, static_cast<unsigned>(P.n_split - 1));
-            s_last = ticket == static_cast<unsigned>(P.n_split - 1);
-        }
-        named_bar_sync(1, 128);
-        if (!s_last) continue;
-        __threadfence();
-        if (valid) {
-            // merge the n_split partials of this unit, in split order
-            float m_all = -INFINITY;
-            for (int s = 0; s < P.n_split; ++s) {
-                const int item = s * P.n_units + w.unit;
-                m_all = fmaxf(m_all, __ldcg(P.part_ml + static_cast<int64_t>(item) * kBlockM + row).x);
-            }
-            float scl[kMaxSplit];
-            float l_tot = 0.f;
-            for (int s = 0; s < P.n_split; ++s) {
-                const int item = s * P.n_units + w.unit;
-                const float2 ml = __ldcg(P.part_ml + static_cast<int64_t>(item) * kBlockM + row);
-                scl[s] = ex2(ml.x - m_all);
-                l_tot += scl[s] * ml.y;
-            }
-            const float inv = 1.f / l_tot;
-#pragma unroll 1
-            for (int c = 0; c < D / 8; ++c) {  // 8 output columns at a time
-                float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-                for (int s = 0; s < P.n_split; ++s) {
-                    const float4 *ps =
-                        P.part_o + static_cast<int64_t>(s * P.n_units + w.unit) * (D / 4) * kBlockM;
-                    const float4 x0 = __ldcg(ps + (2 * c) * kBlockM + row);
-                    const float4 x1 = __ldcg(ps + (2 * c + 1) * kBlockM + row);
-                    const float f = scl[s];
-                    a0.x = fmaf(f, x0.x, a0.x);
-                    a0.y = fmaf(f, x0.y, a0.y);
-                    a0.z = fmaf(f, x0.z, a0.z);
-                    a0.w = fmaf(f, x0.w, a0.w);
-                    a1.x = fmaf(f, x1.x, a1.x);
-                    a1.y = fmaf(f, x1.y, a1.y);
-                    a1.z = fmaf(f, x1.z, a1.z);
-                    a1.w = fmaf(f, x1.w, a1.w);
-                }
-                uint4 v;
-                v.x = pack_bf16x2(a0.x * inv, a0.y * inv);
-                v.y = pack_bf16x2(a0.z * inv, a0.w * inv);
-                v.z = pack_bf16x2(a1.x * inv, a1.y * inv);
-                v.w = pack_bf16x2(a1.z * inv, a1.w * inv);
-                *reinterpret_cast<uint4 *>(orow + c * 8) = v;
-            }
-        }
-        __syncwarp();
+        if (!failed && s_last) merge_unit<D>(P, w, ltid);
+        named_bar_sync(1, 128);  // s_last is rewritten by the next piece
     }
 }
 
-// Prologue: every fresh row of every (b, KV head) is written into the caches.
+// Fresh K/V rows into the caches.  Lets the attention grid launch at once.
 template <int D>
-__device__ void write_back(const Params &P)
+__global__ void __launch_bounds__(256) write_back_kernel(const Params P)
 {
+    pdl_launch_dependents();
     constexpr int kChunks = D / 8;
     const int64_t total = static_cast<int64_t>(P.B) * P.r_max * P.Hkv * kChunks;
-    for (int64_t e = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; e < total;
-         e += static_cast<int64_t>(gridDim.x) * kThreads) {
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int ch = static_cast<int>(e % kChunks);
         const int64_t rg = e / kChunks;  // (b, r, g) flattened
         const int g = static_cast<int>(rg % P.Hkv);
@@ -518,23 +600,21 @@ __device__ void write_back(const Params &P)
         const int b = static_cast<int>(br / P.r_max);
         const int c = __ldg(P.count + b);
         if (ch == 0 && g == 0 && r == 0 && (c < 0 || c > P.r_max))
-            flag_status(P.hdr + kHdrStatus, EC_DEV_BAD_COUNT);
+            flag_status(P.status, EC_DEV_BAD_COUNT);
         if (r >= min(max(c, 0), P.r_max)) continue;
         const int32_t *idx = P.idx + static_cast<int64_t>(b) * P.idx_stride;
         const int p = __ldg(idx + r);
         if (p < 0 || p >= P.L) {
-            if (ch == 0 && g == 0) flag_status(P.hdr + kHdrStatus, EC_DEV_BAD_INDEX);
+            if (ch == 0 && g == 0) flag_status(P.status, EC_DEV_BAD_INDEX);
             continue;
         }
         if (ch == 0 && g == 0 && r > 0 && __ldg(idx + r - 1) >= p)
-            flag_status(P.hdr + kHdrStatus, EC_DEV_BAD_INDEX);
+            flag_status(P.status, EC_DEV_BAD_INDEX);
         const int64_t src = (br * P.Hkv + g) * D + ch * 8;
         const int64_t dst = ((static_cast<int64_t>(b) * P.L + p) * P.Hkv + g) * D + ch * 8;
         *reinterpret_cast<uint4 *>(P.k_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(P.k_new + src));
         *reinterpret_cast<uint4 *>(P.v_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(P.v_new + src));
     }
-    // generic-proxy writes, read next by the TMA (async proxy) of other CTAs
-    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 template <int D>
@@ -551,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 16);
-    Sync S{sbase + C::kOffBar, abort_flag, P.hdr + kHdrStatus};
+    Sync S{sbase + C::kOffBar, abort_flag, P.status};
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -567,31 +647,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
-    write_back<D>(P);
-    const bool ok = grid_barrier(P.hdr, gridDim.x, abort_flag);
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (ok) {
-        if (warp == 0 || warp == 6) {
-            if ((threadIdx.x & 31) == 0) {
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-                if (warp == 0) {
-                    prefetch_tmap(&tm_q);
-                    prefetch_tmap(&tm_k);
-                    producer_qk<D>(P, S, sbase, &tm_q, &tm_k);
-                } else {
-                    prefetch_tmap(&tm_v);
-                    producer_v<D>(P, S, sbase, &tm_v);
-                }
+    if (warp == 0 || warp == 6) {
+        if ((threadIdx.x & 31) == 0) {
+            if (warp == 0) {
+                prefetch_tmap(&tm_q);
+                prefetch_tmap(&tm_k);
+                producer_qk<D>(P, S, sbase, &tm_q, &tm_k);
+            } else {
+                prefetch_tmap(&tm_v);
+                producer_v<D>(P, S, sbase, &tm_v);
             }
-            __syncwarp();
-        } else if (warp == 1) {
-            if ((threadIdx.x & 31) == 0) mma_issuer<D>(P, S, sbase, tmem);
-            __syncwarp();
-        } else {
-            softmax_epilogue<D>(P, S, sbase, tmem);
         }
+        __syncwarp();
+    } else if (warp == 1) {
+        if ((threadIdx.x & 31) == 0) mma_issuer<D>(P, S, sbase, tmem);
+        __syncwarp();
+    } else {
+        softmax_epilogue<D>(P, S, sbase, tmem);
     }
     __syncthreads();
     if (warp == 1) {
@@ -635,9 +711,12 @@ bool encode_4d(CUtensorMap *map, const void *base, int B, int rows, int heads, i
 }
 
 struct Plan {
-    int G, tok_per_tile, n_mt, n_units, n_tiles, n_split, n_items, n_ctas;
+    int G, tok_per_tile, n_mt, n_units, n_tiles, grid, slots;
+    int64_t total;
 };
 
+// Every CTA gets total / grid tiles; the grid is at most one CTA per SM and
+// small enough that a unit is cut into at most kMaxContrib pieces.
 Plan make_plan(int B, int L, int r_max, int H, int Hkv)
 {
     Plan p;
@@ -646,25 +725,14 @@ Plan make_plan(int B, int L, int r_max, int H, int Hkv)
     p.n_mt = (r_max + p.tok_per_tile - 1) / p.tok_per_tile;
     p.n_units = B * Hkv * p.n_mt;
     p.n_tiles = (L + kBlockN - 1) / kBlockN;
-    const int n_sm = device_sm_count();
-    // Pick the split that minimises (rounds of items per CTA) x (tiles per item +
-    // fixed per-item cost); a split keeps at least two tiles.
-    double best = 1e30;
-    p.n_split = 1;
-    const int max_split = std::max(1, std::min(kMaxSplit, p.n_tiles / 2));
-    for (int s = 1; s <= max_split; ++s) {
-        const int64_t items = static_cast<int64_t>(p.n_units) * s;
-        const int64_t rounds = (items + n_sm - 1) / n_sm;
-        const double per_item =
-            std::ceil(static_cast<double>(p.n_tiles) / s) + 1.5 + (s > 1 ? 0.5 : 0.0);
-        const double cost = static_cast<double>(rounds) * per_item;
-        if (cost < best - 1e-9) {
-            best = cost;
-            p.n_split = s;
-        }
-    }
-    p.n_items = p.n_units * p.n_split;
-    p.n_ctas = std::min(p.n_items, n_sm);
+    p.total = static_cast<int64_t>(p.n_units) * p.n_tiles;
+    int64_t g = device_sm_count();
+    g = std::min<int64_t>(g, p.total);
+    g = std::min<int64_t>(g, static_cast<int64_t>(p.n_units) * (kMaxContrib - 2));
+    p.grid = static_cast<int>(std::max<int64_t>(1, g));
+    // a unit of n_tiles tiles meets at most ceil(n_tiles * grid / total) + 1 ranges
+    p.slots = static_cast<int>(std::min<int64_t>(
+        kMaxContrib, (static_cast<int64_t>(p.n_tiles) * p.grid + p.total - 1) / p.total + 1));
     return p;
 }
 
@@ -674,7 +742,7 @@ size_t partial_offsets(const Plan &p, int D, size_t *off_tickets, size_t *off_ml
     *off_tickets = off;
     off = align_up(off + static_cast<size_t>(p.n_units) * sizeof(unsigned), 256);
     *off_ml = off;
-    const size_t parts = p.n_split > 1 ? static_cast<size_t>(p.n_items) : 0;
+    const size_t parts = p.slots > 1 ? static_cast<size_t>(p.n_units) * p.slots : 0;
     off = align_up(off + parts * kBlockM * sizeof(float2), 256);
     *off_o = off;
     return off + parts * kBlockM * static_cast<size_t>(D) * sizeof(float);
@@ -698,14 +766,22 @@ cudaError_t launch_typed(const Params &p, const Plan &plan, const void *q, cudaS
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = 1;
     }
+    // 1. write-back: a few CTAs per SM over the fresh rows
+    const int64_t chunks = static_cast<int64_t>(p.B) * p.r_max * p.Hkv * (D / 8);
+    const int wb_grid = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>((chunks + 255) / 256, 4 * static_cast<int64_t>(device_sm_count()))));
+    write_back_kernel<D><<<wb_grid, 256, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // 2. attention, allowed to start before the write-back finishes (PDL)
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(plan.n_ctas));
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Cfg<D>::kBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident: the grid barrier is safe
-    attr[0].val.cooperative = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, attention_tc_kernel<D>, p, tq, tk, tv);
@@ -755,14 +831,15 @@ cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_
     p.tok_per_tile = plan.tok_per_tile;
     p.n_mt = plan.n_mt;
     p.n_units = plan.n_units;
-    p.n_split = plan.n_split;
-    p.n_items = plan.n_items;
     p.n_tiles = plan.n_tiles;
+    p.grid = plan.grid;
+    p.total = plan.total;
+    p.slots = plan.slots;
     p.scale_log2 = scale * kLog2e;
     char *ws = static_cast<char *>(workspace);
     size_t o_t, o_ml, o_o;
     partial_offsets(plan, head_dim, &o_t, &o_ml, &o_o);
-    p.hdr = reinterpret_cast<uint32_t *>(ws);
+    p.status = reinterpret_cast<uint32_t *>(ws);
     p.tickets = reinterpret_cast<unsigned *>(ws + o_t);
     p.part_ml = reinterpret_cast<float2 *>(ws + o_ml);
     p.part_o = reinterpret_cast<float4 *>(ws + o_o);

@@ -48,19 +48,25 @@ using ptx::Sync;
 
 constexpr int kConsumers = 256;              // 8 folding warps
 constexpr int kConsumerWarps = kConsumers / 32;
-constexpr int kThreads = kConsumers + 32;    // + 1 producer warp
-constexpr int kCtasPerSm = 2;
+constexpr int kThreads = kConsumers + 64;    // + producer warp + finisher warp
+constexpr int kCtasPerSm = 3;
 constexpr uint32_t kChunk = 16384;           // bytes per ring stage
-constexpr int kStages = 6;
+constexpr int kStages = 3;
 constexpr int kVecPerChunk = kChunk / 16;
 constexpr int kVecPerThread = kVecPerChunk / kConsumers;  // 4
+constexpr int kPieceSlots = 4;               // finished row pieces queued for the finisher
 constexpr int kMaxSplits = 64;               // partial slots per row
 constexpr int kMaxStagedRows = 1024;         // selection keys kept in smem up to this many rows
 constexpr int kMaxUnmask = 1024;
-constexpr uint32_t kSmemDyn = kStages * kChunk + 1024 + 128;  // ring + align slack + barriers
-constexpr int kBarConsumers = 1;             // named barrier id of the consumer warps
 
-enum : int { D_FULL = 0, D_EMPTY = kStages, D_COUNT = 2 * kStages };
+enum : int {
+    D_FULL = 0,                        // [kStages] stage landed
+    D_EMPTY = D_FULL + kStages,        // [kStages] stage read by every consumer warp
+    D_PFULL = D_EMPTY + kStages,       // [kPieceSlots] the 8 warp partials of a piece written
+    D_PEMPTY = D_PFULL + kPieceSlots,  // [kPieceSlots] the finisher took them
+    D_COUNT = D_PEMPTY + kPieceSlots
+};
+constexpr uint32_t kSmemDyn = kStages * kChunk + 1024 + 8 * D_COUNT;  // ring + align slack + barriers
 
 struct __align__(16) Partial {
     float m;  // running maximum logit
@@ -259,8 +265,6 @@ __device__ __forceinline__ unsigned long long select_key(float conf, int pos)
            static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(pos));
 }
 
-__device__ __forceinline__ void consumers_sync() { ptx::named_bar_sync(kBarConsumers, kConsumers); }
-
 // The sequence holding row i (rows of a sequence are contiguous), or -1 when the
 // offsets do not place it in a well-formed range.
 __device__ int sequence_of(const Args &A, int i, int &lo, int &cnt)
@@ -280,167 +284,137 @@ __device__ int sequence_of(const Args &A, int i, int &lo, int &cnt)
     return a;
 }
 
-// Rank, gate and state update for sequence b (consumer threads).
+// Ticket with release (publishes this thread's earlier writes) and acquire (the
+// last taker sees every earlier taker's writes) at GPU scope; wraps to 0 after
+// `last`, so the counter is ready for the next launch.
+__device__ __forceinline__ unsigned ticket(unsigned *ctr, unsigned last)
+{
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(ctr), "r"(last)
+                 : "memory");
+    return old;
+}
+
+// Rank, gate and state update for sequence b, by one warp.
 __device__ void finish_sequence(const Args &A, int b, int r0, int cnt)
 {
     __shared__ unsigned long long s_key[kMaxStagedRows];
-    __shared__ int s_sel[kMaxUnmask];
-    __shared__ int s_nsel;
-    __shared__ float s_wmax[kConsumerWarps];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31;
     const bool staged = cnt <= kMaxStagedRows;
     if (staged)
-        for (int i = tid; i < cnt; i += kConsumers)
+        for (int i = lane; i < cnt; i += 32)
             s_key[i] = select_key(__ldcg(A.conf_out + r0 + i), __ldg(A.row_pos + r0 + i));
-    consumers_sync();
+    __syncwarp();
 
     const int take = min(A.n_unmask, cnt);
-    if (warp == 0) {
-        unsigned long long prev = ~0ull;
-        int nsel = 0;
-        for (int s = 0; s < take; ++s) {
-            unsigned long long best = 0ull;
-            int bi = INT_MAX;
-            for (int i = lane; i < cnt; i += 32) {
-                const unsigned long long k =
-                    staged ? s_key[i]
-                           : select_key(__ldcg(A.conf_out + r0 + i), __ldg(A.row_pos + r0 + i));
-                if (k < prev && k > best) {
-                    best = k;
-                    bi = i;
-                }
-            }
-#pragma unroll
-            for (int off = 16; off; off >>= 1) {
-                const unsigned long long ok = __shfl_xor_sync(0xffffffffu, best, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (ok > best || (ok == best && oi < bi)) {
-                    best = ok;
-                    bi = oi;
-                }
-            }
-            if (best == 0ull) break;  // only with duplicate positions (invalid input)
-            if (lane == 0) s_sel[s] = bi;
-            prev = best;
-            ++nsel;
-        }
-        if (lane == 0) s_nsel = nsel;
-    }
-    consumers_sync();
-
-    const int nsel = s_nsel;
+    unsigned long long prev = ~0ull;
     float h = -INFINITY;
-    for (int s = tid; s < A.n_unmask; s += kConsumers) {
-        int32_t *slot = A.unmask_rows + static_cast<int64_t>(b) * A.n_unmask + s;
-        if (s < nsel) {
-            const int r = r0 + s_sel[s];
+    int nsel = 0;
+    for (int s = 0; s < take; ++s) {
+        unsigned long long best = 0ull;
+        int bi = INT_MAX;
+        for (int i = lane; i < cnt; i += 32) {
+            const unsigned long long k =
+                staged ? s_key[i]
+                       : select_key(__ldcg(A.conf_out + r0 + i), __ldg(A.row_pos + r0 + i));
+            if (k < prev && k > best) {
+                best = k;
+                bi = i;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            const unsigned long long ok = __shfl_xor_sync(0xffffffffu, best, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (ok > best || (ok == best && oi < bi)) {
+                best = ok;
+                bi = oi;
+            }
+        }
+        if (best == 0ull) break;  // only with duplicate positions (invalid input)
+        prev = best;
+        ++nsel;
+        if (lane == 0) {
+            const int r = r0 + bi;
             h = fmaxf(h, __ldcg(A.entropy_out + r));
-            const int tok = __ldcg(A.token_out + r);
             const int p = __ldg(A.row_pos + r);
-            *slot = r;
+            A.unmask_rows[static_cast<int64_t>(b) * A.n_unmask + s] = r;
             if (p >= 0 && p < A.seq_len) {
                 const int64_t at = static_cast<int64_t>(b) * A.seq_len + p;
                 A.is_masked[at] = 0;
-                A.seq_tokens[at] = tok;
+                A.seq_tokens[at] = __ldcg(A.token_out + r);
                 A.decode_step[at] = A.step;
             }
-        } else {
-            *slot = -1;
         }
     }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) h = fmaxf(h, __shfl_xor_sync(0xffffffffu, h, off));
-    if (lane == 0) s_wmax[warp] = h;
-    consumers_sync();
-    if (tid == 0) {
-        float e = s_wmax[0];
-        for (int w = 1; w < kConsumerWarps; ++w) e = fmaxf(e, s_wmax[w]);
-        A.max_entropy[b] = e;
-        A.refresh[b] = e > A.tau ? 1 : 0;
+    for (int s = nsel + lane; s < A.n_unmask; s += 32)
+        A.unmask_rows[static_cast<int64_t>(b) * A.n_unmask + s] = -1;
+    if (lane == 0) {
+        A.max_entropy[b] = h;
+        A.refresh[b] = h > A.tau ? 1 : 0;
     }
-    consumers_sync();  // s_key / s_sel / s_wmax may be reused by a later call
+    __syncwarp();  // s_key is reused by the next call
 }
 
-// A finished piece of row i: publish its partial; the row's last contributor
-// merges all of them, and the sequence's last row ranks and gates.  Returns true
-// (in every consumer thread alike) when some consumer warp gave up a wait.
-__device__ bool finish_piece(const Args &A, int i, Partial p, bool failed)
+// Finisher warp: for one finished piece of row i (its CTA partial p, in every
+// lane): publish it; the row's last contributor merges all of them and writes
+// token / conf / entropy; the sequence's last row ranks and gates.
+__device__ void finish_piece(const Args &A, int i, Partial p)
 {
-    __shared__ Partial s_part[kConsumerWarps];
-    __shared__ int s_flag, s_seq, s_lo, s_cnt;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (ptx::named_bar_or(kBarConsumers, kConsumers, failed)) return true;
-    warp_merge(p);
-    if (lane == 0) s_part[warp] = p;
-    consumers_sync();
+    const int lane = threadIdx.x & 31;
     const int c0 = cta_of(A, static_cast<int64_t>(i) * A.units);
     const int c1 = cta_of(A, static_cast<int64_t>(i) * A.units + A.units - 1);
     const int n_contrib = c1 - c0 + 1;
-    if (warp == 0) {
-        p = lane < kConsumerWarps ? s_part[lane] : empty_partial();
-        warp_merge(p);
+    int last = 1;
+    if (n_contrib > 1) {
         if (lane == 0) {
-            int last = 1;
-            if (n_contrib > 1) {
-                const int slot = static_cast<int>(blockIdx.x) - c0;
-                __stcg(reinterpret_cast<float4 *>(A.parts + static_cast<int64_t>(i) * kMaxSplits + slot),
-                       make_float4(p.m, p.s, p.t, __int_as_float(p.idx)));
-                __threadfence();
-                const unsigned ticket = atomicInc(A.row_ctr + i, static_cast<unsigned>(n_contrib - 1));
-                last = ticket == static_cast<unsigned>(n_contrib - 1);
-            }
-            s_flag = last;
+            const int slot = static_cast<int>(blockIdx.x) - c0;
+            __stcg(reinterpret_cast<float4 *>(A.parts + static_cast<int64_t>(i) * kMaxSplits + slot),
+                   make_float4(p.m, p.s, p.t, __int_as_float(p.idx)));
+            last = ticket(A.row_ctr + i, static_cast<unsigned>(n_contrib - 1)) ==
+                   static_cast<unsigned>(n_contrib - 1);
         }
-        __syncwarp();
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (!last) return;
         // the last contributor merges every slot in order
-        if (n_contrib > 1 && s_flag) {
-            __threadfence();
-            p = empty_partial();
-            for (int k = lane; k < n_contrib; k += 32) {
-                const float4 q4 = __ldcg(
-                    reinterpret_cast<const float4 *>(A.parts + static_cast<int64_t>(i) * kMaxSplits + k));
-                Partial q;
-                q.m = q4.x;
-                q.s = q4.y;
-                q.t = q4.z;
-                q.idx = __float_as_int(q4.w);
-                merge(p, q);
-            }
-            warp_merge(p);
+        p = empty_partial();
+        for (int k = lane; k < n_contrib; k += 32) {
+            const float4 q4 = __ldcg(
+                reinterpret_cast<const float4 *>(A.parts + static_cast<int64_t>(i) * kMaxSplits + k));
+            Partial q;
+            q.m = q4.x;
+            q.s = q4.y;
+            q.t = q4.z;
+            q.idx = __float_as_int(q4.w);
+            merge(p, q);
         }
-        if (lane == 0 && s_flag) {
-            // Sums are relative to mb = fl(m log2 e); for any reference point
-            // H = ln S - ln2 * T / S, and the argmax's own term is 2^{m log2 e - mb}.
-            const float S = p.s;
-            const float H = logf(S) - kLn2 * (p.t / S);
-            const float top = ex2(fmaf(p.m, kLog2e, -(p.m * kLog2e)));
-            A.entropy_out[i] = fmaxf(H, 0.f);
-            A.conf_out[i] = top / S;
-            A.token_out[i] = p.idx;
-            const int pos = __ldg(A.row_pos + i);
-            if (pos < 0 || pos >= A.seq_len) flag_status(A.status, EC_DEV_BAD_ROW_POS);
-            int lo = 0, cnt = 0, last_row = 0;
-            const int b = sequence_of(A, i, lo, cnt);
-            if (b < 0) {
-                flag_status(A.status, EC_DEV_BAD_OFFSETS);
-            } else {
-                __threadfence();
-                const unsigned ticket = atomicInc(A.seq_ctr + b, static_cast<unsigned>(cnt - 1));
-                last_row = ticket == static_cast<unsigned>(cnt - 1);
-            }
-            s_seq = last_row ? b : -1;
-            s_lo = lo;
-            s_cnt = cnt;
-        }
+        warp_merge(p);
     }
-    consumers_sync();
-    const int b = s_flag ? s_seq : -1;
-    if (b >= 0) {
-        __threadfence();
-        finish_sequence(A, b, s_lo, s_cnt);
+    int b = -1, lo = 0, cnt = 0, last_row = 0;
+    if (lane == 0) {
+        // Sums are relative to mb = fl(m log2 e); for any reference point
+        // H = ln S - ln2 * T / S, and the argmax's own term is 2^{m log2 e - mb}.
+        const float S = p.s;
+        const float H = logf(S) - kLn2 * (p.t / S);
+        const float top = ex2(fmaf(p.m, kLog2e, -(p.m * kLog2e)));
+        __stcg(A.entropy_out + i, fmaxf(H, 0.f));
+        __stcg(A.conf_out + i, top / S);
+        __stcg(A.token_out + i, p.idx);
+        const int pos = __ldg(A.row_pos + i);
+        if (pos < 0 || pos >= A.seq_len) flag_status(A.status, EC_DEV_BAD_ROW_POS);
+        b = sequence_of(A, i, lo, cnt);
+        if (b < 0)
+            flag_status(A.status, EC_DEV_BAD_OFFSETS);
+        else
+            last_row = ticket(A.seq_ctr + b, static_cast<unsigned>(cnt - 1)) ==
+                       static_cast<unsigned>(cnt - 1);
     }
-    consumers_sync();
-    return false;
+    last_row = __shfl_sync(0xffffffffu, last_row, 0);
+    if (!last_row) return;
+    b = __shfl_sync(0xffffffffu, b, 0);
+    lo = __shfl_sync(0xffffffffu, lo, 0);
+    cnt = __shfl_sync(0xffffffffu, cnt, 0);
+    finish_sequence(A, b, lo, cnt);
 }
 
 template <typename T>
@@ -452,46 +426,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t ring_u32 = ptx::smem_u32(ring);
     __shared__ int s_abort;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    __shared__ Partial s_piece[kPieceSlots][kConsumerWarps];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     Sync S{ring_u32 + kStages * kChunk, reinterpret_cast<volatile int *>(&s_abort), A.status};
 
     if (tid == 0) {
         s_abort = 0;
-        for (int i = 0; i < D_COUNT; ++i)
-            ptx::mbar_init(S.bar(i), i >= D_EMPTY ? static_cast<uint32_t>(kConsumerWarps) : 1u);
+        for (int i = 0; i < D_COUNT; ++i) {
+            uint32_t n = 1;
+            if ((i >= D_EMPTY && i < D_EMPTY + kStages) || (i >= D_PFULL && i < D_PFULL + kPieceSlots))
+                n = kConsumerWarps;
+            ptx::mbar_init(S.bar(i), n);
+        }
         ptx::fence_mbar_init();
     }
     __syncthreads();
 
-    // CTA 0 checks the offsets and finishes sequences that have no rows.
-    if (blockIdx.x == 0 && warp < kConsumerWarps) {
-        for (int b = tid; b <= A.batch; b += kConsumers) {
-            const int o = __ldg(A.offsets + b);
-            bool bad = (b == 0 && o != 0) || (b == A.batch && o != A.n_rows);
-            if (b < A.batch) {
-                const int o1 = __ldg(A.offsets + b + 1);
-                bad |= o1 < o;
-                if (o1 == o) {
-                    for (int s = 0; s < A.n_unmask; ++s)
-                        A.unmask_rows[static_cast<int64_t>(b) * A.n_unmask + s] = -1;
-                    A.max_entropy[b] = -INFINITY;
-                    A.refresh[b] = 0;
-                }
-            }
-            if (bad) flag_status(A.status, EC_DEV_BAD_OFFSETS);
-        }
-    }
-    if (A.total == 0) return;
-
-    const int64_t u_begin = range_begin(A, blockIdx.x);
-    const int64_t u_end = range_begin(A, blockIdx.x + 1);
-    if (u_begin >= u_end) return;
-    const int row_first = static_cast<int>(u_begin / A.units);
-    const int row_last = static_cast<int>((u_end - 1) / A.units);
+    const int64_t u_begin = A.total ? range_begin(A, blockIdx.x) : 0;
+    const int64_t u_end = A.total ? range_begin(A, blockIdx.x + 1) : 0;
+    const int row_first = static_cast<int>(u_begin / (A.units > 0 ? A.units : 1));
+    const int row_last = u_end > u_begin ? static_cast<int>((u_end - 1) / A.units) : row_first - 1;
 
     if (warp == kConsumerWarps) {
         // ---- producer: one thread streams the vector part of every row piece ----
-        if ((tid & 31) == 0) {
+        if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
             for (int i = row_first; i <= row_last && ok; ++i) {
@@ -516,20 +474,52 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
         return;
     }
 
-    // ---- consumers ----
-    uint32_t it = 0;
-    bool failed = false;  // warp-uniform: a wait of this warp gave up
-    for (int i = row_first; i <= row_last; ++i) {
+    if (warp == kConsumerWarps + 1) {
+        // ---- finisher: empty sequences (CTA 0), then every piece of this range ----
+        if (blockIdx.x == 0) {
+            for (int b = lane; b <= A.batch; b += 32) {
+                const int o = __ldg(A.offsets + b);
+                bool bad = (b == 0 && o != 0) || (b == A.batch && o != A.n_rows);
+                if (b < A.batch) {
+                    const int o1 = __ldg(A.offsets + b + 1);
+                    bad |= o1 < o;
+                    if (o1 == o) {
+                        for (int s = 0; s < A.n_unmask; ++s)
+                            A.unmask_rows[static_cast<int64_t>(b) * A.n_unmask + s] = -1;
+                        A.max_entropy[b] = -INFINITY;
+                        A.refresh[b] = 0;
+                    }
+                }
+                if (bad) flag_status(A.status, EC_DEV_BAD_OFFSETS);
+            }
+        }
+        uint32_t pc = 0;
+        for (int i = row_first; i <= row_last; ++i, ++pc) {
+            const int slot = pc % kPieceSlots;
+            if (!S.wait(D_PFULL + slot, (pc / kPieceSlots) & 1)) break;
+            Partial p = lane < kConsumerWarps ? s_piece[slot][lane] : empty_partial();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(S.bar(D_PEMPTY + slot));
+            warp_merge(p);
+            finish_piece(A, i, p);
+        }
+        return;
+    }
+
+    // ---- consumers: fold each stage, hand every finished piece to the finisher ----
+    uint32_t it = 0, pc = 0;
+    for (int i = row_first; i <= row_last; ++i, ++pc) {
         const int64_t base = static_cast<int64_t>(i) * A.units;
         const int64_t ua = max(u_begin, base) - base;
         const int64_t ub = min(u_end, base + A.units) - base;
         const int64_t vb = min(ub, A.nvec);
         Fold f;
         f.reset();
-        for (int64_t v = ua; v < vb && !failed; v += kVecPerChunk, ++it) {
+        bool ok = true;
+        for (int64_t v = ua; v < vb; v += kVecPerChunk, ++it) {
             const int s = it % kStages;
-            failed = !__all_sync(0xffffffffu, S.wait(D_FULL + s, (it / kStages) & 1));
-            if (failed) break;
+            ok = __all_sync(0xffffffffu, S.wait(D_FULL + s, (it / kStages) & 1));
+            if (!ok) break;
             const int nv = static_cast<int>(std::min<int64_t>(kVecPerChunk, vb - v));
             const uint4 *src = reinterpret_cast<const uint4 *>(ring + s * kChunk);
             uint4 raw[kVecPerThread];
@@ -540,13 +530,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
                 raw[u] = j < nv ? src[j] : make_uint4(ni, ni, ni, ni);
             }
             __syncwarp();
-            if ((tid & 31) == 0) ptx::mbar_arrive(S.bar(D_EMPTY + s));
+            if (lane == 0) ptx::mbar_arrive(S.bar(D_EMPTY + s));
             float x[kVecPerThread * E];
 #pragma unroll
             for (int u = 0; u < kVecPerThread; ++u) Elem<T>::unpack(raw[u], x + u * E);
             const int vb0 = static_cast<int>(v) + tid;
             f.add(x, [vb0](int k) { return (vb0 + (k / E) * kConsumers) * E + (k % E); });
         }
+        if (!ok) break;  // the finisher's wait gives up too, and the CTA unwinds
         // the tail unit (vocab % E last elements) belongs to the range holding it
         if (A.tail > 0 && ub == A.units && tid < A.tail) {
             const int j = static_cast<int>(A.nvec * E) + tid;
@@ -554,7 +545,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
             float x[1] = {Elem<T>::scalar(row + j)};
             f.add(x, [j](int) { return j; });
         }
-        if (finish_piece(A, i, f.partial(), failed)) break;  // aborted (same answer in every thread)
+        Partial p = f.partial();
+        warp_merge(p);
+        const int slot = pc % kPieceSlots;
+        if (pc >= static_cast<uint32_t>(kPieceSlots) &&
+            !__all_sync(0xffffffffu, S.wait(D_PEMPTY + slot, ((pc / kPieceSlots) - 1) & 1)))
+            break;
+        if (lane == 0) {
+            s_piece[slot][warp] = p;
+            ptx::mbar_arrive(S.bar(D_PFULL + slot));  // release: the partial is visible
+        }
     }
 }
 
