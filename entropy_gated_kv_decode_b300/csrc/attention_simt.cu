@@ -57,6 +57,8 @@ __global__ void scatter_kv_kernel(const uint4 *__restrict__ k_new, const uint4 *
                                   const int32_t *__restrict__ count, uint4 *k_cache,
                                   uint4 *v_cache, int L, int r_max, int row_vec, uint32_t *status)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int b = blockIdx.y, r = blockIdx.x;
     int c = __ldg(count + b);
     if (c < 0 || c > r_max) {
@@ -83,6 +85,8 @@ __global__ void __launch_bounds__(128) attention_simt_kernel(
     T *__restrict__ out, const int32_t *__restrict__ count, int L, int r_max, int H, int Hkv,
     float scale_log2)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int P = D / 32;
     const int b = blockIdx.y;
     const int lane = threadIdx.x & 31;
@@ -138,15 +142,10 @@ cudaError_t launch_simt_typed(const void *q, const void *kc, const void *vc, voi
     const int64_t warps = static_cast<int64_t>(r_max) * H;
     const dim3 grid(static_cast<unsigned>((warps + 3) / 4), static_cast<unsigned>(batch));
     const float sl2 = scale * kLog2e;
-    if (d == 128)
-        attention_simt_kernel<T, 128><<<grid, 128, 0, stream>>>(
-            static_cast<const T *>(q), static_cast<const T *>(kc), static_cast<const T *>(vc),
-            static_cast<T *>(out), count, L, r_max, H, Hkv, sl2);
-    else
-        attention_simt_kernel<T, 64><<<grid, 128, 0, stream>>>(
-            static_cast<const T *>(q), static_cast<const T *>(kc), static_cast<const T *>(vc),
-            static_cast<T *>(out), count, L, r_max, H, Hkv, sl2);
-    return cudaGetLastError();
+    auto kernel = d == 128 ? attention_simt_kernel<T, 128> : attention_simt_kernel<T, 64>;
+    return launch(kernel, grid, dim3(128), 0, stream, static_cast<const T *>(q),
+                  static_cast<const T *>(kc), static_cast<const T *>(vc), static_cast<T *>(out),
+                  count, L, r_max, H, Hkv, sl2);
 }
 
 }  // namespace
@@ -170,11 +169,10 @@ cudaError_t launch_scatter_kv(const void *k_new, const void *v_new, const int32_
     const int elem = dtype == EC_BF16 ? 2 : 4;
     const int row_vec = n_kv_heads * head_dim * elem / 16;
     const dim3 grid(static_cast<unsigned>(r_max), static_cast<unsigned>(batch));
-    scatter_kv_kernel<<<grid, 128, 0, stream>>>(
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), idx, idx_stride,
-        count, static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), seq_len, r_max,
-        row_vec, status);
-    return cudaGetLastError();
+    return launch(scatter_kv_kernel, grid, dim3(128), 0, stream,
+                  static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), idx,
+                  idx_stride, count, static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache),
+                  seq_len, r_max, row_vec, status);
 }
 
 cudaError_t launch_attention_simt(const void *q, const void *k_cache, const void *v_cache,

@@ -33,7 +33,8 @@
 //   warps 2-5  one thread per query row: online softmax in the log2 domain on S
 //              read by tcgen05.ld (the reference maximum moves only when it
 //              grows by more than 8 in log2 units, rescaling O in TMEM when it
-//              does), P as bf16 into shared memory, and the epilogue.
+//              does), P as bf16 into TMEM (the PV product takes its A operand
+//              from there), and the epilogue.
 // Every wait is bounded (~2 s); a timeout sets EC_DEV_TIMEOUT and unwinds.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -65,13 +66,15 @@ struct Cfg {
     static constexpr uint32_t kOffQ = 0;
     static constexpr uint32_t kOffK = kOffQ + kQBufs * kTile;
     static constexpr uint32_t kOffV = kOffK + kKStages * kTile;
-    static constexpr uint32_t kOffP = kOffV + kVStages * kTile;
-    static constexpr uint32_t kOffBar = kOffP + kBlockM * kBlockN * 2;
+    static constexpr uint32_t kOffScratch = kOffV + kVStages * kTile;  // split-merge weights
+    static constexpr uint32_t kOffBar = kOffScratch + kBlockM * 64 * 4;
     static constexpr uint32_t kOffMisc = kOffBar + 256;
     static constexpr uint32_t kBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1 KB
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColS = 0;    // two S buffers: columns [0, 128) and [128, 256)
     static constexpr uint32_t kColO = 256;  // O: columns [256, 256 + D)
+    static constexpr uint32_t kColP = 384;  // P (bf16 pairs): columns [384, 448)
+    static constexpr uint32_t kColQ = 448;  // Q (bf16 pairs): columns [448, 448 + D / 2)
 };
 
 enum : int {
@@ -80,7 +83,7 @@ enum : int {
     B_VFULL = 8,    // [3] V tile landed
     B_VEMPTY = 11,  // [3] V stage consumed (its PV done)
     B_QFULL = 14,   // [2] Q tile landed
-    B_QEMPTY = 16,  // [2] Q tile consumed (last QK of its piece done)
+    B_QEMPTY = 16,  // [2] Q tile copied into TMEM
     B_SFULL = 18,   // [2] S buffer written
     B_SFREE = 20,   // [2] S buffer read by the softmax warps
     B_PFULL = 22,   // P written, O corrected
@@ -161,12 +164,6 @@ __device__ __forceinline__ bool piece_active(const Params &P, const Piece &p)
     return p.mt * P.tok_per_tile < p.cnt && p.t1 > p.t0;
 }
 
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 __device__ __forceinline__ unsigned ticket(unsigned *ctr, unsigned last)
 {
     unsigned old;
@@ -174,6 +171,10 @@ __device__ __forceinline__ unsigned ticket(unsigned *ctr, unsigned last)
                  : "memory");
     return old;
 }
+
+static_assert(Cfg<128>::kColO + 128 <= Cfg<128>::kColP, "TMEM columns overlap");
+static_assert(Cfg<128>::kColP + kBlockN / 2 <= Cfg<128>::kColQ, "TMEM columns overlap");
+static_assert(Cfg<128>::kColQ + 128 / 2 <= Cfg<128>::kTmemCols, "TMEM columns overflow");
 
 // Q and K producer (one thread): per piece its Q tile, then its K tiles.
 template <int D>
@@ -184,7 +185,7 @@ __device__ void producer_qk(const Params &P, const Sync &S, uint32_t sbase, cons
     const uint32_t q_bytes = static_cast<uint32_t>(P.tok_per_tile * P.G) * D * 2;
     const Range r = my_range(P);
     uint32_t T = 0, it = 0;
-    bool ok = true, waited = false;
+    bool ok = true;
     for (int u = r.u_first; u <= r.u_last && ok; ++u) {
         const Piece w = make_piece(P, r, u);
         if (!piece_active(P, w)) continue;
@@ -198,10 +199,6 @@ __device__ void producer_qk(const Params &P, const Sync &S, uint32_t sbase, cons
             tma_load_4d(qdst + c * C::kCol, tm_q, S.bar(B_QFULL + qb), c * 64, w.g * P.G,
                         w.mt * P.tok_per_tile, w.b);
         ++it;
-        if (!waited) {  // the caches are read only after the write-back grid finished
-            pdl_wait();
-            waited = true;
-        }
         for (int t = w.t0; t < w.t1 && ok; ++t, ++T) {
             const int s = T % C::kKStages;
             if (T >= static_cast<uint32_t>(C::kKStages))
@@ -230,7 +227,6 @@ __device__ void producer_v(const Params &P, const Sync &S, uint32_t sbase, const
     const Range r = my_range(P);
     uint32_t T = 0;
     bool ok = true;
-    pdl_wait();
     for (int u = r.u_first; u <= r.u_last && ok; ++u) {
         const Piece w = make_piece(P, r, u);
         if (!piece_active(P, w)) continue;
@@ -270,11 +266,10 @@ __device__ void mma_issuer(const Params &P, const Sync &S, uint32_t sbase, uint3
         tc_fence_after();
         const uint32_t vbase = sbase + C::kOffV + s * C::kTile;
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            const uint64_t a =
-                desc_sw128(sbase + C::kOffP + (kk >> 2) * C::kCol + (kk & 3) * 32, 16, 1024);
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {  // P from TMEM, V from shared memory
             const uint64_t bd = desc_sw128(vbase + kk * 16 * 128, C::kCol, 1024);
-            umma_bf16(tmem + C::kColO, a, bd, kIdescPV, (!pv_first || kk > 0) ? 1u : 0u);
+            umma_bf16_ts(tmem + C::kColO, tmem + C::kColP + kk * 8, bd, kIdescPV,
+                         (!pv_first || kk > 0) ? 1u : 0u);
         }
         umma_commit(S.bar(B_VEMPTY + s));
         umma_commit(S.bar(B_PVDONE));
@@ -286,7 +281,15 @@ __device__ void mma_issuer(const Params &P, const Sync &S, uint32_t sbase, uint3
         const int qb = it % C::kQBufs;
         ok = S.wait(B_QFULL + qb, (it / C::kQBufs) & 1);
         if (!ok) break;
+        tc_fence_after();
+        // Q into TMEM once per piece (after the previous piece's last QK, in issue
+        // order); its shared-memory buffer is free for the next piece's Q after that
         const uint32_t qbase = sbase + C::kOffQ + qb * C::kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+            tmem_copy_128x256b(tmem + C::kColQ + kk * 8,
+                               desc_sw128(qbase + (kk >> 2) * C::kCol + (kk & 3) * 32, 16, 1024));
+        umma_commit(S.bar(B_QEMPTY + qb));
         for (int t = w.t0; t < w.t1; ++t, ++T) {
             const int s = T % C::kKStages, sb = T & 1;
             ok = S.wait(B_KFULL + s, (T / C::kKStages) & 1);
@@ -295,14 +298,13 @@ __device__ void mma_issuer(const Params &P, const Sync &S, uint32_t sbase, uint3
             tc_fence_after();
             const uint32_t kbase = sbase + C::kOffK + s * C::kTile;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int kk = 0; kk < D / 16; ++kk) {  // Q from TMEM, K from shared memory
                 const uint32_t off = (kk >> 2) * C::kCol + (kk & 3) * 32;
-                umma_bf16(tmem + C::kColS + sb * kBlockN, desc_sw128(qbase + off, 16, 1024),
-                          desc_sw128(kbase + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+                umma_bf16_ts(tmem + C::kColS + sb * kBlockN, tmem + C::kColQ + kk * 8,
+                             desc_sw128(kbase + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
             }
             umma_commit(S.bar(B_SFULL + sb));
             umma_commit(S.bar(B_KEMPTY + s));
-            if (t == w.t1 - 1) umma_commit(S.bar(B_QEMPTY + qb));
             if (pv_pending) issue_pv();
             if (!ok) break;
             pv_pending = true;
@@ -346,61 +348,81 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
     return d;
 }
 
-// Merge of a unit's n partials (last contributor), by the 128 softmax threads:
-// work items (row, 32-column chunk); every load of an item is issued before use.
+// Merge of a unit's n partials (last contributor), by the 128 softmax threads.
+// Phase 1, one thread per row: the weight of every partial, w_s = 2^{(m_s - m) c}
+// / sum_s 2^{(m_s - m) c} l_s with m the largest m_s, into a shared-memory
+// scratch region.  Phase 2, work items (row,
+// 32-column chunk): the partials are read four at a time with every load issued
+// before use.
 template <int D>
-__device__ void merge_unit(const Params &P, const Piece &w, int ltid)
+__device__ void merge_unit(const Params &P, const Piece &w, int ltid, float *s_w)
 {
     constexpr int kChunks = D / 32;
     const int n = w.n_contrib;
     const int rows = min(kBlockM, P.tok_per_tile * P.G);
     const float2 *ml = P.part_ml + static_cast<int64_t>(w.unit) * P.slots * kBlockM;
     const float4 *po = P.part_o + static_cast<int64_t>(w.unit) * P.slots * (D / 4) * kBlockM;
-    for (int item = ltid; item < rows * kChunks; item += 128) {
-        const int row = item % rows, ch = item / rows;
-        const int tok = w.mt * P.tok_per_tile + row / P.G;
-        if (tok >= w.cnt) continue;
+    const int row_valid_max = min(rows, (w.cnt - w.mt * P.tok_per_tile) * P.G);
+    if (ltid < row_valid_max) {
         float m_all = -INFINITY;
-        for (int s = 0; s < n; ++s) m_all = fmaxf(m_all, __ldcg(ml + s * kBlockM + row).x);
+        for (int s = 0; s < n; ++s) m_all = fmaxf(m_all, __ldcg(ml + s * kBlockM + ltid).x);
+        float l_tot = 0.f;
+        for (int s = 0; s < n; ++s) {
+            const float2 v = __ldcg(ml + s * kBlockM + ltid);
+            const float e = ex2((v.x - m_all) * P.scale_log2);
+            s_w[ltid * kMaxContrib + s] = e;
+            l_tot = fmaf(e, v.y, l_tot);
+        }
+        const float inv = 1.f / l_tot;
+        for (int s = 0; s < n; ++s) s_w[ltid * kMaxContrib + s] *= inv;
+    }
+    named_bar_sync(1, 128);
+    for (int item = ltid; item < row_valid_max * kChunks; item += 128) {
+        const int row = item % row_valid_max, ch = item / row_valid_max;
+        const int tok = w.mt * P.tok_per_tile + row / P.G;
         float acc[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-        float l_tot = 0.f;
-        for (int s = 0; s < n; ++s) {
-            const float2 mls = __ldcg(ml + s * kBlockM + row);
-            const float f = ex2((mls.x - m_all) * P.scale_log2);
-            l_tot = fmaf(f, mls.y, l_tot);
-            const float4 *src = po + (static_cast<int64_t>(s) * (D / 4) + ch * 8) * kBlockM + row;
-            float4 x[8];
+        for (int s0 = 0; s0 < n; s0 += 4) {
+            float4 x[4][8];
+            float f[4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) x[q] = __ldcg(src + q * kBlockM);
+            for (int k = 0; k < 4; ++k) {
+                const int s = s0 + k;
+                f[k] = s < n ? s_w[row * kMaxContrib + s] : 0.f;
+                const float4 *src =
+                    po + (static_cast<int64_t>(s < n ? s : s0) * (D / 4) + ch * 8) * kBlockM + row;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                acc[4 * q] = fmaf(f, x[q].x, acc[4 * q]);
-                acc[4 * q + 1] = fmaf(f, x[q].y, acc[4 * q + 1]);
-                acc[4 * q + 2] = fmaf(f, x[q].z, acc[4 * q + 2]);
-                acc[4 * q + 3] = fmaf(f, x[q].w, acc[4 * q + 3]);
+                for (int q = 0; q < 8; ++q) x[k][q] = __ldcg(src + q * kBlockM);
             }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    acc[4 * q] = fmaf(f[k], x[k][q].x, acc[4 * q]);
+                    acc[4 * q + 1] = fmaf(f[k], x[k][q].y, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(f[k], x[k][q].z, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(f[k], x[k][q].w, acc[4 * q + 3]);
+                }
         }
-        const float inv = 1.f / l_tot;
         const int h = w.g * P.G + row % P.G;
-        __nv_bfloat16 *orow =
-            P.out + ((static_cast<int64_t>(w.b) * P.r_max + tok) * P.H + h) * D + ch * 32;
-        uint4 *dst = reinterpret_cast<uint4 *>(orow);
+        uint4 *dst = reinterpret_cast<uint4 *>(
+            P.out + ((static_cast<int64_t>(w.b) * P.r_max + tok) * P.H + h) * D + ch * 32);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            uint4 v;
-            v.x = pack_bf16x2(acc[8 * q] * inv, acc[8 * q + 1] * inv);
-            v.y = pack_bf16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv);
-            v.z = pack_bf16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv);
-            v.w = pack_bf16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv);
-            dst[q] = v;
+            uint4 o;
+            o.x = pack_bf16x2(acc[8 * q], acc[8 * q + 1]);
+            o.y = pack_bf16x2(acc[8 * q + 2], acc[8 * q + 3]);
+            o.z = pack_bf16x2(acc[8 * q + 4], acc[8 * q + 5]);
+            o.w = pack_bf16x2(acc[8 * q + 6], acc[8 * q + 7]);
+            dst[q] = o;
         }
     }
 }
 
 template <int D>
-__device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem)
+__device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem,
+                                 uint8_t *smem_generic)
 {
     using C = Cfg<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -492,7 +514,7 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase,
             l_run = l_run * alpha + rowsum;
             m_run = m_use;
 
-            // P buffer and O are free once the previous PV of this piece completed
+            // the P columns and O are free once the previous PV of this piece completed
             // (for a piece's first tile the previous epilogue already waited).
             if (t > w.t0) {
                 ok = __all_sync(0xffffffffu, S.wait(B_PVDONE, (T - 1) & 1));
@@ -512,11 +534,10 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase,
                 }
                 tmem_wait_st();
             }
-#pragma unroll
-            for (int ch = 0; ch < kBlockN / 8; ++ch)
-                st_shared_v4(sbase + C::kOffP + sw128_offset(row, ch, C::kCol), pk[4 * ch],
-                             pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            fence_async_smem();
+            // P (bf16 pairs) into this row's TMEM lane; the PV product reads it there
+            tmem_st32(tmem + lane_off + C::kColP, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+            tmem_st32(tmem + lane_off + C::kColP + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(S.bar(B_PFULL));
@@ -578,7 +599,8 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase,
             s_last = ticket(P.tickets + w.unit, static_cast<unsigned>(w.n_contrib - 1)) ==
                      static_cast<unsigned>(w.n_contrib - 1);
         named_bar_sync(1, 128);
-        if (!failed && s_last) merge_unit<D>(P, w, ltid);
+        if (!failed && s_last)
+            merge_unit<D>(P, w, ltid, reinterpret_cast<float *>(smem_generic + C::kOffScratch));
         named_bar_sync(1, 128);  // s_last is rewritten by the next piece
     }
 }
@@ -588,6 +610,7 @@ template <int D>
 __global__ void __launch_bounds__(256) write_back_kernel(const Params P)
 {
     pdl_launch_dependents();
+    pdl_wait();
     constexpr int kChunks = D / 8;
     const int64_t total = static_cast<int64_t>(P.B) * P.r_max * P.Hkv * kChunks;
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
@@ -633,6 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 16);
     Sync S{sbase + C::kOffBar, abort_flag, P.status};
 
+    pdl_launch_dependents();
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         for (int i = 0; i < B_COUNT; ++i)
@@ -647,27 +671,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
+    if (warp == 0 && (threadIdx.x & 31) == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();  // the write-back grid (and everything before it) has completed
 
     if (warp == 0 || warp == 6) {
         if ((threadIdx.x & 31) == 0) {
-            if (warp == 0) {
-                prefetch_tmap(&tm_q);
-                prefetch_tmap(&tm_k);
+            if (warp == 0)
                 producer_qk<D>(P, S, sbase, &tm_q, &tm_k);
-            } else {
-                prefetch_tmap(&tm_v);
+            else
                 producer_v<D>(P, S, sbase, &tm_v);
-            }
         }
         __syncwarp();
     } else if (warp == 1) {
         if ((threadIdx.x & 31) == 0) mma_issuer<D>(P, S, sbase, tmem);
         __syncwarp();
     } else {
-        softmax_epilogue<D>(P, S, sbase, tmem);
+        softmax_epilogue<D>(P, S, sbase, tmem, smem);
     }
     __syncthreads();
     if (warp == 1) {
@@ -756,35 +782,15 @@ cudaError_t launch_typed(const Params &p, const Plan &plan, const void *q, cudaS
         !encode_4d(&tk, p.k_cache, p.B, p.L, p.Hkv, D, 1, kBlockN) ||
         !encode_4d(&tv, p.v_cache, p.B, p.L, p.Hkv, D, 1, kBlockN))
         return cudaErrorInvalidValue;
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<D>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(Cfg<D>::kBytes));
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = 1;
-    }
     // 1. write-back: a few CTAs per SM over the fresh rows
     const int64_t chunks = static_cast<int64_t>(p.B) * p.r_max * p.Hkv * (D / 8);
     const int wb_grid = static_cast<int>(std::max<int64_t>(
         1, std::min<int64_t>((chunks + 255) / 256, 4 * static_cast<int64_t>(device_sm_count()))));
-    write_back_kernel<D><<<wb_grid, 256, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch(write_back_kernel<D>, dim3(wb_grid), dim3(256), 0, stream, p);
     if (e != cudaSuccess) return e;
-    // 2. attention, allowed to start before the write-back finishes (PDL)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg<D>::kBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attention_tc_kernel<D>, p, tq, tk, tv);
+    // 2. attention; its set-up overlaps the write-back (programmatic dependent launch)
+    return launch(attention_tc_kernel<D>, dim3(plan.grid), dim3(kThreads), Cfg<D>::kBytes, stream,
+                  p, tq, tk, tv);
 }
 
 }  // namespace

@@ -161,14 +161,46 @@ struct Elem<uint16_t> {
     }
 };
 
-// Running fold state of one thread.
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t pack2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Running fold state of one thread (scalar sums for fp32 input, two-wide sums
+// s2 / t2 for bf16 input; a partial adds both).
 struct Fold {
     float m, s0, s1, t0, t1;
+    uint64_t s2, t2;
     int a;
     __device__ void reset()
     {
         m = -INFINITY;
         s0 = s1 = t0 = t1 = 0.f;
+        s2 = t2 = 0ull;
         a = INT_MAX;
     }
     // Fold elements x[0..N) with row indices index_of(i) (increasing in i;
@@ -184,15 +216,20 @@ struct Fold {
 #pragma unroll
             for (int i = N - 1; i >= 0; --i)
                 if (x[i] == cm) first = index_of(i);
-            const float s = s0 + s1;
+            float s_lo, s_hi, t_lo, t_hi;
+            unpack2(s2, s_lo, s_hi);
+            unpack2(t2, t_lo, t_hi);
+            const float s = (s0 + s1) + (s_lo + s_hi);
+            const float t = (t0 + t1) + (t_lo + t_hi);
+            s1 = t1 = 0.f;
+            s2 = t2 = 0ull;
             if (s > 0.f) {
                 const float d = m * kLog2e - cm * kLog2e;
                 const float f = ex2(d);
-                const float t = t0 + t1;
                 t0 = f * fmaf(d, s, t);
-                t1 = 0.f;
                 s0 = f * s;
-                s1 = 0.f;
+            } else {
+                s0 = t0 = 0.f;
             }
             m = cm;
             a = first;
@@ -212,12 +249,68 @@ struct Fold {
             }
         }
     }
+    // bf16 words w[0..N) (element 2i in the low half of w[i], 2i+1 in the high
+    // half), row index of element k = index_of(k).  Two-wide math: the batch
+    // maximum on packed bf16 pairs, the exponent argument, S and T with f32x2
+    // FMA / add.  -inf elements are clamped to -1e30 (an unsigned 16-bit minimum
+    // on the bit patterns) only after a finite maximum exists, so their weights
+    // 2^{(x - m) log2 e} underflow to exact zeros.
+    template <int N, typename IndexOf>
+    __device__ __forceinline__ void add_bf16(const uint32_t (&w)[N], IndexOf index_of)
+    {
+        uint32_t mw = w[0];
+#pragma unroll
+        for (int i = 1; i < N; ++i) mw = bf16x2_max(mw, w[i]);
+        const float cm = fmaxf(__uint_as_float(mw << 16), __uint_as_float(mw & 0xffff0000u));
+        if (cm > m) {  // rare after the first elements: new maximum, rescale the sums
+            int first = INT_MAX;
+#pragma unroll
+            for (int i = N - 1; i >= 0; --i) {
+                if (__uint_as_float(w[i] & 0xffff0000u) == cm) first = index_of(2 * i + 1);
+                if (__uint_as_float(w[i] << 16) == cm) first = index_of(2 * i);
+            }
+            float s_lo, s_hi, t_lo, t_hi;
+            unpack2(s2, s_lo, s_hi);
+            unpack2(t2, t_lo, t_hi);
+            const float s = s0 + s1 + s_lo + s_hi;
+            float t = t0 + t1 + t_lo + t_hi;
+            s0 = s1 = t0 = t1 = 0.f;
+            if (s > 0.f) {
+                const float d = m * kLog2e - cm * kLog2e;
+                const float fct = ex2(d);
+                t = fct * fmaf(d, s, t);
+                s2 = pack2(fct * s, 0.f);
+                t2 = pack2(t, 0.f);
+            } else {
+                s2 = t2 = 0ull;
+            }
+            m = cm;
+            a = first;
+        }
+        if (m == -INFINITY) return;  // nothing but -inf so far: every weight is zero
+        const float mb = m * kLog2e;
+        const uint64_t l2e = pack2(kLog2e, kLog2e), nmb = pack2(-mb, -mb);
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const uint32_t c = __vminu2(w[i], 0xf14af14au);  // -inf (0xff80) -> -1e30 (0xf14a)
+            const uint64_t y2 = ffma2(pack2(__uint_as_float(c << 16), __uint_as_float(c & 0xffff0000u)),
+                                      l2e, nmb);
+            float y0, y1;
+            unpack2(y2, y0, y1);
+            const uint64_t e2 = pack2(ex2(y0), ex2(y1));
+            s2 = fadd2(s2, e2);
+            t2 = ffma2(e2, y2, t2);
+        }
+    }
     __device__ Partial partial() const
     {
+        float s_lo, s_hi, t_lo, t_hi;
+        unpack2(s2, s_lo, s_hi);
+        unpack2(t2, t_lo, t_hi);
         Partial p;
         p.m = m;
-        p.s = s0 + s1;
-        p.t = t0 + t1;
+        p.s = (s0 + s1) + (s_lo + s_hi);
+        p.t = (t0 + t1) + (t_lo + t_hi);
         p.idx = a;
         if (p.s == 0.f) p = empty_partial();
         return p;
@@ -266,16 +359,20 @@ __device__ __forceinline__ unsigned long long select_key(float conf, int pos)
 }
 
 // The sequence holding row i (rows of a sequence are contiguous), or -1 when the
-// offsets do not place it in a well-formed range.
+// offsets do not place it in a well-formed range.  Whole warp: a 32-way search
+// (one load per lane per round), the same answer in every lane.
 __device__ int sequence_of(const Args &A, int i, int &lo, int &cnt)
 {
-    int a = 0, z = A.batch;  // find the last b with offsets[b] <= i
+    const int lane = threadIdx.x & 31;
+    int a = 0, z = A.batch;  // the answer is the last b in [a, z) with offsets[b] <= i
     while (z - a > 1) {
-        const int mid = (a + z) >> 1;
-        if (__ldg(A.offsets + mid) <= i)
-            a = mid;
-        else
-            z = mid;
+        const int step = (z - a + 31) / 32;
+        const int b = a + lane * step;
+        const bool le = b < z && __ldg(A.offsets + b) <= i;
+        const unsigned mask = __ballot_sync(0xffffffffu, le);
+        const int k = mask ? 31 - __clz(static_cast<int>(mask)) : 0;
+        a = a + k * step;
+        z = min(z, a + step);
     }
     const int o0 = __ldg(A.offsets + a), o1 = __ldg(A.offsets + a + 1);
     if (o0 < 0 || o1 > A.n_rows || o0 > i || i >= o1) return -1;
@@ -299,6 +396,7 @@ __device__ __forceinline__ unsigned ticket(unsigned *ctr, unsigned last)
 __device__ void finish_sequence(const Args &A, int b, int r0, int cnt)
 {
     __shared__ unsigned long long s_key[kMaxStagedRows];
+    __shared__ int s_sel[kMaxUnmask];
     const int lane = threadIdx.x & 31;
     const bool staged = cnt <= kMaxStagedRows;
     if (staged)
@@ -308,7 +406,6 @@ __device__ void finish_sequence(const Args &A, int b, int r0, int cnt)
 
     const int take = min(A.n_unmask, cnt);
     unsigned long long prev = ~0ull;
-    float h = -INFINITY;
     int nsel = 0;
     for (int s = 0; s < take; ++s) {
         unsigned long long best = 0ull;
@@ -332,28 +429,38 @@ __device__ void finish_sequence(const Args &A, int b, int r0, int cnt)
             }
         }
         if (best == 0ull) break;  // only with duplicate positions (invalid input)
+        if (lane == 0) s_sel[s] = bi;
         prev = best;
         ++nsel;
-        if (lane == 0) {
-            const int r = r0 + bi;
+    }
+    __syncwarp();
+    // the selected rows' state updates and the maximum entropy, lanes in parallel
+    float h = -INFINITY;
+    for (int s = lane; s < A.n_unmask; s += 32) {
+        int32_t *slot = A.unmask_rows + static_cast<int64_t>(b) * A.n_unmask + s;
+        if (s < nsel) {
+            const int r = r0 + s_sel[s];
             h = fmaxf(h, __ldcg(A.entropy_out + r));
+            const int tok = __ldcg(A.token_out + r);
             const int p = __ldg(A.row_pos + r);
-            A.unmask_rows[static_cast<int64_t>(b) * A.n_unmask + s] = r;
+            *slot = r;
             if (p >= 0 && p < A.seq_len) {
                 const int64_t at = static_cast<int64_t>(b) * A.seq_len + p;
                 A.is_masked[at] = 0;
-                A.seq_tokens[at] = __ldcg(A.token_out + r);
+                A.seq_tokens[at] = tok;
                 A.decode_step[at] = A.step;
             }
+        } else {
+            *slot = -1;
         }
     }
-    for (int s = nsel + lane; s < A.n_unmask; s += 32)
-        A.unmask_rows[static_cast<int64_t>(b) * A.n_unmask + s] = -1;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) h = fmaxf(h, __shfl_xor_sync(0xffffffffu, h, off));
     if (lane == 0) {
         A.max_entropy[b] = h;
         A.refresh[b] = h > A.tau ? 1 : 0;
     }
-    __syncwarp();  // s_key is reused by the next call
+    __syncwarp();  // s_key / s_sel are reused by the next call
 }
 
 // Finisher warp: for one finished piece of row i (its CTA partial p, in every
@@ -390,7 +497,8 @@ __device__ void finish_piece(const Args &A, int i, Partial p)
         }
         warp_merge(p);
     }
-    int b = -1, lo = 0, cnt = 0, last_row = 0;
+    int lo = 0, cnt = 0, last_row = 0;
+    const int b = sequence_of(A, i, lo, cnt);
     if (lane == 0) {
         // Sums are relative to mb = fl(m log2 e); for any reference point
         // H = ln S - ln2 * T / S, and the argmax's own term is 2^{m log2 e - mb}.
@@ -400,20 +508,17 @@ __device__ void finish_piece(const Args &A, int i, Partial p)
         __stcg(A.entropy_out + i, fmaxf(H, 0.f));
         __stcg(A.conf_out + i, top / S);
         __stcg(A.token_out + i, p.idx);
-        const int pos = __ldg(A.row_pos + i);
-        if (pos < 0 || pos >= A.seq_len) flag_status(A.status, EC_DEV_BAD_ROW_POS);
-        b = sequence_of(A, i, lo, cnt);
         if (b < 0)
             flag_status(A.status, EC_DEV_BAD_OFFSETS);
         else
             last_row = ticket(A.seq_ctr + b, static_cast<unsigned>(cnt - 1)) ==
                        static_cast<unsigned>(cnt - 1);
+    } else if (lane == 1) {
+        const int pos = __ldg(A.row_pos + i);
+        if (pos < 0 || pos >= A.seq_len) flag_status(A.status, EC_DEV_BAD_ROW_POS);
     }
     last_row = __shfl_sync(0xffffffffu, last_row, 0);
     if (!last_row) return;
-    b = __shfl_sync(0xffffffffu, b, 0);
-    lo = __shfl_sync(0xffffffffu, lo, 0);
-    cnt = __shfl_sync(0xffffffffu, cnt, 0);
     finish_sequence(A, b, lo, cnt);
 }
 
@@ -430,6 +535,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     Sync S{ring_u32 + kStages * kChunk, reinterpret_cast<volatile int *>(&s_abort), A.status};
 
+    pdl_launch_dependents();
     if (tid == 0) {
         s_abort = 0;
         for (int i = 0; i < D_COUNT; ++i) {
@@ -441,6 +547,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
         ptx::fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();  // inputs and outputs belong to the previous kernel until here
 
     const int64_t u_begin = A.total ? range_begin(A, blockIdx.x) : 0;
     const int64_t u_end = A.total ? range_begin(A, blockIdx.x + 1) : 0;
@@ -531,11 +638,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(S.bar(D_EMPTY + s));
-            float x[kVecPerThread * E];
-#pragma unroll
-            for (int u = 0; u < kVecPerThread; ++u) Elem<T>::unpack(raw[u], x + u * E);
             const int vb0 = static_cast<int>(v) + tid;
-            f.add(x, [vb0](int k) { return (vb0 + (k / E) * kConsumers) * E + (k % E); });
+            if constexpr (sizeof(T) == 2) {
+                uint32_t wv[kVecPerThread * 4];
+#pragma unroll
+                for (int u = 0; u < kVecPerThread; ++u) {
+                    wv[4 * u] = raw[u].x;
+                    wv[4 * u + 1] = raw[u].y;
+                    wv[4 * u + 2] = raw[u].z;
+                    wv[4 * u + 3] = raw[u].w;
+                }
+                f.add_bf16(wv, [vb0](int k) { return (vb0 + (k / E) * kConsumers) * E + (k % E); });
+            } else {
+                float x[kVecPerThread * E];
+#pragma unroll
+                for (int u = 0; u < kVecPerThread; ++u) Elem<T>::unpack(raw[u], x + u * E);
+                f.add(x, [vb0](int k) { return (vb0 + (k / E) * kConsumers) * E + (k % E); });
+            }
         }
         if (!ok) break;  // the finisher's wait gives up too, and the CTA unwinds
         // the tail unit (vocab % E last elements) belongs to the range holding it
@@ -628,24 +747,10 @@ cudaError_t launch_decode_gate(const void *logits, int dtype, int64_t row_stride
     off = align_up(off + static_cast<size_t>(batch) * sizeof(unsigned), 256);
     A.parts = reinterpret_cast<Partial *>(ws + off);
 
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_gate_kernel<uint16_t>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDyn);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_gate_kernel<float>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDyn);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = 1;
-    }
-    const unsigned grid = static_cast<unsigned>(A.grid);
+    const dim3 grid(static_cast<unsigned>(A.grid));
     if (dtype == EC_BF16)
-        decode_gate_kernel<uint16_t><<<grid, kThreads, kSmemDyn, stream>>>(A);
-    else
-        decode_gate_kernel<float><<<grid, kThreads, kSmemDyn, stream>>>(A);
-    return cudaGetLastError();
+        return launch(decode_gate_kernel<uint16_t>, grid, dim3(kThreads), kSmemDyn, stream, A);
+    return launch(decode_gate_kernel<float>, grid, dim3(kThreads), kSmemDyn, stream, A);
 }
 
 }  // namespace ec

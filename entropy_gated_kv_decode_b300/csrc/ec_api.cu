@@ -2,9 +2,37 @@
 // Every check here runs on the host before anything is enqueued.
 #include <math.h>
 
+#include <mutex>
+
 #include "ec_internal.cuh"
 
 namespace ec {
+
+cudaError_t configure_kernel(const void *kernel, int dynamic_smem)
+{
+    struct Done {
+        const void *kernel;
+        int dev;
+    };
+    static std::mutex mu;
+    static Done done[256];
+    static int n_done = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done[i].kernel == kernel && done[i].dev == dev) return cudaSuccess;
+    if (dynamic_smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dynamic_smem);
+        if (e != cudaSuccess) return e;
+    }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    if (n_done < 256) done[n_done++] = Done{kernel, dev};
+    return cudaSuccess;
+}
 
 int device_sm_count()
 {

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "ec.h"
 
 namespace ec {
@@ -41,6 +43,43 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
 }
 
 int device_sm_count();  // SM count of the current device (cached per device)
+
+// ---- launches ----
+// Every kernel of the library is launched with programmatic dependent launch:
+// it may start while the previous kernel on the stream is still running.  Its
+// CTAs first do their set-up that touches no global memory (barriers, TMEM,
+// tensor-map prefetch), then pdl_wait() until the previous grid has completed
+// and its writes are visible, and only then read or write global memory.  Each
+// kernel calls pdl_launch_dependents() on entry so the next one can start early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Per (kernel, device), once: the dynamic shared-memory limit (when above the
+// default) and the largest shared-memory carveout, so that SMs need no
+// reconfiguration between the library's kernels.
+cudaError_t configure_kernel(const void *kernel, int dynamic_smem);
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                   cudaStream_t stream, Args &&...args)
+{
+    cudaError_t e = configure_kernel(reinterpret_cast<const void *>(kernel), static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- launchers (each returns cudaSuccess or the launch error) ----
 

@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 16);
     Sync S{sbase + C::kOffBar, abort_flag, P.status};
 
+    pdl_launch_dependents();
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         for (int i = 0; i < G_COUNT; ++i) mbar_init(S.bar(i), (i == G_ACC_EMPTY || i == G_ACC_EMPTY + 1) ? 4u : 1u);
@@ -224,16 +225,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
+    if (warp == 0 && (threadIdx.x & 31) == 0) {
+        prefetch_tmap(&tm_x);
+        prefetch_tmap(&tm_w);
+    }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();  // inputs and outputs belong to the previous kernel until here
 
     if (warp == 0) {
-        if ((threadIdx.x & 31) == 0) {
-            prefetch_tmap(&tm_x);
-            prefetch_tmap(&tm_w);
-            gemm_producer<BN>(P, S, sbase, &tm_x, &tm_w);
-        }
+        if ((threadIdx.x & 31) == 0) gemm_producer<BN>(P, S, sbase, &tm_x, &tm_w);
         __syncwarp();
     } else if (warp == 1) {
         if ((threadIdx.x & 31) == 0) gemm_mma<BN>(P, S, sbase, tmem);
@@ -310,19 +312,8 @@ cudaError_t launch_bn(GemmParams p, const void *x, const void *w, cudaStream_t s
     const cuuint64_t ws[1] = {static_cast<cuuint64_t>(p.hidden) * 2};
     const cuuint32_t wbx[2] = {kBK, BN};
     if (!encode(&tx, x, 3, xd, xs, xb) || !encode(&tw, w, 2, wd, ws, wbx)) return cudaErrorInvalidValue;
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(qkv_gemm_kernel<BN>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(C::kBytes));
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = 1;
-    }
     const int grid = std::min(p.n_tiles, device_sm_count());
-    qkv_gemm_kernel<BN><<<grid, kThreads, C::kBytes, stream>>>(p, tx, tw);
-    return cudaGetLastError();
+    return launch(qkv_gemm_kernel<BN>, dim3(grid), dim3(kThreads), C::kBytes, stream, p, tx, tw);
 }
 
 // ---- embedding gather ----
@@ -335,6 +326,8 @@ __global__ void embed_rows_kernel(const uint4 *__restrict__ table, int64_t table
                                   const uint8_t *__restrict__ is_masked, int32_t mask_id, int L,
                                   int r_max, uint4 *__restrict__ x, uint32_t *status)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int b = blockIdx.y;
     const int c = max(0, min(__ldg(count + b), r_max));
     for (int r = blockIdx.x; r < c; r += gridDim.x) {
@@ -395,11 +388,9 @@ cudaError_t launch_embed_rows(const void *table, int64_t table_rows, int32_t hid
     const int row_vec = hidden * 2 / 16;
     const dim3 grid(static_cast<unsigned>(std::min(r_max, 4 * device_sm_count())),
                     static_cast<unsigned>(batch));
-    embed_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4 *>(table), table_rows,
-                                                row_vec, idx, idx_stride, count, seq_tokens,
-                                                is_masked, mask_id, seq_len, r_max,
-                                                static_cast<uint4 *>(x), status);
-    return cudaGetLastError();
+    return launch(embed_rows_kernel, grid, dim3(256), 0, stream,
+                  static_cast<const uint4 *>(table), table_rows, row_vec, idx, idx_stride, count,
+                  seq_tokens, is_masked, mask_id, seq_len, r_max, static_cast<uint4 *>(x), status);
 }
 
 }  // namespace ec

@@ -92,6 +92,8 @@ __global__ void __launch_bounds__(kThreads) recompute_set_kernel(
 {
     __shared__ int s_red[kWarps];
     __shared__ uint32_t s_scan[kWarps];
+    pdl_launch_dependents();
+    pdl_wait();
     const int b = blockIdx.x, tid = threadIdx.x;
     const uint8_t *im = is_masked + static_cast<int64_t>(b) * L;
     const int32_t *ds = decode_step + static_cast<int64_t>(b) * L;
@@ -176,9 +178,8 @@ cudaError_t launch_recompute_set(const uint8_t *is_masked, const int32_t *decode
                                  int32_t block_lo, int32_t block_hi, int32_t k, int32_t *idx,
                                  int32_t *count, cudaStream_t stream)
 {
-    recompute_set_kernel<<<batch, kThreads, 0, stream>>>(is_masked, decode_step, refresh, seq_len,
-                                                         block_lo, block_hi, k, idx, count);
-    return cudaGetLastError();
+    return launch(recompute_set_kernel, dim3(batch), dim3(kThreads), 0, stream, is_masked,
+                  decode_step, refresh, seq_len, block_lo, block_hi, k, idx, count);
 }
 
 }  // namespace ec

@@ -224,6 +224,25 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]; A is M lanes x (K / 2) columns of bf16 pairs
+// (row i in lane i, elements 2c and 2c+1 of the K slice in column c).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Copy a 128-row x 256-bit slice (16 bf16 of K per row) of a shared-memory
+// matrix, given by its descriptor, into TMEM lanes 0..127, 8 columns from taddr:
+// the layout a tcgen05.mma A operand in TMEM takes.  Ordered with the MMAs
+// this thread issues.
+__device__ __forceinline__ void tmem_copy_128x256b(uint32_t taddr, uint64_t s_desc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
 // Arrive on an mbarrier once every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
