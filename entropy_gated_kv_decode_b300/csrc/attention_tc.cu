@@ -28,8 +28,10 @@
 //              of V tiles: TMA, 128-byte swizzle, rings of stages; a K stage is
 //              released when its QK product completes, a V stage when its PV
 //              product does;
-//   warp 1     TMEM allocation and tcgen05.mma issue: S = Q K^T into one of two
-//              TMEM S buffers, O += P V into the TMEM O accumulator;
+//   warp 1     TMEM allocation; Q into TMEM (tcgen05.cp) and S = Q K^T into one
+//              of two TMEM S buffers (tcgen05.mma);
+//   warp 7     O += P V into the TMEM O accumulator: a second issuing thread, so
+//              the next tile's QK never queues behind this tile's PV;
 //   warps 2-5  one thread per query row: online softmax in the log2 domain on S
 //              read by tcgen05.ld (the reference maximum moves only when it
 //              grows by more than 8 in log2 units, rescaling O in TMEM when it
@@ -52,17 +54,18 @@ using namespace ptx;
 
 constexpr int kBlockM = 128;   // query rows per unit = TMEM lanes
 constexpr int kBlockN = 128;   // keys per tile
-constexpr int kThreads = 224;  // 7 warps
+constexpr int kThreads = 256;  // 8 warps
 constexpr int kMaxContrib = 64;  // pieces a unit may be cut into
 
 template <int D>
 struct Cfg {
     static constexpr uint32_t kTile = kBlockM * D * 2;  // bytes of one Q / K / V tile
     static constexpr uint32_t kCol = kBlockM * 128;     // one 64-element column: 16 KB
-    // stage counts: 1 Q + 3 K + 2 V (+ P) fill 224 KB at D = 128
+    // stage counts at D = 128: 1 Q + 2 K + 3 V (+ merge scratch) fill 224 KB; V, used
+    // last in a tile, gets the deeper ring
     static constexpr int kQBufs = D == 128 ? 1 : 2;
-    static constexpr int kKStages = D == 128 ? 3 : 4;
-    static constexpr int kVStages = D == 128 ? 2 : 3;
+    static constexpr int kKStages = D == 128 ? 2 : 4;
+    static constexpr int kVStages = D == 128 ? 3 : 3;
     static constexpr uint32_t kOffQ = 0;
     static constexpr uint32_t kOffK = kOffQ + kQBufs * kTile;
     static constexpr uint32_t kOffV = kOffK + kKStages * kTile;
@@ -88,8 +91,9 @@ enum : int {
     B_SFREE = 20,   // [2] S buffer read by the softmax warps
     B_PFULL = 22,   // P written, O corrected
     B_PVDONE = 23,
-    B_DRAIN = 24,
-    B_COUNT = 25
+    B_DRAIN = 24,   // QK issuer's products all complete
+    B_DRAIN2 = 25,  // PV issuer's products all complete
+    B_COUNT = 26
 };
 
 struct Params {
@@ -104,6 +108,7 @@ struct Params {
     int n_units, n_tiles, grid;
     int64_t total;     // n_units * n_tiles
     int slots;         // partial slots per unit (most pieces a unit is cut into)
+    int n_split;       // > 0: split-major items (see piece_at); 0: stream-K ranges
     float scale_log2;
     uint32_t *status;   // workspace status word
     unsigned *tickets;  // [n_units]
@@ -125,34 +130,66 @@ __device__ __forceinline__ int cta_of(const Params &P, int64_t w)
     return static_cast<int>(((w + 1) * P.grid - 1) / P.total);
 }
 
-// The pieces of CTA blockIdx.x, in order: units u_first .. u_last.
+// The pieces of CTA blockIdx.x, in order.
+//   stream-K (n_split == 0): the units' tiles laid end to end, one equal
+//     contiguous range per CTA; the pieces are the units that range meets.
+//   split-major items (n_split > 0): item i = ((b, g, split), mt) with mt
+//     varying fastest is tiles [split * n_tiles / n_split, ...) of unit
+//     (b, g, mt); items are dealt round-robin.  The CTAs working on the row
+//     tiles of one KV head then read the same K/V tiles at the same time, so
+//     each tile comes from HBM once and from L2 for the others (used when the
+//     caches do not fit in L2).
 struct Range {
     int64_t w0, w1;
-    int u_first, u_last;
+    int u_first, count;
 };
 __device__ __forceinline__ Range my_range(const Params &P)
 {
     Range r;
+    if (P.n_split > 0) {
+        const int n_items = P.n_units * P.n_split;
+        r.w0 = r.w1 = 0;
+        r.u_first = 0;
+        r.count = static_cast<int>(blockIdx.x) < n_items
+                      ? (n_items - 1 - static_cast<int>(blockIdx.x)) / P.grid + 1
+                      : 0;
+        return r;
+    }
     r.w0 = range_begin(P, blockIdx.x);
     r.w1 = range_begin(P, blockIdx.x + 1);
     r.u_first = static_cast<int>(r.w0 / P.n_tiles);
-    r.u_last = r.w1 > r.w0 ? static_cast<int>((r.w1 - 1) / P.n_tiles) : r.u_first - 1;
+    r.count = r.w1 > r.w0 ? static_cast<int>((r.w1 - 1) / P.n_tiles) - r.u_first + 1 : 0;
     return r;
 }
 
-__device__ __forceinline__ Piece make_piece(const Params &P, const Range &r, int u)
+__device__ __forceinline__ Piece piece_at(const Params &P, const Range &r, int k)
 {
     Piece p;
-    p.unit = u;
-    p.mt = u % P.n_mt;
-    p.g = (u / P.n_mt) % P.Hkv;
-    p.b = u / (P.n_mt * P.Hkv);
-    const int64_t base = static_cast<int64_t>(u) * P.n_tiles;
-    p.t0 = static_cast<int>(max(r.w0, base) - base);
-    p.t1 = static_cast<int>(min(r.w1, base + P.n_tiles) - base);
-    const int c0 = cta_of(P, base), c1 = cta_of(P, base + P.n_tiles - 1);
-    p.slot = static_cast<int>(blockIdx.x) - c0;
-    p.n_contrib = c1 - c0 + 1;
+    if (P.n_split > 0) {
+        const int i = static_cast<int>(blockIdx.x) + k * P.grid;
+        p.mt = i % P.n_mt;
+        const int split = (i / P.n_mt) % P.n_split;
+        const int bg = i / (P.n_mt * P.n_split);
+        p.unit = bg * P.n_mt + p.mt;
+        p.g = bg % P.Hkv;
+        p.b = bg / P.Hkv;
+        p.t0 = static_cast<int>(static_cast<int64_t>(P.n_tiles) * split / P.n_split);
+        p.t1 = static_cast<int>(static_cast<int64_t>(P.n_tiles) * (split + 1) / P.n_split);
+        p.slot = split;
+        p.n_contrib = P.n_split;
+    } else {
+        const int u = r.u_first + k;
+        p.unit = u;
+        p.mt = u % P.n_mt;
+        p.g = (u / P.n_mt) % P.Hkv;
+        p.b = u / (P.n_mt * P.Hkv);
+        const int64_t base = static_cast<int64_t>(u) * P.n_tiles;
+        p.t0 = static_cast<int>(max(r.w0, base) - base);
+        p.t1 = static_cast<int>(min(r.w1, base + P.n_tiles) - base);
+        const int c0 = cta_of(P, base), c1 = cta_of(P, base + P.n_tiles - 1);
+        p.slot = static_cast<int>(blockIdx.x) - c0;
+        p.n_contrib = c1 - c0 + 1;
+    }
     p.cnt = max(0, min(__ldg(P.count + p.b), P.r_max));
     return p;
 }
@@ -186,8 +223,8 @@ __device__ void producer_qk(const Params &P, const Sync &S, uint32_t sbase, cons
     const Range r = my_range(P);
     uint32_t T = 0, it = 0;
     bool ok = true;
-    for (int u = r.u_first; u <= r.u_last && ok; ++u) {
-        const Piece w = make_piece(P, r, u);
+    for (int k = 0; k < r.count && ok; ++k) {
+        const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
         const int qb = it % C::kQBufs;
         if (it >= static_cast<uint32_t>(C::kQBufs))
@@ -227,8 +264,8 @@ __device__ void producer_v(const Params &P, const Sync &S, uint32_t sbase, const
     const Range r = my_range(P);
     uint32_t T = 0;
     bool ok = true;
-    for (int u = r.u_first; u <= r.u_last && ok; ++u) {
-        const Piece w = make_piece(P, r, u);
+    for (int k = 0; k < r.count && ok; ++k) {
+        const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
         for (int t = w.t0; t < w.t1 && ok; ++t, ++T) {
             const int s = T % C::kVStages;
@@ -247,36 +284,20 @@ __device__ void producer_v(const Params &P, const Sync &S, uint32_t sbase, const
             S.drain(B_VFULL + u % C::kVStages, (u / C::kVStages) & 1);
 }
 
+// QK issuer (one thread): per piece Q into TMEM, then S = Q K^T for each tile
+// into one of the two S buffers as soon as its K tile landed and the buffer was
+// read.  It never waits for P, so the next tile's scores are ready while the
+// softmax warps still work on this one.
 template <int D>
-__device__ void mma_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem)
+__device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem)
 {
     using C = Cfg<D>;
     constexpr uint32_t kIdescQK = idesc_bf16(kBlockM, kBlockN, false, false);
-    constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, false, true);
     const Range r = my_range(P);
     uint32_t T = 0, it = 0;
     bool ok = true;
-    // the PV product of the previous tile, issued after the next QK
-    bool pv_pending = false, pv_first = false;
-    uint32_t pv_T = 0;
-    auto issue_pv = [&]() {
-        const int s = pv_T % C::kVStages;
-        ok = ok && S.wait(B_PFULL, pv_T & 1) && S.wait(B_VFULL + s, (pv_T / C::kVStages) & 1);
-        if (!ok) return;
-        tc_fence_after();
-        const uint32_t vbase = sbase + C::kOffV + s * C::kTile;
-#pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {  // P from TMEM, V from shared memory
-            const uint64_t bd = desc_sw128(vbase + kk * 16 * 128, C::kCol, 1024);
-            umma_bf16_ts(tmem + C::kColO, tmem + C::kColP + kk * 8, bd, kIdescPV,
-                         (!pv_first || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(S.bar(B_VEMPTY + s));
-        umma_commit(S.bar(B_PVDONE));
-        pv_pending = false;
-    };
-    for (int u = r.u_first; u <= r.u_last && ok; ++u) {
-        const Piece w = make_piece(P, r, u);
+    for (int k = 0; k < r.count && ok; ++k) {
+        const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
         const int qb = it % C::kQBufs;
         ok = S.wait(B_QFULL + qb, (it / C::kQBufs) & 1);
@@ -305,18 +326,45 @@ __device__ void mma_issuer(const Params &P, const Sync &S, uint32_t sbase, uint3
             }
             umma_commit(S.bar(B_SFULL + sb));
             umma_commit(S.bar(B_KEMPTY + s));
-            if (pv_pending) issue_pv();
-            if (!ok) break;
-            pv_pending = true;
-            pv_first = t == w.t0;
-            pv_T = T;
         }
         ++it;
     }
-    if (ok && pv_pending) issue_pv();
     // everything issued has completed before TMEM is released
     umma_commit(S.bar(B_DRAIN));
     S.drain(B_DRAIN, 0);
+}
+
+// PV issuer (one thread): O (+)= P V for each tile once the softmax warps wrote
+// P into TMEM and its V tile landed; the first tile of a piece overwrites O.
+template <int D>
+__device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem)
+{
+    using C = Cfg<D>;
+    constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, false, true);
+    const Range r = my_range(P);
+    uint32_t T = 0;
+    bool ok = true;
+    for (int k = 0; k < r.count && ok; ++k) {
+        const Piece w = piece_at(P, r, k);
+        if (!piece_active(P, w)) continue;
+        for (int t = w.t0; t < w.t1; ++t, ++T) {
+            const int s = T % C::kVStages;
+            ok = S.wait(B_PFULL, T & 1) && S.wait(B_VFULL + s, (T / C::kVStages) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t vbase = sbase + C::kOffV + s * C::kTile;
+#pragma unroll
+            for (int kk = 0; kk < kBlockN / 16; ++kk) {  // P from TMEM, V from shared memory
+                const uint64_t bd = desc_sw128(vbase + kk * 16 * 128, C::kCol, 1024);
+                umma_bf16_ts(tmem + C::kColO, tmem + C::kColP + kk * 8, bd, kIdescPV,
+                             (t > w.t0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(S.bar(B_VEMPTY + s));
+            umma_commit(S.bar(B_PVDONE));
+        }
+    }
+    umma_commit(S.bar(B_DRAIN2));
+    S.drain(B_DRAIN2, 0);
 }
 
 __device__ __forceinline__ uint64_t f2x2(float lo, float hi)
@@ -440,8 +488,8 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase,
     // After a failed (timed-out) wait a warp skips all further work but keeps
     // walking the same pieces, so the four softmax warps always meet at the same
     // named barriers; every later wait returns at once (the abort flag is set).
-    for (int u = r.u_first; u <= r.u_last; ++u) {
-        const Piece w = make_piece(P, r, u);
+    for (int k = 0; k < r.count; ++k) {
+        const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
         float m_run = -INFINITY, l_run = 0.f;  // m in raw score units
         for (int t = w.t0; t < w.t1; ++t, ++T) {
@@ -689,8 +737,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 producer_v<D>(P, S, sbase, &tm_v);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        if ((threadIdx.x & 31) == 0) mma_issuer<D>(P, S, sbase, tmem);
+    } else if (warp == 1 || warp == 7) {
+        if ((threadIdx.x & 31) == 0) {
+            if (warp == 1)
+                qk_issuer<D>(P, S, sbase, tmem);
+            else
+                pv_issuer<D>(P, S, sbase, tmem);
+        }
         __syncwarp();
     } else {
         softmax_epilogue<D>(P, S, sbase, tmem, smem);
@@ -737,7 +790,7 @@ bool encode_4d(CUtensorMap *map, const void *base, int B, int rows, int heads, i
 }
 
 struct Plan {
-    int G, tok_per_tile, n_mt, n_units, n_tiles, grid, slots;
+    int G, tok_per_tile, n_mt, n_units, n_tiles, grid, slots, n_split;
     int64_t total;
 };
 
@@ -759,6 +812,27 @@ Plan make_plan(int B, int L, int r_max, int H, int Hkv)
     // a unit of n_tiles tiles meets at most ceil(n_tiles * grid / total) + 1 ranges
     p.slots = static_cast<int>(std::min<int64_t>(
         kMaxContrib, (static_cast<int64_t>(p.n_tiles) * p.grid + p.total - 1) / p.total + 1));
+    p.n_split = 0;
+    // Several row tiles per KV head and caches larger than half of L2: stream-K
+    // would read each K/V tile from HBM once per row tile, so deal split-major
+    // items instead (the splits that give the fewest rounds x tiles per item).
+    const int64_t kv_bytes = 2LL * B * L * Hkv * 128 * 2;
+    if (p.n_mt > 1 && kv_bytes > (64LL << 20)) {
+        const int n_sm = device_sm_count();
+        double best = 1e30;
+        for (int sp = 1; sp <= std::min(kMaxContrib, std::max(1, p.n_tiles / 2)); ++sp) {
+            const int64_t items = static_cast<int64_t>(p.n_units) * sp;
+            const int64_t rounds = (items + n_sm - 1) / n_sm;
+            const double cost = static_cast<double>(rounds) *
+                                (std::ceil(static_cast<double>(p.n_tiles) / sp) + 2.0);
+            if (cost < best - 1e-9) {
+                best = cost;
+                p.n_split = sp;
+            }
+        }
+        p.grid = static_cast<int>(std::min<int64_t>(n_sm, static_cast<int64_t>(p.n_units) * p.n_split));
+        p.slots = p.n_split;
+    }
     return p;
 }
 
@@ -841,6 +915,7 @@ cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_
     p.grid = plan.grid;
     p.total = plan.total;
     p.slots = plan.slots;
+    p.n_split = plan.n_split;
     p.scale_log2 = scale * kLog2e;
     char *ws = static_cast<char *>(workspace);
     size_t o_t, o_ml, o_o;

@@ -56,6 +56,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
         : "memory");
     return ok != 0;
 }
+// As mbar_try_wait, but the thread sleeps in the barrier until the phase
+// completes or about `ns` nanoseconds pass, instead of returning at once: a
+// waiting warp then takes no issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 
 // ---- proxies / fences ----
 __device__ __forceinline__ void fence_async_smem()
@@ -277,6 +292,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk16, uint32_t 
 
 // ---- bounded waits on a CTA's array of mbarriers ----
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s: a wait this long is a fault
+constexpr uint32_t kSleepNs = 20000;              // longest sleep of one try_wait
 
 // mbarrier i lives at bars + 8 i.  wait() gives up after ~2 s (or as soon as
 // another role of the CTA gave up): it raises the CTA's abort flag, sets
@@ -292,8 +308,8 @@ struct Sync {
         if (mbar_try_wait(b, parity)) return true;
         const long long t0 = clock64();
         for (uint32_t it = 1;; ++it) {
-            if (mbar_try_wait(b, parity)) return true;
-            if ((it & 127u) == 0u) {
+            if (mbar_try_wait_sleep(b, parity, kSleepNs)) return true;
+            if ((it & 15u) == 0u) {
                 if (*abort_flag) return false;
                 if (clock64() - t0 > kWaitCycles) {
                     *abort_flag = 1;
