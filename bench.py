@@ -241,11 +241,15 @@ class GpuStep:
         self.recompute()
 
 
-def kernels_per_step(w: synth.Workload):
-    """Launches of our kernels per step: bf16 attention is one tensor-core kernel
-    with the write-back fused; float32 attention is a write-back kernel plus the
-    SIMT kernel."""
-    return {"attention": 1 if w.attn_dtype == synth.BF16 else 2, "decode": 1, "recompute": 1}
+def kernels_per_step(nat, w: synth.Workload):
+    """Launches of our kernels per step, as the library reports them: the attention
+    call runs a write-back, the attention kernel and (when some unit is split over
+    several CTAs) a merge kernel."""
+    import torch
+    dt = torch.bfloat16 if w.attn_dtype == synth.BF16 else torch.float32
+    n_att = nat.ec_attention_kernel_count(dt, w.batch, w.seq_len, w.r_max, w.n_heads,
+                                          w.n_kv_heads, w.head_dim)
+    return {"attention": n_att, "decode": 1, "recompute": 1}
 
 
 def dist_setup(args):
@@ -310,39 +314,50 @@ def run_ours(args):
         flush()
         step.run()
     torch.cuda.synchronize(device)
-    # One step = one replay of a CUDA graph holding the three calls with timing
-    # events between them, so host launch cost stays out of the device timings.
-    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
-    graph, mode = None, "cuda-graph replay per step"
+    # One step = one replay of a CUDA graph holding the three calls between two
+    # timing events, so host launch cost stays out of the device time and the calls
+    # chain as they do in use (each kernel's set-up overlaps its predecessor's
+    # tail).  A second graph puts events between the calls for the per-call
+    # breakdown; each of its parts includes one event node's gap.
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
+    graph = graph_parts = None
+    mode = "cuda-graph replay per step"
+
+    def record_step():
+        ev[4].record()
+        step.run()
+        ev[5].record()
+
+    def record_parts():
+        ev[0].record()
+        step.attention()
+        ev[1].record()
+        step.decode()
+        ev[2].record()
+        step.recompute()
+        ev[3].record()
+
     if args.eager:
         mode = "eager launches"
     else:
         try:
-            graph = torch.cuda.CUDAGraph()
+            graph, graph_parts = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
-                ev[0].record()
-                step.attention()
-                ev[1].record()
-                step.decode()
-                ev[2].record()
-                step.recompute()
-                ev[3].record()
+                record_step()
+            with torch.cuda.graph(graph_parts, stream=stream):
+                record_parts()
             graph.replay()
+            graph_parts.replay()
             torch.cuda.synchronize(device)
         except Exception as exc:  # capture not possible: time eager launches instead
-            graph, mode = None, f"eager launches (graph capture failed: {type(exc).__name__})"
+            graph = graph_parts = None
+            mode = f"eager launches (graph capture failed: {type(exc).__name__})"
 
     def one_step():
-        if graph is not None:
-            graph.replay()
-        else:
-            ev[0].record()
-            step.attention()
-            ev[1].record()
-            step.decode()
-            ev[2].record()
-            step.recompute()
-            ev[3].record()
+        graph.replay() if graph is not None else record_step()
+
+    def one_parts():
+        graph_parts.replay() if graph_parts is not None else record_parts()
 
     uuid = None
     try:
@@ -355,19 +370,25 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize(device)
     t_wall = time.perf_counter()
-    t_att = t_dec = t_rec = 0.0
+    t_step = 0.0
     for _ in range(K):
         flush()
         one_step()
+        ev[5].synchronize()
+        t_step += ev[4].elapsed_time(ev[5]) / 1e3
+    torch.cuda.synchronize(device)
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    # per-call breakdown (same steps, events between the calls)
+    t_att = t_dec = t_rec = 0.0
+    for _ in range(K):
+        flush()
+        one_parts()
         ev[3].synchronize()
         t_att += ev[0].elapsed_time(ev[1]) / 1e3
         t_dec += ev[1].elapsed_time(ev[2]) / 1e3
         t_rec += ev[2].elapsed_time(ev[3]) / 1e3
-    torch.cuda.synchronize(device)
-    barrier(world)
-    wall = time.perf_counter() - t_wall
     clocks = sampler.stop()
-    t_step = t_att + t_dec + t_rec
     t_step_max = reduce_max(t_step, world)
     status = nat.ec_read_device_status(step.ws_dec) | nat.ec_read_device_status(step.ws_att)
 
@@ -377,7 +398,6 @@ def run_ours(args):
     hbm = float(peaks["hbm_gbs"])
     tc = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     us = lambda t: t / K * 1e6  # noqa: E731
-    dec_gbs = geo["logits_bytes"] * K / (t_dec + t_rec) / 1e9
     att_tflops = geo["attn_flops"] * K / t_att / 1e12
     att_gbs = geo["attn_bytes"] * K / t_att / 1e9
     att_ai = geo["attn_flops"] / geo["attn_bytes"]
@@ -386,7 +406,7 @@ def run_ours(args):
         "attention": {"us": us(t_att), "tflops": att_tflops, "frac_tensor_peak": att_tflops / tc,
                       "gbs": att_gbs, "frac_hbm": att_gbs / hbm,
                       "frac_attainable": att_tflops / att_roof, "intensity_flop_per_byte": att_ai,
-                      "launches": kernels_per_step(w)["attention"]},
+                      "launches": kernels_per_step(nat, w)["attention"]},
         "decode_gate": {"us": us(t_dec), "gbs": geo["logits_bytes"] * K / t_dec / 1e9,
                         "frac_hbm": geo["logits_bytes"] * K / t_dec / 1e9 / hbm, "launches": 1},
         "recompute_set": {"us": us(t_rec), "launches": 1},
@@ -400,7 +420,7 @@ def run_ours(args):
         else:
             roof = {"bound": "tensor", "achieved": att_tflops, "peak": tc, "unit": "TFLOP/s",
                     "frac": att_tflops / tc}
-        roof["kernel"] = "ec_selective_attention (write-back + attention)"
+        roof["kernel"] = "ec_selective_attention (write-back + attention + merge)"
     else:
         g = parts["decode_gate"]["gbs"]
         roof = {"bound": "hbm", "achieved": g, "peak": hbm, "unit": "GB/s", "frac": g / hbm,
@@ -424,8 +444,11 @@ def run_ours(args):
                    "k": w.k, "tau": w.tau, "accumulate": "f32",
                    "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)", "launch": mode,
                    "parallelism": f"replicas x{world}"},
-        "parts": parts, "roofline": roof, "clocks": clocks, "e2e": e2e,
-        "gpu_launches": sum(kernels_per_step(w).values()) * K,
+        "parts": parts,
+        "parts_note": "each call timed between its own events in a second graph (one event-node "
+                      "gap each); ms_per_step has events only around the whole step",
+        "roofline": roof, "clocks": clocks, "e2e": e2e,
+        "gpu_launches": sum(kernels_per_step(nat, w).values()) * K,
         "cpu_baseline": cpu, "device_status": status, "wall_s_timed_region": wall,
     }
     if rank == 0:

@@ -27,7 +27,8 @@ DEV_TIMEOUT = 0x10
 
 EXPORTED = ("ec_status_str", "ec_abi_version", "ec_workspace_init", "ec_read_device_status",
             "ec_decode_workspace_size", "ec_decode_step", "ec_decode_step_noalloc",
-            "ec_build_recompute_set", "ec_attention_workspace_size", "ec_selective_attention",
+            "ec_build_recompute_set", "ec_attention_workspace_size", "ec_attention_kernel_count",
+            "ec_selective_attention",
             "ec_embed_rows", "ec_qkv_projection")
 
 
@@ -68,6 +69,8 @@ def lib() -> ctypes.CDLL:
         L.ec_build_recompute_set.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
         L.ec_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         L.ec_attention_workspace_size.restype = sz
+        L.ec_attention_kernel_count.argtypes = [ctypes.c_int, i32, i32, i32, i32, i32, i32]
+        L.ec_attention_kernel_count.restype = i32
         L.ec_selective_attention.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, ctypes.c_int,
                                              i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
         L.ec_embed_rows.argtypes = [vp, i64, i32, vp, i64, vp, vp, vp, i32, i32, i32, i32, vp, vp,
@@ -135,6 +138,14 @@ def ec_decode_workspace_size(n_rows: int, batch: int) -> int:
 
 def ec_attention_workspace_size(batch, seq_len, r_max, n_heads, n_kv_heads, head_dim) -> int:
     return lib().ec_attention_workspace_size(batch, seq_len, r_max, n_heads, n_kv_heads, head_dim)
+
+
+def ec_attention_kernel_count(dtype, batch, seq_len, r_max, n_heads, n_kv_heads, head_dim) -> int:
+    """Kernels one ec_selective_attention call launches (dtype: torch.bfloat16 or
+    torch.float32); -1 for arguments the call rejects."""
+    code = {torch.bfloat16: EC_BF16, torch.float32: EC_F32}[dtype]
+    return lib().ec_attention_kernel_count(code, batch, seq_len, r_max, n_heads, n_kv_heads,
+                                           head_dim)
 
 
 def new_workspace(nbytes: int, device="cuda") -> torch.Tensor:

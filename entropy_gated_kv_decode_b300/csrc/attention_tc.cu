@@ -6,12 +6,14 @@
 // bidirectional) and "Algoritmo di Funzionamento" step 2 (the partial forward
 // recomputes K/V only for the selected tokens; the cache supplies the rest).
 //
-// Two launches, chained by programmatic dependent launch (PDL):
+// Up to three launches, chained by programmatic dependent launch (PDL):
 //   write_back_kernel   copies every fresh K/V row into the caches and at once
 //                       lets the attention grid start;
 //   attention_tc_kernel allocates TMEM, sets up its barriers and loads its first
 //                       Q tile while the write-back runs, and waits for it
-//                       (griddepcontrol.wait) only before its first K/V load.
+//                       (griddepcontrol.wait) only before its first K/V load;
+//   merge_kernel        (only when some unit is split over several CTAs)
+//                       combines the split units' partials into the output.
 //
 // Attention kernel: persistent, one CTA per SM.
 //   units      up to 128 query rows of one (sequence b, KV head g): the
@@ -21,22 +23,25 @@
 //              equal contiguous range per CTA (stream-K), so every CTA does the
 //              same number of tiles.  A range covers pieces of one or more
 //              units.  A piece that is a whole unit writes its output directly;
-//              otherwise it stores a partial (O, m, l) and the unit's last
-//              contributor (an acquire-release ticket; no CTA waits on another)
-//              merges the unit's partials.
+//              otherwise it stores a partial (O, m, l) and moves on: no CTA
+//              waits for another, and the merge kernel, spread over the whole
+//              GPU, combines the partials afterwards.
 //   warp 0     producer of Q (one tile per piece) and K tiles, warp 6 producer
 //              of V tiles: TMA, 128-byte swizzle, rings of stages; a K stage is
 //              released when its QK product completes, a V stage when its PV
 //              product does;
 //   warp 1     TMEM allocation; Q into TMEM (tcgen05.cp) and S = Q K^T into one
-//              of two TMEM S buffers (tcgen05.mma);
+//              of two TMEM S buffers (tcgen05.mma) once the PV product that read
+//              that buffer's P has completed;
 //   warp 7     O += P V into the TMEM O accumulator: a second issuing thread, so
 //              the next tile's QK never queues behind this tile's PV;
 //   warps 2-5  one thread per query row: online softmax in the log2 domain on S
 //              read by tcgen05.ld (the reference maximum moves only when it
 //              grows by more than 8 in log2 units, rescaling O in TMEM when it
-//              does), P as bf16 into TMEM (the PV product takes its A operand
-//              from there), and the epilogue.
+//              does), P as bf16 over the first half of the same S buffer (the
+//              PV product takes its A operand from there), and the epilogue.
+//              With P in its own S buffer the softmax never waits for the
+//              previous tile's PV product, except to rescale O.
 // Every wait is bounded (~2 s); a timeout sets EC_DEV_TIMEOUT and unwinds.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -61,39 +66,37 @@ template <int D>
 struct Cfg {
     static constexpr uint32_t kTile = kBlockM * D * 2;  // bytes of one Q / K / V tile
     static constexpr uint32_t kCol = kBlockM * 128;     // one 64-element column: 16 KB
-    // stage counts at D = 128: 1 Q + 2 K + 3 V (+ merge scratch) fill 224 KB; V, used
-    // last in a tile, gets the deeper ring
+    // stage counts at D = 128: 1 Q + 3 K + 3 V tiles fill 224 KB
     static constexpr int kQBufs = D == 128 ? 1 : 2;
-    static constexpr int kKStages = D == 128 ? 2 : 4;
-    static constexpr int kVStages = D == 128 ? 3 : 3;
+    static constexpr int kKStages = D == 128 ? 3 : 4;
+    static constexpr int kVStages = D == 128 ? 3 : 4;
     static constexpr uint32_t kOffQ = 0;
     static constexpr uint32_t kOffK = kOffQ + kQBufs * kTile;
     static constexpr uint32_t kOffV = kOffK + kKStages * kTile;
-    static constexpr uint32_t kOffScratch = kOffV + kVStages * kTile;  // split-merge weights
-    static constexpr uint32_t kOffBar = kOffScratch + kBlockM * 64 * 4;
+    static constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
     static constexpr uint32_t kOffMisc = kOffBar + 256;
     static constexpr uint32_t kBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1 KB
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColS = 0;    // two S buffers: columns [0, 128) and [128, 256)
+    // two S buffers, columns [0, 128) and [128, 256); P (bf16 pairs) of a tile
+    // overwrites the first 64 columns of its own S buffer
+    static constexpr uint32_t kColS = 0;
     static constexpr uint32_t kColO = 256;  // O: columns [256, 256 + D)
-    static constexpr uint32_t kColP = 384;  // P (bf16 pairs): columns [384, 448)
     static constexpr uint32_t kColQ = 448;  // Q (bf16 pairs): columns [448, 448 + D / 2)
 };
 
 enum : int {
     B_KFULL = 0,    // [4] K tile landed
     B_KEMPTY = 4,   // [4] K stage consumed (its QK done)
-    B_VFULL = 8,    // [3] V tile landed
-    B_VEMPTY = 11,  // [3] V stage consumed (its PV done)
-    B_QFULL = 14,   // [2] Q tile landed
-    B_QEMPTY = 16,  // [2] Q tile copied into TMEM
-    B_SFULL = 18,   // [2] S buffer written
-    B_SFREE = 20,   // [2] S buffer read by the softmax warps
-    B_PFULL = 22,   // P written, O corrected
-    B_PVDONE = 23,
-    B_DRAIN = 24,   // QK issuer's products all complete
-    B_DRAIN2 = 25,  // PV issuer's products all complete
-    B_COUNT = 26
+    B_VFULL = 8,    // [4] V tile landed
+    B_VEMPTY = 12,  // [4] V stage consumed (its PV done)
+    B_QFULL = 16,   // [2] Q tile landed
+    B_QEMPTY = 18,  // [2] Q tile copied into TMEM
+    B_SFULL = 20,   // [2] S buffer written by its QK product
+    B_PFULL = 22,   // [2] P written over its S buffer (and O corrected): 4 softmax warps
+    B_SFREE = 24,   // [2] the PV product that read the buffer's P completed (O updated)
+    B_DRAIN = 26,   // QK issuer's products all complete
+    B_DRAIN2 = 27,  // PV issuer's products all complete
+    B_COUNT = 28
 };
 
 struct Params {
@@ -111,7 +114,6 @@ struct Params {
     int n_split;       // > 0: split-major items (see piece_at); 0: stream-K ranges
     float scale_log2;
     uint32_t *status;   // workspace status word
-    unsigned *tickets;  // [n_units]
     float2 *part_ml;    // [n_units][slots][128] (m, l), m in raw score units
     float4 *part_o;     // [n_units][slots][D / 4][128] unnormalised O
 };
@@ -201,17 +203,10 @@ __device__ __forceinline__ bool piece_active(const Params &P, const Piece &p)
     return p.mt * P.tok_per_tile < p.cnt && p.t1 > p.t0;
 }
 
-__device__ __forceinline__ unsigned ticket(unsigned *ctr, unsigned last)
-{
-    unsigned old;
-    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(ctr), "r"(last)
-                 : "memory");
-    return old;
-}
-
-static_assert(Cfg<128>::kColO + 128 <= Cfg<128>::kColP, "TMEM columns overlap");
-static_assert(Cfg<128>::kColP + kBlockN / 2 <= Cfg<128>::kColQ, "TMEM columns overlap");
+static_assert(Cfg<128>::kColS + 2 * kBlockN <= Cfg<128>::kColO, "TMEM columns overlap");
+static_assert(Cfg<128>::kColO + 128 <= Cfg<128>::kColQ, "TMEM columns overlap");
 static_assert(Cfg<128>::kColQ + 128 / 2 <= Cfg<128>::kTmemCols, "TMEM columns overflow");
+static_assert(Cfg<128>::kBytes <= 227 * 1024 && Cfg<64>::kBytes <= 227 * 1024, "shared memory");
 
 // Q and K producer (one thread): per piece its Q tile, then its K tiles.
 template <int D>
@@ -285,9 +280,9 @@ __device__ void producer_v(const Params &P, const Sync &S, uint32_t sbase, const
 }
 
 // QK issuer (one thread): per piece Q into TMEM, then S = Q K^T for each tile
-// into one of the two S buffers as soon as its K tile landed and the buffer was
-// read.  It never waits for P, so the next tile's scores are ready while the
-// softmax warps still work on this one.
+// into one of the two S buffers as soon as its K tile landed and the PV product
+// of the tile two back (which read its P from that buffer) completed.  The next
+// tile's scores are then ready while the softmax warps still work on this one.
 template <int D>
 __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem)
 {
@@ -335,7 +330,8 @@ __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
 }
 
 // PV issuer (one thread): O (+)= P V for each tile once the softmax warps wrote
-// P into TMEM and its V tile landed; the first tile of a piece overwrites O.
+// P over its S buffer and its V tile landed; the first tile of a piece
+// overwrites O.  Its completion frees the V stage and the S buffer.
 template <int D>
 __device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem)
 {
@@ -348,19 +344,20 @@ __device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
         const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
         for (int t = w.t0; t < w.t1; ++t, ++T) {
-            const int s = T % C::kVStages;
-            ok = S.wait(B_PFULL, T & 1) && S.wait(B_VFULL + s, (T / C::kVStages) & 1);
+            const int s = T % C::kVStages, sb = T & 1;
+            ok = S.wait(B_PFULL + sb, (T >> 1) & 1) && S.wait(B_VFULL + s, (T / C::kVStages) & 1);
             if (!ok) break;
             tc_fence_after();
             const uint32_t vbase = sbase + C::kOffV + s * C::kTile;
+            const uint32_t pcol = tmem + C::kColS + sb * kBlockN;
 #pragma unroll
             for (int kk = 0; kk < kBlockN / 16; ++kk) {  // P from TMEM, V from shared memory
                 const uint64_t bd = desc_sw128(vbase + kk * 16 * 128, C::kCol, 1024);
-                umma_bf16_ts(tmem + C::kColO, tmem + C::kColP + kk * 8, bd, kIdescPV,
+                umma_bf16_ts(tmem + C::kColO, pcol + kk * 8, bd, kIdescPV,
                              (t > w.t0 || kk > 0) ? 1u : 0u);
             }
             umma_commit(S.bar(B_VEMPTY + s));
-            umma_commit(S.bar(B_PVDONE));
+            umma_commit(S.bar(B_SFREE + sb));
         }
     }
     umma_commit(S.bar(B_DRAIN2));
@@ -396,81 +393,8 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
     return d;
 }
 
-// Merge of a unit's n partials (last contributor), by the 128 softmax threads.
-// Phase 1, one thread per row: the weight of every partial, w_s = 2^{(m_s - m) c}
-// / sum_s 2^{(m_s - m) c} l_s with m the largest m_s, into a shared-memory
-// scratch region.  Phase 2, work items (row,
-// 32-column chunk): the partials are read four at a time with every load issued
-// before use.
 template <int D>
-__device__ void merge_unit(const Params &P, const Piece &w, int ltid, float *s_w)
-{
-    constexpr int kChunks = D / 32;
-    const int n = w.n_contrib;
-    const int rows = min(kBlockM, P.tok_per_tile * P.G);
-    const float2 *ml = P.part_ml + static_cast<int64_t>(w.unit) * P.slots * kBlockM;
-    const float4 *po = P.part_o + static_cast<int64_t>(w.unit) * P.slots * (D / 4) * kBlockM;
-    const int row_valid_max = min(rows, (w.cnt - w.mt * P.tok_per_tile) * P.G);
-    if (ltid < row_valid_max) {
-        float m_all = -INFINITY;
-        for (int s = 0; s < n; ++s) m_all = fmaxf(m_all, __ldcg(ml + s * kBlockM + ltid).x);
-        float l_tot = 0.f;
-        for (int s = 0; s < n; ++s) {
-            const float2 v = __ldcg(ml + s * kBlockM + ltid);
-            const float e = ex2((v.x - m_all) * P.scale_log2);
-            s_w[ltid * kMaxContrib + s] = e;
-            l_tot = fmaf(e, v.y, l_tot);
-        }
-        const float inv = 1.f / l_tot;
-        for (int s = 0; s < n; ++s) s_w[ltid * kMaxContrib + s] *= inv;
-    }
-    named_bar_sync(1, 128);
-    for (int item = ltid; item < row_valid_max * kChunks; item += 128) {
-        const int row = item % row_valid_max, ch = item / row_valid_max;
-        const int tok = w.mt * P.tok_per_tile + row / P.G;
-        float acc[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-        for (int s0 = 0; s0 < n; s0 += 4) {
-            float4 x[4][8];
-            float f[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int s = s0 + k;
-                f[k] = s < n ? s_w[row * kMaxContrib + s] : 0.f;
-                const float4 *src =
-                    po + (static_cast<int64_t>(s < n ? s : s0) * (D / 4) + ch * 8) * kBlockM + row;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) x[k][q] = __ldcg(src + q * kBlockM);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    acc[4 * q] = fmaf(f[k], x[k][q].x, acc[4 * q]);
-                    acc[4 * q + 1] = fmaf(f[k], x[k][q].y, acc[4 * q + 1]);
-                    acc[4 * q + 2] = fmaf(f[k], x[k][q].z, acc[4 * q + 2]);
-                    acc[4 * q + 3] = fmaf(f[k], x[k][q].w, acc[4 * q + 3]);
-                }
-        }
-        const int h = w.g * P.G + row % P.G;
-        uint4 *dst = reinterpret_cast<uint4 *>(
-            P.out + ((static_cast<int64_t>(w.b) * P.r_max + tok) * P.H + h) * D + ch * 32);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint4 o;
-            o.x = pack_bf16x2(acc[8 * q], acc[8 * q + 1]);
-            o.y = pack_bf16x2(acc[8 * q + 2], acc[8 * q + 3]);
-            o.z = pack_bf16x2(acc[8 * q + 4], acc[8 * q + 5]);
-            o.w = pack_bf16x2(acc[8 * q + 6], acc[8 * q + 7]);
-            dst[q] = o;
-        }
-    }
-}
-
-template <int D>
-__device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem,
-                                 uint8_t *smem_generic)
+__device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
 {
     using C = Cfg<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -481,13 +405,11 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase,
     const float c = P.scale_log2;           // log2 units per raw score unit
     const float move = 8.f / c;             // raw-score growth that moves the reference
     const int kv_tail = P.L - (P.n_tiles - 1) * kBlockN;  // keys in the last tile
-    __shared__ int s_last;
     const Range r = my_range(P);
     uint32_t T = 0;
     bool ok = true;
-    // After a failed (timed-out) wait a warp skips all further work but keeps
-    // walking the same pieces, so the four softmax warps always meet at the same
-    // named barriers; every later wait returns at once (the abort flag is set).
+    // After a failed (timed-out) wait a warp skips all further work; every later
+    // wait of any role returns at once (the abort flag is set).
     for (int k = 0; k < r.count; ++k) {
         const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
@@ -503,9 +425,6 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase,
                 tmem_ld32(tmem + lane_off + C::kColS + sb * kBlockN + cc * 32, sr[cc]);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) tmem_wait_ld(sr[cc]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(S.bar(B_SFREE + sb));
 
             if (t == P.n_tiles - 1 && kv_tail < kBlockN) {  // keys past L do not exist
 #pragma unroll
@@ -562,14 +481,13 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase,
             l_run = l_run * alpha + rowsum;
             m_run = m_use;
 
-            // the P columns and O are free once the previous PV of this piece completed
-            // (for a piece's first tile the previous epilogue already waited).
-            if (t > w.t0) {
-                ok = __all_sync(0xffffffffu, S.wait(B_PVDONE, (T - 1) & 1));
-                if (!ok) continue;
-            }
-            tc_fence_after();
+            // O may be rescaled only after the previous tile's PV product completed
+            // (the completion that freed the other S buffer)
             if (rescale) {
+                const uint32_t Tp = T - 1;
+                ok = __all_sync(0xffffffffu, S.wait(B_SFREE + (Tp & 1), (Tp >> 1) & 1));
+                if (!ok) continue;
+                tc_fence_after();
 #pragma unroll
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
@@ -582,16 +500,21 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase,
                 }
                 tmem_wait_st();
             }
-            // P (bf16 pairs) into this row's TMEM lane; the PV product reads it there
-            tmem_st32(tmem + lane_off + C::kColP, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-            tmem_st32(tmem + lane_off + C::kColP + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+            // P (bf16 pairs) over the first half of this S buffer, in this row's
+            // TMEM lane; the PV product reads it there
+            const uint32_t pcol = tmem + lane_off + C::kColS + sb * kBlockN;
+            tmem_st32(pcol, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+            tmem_st32(pcol + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(S.bar(B_PFULL));
+            if (lane == 0) mbar_arrive(S.bar(B_PFULL + sb));
         }
-        // ---- epilogue of the piece ----
-        if (ok) ok = __all_sync(0xffffffffu, S.wait(B_PVDONE, (T - 1) & 1));
+        // ---- epilogue of the piece: O is final once the last PV product completed ----
+        if (ok) {
+            const uint32_t Tp = T - 1;
+            ok = __all_sync(0xffffffffu, S.wait(B_SFREE + (Tp & 1), (Tp >> 1) & 1));
+        }
         tc_fence_after();
         const int tok = w.mt * P.tok_per_tile + row / P.G;
         const bool valid = row < P.tok_per_tile * P.G && tok < w.cnt;
@@ -621,11 +544,11 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase,
             tc_fence_before();
             continue;
         }
-        // part of a unit: store the partial, then the unit's last contributor merges
+        // part of a unit: store the partial (the merge kernel combines them)
+        if (!ok) continue;
         float4 *po = P.part_o + (static_cast<int64_t>(w.unit) * P.slots + w.slot) * (D / 4) * kBlockM;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
-            if (!ok) break;
             uint32_t o[32];
             tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
             tmem_wait_ld(o);
@@ -638,19 +561,109 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t sbase,
             }
         }
         tc_fence_before();
-        if (ok && valid)
+        if (valid)
             __stcg(P.part_ml + (static_cast<int64_t>(w.unit) * P.slots + w.slot) * kBlockM + row,
                    make_float2(m_run, l_run));
-        // all four warps meet here whatever happened; a failure anywhere drops the piece
-        const bool failed = named_bar_or(1, 128, !ok);
-        if (!failed && ltid == 0)  // release: the partials above; acquire: the others'
-            s_last = ticket(P.tickets + w.unit, static_cast<unsigned>(w.n_contrib - 1)) ==
-                     static_cast<unsigned>(w.n_contrib - 1);
-        named_bar_sync(1, 128);
-        if (!failed && s_last)
-            merge_unit<D>(P, w, ltid, reinterpret_cast<float *>(smem_generic + C::kOffScratch));
-        named_bar_sync(1, 128);  // s_last is rewritten by the next piece
     }
+}
+
+// Merge of the split units, a grid of its own after the attention grid.  For
+// every valid row of a unit cut into n >= 2 pieces with partials (O_s, m_s, l_s):
+//   out = sum_s 2^{(m_s - M) c} O_s / sum_s 2^{(m_s - M) c} l_s,   M = max_s m_s,
+// the standard combination of softmax partials (m in raw score units, c the
+// scale in log2 units).  Block (unit, 32-row group), thread (row, 8-column
+// group): the partials keep rows innermost, so a warp reads 512 contiguous bytes
+// per load.  Slots are taken eight at a time and every load of a batch, the
+// sequence's row count included, is issued (volatile, in order) before any is
+// used: a unit cut into up to eight pieces costs one round trip to L2.
+__device__ __forceinline__ float4 ld_cg_v4(const float4 *p)
+{
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float2 ld_cg_v2(const float2 *p)
+{
+    float2 v;
+    asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(D * 4) merge_kernel(const Params P)
+{
+    constexpr int kBatch = 8;
+    pdl_launch_dependents();
+    pdl_wait();
+    const int unit = blockIdx.x;
+    const int row = blockIdx.y * 32 + (threadIdx.x & 31);
+    const int grp = threadIdx.x >> 5;  // columns [8 grp, 8 grp + 8)
+    const int mt = unit % P.n_mt, bg = unit / P.n_mt;
+    const int g = bg % P.Hkv, b = bg / P.Hkv;
+    int n = P.n_split;
+    if (n == 0) {
+        const int64_t base = static_cast<int64_t>(unit) * P.n_tiles;
+        n = cta_of(P, base + P.n_tiles - 1) - cta_of(P, base) + 1;
+    }
+    if (n < 2 || row >= P.tok_per_tile * P.G) return;  // whole units were written by their piece
+    const int count_b = __ldg(P.count + b);
+    const float c = P.scale_log2;
+    const int64_t s_base = static_cast<int64_t>(unit) * P.slots;
+    float M = -INFINITY, l_sum = 0.f, acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    // rows past the sequence's count hold no partials; their loads stay inside the
+    // workspace and their results are dropped below
+    for (int s0 = 0; s0 < n; s0 += kBatch) {
+        float2 ml[kBatch];
+        float4 o[kBatch][2];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            ml[k] = make_float2(-INFINITY, 0.f);
+            o[k][0] = o[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s0 + k < n) {  // uniform over the block
+                const int64_t sl = s_base + s0 + k;
+                ml[k] = ld_cg_v2(P.part_ml + sl * kBlockM + row);
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    o[k][q] = ld_cg_v4(P.part_o + (sl * (D / 4) + grp * 2 + q) * kBlockM + row);
+            }
+        }
+        float mb = M;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k)
+            if (s0 + k < n) mb = fmaxf(mb, ml[k].x);
+        const float alpha = ex2((M - mb) * c);  // 0 on the first batch
+        l_sum *= alpha;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] *= alpha;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const float e = s0 + k < n ? ex2((ml[k].x - mb) * c) : 0.f;
+            l_sum = fmaf(e, ml[k].y, l_sum);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                acc[4 * q] = fmaf(e, o[k][q].x, acc[4 * q]);
+                acc[4 * q + 1] = fmaf(e, o[k][q].y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(e, o[k][q].z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(e, o[k][q].w, acc[4 * q + 3]);
+            }
+        }
+        M = mb;
+    }
+    const int cnt = max(0, min(count_b, P.r_max));
+    const int tok = mt * P.tok_per_tile + row / P.G;
+    if (tok >= cnt) return;
+    const float inv = 1.f / l_sum;
+    const int h = g * P.G + row % P.G;
+    uint4 v;
+    v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4 *>(P.out + ((static_cast<int64_t>(b) * P.r_max + tok) * P.H + h) * D +
+                               grp * 8) = v;
 }
 
 // Fresh K/V rows into the caches.  Lets the attention grid launch at once.
@@ -708,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         for (int i = 0; i < B_COUNT; ++i)
-            mbar_init(S.bar(i), (i == B_SFREE || i == B_SFREE + 1 || i == B_PFULL) ? 4u : 1u);
+            mbar_init(S.bar(i), (i == B_PFULL || i == B_PFULL + 1) ? 4u : 1u);
         fence_mbar_init();
     }
     // Q rows past tok_per_tile * G are never loaded: keep them zero
@@ -746,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        softmax_epilogue<D>(P, S, sbase, tmem, smem);
+        softmax_epilogue<D>(P, S, tmem);
     }
     __syncthreads();
     if (warp == 1) {
@@ -792,12 +805,21 @@ bool encode_4d(CUtensorMap *map, const void *base, int B, int rows, int heads, i
 struct Plan {
     int G, tok_per_tile, n_mt, n_units, n_tiles, grid, slots, n_split;
     int64_t total;
+    bool split;  // some unit is cut into several pieces: the merge kernel runs
 };
 
-// Every CTA gets total / grid tiles; the grid is at most one CTA per SM and
-// small enough that a unit is cut into at most kMaxContrib pieces.
+// The work split, chosen by a cost model counted in tile times (one 128 x 128
+// tile is about 1 us per SM at steady state):
+//   whole units      split-major items with one split: no partials, no merge;
+//   stream-K         equal contiguous tile ranges on every SM, plus the merge;
+//   split-major      items of n_tiles / sp tiles dealt round-robin, plus the merge.
+// A piece's epilogue costs about one tile and the merge kernel (its launch, one
+// round trip to L2 and the writes, after the last attention CTA) about seven.
+// With several row tiles per KV head and caches larger than half of L2, stream-K
+// would read each K/V tile from HBM once per row tile and is not taken.
 Plan make_plan(int B, int L, int r_max, int H, int Hkv)
 {
+    constexpr double kPiece = 1.0, kMerge = 7.0;
     Plan p;
     p.G = H / Hkv;
     p.tok_per_tile = kBlockM / p.G;
@@ -805,44 +827,58 @@ Plan make_plan(int B, int L, int r_max, int H, int Hkv)
     p.n_units = B * Hkv * p.n_mt;
     p.n_tiles = (L + kBlockN - 1) / kBlockN;
     p.total = static_cast<int64_t>(p.n_units) * p.n_tiles;
-    int64_t g = device_sm_count();
-    g = std::min<int64_t>(g, p.total);
-    g = std::min<int64_t>(g, static_cast<int64_t>(p.n_units) * (kMaxContrib - 2));
-    p.grid = static_cast<int>(std::max<int64_t>(1, g));
-    // a unit of n_tiles tiles meets at most ceil(n_tiles * grid / total) + 1 ranges
-    p.slots = static_cast<int>(std::min<int64_t>(
-        kMaxContrib, (static_cast<int64_t>(p.n_tiles) * p.grid + p.total - 1) / p.total + 1));
-    p.n_split = 0;
-    // Several row tiles per KV head and caches larger than half of L2: stream-K
-    // would read each K/V tile from HBM once per row tile, so deal split-major
-    // items instead (the splits that give the fewest rounds x tiles per item).
-    const int64_t kv_bytes = 2LL * B * L * Hkv * 128 * 2;
-    if (p.n_mt > 1 && kv_bytes > (64LL << 20)) {
-        const int n_sm = device_sm_count();
-        double best = 1e30;
-        for (int sp = 1; sp <= std::min(kMaxContrib, std::max(1, p.n_tiles / 2)); ++sp) {
-            const int64_t items = static_cast<int64_t>(p.n_units) * sp;
-            const int64_t rounds = (items + n_sm - 1) / n_sm;
-            const double cost = static_cast<double>(rounds) *
-                                (std::ceil(static_cast<double>(p.n_tiles) / sp) + 2.0);
-            if (cost < best - 1e-9) {
-                best = cost;
-                p.n_split = sp;
-            }
+    const int n_sm = device_sm_count();
+    auto ceil_div = [](int64_t a, int64_t b) { return (a + b - 1) / b; };
+
+    // whole units
+    double best = static_cast<double>(ceil_div(p.n_units, n_sm)) * (p.n_tiles + kPiece);
+    p.n_split = 1;
+    // split-major items
+    for (int sp = 2; sp <= std::min(kMaxContrib, p.n_tiles / 2); ++sp) {
+        const int64_t rounds = ceil_div(static_cast<int64_t>(p.n_units) * sp, n_sm);
+        const double cost =
+            static_cast<double>(rounds) * (ceil_div(p.n_tiles, sp) + kPiece) + kMerge;
+        if (cost < best - 1e-9) {
+            best = cost;
+            p.n_split = sp;
         }
+    }
+    // stream-K
+    const int64_t kv_bytes = 2LL * B * L * Hkv * 128 * 2;
+    int64_t g = std::min<int64_t>(n_sm, p.total);
+    g = std::max<int64_t>(1, std::min<int64_t>(g, static_cast<int64_t>(p.n_units) * (kMaxContrib - 2)));
+    if (!(p.n_mt > 1 && kv_bytes > (64LL << 20))) {
+        const int64_t per_cta = ceil_div(p.total, g);
+        const double cost = static_cast<double>(per_cta) +
+                            kPiece * static_cast<double>(ceil_div(per_cta, p.n_tiles) + 1) + kMerge;
+        if (cost < best - 1e-9) {
+            best = cost;
+            p.n_split = 0;
+        }
+    }
+    if (p.n_split == 0) {
+        p.grid = static_cast<int>(g);
+        // a unit of n_tiles tiles meets at most ceil(n_tiles * grid / total) + 1 ranges
+        p.slots = static_cast<int>(std::min<int64_t>(
+            kMaxContrib, ceil_div(static_cast<int64_t>(p.n_tiles) * p.grid, p.total) + 1));
+        // a unit is split when a range boundary falls inside it
+        auto cta = [&](int64_t w) { return ((w + 1) * p.grid - 1) / p.total; };
+        p.split = false;
+        for (int64_t u = 0; u < p.n_units && !p.split; ++u)
+            p.split = cta(u * p.n_tiles) != cta(u * p.n_tiles + p.n_tiles - 1);
+    } else {
         p.grid = static_cast<int>(std::min<int64_t>(n_sm, static_cast<int64_t>(p.n_units) * p.n_split));
         p.slots = p.n_split;
+        p.split = p.n_split > 1;
     }
     return p;
 }
 
-size_t partial_offsets(const Plan &p, int D, size_t *off_tickets, size_t *off_ml, size_t *off_o)
+size_t partial_offsets(const Plan &p, int D, size_t *off_ml, size_t *off_o)
 {
     size_t off = kWsHeader;
-    *off_tickets = off;
-    off = align_up(off + static_cast<size_t>(p.n_units) * sizeof(unsigned), 256);
     *off_ml = off;
-    const size_t parts = p.slots > 1 ? static_cast<size_t>(p.n_units) * p.slots : 0;
+    const size_t parts = p.split ? static_cast<size_t>(p.n_units) * p.slots : 0;
     off = align_up(off + parts * kBlockM * sizeof(float2), 256);
     *off_o = off;
     return off + parts * kBlockM * static_cast<size_t>(D) * sizeof(float);
@@ -863,8 +899,12 @@ cudaError_t launch_typed(const Params &p, const Plan &plan, const void *q, cudaS
     cudaError_t e = launch(write_back_kernel<D>, dim3(wb_grid), dim3(256), 0, stream, p);
     if (e != cudaSuccess) return e;
     // 2. attention; its set-up overlaps the write-back (programmatic dependent launch)
-    return launch(attention_tc_kernel<D>, dim3(plan.grid), dim3(kThreads), Cfg<D>::kBytes, stream,
-                  p, tq, tk, tv);
+    e = launch(attention_tc_kernel<D>, dim3(plan.grid), dim3(kThreads), Cfg<D>::kBytes, stream, p,
+               tq, tk, tv);
+    if (e != cudaSuccess || !plan.split) return e;
+    // 3. merge of the split units: (unit, 32-row group) blocks
+    const int row_groups = (std::min(kBlockM, p.tok_per_tile * p.G) + 31) / 32;
+    return launch(merge_kernel<D>, dim3(p.n_units, row_groups), dim3(D * 4), 0, stream, p);
 }
 
 }  // namespace
@@ -874,14 +914,20 @@ bool attention_tc_supported(int dtype, int32_t seq_len, int32_t head_dim)
     return dtype == EC_BF16 && (head_dim == 64 || head_dim == 128) && seq_len >= 1;
 }
 
+int32_t attention_tc_kernel_count(int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
+                                  int32_t n_kv_heads)
+{
+    return make_plan(batch, seq_len, r_max, n_heads, n_kv_heads).split ? 3 : 2;
+}
+
 size_t attention_tc_workspace_bytes(int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
                                     int32_t n_kv_heads, int32_t head_dim)
 {
     if (batch < 1 || seq_len < 1 || r_max < 1 || n_kv_heads < 1 || n_heads < n_kv_heads)
         return kWsHeader;
     const Plan p = make_plan(batch, seq_len, r_max, n_heads, n_kv_heads);
-    size_t a, b, c;
-    return partial_offsets(p, head_dim, &a, &b, &c);
+    size_t a, b;
+    return partial_offsets(p, head_dim, &a, &b);
 }
 
 cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_new,
@@ -918,10 +964,9 @@ cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_
     p.n_split = plan.n_split;
     p.scale_log2 = scale * kLog2e;
     char *ws = static_cast<char *>(workspace);
-    size_t o_t, o_ml, o_o;
-    partial_offsets(plan, head_dim, &o_t, &o_ml, &o_o);
+    size_t o_ml, o_o;
+    partial_offsets(plan, head_dim, &o_ml, &o_o);
     p.status = reinterpret_cast<uint32_t *>(ws);
-    p.tickets = reinterpret_cast<unsigned *>(ws + o_t);
     p.part_ml = reinterpret_cast<float2 *>(ws + o_ml);
     p.part_o = reinterpret_cast<float4 *>(ws + o_o);
     return head_dim == 128 ? launch_typed<128>(p, plan, q, stream)

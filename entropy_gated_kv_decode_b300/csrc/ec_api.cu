@@ -152,6 +152,19 @@ size_t ec_attention_workspace_size(int32_t batch, int32_t seq_len, int32_t r_max
     return ec::attention_workspace_bytes(batch, seq_len, r_max, n_heads, n_kv_heads, head_dim);
 }
 
+int32_t ec_attention_kernel_count(ec_dtype dtype, int32_t batch, int32_t seq_len, int32_t r_max,
+                                  int32_t n_heads, int32_t n_kv_heads, int32_t head_dim)
+{
+    if ((dtype != EC_F32 && dtype != EC_BF16) || batch < 1 || seq_len < 1 || r_max < 0 ||
+        n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads != 0 ||
+        (head_dim != 64 && head_dim != 128))
+        return -1;
+    if (r_max == 0) return 0;
+    if (ec::attention_tc_supported(dtype, seq_len, head_dim))
+        return ec::attention_tc_kernel_count(batch, seq_len, r_max, n_heads, n_kv_heads);
+    return 2;
+}
+
 ec_status ec_selective_attention(const void *q, const void *k_new, const void *v_new,
                                  const int32_t *idx, int64_t idx_stride, const int32_t *count,
                                  void *k_cache, void *v_cache, void *out, ec_dtype dtype,
@@ -175,7 +188,7 @@ ec_status ec_selective_attention(const void *q, const void *k_new, const void *v
         return EC_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint32_t *status = static_cast<uint32_t *>(workspace);
-    if (ec::attention_tc_supported(dtype, seq_len, head_dim))  // one launch, write-back fused
+    if (ec::attention_tc_supported(dtype, seq_len, head_dim))  // write-back, attention, merge
         return launched(ec::launch_attention_tc(q, k_new, v_new, idx, idx_stride, count, k_cache,
                                                 v_cache, out, batch, seq_len, r_max, n_heads,
                                                 n_kv_heads, head_dim, scale, workspace, s));

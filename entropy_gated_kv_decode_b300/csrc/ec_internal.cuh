@@ -116,6 +116,8 @@ cudaError_t launch_attention_simt(const void *q, const void *k_cache, const void
 
 // attention_tc.cu
 bool attention_tc_supported(int dtype, int32_t seq_len, int32_t head_dim);
+int32_t attention_tc_kernel_count(int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
+                                  int32_t n_kv_heads);
 size_t attention_tc_workspace_bytes(int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
                                     int32_t n_kv_heads, int32_t head_dim);
 cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_new,

@@ -198,6 +198,14 @@ ec_status ec_build_recompute_set(const uint8_t *is_masked, const int32_t *decode
 size_t ec_attention_workspace_size(int32_t batch, int32_t seq_len, int32_t r_max,
                                    int32_t n_heads, int32_t n_kv_heads, int32_t head_dim);
 
+/* Kernels one ec_selective_attention call with these arguments launches on the
+ * current device (for launch accounting): bf16 with head_dim 64/128 runs the
+ * KV write-back, the tensor-core attention and, when the keys of some unit are
+ * split over several CTAs, a merge kernel; float32 runs a write-back and the
+ * CUDA-core attention.  0 when r_max == 0; -1 for arguments the call rejects. */
+int32_t ec_attention_kernel_count(ec_dtype dtype, int32_t batch, int32_t seq_len, int32_t r_max,
+                                  int32_t n_heads, int32_t n_kv_heads, int32_t head_dim);
+
 /*
  * Write the freshly projected K/V rows into the caches and run bidirectional
  * attention of the recomputed query rows over every cached key ([EC-it] step 2:
