@@ -400,7 +400,6 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
-    const int ltid = (warp - 2) * 32 + lane;  // 0 .. 127 over the softmax warps
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = P.scale_log2;           // log2 units per raw score unit
     const float move = 8.f / c;             // raw-score growth that moves the reference

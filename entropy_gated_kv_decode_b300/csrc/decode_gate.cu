@@ -399,9 +399,22 @@ __device__ void finish_sequence(const Args &A, int b, int r0, int cnt)
     __shared__ int s_sel[kMaxUnmask];
     const int lane = threadIdx.x & 31;
     const bool staged = cnt <= kMaxStagedRows;
-    if (staged)
-        for (int i = lane; i < cnt; i += 32)
-            s_key[i] = select_key(__ldcg(A.conf_out + r0 + i), __ldg(A.row_pos + r0 + i));
+    if (staged)  // eight rows per lane per round, every load issued before any is used
+        for (int i0 = 0; i0 < cnt; i0 += 32 * 8) {
+            float cf[8];
+            int ps[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * 32 + lane;
+                cf[u] = i < cnt ? __ldcg(A.conf_out + r0 + i) : 0.f;
+                ps[u] = i < cnt ? __ldg(A.row_pos + r0 + i) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * 32 + lane;
+                if (i < cnt) s_key[i] = select_key(cf[u], ps[u]);
+            }
+        }
     __syncwarp();
 
     const int take = min(A.n_unmask, cnt);

@@ -75,7 +75,9 @@ int ec_abi_version(void);
 /*
  * Zero a workspace (cudaMemsetAsync).  Every workspace must be zeroed once
  * before its first use; the kernels leave their counters at zero on exit, so
- * later calls need no further reset.  Returns EC_ERR_CUDA if the memset fails.
+ * later calls need no further reset.  After a call whose device status reports
+ * EC_DEV_TIMEOUT the counters may not be back at zero: zero the workspace again.
+ * Returns EC_ERR_CUDA if the memset fails.
  */
 ec_status ec_workspace_init(void *workspace, size_t workspace_bytes, ec_stream_t stream);
 

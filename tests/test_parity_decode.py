@@ -133,6 +133,33 @@ def test_repeated_calls_reuse_the_workspace(orc):
     check_decode(first, ref, st, w.n_unmask, w.tau, st.step)
 
 
+@pytest.mark.parametrize("dt", [synth.BF16, synth.F32])
+def test_batched_ragged_vocab(orc, dt):
+    # full batched size with an odd vocabulary: rows cut over two or three CTAs,
+    # the piece ending each row holding the vocab % 8 (bf16) or % 4 (fp32) tail
+    w = synth.scaled(synth.WORKLOADS["batched"], vocab=152063, logits_dtype=dt)
+    per_vec = 8 if dt == synth.BF16 else 4
+    _case(orc, w, seed=31, row_stride=-(-w.vocab // per_vec) * per_vec)
+
+
+def test_repeated_calls_split_rows(orc):
+    # rows split over several CTAs: the tickets must return to zero after every
+    # call and repeated calls give identical results
+    nat = native()
+    w = synth.WORKLOADS["long_ctx"]
+    rng = np.random.default_rng(41)
+    st = synth.make_state(rng, w)
+    logits = synth.make_logits(rng, w.n_rows, w.vocab, w.logits_dtype, w.near_uniform_frac)
+    ws = nat.new_workspace(nat.ec_decode_workspace_size(w.n_rows, w.batch))
+    runs = [run_decode_gpu(nat, logits, st, w.n_unmask, w.tau, st.step, workspace=ws)
+            for _ in range(4)]
+    for gpu in runs[1:]:
+        for k in ("token", "conf", "entropy", "unmask_rows", "refresh", "max_entropy"):
+            assert np.array_equal(gpu[k], runs[0][k]), k
+    ref = run_decode_oracle(orc, logits, st, w.n_unmask, w.tau, st.step)
+    check_decode(runs[0], ref, st, w.n_unmask, w.tau, st.step)
+
+
 def test_report_exclusions():
     for name, seed, excl in REPORT:
         if excl:
