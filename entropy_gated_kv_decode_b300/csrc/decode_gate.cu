@@ -341,6 +341,14 @@ struct Args {
     Partial *parts;
 };
 
+// A piece: units [ua, ub) of row `row`, its partial slot (the row's pieces in CTA
+// order) and the row's number of pieces.
+struct Piece {
+    int row;
+    int64_t ua, ub;
+    int slot, n_contrib;
+};
+
 // First unit of CTA c's range, and the CTA whose range holds unit u.
 __device__ __forceinline__ int64_t range_begin(const Args &A, int c)
 {
@@ -349,6 +357,20 @@ __device__ __forceinline__ int64_t range_begin(const Args &A, int c)
 __device__ __forceinline__ int cta_of(const Args &A, int64_t u)
 {
     return static_cast<int>(((u + 1) * A.grid - 1) / A.total);
+}
+
+// This CTA's piece of row i (its range [u_begin, u_end) meets the row).
+__device__ __forceinline__ Piece row_piece(const Args &A, int i, int64_t u_begin, int64_t u_end)
+{
+    Piece p;
+    const int64_t base = static_cast<int64_t>(i) * A.units;
+    p.row = i;
+    p.ua = max(u_begin, base) - base;
+    p.ub = min(u_end, base + A.units) - base;
+    const int c0 = cta_of(A, base);
+    p.slot = static_cast<int>(blockIdx.x) - c0;
+    p.n_contrib = cta_of(A, base + A.units - 1) - c0 + 1;
+    return p;
 }
 
 __device__ __forceinline__ unsigned long long select_key(float conf, int pos)
@@ -476,19 +498,16 @@ __device__ void finish_sequence(const Args &A, int b, int r0, int cnt)
     __syncwarp();  // s_key / s_sel are reused by the next call
 }
 
-// Finisher warp: for one finished piece of row i (its CTA partial p, in every
-// lane): publish it; the row's last contributor merges all of them and writes
+// Finisher warp: for one finished piece (its CTA partial p, in every lane):
+// publish it; the row's last contributor merges all of them and writes
 // token / conf / entropy; the sequence's last row ranks and gates.
-__device__ void finish_piece(const Args &A, int i, Partial p)
+__device__ void finish_piece(const Args &A, const Piece &pc, Partial p)
 {
     const int lane = threadIdx.x & 31;
-    const int c0 = cta_of(A, static_cast<int64_t>(i) * A.units);
-    const int c1 = cta_of(A, static_cast<int64_t>(i) * A.units + A.units - 1);
-    const int n_contrib = c1 - c0 + 1;
+    const int i = pc.row, n_contrib = pc.n_contrib, slot = pc.slot;
     int last = 1;
     if (n_contrib > 1) {
         if (lane == 0) {
-            const int slot = static_cast<int>(blockIdx.x) - c0;
             __stcg(reinterpret_cast<float4 *>(A.parts + static_cast<int64_t>(i) * kMaxSplits + slot),
                    make_float4(p.m, p.s, p.t, __int_as_float(p.idx)));
             last = ticket(A.row_ctr + i, static_cast<unsigned>(n_contrib - 1)) ==
@@ -535,16 +554,93 @@ __device__ void finish_piece(const Args &A, int i, Partial p)
     finish_sequence(A, b, lo, cnt);
 }
 
+// A consumer warp's partial of a piece (and, from warp 0, the piece itself) into
+// the finisher's queue; a piece with row -1 tells the finisher that no more come.
+__device__ __forceinline__ bool hand_over(const Sync &S, const Piece &pc, const Partial &p,
+                                          uint32_t &n_pieces, Partial (*s_piece)[kConsumerWarps],
+                                          Piece *s_info)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slot = n_pieces % kPieceSlots;
+    if (n_pieces >= static_cast<uint32_t>(kPieceSlots) &&
+        !__all_sync(0xffffffffu, S.wait(D_PEMPTY + slot, ((n_pieces / kPieceSlots) - 1) & 1)))
+        return false;
+    if (lane == 0) {
+        s_piece[slot][warp] = p;
+        if (warp == 0) s_info[slot] = pc;
+        ptx::mbar_arrive(S.bar(D_PFULL + slot));  // release: the partial is visible
+    }
+    ++n_pieces;
+    return true;
+}
+
+// Consumer side of one piece: fold its stages (and the tail unit when the piece
+// ends the row) into the thread's state and hand the block's partial to the
+// finisher.  Returns false after a failed wait.
+template <typename T>
+__device__ bool fold_piece(const Args &A, const Sync &S, const uint8_t *ring, const Piece &pc,
+                           uint32_t &it, uint32_t &n_pieces, Partial (*s_piece)[kConsumerWarps],
+                           Piece *s_info)
+{
+    constexpr int E = Elem<T>::kPerVec;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int64_t vb = min(pc.ub, A.nvec);
+    Fold f;
+    f.reset();
+    for (int64_t v = pc.ua; v < vb; v += kVecPerChunk, ++it) {
+        const int s = it % kStages;
+        if (!__all_sync(0xffffffffu, S.wait(D_FULL + s, (it / kStages) & 1))) return false;
+        const int nv = static_cast<int>(std::min<int64_t>(kVecPerChunk, vb - v));
+        const uint4 *src = reinterpret_cast<const uint4 *>(ring + s * kChunk);
+        uint4 raw[kVecPerThread];
+#pragma unroll
+        for (int u = 0; u < kVecPerThread; ++u) {
+            const int j = tid + u * kConsumers;
+            const uint32_t ni = Elem<T>::kNegInfWord;
+            raw[u] = j < nv ? src[j] : make_uint4(ni, ni, ni, ni);
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(S.bar(D_EMPTY + s));
+        const int vb0 = static_cast<int>(v) + tid;
+        if constexpr (sizeof(T) == 2) {
+            uint32_t wv[kVecPerThread * 4];
+#pragma unroll
+            for (int u = 0; u < kVecPerThread; ++u) {
+                wv[4 * u] = raw[u].x;
+                wv[4 * u + 1] = raw[u].y;
+                wv[4 * u + 2] = raw[u].z;
+                wv[4 * u + 3] = raw[u].w;
+            }
+            f.add_bf16(wv, [vb0](int k) { return (vb0 + (k / E) * kConsumers) * E + (k % E); });
+        } else {
+            float x[kVecPerThread * E];
+#pragma unroll
+            for (int u = 0; u < kVecPerThread; ++u) Elem<T>::unpack(raw[u], x + u * E);
+            f.add(x, [vb0](int k) { return (vb0 + (k / E) * kConsumers) * E + (k % E); });
+        }
+    }
+    // the tail unit (vocab % E last elements) belongs to the piece ending the row
+    if (A.tail > 0 && pc.ub == A.units && tid < A.tail) {
+        const int j = static_cast<int>(A.nvec * E) + tid;
+        const T *row = static_cast<const T *>(A.logits) + static_cast<int64_t>(pc.row) * A.row_stride;
+        float x[1] = {Elem<T>::scalar(row + j)};
+        f.add(x, [j](int) { return j; });
+    }
+    Partial p = f.partial();
+    warp_merge(p);
+    return hand_over(S, pc, p, n_pieces, s_piece, s_info);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const Args A)
 {
-    constexpr int E = Elem<T>::kPerVec;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t ring_u32 = ptx::smem_u32(ring);
     __shared__ int s_abort;
     __shared__ Partial s_piece[kPieceSlots][kConsumerWarps];
+    __shared__ Piece s_info[kPieceSlots];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     Sync S{ring_u32 + kStages * kChunk, reinterpret_cast<volatile int *>(&s_abort), A.status};
 
@@ -564,23 +660,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
 
     const int64_t u_begin = A.total ? range_begin(A, blockIdx.x) : 0;
     const int64_t u_end = A.total ? range_begin(A, blockIdx.x + 1) : 0;
-    const int row_first = static_cast<int>(u_begin / (A.units > 0 ? A.units : 1));
-    const int row_last = u_end > u_begin ? static_cast<int>((u_end - 1) / A.units) : row_first - 1;
+    const int64_t su = A.units > 0 ? A.units : 1;
+    const int row_first = static_cast<int>(u_begin / su);
+    const int row_last = u_end > u_begin ? static_cast<int>((u_end - 1) / su) : row_first - 1;
 
     if (warp == kConsumerWarps) {
-        // ---- producer: one thread streams the vector part of every row piece ----
+        // ---- producer: one thread streams the vector part of every piece ----
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
             for (int i = row_first; i <= row_last && ok; ++i) {
-                const int64_t base = static_cast<int64_t>(i) * A.units;
-                const int64_t va = max(u_begin, base) - base;
-                const int64_t vb = min(min(u_end, base + A.units) - base, A.nvec);
-                const char *row =
-                    static_cast<const char *>(A.logits) + static_cast<int64_t>(i) * A.row_stride * sizeof(T);
-                for (int64_t v = va; v < vb && ok; v += kVecPerChunk, ++it) {
+                const Piece pc = row_piece(A, i, u_begin, u_end);
+                const char *row = static_cast<const char *>(A.logits) +
+                                  static_cast<int64_t>(i) * A.row_stride * sizeof(T);
+                const int64_t vb = min(pc.ub, A.nvec);
+                for (int64_t v = pc.ua; v < vb && ok; v += kVecPerChunk, ++it) {
                     const int s = it % kStages;
-                    if (it >= static_cast<uint32_t>(kStages)) ok = S.wait(D_EMPTY + s, ((it / kStages) - 1) & 1);
+                    if (it >= static_cast<uint32_t>(kStages))
+                        ok = S.wait(D_EMPTY + s, ((it / kStages) - 1) & 1);
                     if (!ok) break;
                     const uint32_t bytes = static_cast<uint32_t>(std::min<int64_t>(kVecPerChunk, vb - v) * 16);
                     ptx::mbar_expect_tx(S.bar(D_FULL + s), bytes);
@@ -595,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
     }
 
     if (warp == kConsumerWarps + 1) {
-        // ---- finisher: empty sequences (CTA 0), then every piece of this range ----
+        // ---- finisher: empty sequences (CTA 0), then every piece of this CTA ----
         if (blockIdx.x == 0) {
             for (int b = lane; b <= A.batch; b += 32) {
                 const int o = __ldg(A.offsets + b);
@@ -613,80 +710,32 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
                 if (bad) flag_status(A.status, EC_DEV_BAD_OFFSETS);
             }
         }
-        uint32_t pc = 0;
-        for (int i = row_first; i <= row_last; ++i, ++pc) {
+        for (uint32_t pc = 0;; ++pc) {
             const int slot = pc % kPieceSlots;
             if (!S.wait(D_PFULL + slot, (pc / kPieceSlots) & 1)) break;
+            const Piece piece = s_info[slot];
             Partial p = lane < kConsumerWarps ? s_piece[slot][lane] : empty_partial();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(S.bar(D_PEMPTY + slot));
+            if (piece.row < 0) break;  // the consumers' end marker
             warp_merge(p);
-            finish_piece(A, i, p);
+            finish_piece(A, piece, p);
         }
         return;
     }
 
     // ---- consumers: fold each stage, hand every finished piece to the finisher ----
-    uint32_t it = 0, pc = 0;
-    for (int i = row_first; i <= row_last; ++i, ++pc) {
-        const int64_t base = static_cast<int64_t>(i) * A.units;
-        const int64_t ua = max(u_begin, base) - base;
-        const int64_t ub = min(u_end, base + A.units) - base;
-        const int64_t vb = min(ub, A.nvec);
-        Fold f;
-        f.reset();
-        bool ok = true;
-        for (int64_t v = ua; v < vb; v += kVecPerChunk, ++it) {
-            const int s = it % kStages;
-            ok = __all_sync(0xffffffffu, S.wait(D_FULL + s, (it / kStages) & 1));
-            if (!ok) break;
-            const int nv = static_cast<int>(std::min<int64_t>(kVecPerChunk, vb - v));
-            const uint4 *src = reinterpret_cast<const uint4 *>(ring + s * kChunk);
-            uint4 raw[kVecPerThread];
-#pragma unroll
-            for (int u = 0; u < kVecPerThread; ++u) {
-                const int j = tid + u * kConsumers;
-                const uint32_t ni = Elem<T>::kNegInfWord;
-                raw[u] = j < nv ? src[j] : make_uint4(ni, ni, ni, ni);
-            }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(S.bar(D_EMPTY + s));
-            const int vb0 = static_cast<int>(v) + tid;
-            if constexpr (sizeof(T) == 2) {
-                uint32_t wv[kVecPerThread * 4];
-#pragma unroll
-                for (int u = 0; u < kVecPerThread; ++u) {
-                    wv[4 * u] = raw[u].x;
-                    wv[4 * u + 1] = raw[u].y;
-                    wv[4 * u + 2] = raw[u].z;
-                    wv[4 * u + 3] = raw[u].w;
-                }
-                f.add_bf16(wv, [vb0](int k) { return (vb0 + (k / E) * kConsumers) * E + (k % E); });
-            } else {
-                float x[kVecPerThread * E];
-#pragma unroll
-                for (int u = 0; u < kVecPerThread; ++u) Elem<T>::unpack(raw[u], x + u * E);
-                f.add(x, [vb0](int k) { return (vb0 + (k / E) * kConsumers) * E + (k % E); });
-            }
-        }
-        if (!ok) break;  // the finisher's wait gives up too, and the CTA unwinds
-        // the tail unit (vocab % E last elements) belongs to the range holding it
-        if (A.tail > 0 && ub == A.units && tid < A.tail) {
-            const int j = static_cast<int>(A.nvec * E) + tid;
-            const T *row = static_cast<const T *>(A.logits) + static_cast<int64_t>(i) * A.row_stride;
-            float x[1] = {Elem<T>::scalar(row + j)};
-            f.add(x, [j](int) { return j; });
-        }
-        Partial p = f.partial();
-        warp_merge(p);
-        const int slot = pc % kPieceSlots;
-        if (pc >= static_cast<uint32_t>(kPieceSlots) &&
-            !__all_sync(0xffffffffu, S.wait(D_PEMPTY + slot, ((pc / kPieceSlots) - 1) & 1)))
-            break;
-        if (lane == 0) {
-            s_piece[slot][warp] = p;
-            ptx::mbar_arrive(S.bar(D_PFULL + slot));  // release: the partial is visible
-        }
+    uint32_t it = 0, n_pieces = 0;
+    bool ok = true;
+    for (int i = row_first; i <= row_last && ok; ++i)
+        ok = fold_piece<T>(A, S, ring, row_piece(A, i, u_begin, u_end), it, n_pieces, s_piece,
+                           s_info);
+    if (ok) {  // after a failure the finisher's wait gives up by itself
+        Piece end;
+        end.row = -1;
+        end.ua = end.ub = 0;
+        end.slot = end.n_contrib = 0;
+        hand_over(S, end, empty_partial(), n_pieces, s_piece, s_info);
     }
 }
 
