@@ -577,9 +577,21 @@ __device__ __forceinline__ bool hand_over(const Sync &S, const Piece &pc, const 
 // Consumer side of one piece: fold its stages (and the tail unit when the piece
 // ends the row) into the thread's state and hand the block's partial to the
 // finisher.  Returns false after a failed wait.
+struct RingPos {
+    int s;         // stage index
+    uint32_t ph;   // its phase parity
+    __device__ void next()
+    {
+        if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
 template <typename T>
 __device__ bool fold_piece(const Args &A, const Sync &S, const uint8_t *ring, const Piece &pc,
-                           uint32_t &it, uint32_t &n_pieces, Partial (*s_piece)[kConsumerWarps],
+                           RingPos &rp, uint32_t &n_pieces, Partial (*s_piece)[kConsumerWarps],
                            Piece *s_info)
 {
     constexpr int E = Elem<T>::kPerVec;
@@ -587,17 +599,21 @@ __device__ bool fold_piece(const Args &A, const Sync &S, const uint8_t *ring, co
     const int64_t vb = min(pc.ub, A.nvec);
     Fold f;
     f.reset();
-    for (int64_t v = pc.ua; v < vb; v += kVecPerChunk, ++it) {
-        const int s = it % kStages;
-        if (!__all_sync(0xffffffffu, S.wait(D_FULL + s, (it / kStages) & 1))) return false;
-        const int nv = static_cast<int>(std::min<int64_t>(kVecPerChunk, vb - v));
-        const uint4 *src = reinterpret_cast<const uint4 *>(ring + s * kChunk);
+    for (int64_t v = pc.ua; v < vb; v += kVecPerChunk, rp.next()) {
+        const int s = rp.s;
+        if (!__all_sync(0xffffffffu, S.wait(D_FULL + s, rp.ph))) return false;
+        const uint4 *src = reinterpret_cast<const uint4 *>(ring + s * kChunk) + tid;
         uint4 raw[kVecPerThread];
+        if (vb - v >= kVecPerChunk) {  // a full stage
 #pragma unroll
-        for (int u = 0; u < kVecPerThread; ++u) {
-            const int j = tid + u * kConsumers;
-            const uint32_t ni = Elem<T>::kNegInfWord;
-            raw[u] = j < nv ? src[j] : make_uint4(ni, ni, ni, ni);
+            for (int u = 0; u < kVecPerThread; ++u) raw[u] = src[u * kConsumers];
+        } else {
+            const int nv = static_cast<int>(vb - v) - tid;
+#pragma unroll
+            for (int u = 0; u < kVecPerThread; ++u) {
+                const uint32_t ni = Elem<T>::kNegInfWord;
+                raw[u] = u * kConsumers < nv ? src[u * kConsumers] : make_uint4(ni, ni, ni, ni);
+            }
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(S.bar(D_EMPTY + s));
@@ -725,10 +741,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
     }
 
     // ---- consumers: fold each stage, hand every finished piece to the finisher ----
-    uint32_t it = 0, n_pieces = 0;
+    RingPos rp{0, 0u};
+    uint32_t n_pieces = 0;
     bool ok = true;
     for (int i = row_first; i <= row_last && ok; ++i)
-        ok = fold_piece<T>(A, S, ring, row_piece(A, i, u_begin, u_end), it, n_pieces, s_piece,
+        ok = fold_piece<T>(A, S, ring, row_piece(A, i, u_begin, u_end), rp, n_pieces, s_piece,
                            s_info);
     if (ok) {  // after a failure the finisher's wait gives up by itself
         Piece end;
