@@ -90,3 +90,16 @@ def test_zero_rows(orc):
     w = synth.scaled(synth.WORKLOADS["single_seq"], seq_len=256, n_heads=4, n_kv_heads=4)
     idx = np.full((1, 8), -1, np.int32)
     run_case(orc, w, idx, np.zeros(1, np.int32), 8)
+
+
+@pytest.mark.parametrize("batch,L,H,r", [(1, 2048, 4, 48), (1, 1024, 32, 48), (2, 512, 32, 100),
+                                         (1, 1100, 4, 130)])
+def test_few_units(orc, batch, L, H, r):
+    # few units (4 to 64), each a whole unit on one CTA; the last case also has a
+    # ragged key tile and a partial second row tile
+    w = synth.scaled(synth.WORKLOADS["single_seq"], batch=batch, seq_len=L, n_heads=H,
+                     n_kv_heads=H, qkv_std=1.0)
+    rng = np.random.default_rng(L + H + r)
+    cnt = np.full(batch, r, np.int32)
+    idx = synth.random_index_set(rng, batch, L, cnt, stride=r)
+    run_case(orc, w, idx, cnt, r, seed=L + r)
