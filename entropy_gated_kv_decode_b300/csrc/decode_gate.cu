@@ -660,7 +660,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     Sync S{ring_u32 + kStages * kChunk, reinterpret_cast<volatile int *>(&s_abort), A.status};
 
-    pdl_launch_dependents();
     if (tid == 0) {
         s_abort = 0;
         for (int i = 0; i < D_COUNT; ++i) {
@@ -747,6 +746,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
     for (int i = row_first; i <= row_last && ok; ++i)
         ok = fold_piece<T>(A, S, ring, row_piece(A, i, u_begin, u_end), rp, n_pieces, s_piece,
                            s_info);
+    // The next kernel may become resident once every CTA has streamed its bytes:
+    // triggered earlier, its CTAs would take SM slots this grid's CTAs still need.
+    pdl_launch_dependents();
     if (ok) {  // after a failure the finisher's wait gives up by itself
         Piece end;
         end.row = -1;
