@@ -47,6 +47,30 @@ DEFAULT_WORKLOAD = "single_seq"
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
+# DRAM bytes (read + write) per call of the dominant call, from one ncu capture of
+# the same bench command (dram__bytes_read.sum + dram__bytes_write.sum summed over
+# the call's kernels, per launch; profiles/ has the summary).  Used only while the
+# kernel sources hash to the value they had when the counters were taken.
+MEASURED_TRAFFIC = {}
+
+
+def kernel_sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "entropy_gated_kv_decode_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, call: str):
+    t = MEASURED_TRAFFIC.get((workload, call))
+    if t is None or t["sources"] != kernel_sources_hash():
+        return None
+    return t["bytes"]
+
 
 class L2Flush:
     """Evicts L2 between timed steps: writes one 256 MiB buffer, then reads a
@@ -421,11 +445,11 @@ def run_ours(args):
             roof = {"bound": "tensor", "achieved": att_tflops, "peak": tc, "unit": "TFLOP/s",
                     "frac": att_tflops / tc}
         roof["kernel"] = "ec_selective_attention (write-back + attention + merge)"
+        roof["traffic"] = measured_traffic(w.name, "attention")
     else:
         g = parts["decode_gate"]["gbs"]
         roof = {"bound": "hbm", "achieved": g, "peak": hbm, "unit": "GB/s", "frac": g / hbm,
-                "kernel": "decode_gate_kernel"}
-    roof["traffic"] = None
+                "kernel": "decode_gate_kernel", "traffic": measured_traffic(w.name, "decode")}
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
 
     cpu = None
