@@ -51,7 +51,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # the same bench command (dram__bytes_read.sum + dram__bytes_write.sum summed over
 # the call's kernels, per launch; profiles/ has the summary).  Used only while the
 # kernel sources hash to the value they had when the counters were taken.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {
+    # profiles/launches_single_seq.md: attention_tc_kernel 17,260,288 B + write_back_kernel
+    # 794,624 B per call (median of 21 launches; the output writes stay in L2)
+    ("single_seq", "attention"): {"sources": "ea3c8e59a7c95f7a", "bytes": 18054912},
+}
 
 
 def kernel_sources_hash() -> str:
