@@ -79,24 +79,6 @@ __device__ __forceinline__ void fence_async_smem()
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// bar.red.or on a named barrier: true in every participating thread when any of
-// them passed true.
-__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t threads, bool v)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(threads)
-        : "memory");
-    return r != 0;
-}
 
 // ---- TMA ----
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
@@ -281,14 +263,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-// Byte offset of 16-byte chunk `chunk` of row `row` inside a 128B-swizzled
-// K-major tile whose 64-element columns are `col_bytes` apart.
-__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk16, uint32_t col_bytes)
-{
-    const int col = chunk16 >> 3, c = chunk16 & 7;
-    return static_cast<uint32_t>(col) * col_bytes + static_cast<uint32_t>(row) * 128u +
-           (static_cast<uint32_t>(c ^ (row & 7)) << 4);
-}
 
 // ---- bounded waits on a CTA's array of mbarriers ----
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s: a wait this long is a fault
