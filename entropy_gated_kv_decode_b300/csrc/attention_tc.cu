@@ -812,13 +812,15 @@ struct Plan {
 //   whole units      split-major items with one split: no partials, no merge;
 //   stream-K         equal contiguous tile ranges on every SM, plus the merge;
 //   split-major      items of n_tiles / sp tiles dealt round-robin, plus the merge.
-// A piece's epilogue costs about one tile and the merge kernel (its launch, one
-// round trip to L2 and the writes, after the last attention CTA) about seven.
+// A piece's epilogue costs about one tile and the merge kernel about five (its
+// CTAs become resident while the attention grid runs; after it, one round trip
+// to L2 and the writes).  Calibrated on whole decode steps: the single-sequence
+// step (32 units of 8 tiles) is faster cut into 4 splits than in whole units.
 // With several row tiles per KV head and caches larger than half of L2, stream-K
 // would read each K/V tile from HBM once per row tile and is not taken.
 Plan make_plan(int B, int L, int r_max, int H, int Hkv)
 {
-    constexpr double kPiece = 1.0, kMerge = 7.0;
+    constexpr double kPiece = 1.0, kMerge = 5.0;
     Plan p;
     p.G = H / Hkv;
     p.tok_per_tile = kBlockM / p.G;
