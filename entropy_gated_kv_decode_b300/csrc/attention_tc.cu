@@ -605,7 +605,8 @@ __global__ void __launch_bounds__(D * 4) merge_kernel(const Params P)
         const int64_t base = static_cast<int64_t>(unit) * P.n_tiles;
         n = cta_of(P, base + P.n_tiles - 1) - cta_of(P, base) + 1;
     }
-    if (n < 2 || row >= P.tok_per_tile * P.G) return;  // whole units were written by their piece
+    // whole units were written by their piece; rows past r_max hold no token
+    if (n < 2 || row >= P.tok_per_tile * P.G || mt * P.tok_per_tile + row / P.G >= P.r_max) return;
     const int count_b = __ldg(P.count + b);
     const float c = P.scale_log2;
     const int64_t s_base = static_cast<int64_t>(unit) * P.slots;
@@ -903,8 +904,9 @@ cudaError_t launch_typed(const Params &p, const Plan &plan, const void *q, cudaS
     e = launch(attention_tc_kernel<D>, dim3(plan.grid), dim3(kThreads), Cfg<D>::kBytes, stream, p,
                tq, tk, tv);
     if (e != cudaSuccess || !plan.split) return e;
-    // 3. merge of the split units: (unit, 32-row group) blocks
-    const int row_groups = (std::min(kBlockM, p.tok_per_tile * p.G) + 31) / 32;
+    // 3. merge of the split units: (unit, 32-row group) blocks over the rows a unit
+    //    can hold (at most r_max tokens)
+    const int row_groups = (std::min(kBlockM, std::min(p.tok_per_tile, p.r_max) * p.G) + 31) / 32;
     return launch(merge_kernel<D>, dim3(p.n_units, row_groups), dim3(D * 4), 0, stream, p);
 }
 
