@@ -52,9 +52,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # the call's kernels, per launch; profiles/ has the summary).  Used only while the
 # kernel sources hash to the value they had when the counters were taken.
 MEASURED_TRAFFIC = {
-    # profiles/launches_single_seq.md: attention_tc_kernel 17,260,288 B + write_back_kernel
-    # 794,624 B per call (median of 21 launches; the output writes stay in L2)
-    ("single_seq", "attention"): {"sources": "ea3c8e59a7c95f7a", "bytes": 18054912},
+    # profiles/launches_single_seq.md: write_back_kernel 794,880 B + attention_tc_kernel
+    # 17,260,544 B + merge_kernel 3,208,448 B per call (medians of 21 launches; ncu empties
+    # the caches between kernels, so the merge reads its partials from DRAM; writes stay in L2)
+    ("single_seq", "attention"): {"sources": "1a8ff541fc1a3a54", "bytes": 21263872},
 }
 
 
