@@ -106,3 +106,61 @@ def test_recompute_set_and_attention_reject_bad_arguments(L):
     assert call(q=0x1004) == -4
     assert call(ws=0x10040) == -5
     assert call(wsb=8) == -5
+
+
+def test_projection_and_gather_reject_bad_arguments(L):
+    p = L.ec_qkv_projection
+    #       x       count   B  R   hidden  w       width  q       k       v       ws       wsb
+    base = [0x1000, 0x2000, 1, 48, 4096, 0x3000, 12288, 0x4000, 0x5000, 0x6000, 0x10000, 256, None]
+
+    def proj(i, v):
+        args = list(base)
+        args[i] = v
+        return p(*args)
+
+    assert proj(4, 4100) == -2     # hidden not a multiple of the 64-wide K step
+    assert proj(6, 12290) == -2    # width not a multiple of 64
+    assert proj(2, 0) == -2        # no sequences
+    assert proj(10, None) == -1    # no workspace
+    assert proj(0, None) == -1     # no X with rows to project
+    assert proj(0, 0x1008) == -4   # X not 16-byte aligned
+    assert proj(10, 0x10010) == -5  # workspace not aligned
+    assert proj(11, 16) == -5      # workspace below the status header
+
+    e = L.ec_embed_rows
+    #       table   rows    hidden idx     stride count   tokens  masked  mask_id B  L     R   x       ws       wsb
+    base = [0x1000, 126465, 4096, 0x2000, 48, 0x3000, 0x4000, 0x5000, 126464, 1, 1024, 48, 0x6000, 0x10000, 256, None]
+
+    def emb(i, v):
+        args = list(base)
+        args[i] = v
+        return e(*args)
+
+    assert emb(2, 12) == -2        # hidden not a multiple of 8
+    assert emb(8, 126465) == -2    # mask id outside the table
+    assert emb(4, 40) == -2        # index stride below r_max
+    assert emb(5, None) == -1      # no counts
+    assert emb(0, None) == -1      # no table with rows to gather
+    assert emb(12, 0x6008) == -4   # X not 16-byte aligned
+    assert emb(14, 8) == -5        # workspace below the status header
+
+
+def test_noalloc_decode_rejects_bad_arguments(L):
+    f = L.ec_decode_step_noalloc
+    #       logits  dt row_stride n_rows vocab   offsets row_pos B  L     n  tau  step tok     conf    ent     unmask  emax    refresh masked  tokens  dstep   stream
+    base = [0x1000, 1, 126464,    32,    126464, 0x2000, 0x3000, 1, 1024, 2, 0.5, 0,   0x4000, 0x5000, 0x6000, 0x7000, 0x8000, 0x9000, 0xa000, 0xb000, 0xc000, None]
+
+    def call(i, v):
+        args = list(base)
+        args[i] = v
+        return f(*args)
+
+    assert call(1, 7) == -3           # dtype
+    assert call(4, 0) == -2           # vocab
+    assert call(9, 0) == -2           # n_unmask
+    assert call(2, 100) == -2         # row stride below vocab
+    assert call(5, None) == -1        # offsets
+    assert call(0, None) == -1        # logits with rows
+    assert call(0, 0x1008) == -4      # logits not 16-byte aligned
+    # a request whose scratch exceeds the fixed 2 MiB array (checked before any CUDA call)
+    assert call(3, 1 << 20) == -8     # EC_ERR_SCRATCH_LIMIT
