@@ -201,9 +201,29 @@ class ClockSampler:
 # our CUDA path
 
 
+class Packed:
+    """Tensors laid out in one byte buffer, each 256-byte aligned, so that a step's
+    inputs (or results) move between host and device in a single copy."""
+
+    def __init__(self, specs, device, pinned=False):
+        import torch
+        self.offsets, off = [], 0
+        for _, shape, dtype in specs:
+            self.offsets.append(off)
+            n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            off += (n + 255) // 256 * 256
+        self.nbytes = off
+        self.blob = torch.empty(off, dtype=torch.uint8, device=device, pin_memory=pinned)
+        self.views = {}
+        for (name, shape, dtype), o in zip(specs, self.offsets):
+            n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            self.views[name] = self.blob[o:o + n].view(dtype).view(shape)
+
+
 class GpuStep:
     """Device-resident inputs, outputs and workspaces of one step, and the three
-    C-ABI calls that make it up."""
+    C-ABI calls that make it up.  The inputs that change every step (logits, Q and
+    the fresh K/V rows) share one device buffer, and so do the step's results."""
 
     def __init__(self, nat, w: synth.Workload, st, logits, att, device, stream):
         import torch
@@ -218,24 +238,37 @@ class GpuStep:
 
         self.up = up
         B, L, N, n = w.batch, w.seq_len, w.n_rows, w.n_unmask
-        self.logits = up(logits)
+        i32, f32, u8 = torch.int32, torch.float32, torch.uint8
+        def tdtype(a):  # bf16 arrays are held as uint16 bit patterns
+            return torch.bfloat16 if a.dtype == np.uint16 else torch.from_numpy(a.ravel()[:0]).dtype
+
+        self.in_specs = [("logits", logits.shape, tdtype(logits)), ("q", att.q.shape, tdtype(att.q)),
+                         ("k_new", att.k_new.shape, tdtype(att.k_new)),
+                         ("v_new", att.v_new.shape, tdtype(att.v_new))]
+        self.inputs = Packed(self.in_specs, device)
+        for name, a in (("logits", logits), ("q", att.q), ("k_new", att.k_new), ("v_new", att.v_new)):
+            self.inputs.views[name].copy_(up(a))
+        self.out_specs = [("token", (N,), i32), ("conf", (N,), f32), ("entropy", (N,), f32),
+                          ("unmask", (B * n,), i32), ("emax", (B,), f32), ("refresh", (B,), u8),
+                          ("idx_next", (B, L), i32), ("count_next", (B,), i32),
+                          ("out", att.q.shape, self.inputs.views["q"].dtype)]
+        self.results = Packed(self.out_specs, device)
+        r = self.results.views
+        self.logits = self.inputs.views["logits"]
         self.offsets = up(st.seq_row_offsets)
         self.row_pos = up(st.row_pos)
         self.is_masked = up(st.is_masked)
         self.tokens = up(st.tokens)
         self.decode_step = up(st.decode_step)
         self.step_index = st.step
-        i32, f32, u8 = torch.int32, torch.float32, torch.uint8
-        self.token = torch.empty(N, dtype=i32, device=device)
-        self.conf = torch.empty(N, dtype=f32, device=device)
-        self.entropy = torch.empty(N, dtype=f32, device=device)
-        self.unmask = torch.empty(B * n, dtype=i32, device=device)
-        self.emax = torch.empty(B, dtype=f32, device=device)
-        self.refresh = torch.zeros(B, dtype=u8, device=device)
+        self.token, self.conf, self.entropy = r["token"], r["conf"], r["entropy"]
+        self.unmask, self.emax, self.refresh = r["unmask"], r["emax"], r["refresh"]
+        self.refresh.zero_()
         self.ws_dec = nat.new_workspace(nat.ec_decode_workspace_size(N, B), device)
-        self.q, self.k_new, self.v_new = up(att.q), up(att.k_new), up(att.v_new)
+        self.q, self.k_new, self.v_new = (self.inputs.views[k] for k in ("q", "k_new", "v_new"))
         self.k_cache, self.v_cache = up(att.k_cache), up(att.v_cache)
-        self.out = torch.zeros_like(self.q)
+        self.out = r["out"]
+        self.out.zero_()
         self.ws_att = nat.new_workspace(
             nat.ec_attention_workspace_size(B, L, w.r_max, w.n_heads, w.n_kv_heads,
                                            w.head_dim), device)
@@ -244,8 +277,7 @@ class GpuStep:
         self.count = torch.empty(B, dtype=i32, device=device)
         nat.ec_build_recompute_set(self.is_masked, self.decode_step, self.refresh, st.block_lo,
                                    st.block_hi, w.k, self.idx, self.count)
-        self.idx_next = torch.empty((B, L), dtype=i32, device=device)
-        self.count_next = torch.empty(B, dtype=i32, device=device)
+        self.idx_next, self.count_next = r["idx_next"], r["count_next"]
         self.block = (st.block_lo, st.block_hi)
         self.scale = 1.0 / math.sqrt(w.head_dim)
         torch.cuda.synchronize(device)
@@ -493,26 +525,24 @@ def run_e2e(step: GpuStep, geo, w, logits, att, K, world):
     import torch
     dev = step.dev
 
-    def pinned(a):
+    def host(a):
         if a.dtype == np.uint16:
-            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
-        return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a))
 
-    h_in = [(pinned(logits), step.logits), (pinned(att.q), step.q), (pinned(att.k_new), step.k_new),
-            (pinned(att.v_new), step.v_new)]
-    d_out = [step.token, step.conf, step.entropy, step.unmask, step.emax, step.refresh,
-             step.idx_next, step.count_next, step.out]
-    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in d_out]
-    bi = sum(h.numel() * h.element_size() for h, _ in h_in)
-    bo = sum(h.numel() * h.element_size() for h in h_out)
+    # the step's inputs in one pinned buffer with the device buffer's layout, and
+    # one pinned buffer for its results: one copy each way per step
+    h_in = Packed(step.in_specs, "cpu", pinned=True)
+    for name, a in (("logits", logits), ("q", att.q), ("k_new", att.k_new), ("v_new", att.v_new)):
+        h_in.views[name].copy_(host(a))
+    h_out = Packed(step.out_specs, "cpu", pinned=True)
+    bi, bo = h_in.nbytes, h_out.nbytes
     flush = L2Flush(dev)
 
     def one():
-        for h, d in h_in:
-            d.copy_(h, non_blocking=True)
+        step.inputs.blob.copy_(h_in.blob, non_blocking=True)
         step.run()
-        for d, h in zip(d_out, h_out):
-            h.copy_(d, non_blocking=True)
+        h_out.blob.copy_(step.results.blob, non_blocking=True)
 
     for _ in range(3):
         one()
