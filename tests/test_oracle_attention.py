@@ -121,3 +121,33 @@ def test_bf16_inputs_widen_exactly(orc):
     widened = [synth.bf16_bits_to_f32(x).astype(np.float64) for x in (qb, kb, vb)]
     via_f64 = orc.attention(*widened, np.array([2], np.int32), 0.3)
     assert np.array_equal(via_bits, via_f64)
+
+
+@pytest.mark.parametrize("cuts", [[0, 5, 11], [0, 1, 2, 3, 17], [0, 9]])
+def test_key_split_partials_combine_to_the_full_attention(orc, cuts):
+    # The GPU path may cut a row's keys into pieces, keep per piece the raw-score
+    # maximum m_s, l_s = sum 2^{(s - m_s) c} and the unnormalised O_s, and combine
+    # out = sum_s 2^{(m_s - M) c} O_s / sum_s 2^{(m_s - M) c} l_s (M = max m_s, c =
+    # scale * log2 e).  Pin that identity against the oracle's unsplit attention.
+    rng = np.random.default_rng(len(cuts))
+    L, R, H, d = 23, 4, 2, 8
+    q = rng.standard_normal((1, R, H, d)) * 3
+    kc = rng.standard_normal((1, L, H, d))
+    vc = rng.standard_normal((1, L, H, d))
+    count = np.array([R], np.int32)
+    scale = 1 / np.sqrt(d)
+    c = scale * np.log2(np.e)
+    full = orc.attention(q, kc, vc, count, scale)
+    bounds = cuts + [L]
+    for r in range(R):
+        for h in range(H):
+            raw = kc[0, :, h] @ q[0, r, h]  # raw scores
+            parts = []
+            for a, z in zip(bounds[:-1], bounds[1:]):
+                m = raw[a:z].max()
+                p = np.exp2((raw[a:z] - m) * c)
+                parts.append((m, p.sum(), p @ vc[0, a:z, h]))
+            M = max(m for m, _, _ in parts)
+            w = [np.exp2((m - M) * c) for m, _, _ in parts]
+            out = sum(wi * o for wi, (_, _, o) in zip(w, parts)) / sum(wi * l for wi, (_, l, _) in zip(w, parts))
+            assert np.allclose(out, full[0, r, h], rtol=1e-12, atol=1e-13)
