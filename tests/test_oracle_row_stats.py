@@ -185,3 +185,40 @@ def test_row_stride_is_honoured(orc):
                                  t.ctypes.data_as(ctypes.c_void_p))
     assert rc == 0
     assert np.array_equal(h, h_full) and np.array_equal(t, t_full)
+
+
+@pytest.mark.parametrize("cuts", [[0, 100], [0, 1, 2, 3, 4999], [0, 1250, 2500, 3750]])
+def test_piece_states_merge_to_the_row_statistics(orc, cuts):
+    # The GPU path folds pieces of a row into states (m, S, T, a) in the log2 domain,
+    # S = sum 2^y, T = sum 2^y y, y = (x - m) log2 e, and merges two states by
+    # rescaling the one with the smaller maximum by f = 2^d, d = (m_lo - m_hi) log2 e:
+    # S = f S_lo + S_hi, T = f (d S_lo + T_lo) + T_hi, keeping the larger maximum
+    # (lower index on a tie).  Pin that merge against the oracle's direct
+    # statistics: H = ln S - ln2 T / S, conf = 1 / S, token = a.
+    rng = np.random.default_rng(len(cuts))
+    x = rng.standard_normal((4, 5000)) * 2
+    x[1, 3333] += 9
+    x[2, [10, 4000]] = 7.5  # a tie across pieces
+    h, c, t = orc.row_stats(x)
+    l2e = 1 / math.log(2)
+    bounds = cuts + [x.shape[1]]
+    for i in range(x.shape[0]):
+        state = None
+        for a, z in zip(bounds[:-1], bounds[1:]):
+            piece = x[i, a:z]
+            m = piece.max()
+            y = (piece - m) * l2e
+            s = np.exp2(y).sum()
+            tt = (np.exp2(y) * y).sum()
+            cur = (m, s, tt, a + int(np.argmax(piece)))
+            if state is None:
+                state = cur
+                continue
+            hi, lo = (cur, state) if (cur[0] > state[0] or (cur[0] == state[0] and cur[3] < state[3])) else (state, cur)
+            d = (lo[0] - hi[0]) * l2e
+            f = 2.0 ** d
+            state = (hi[0], f * lo[1] + hi[1], f * (d * lo[1] + lo[2]) + hi[2], hi[3])
+        m, s, tt, a = state
+        assert math.isclose(math.log(s) - math.log(2) * tt / s, h[i], rel_tol=0, abs_tol=1e-10)
+        assert math.isclose(1 / s, c[i], rel_tol=1e-12)
+        assert a == t[i]
