@@ -19,6 +19,10 @@ def native():
     ((1, 1024, 1024, 32, 32, 128), 2),   # full refresh: 256 whole units
     ((1, 64, 32, 2, 2, 64), 2),          # one key tile per unit: nothing to split
     ((1, 1, 48, 32, 32, 128), 2),        # a single key
+    ((1, 256, 48, 32, 32, 128), 2),      # two key tiles: too short to split
+    ((4, 512, 64, 8, 8, 128), 2),        # 32 units of 4 tiles: whole units beat a split + merge
+    ((1, 1024, 48, 32, 32, 64), 3),      # head_dim 64, as the single sequence
+    ((2, 4096, 200, 16, 2, 128), 3),     # GQA 8:1, several row tiles per KV head
     ((1, 1024, 0, 32, 32, 128), 0),      # no recomputed rows: no launch at all
 ])
 def test_attention_launches(shape, launches):
