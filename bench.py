@@ -9,20 +9,22 @@ in the order a denoising step runs it:
      confidence-ranked unmasking, max entropy E and the E > tau gate;
   3. ec_build_recompute_set  — the index set of the next forward.
 
-Metric: entropy/gate GB/s = bytes of logits consumed per second by the whole
-step (N * V * element size / step time).  The line also breaks the step into
-its parts (decode-and-gate GB/s and fraction of HBM, attention TFLOP/s and
-fraction of the tensor peak) and carries a roofline object for the dominant
-kernel, measured live with CUDA events on the launching stream.  L2 is flushed
-(a 256 MiB write, then a 256 MiB read) between timed steps, outside the timed
-intervals.
+Metric: entropy/gate GB/s = bytes of logits the decode-and-gate call consumes
+per second of its own device time (N * V * element size / call time).  The
+line also carries the whole step's time and logits rate, the attention call's
+TFLOP/s and fraction of the tensor peak, and a roofline object for the
+dominant call, all measured live with CUDA events on the launching stream.
+Each call (and the whole step) is a CUDA graph with its own pair of events; L2
+is flushed (a 256 MiB write, then a 256 MiB read) before every timed replay,
+outside the timed intervals.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|all]
+                  [--impl ours|reference]
 
 N > 1 runs under torchrun: every rank runs an independent replica (the path
 has no exchange step), the timed region is bracketed by barriers, and the
 slowest rank's time is used.  --impl reference times the float64 CPU oracle
-on the host cores instead.
+on the host cores instead.  --workload all prints one line per workload.
 """
 from __future__ import annotations
 
@@ -43,20 +45,15 @@ sys.path.insert(0, ROOT)
 from entropy_gated_kv_decode_b300 import synth  # noqa: E402
 
 METRIC = "entropy/gate GB/s (% HBM peak); selective-recompute attention TFLOP/s (% peak)"
-DEFAULT_WORKLOAD = "single_seq"
+DEFAULT_WORKLOAD = "batched"
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 # DRAM bytes (read + write) per call of the dominant call, from one ncu capture of
 # the same bench command (dram__bytes_read.sum + dram__bytes_write.sum summed over
-# the call's kernels, per launch; profiles/ has the summary).  Used only while the
-# kernel sources hash to the value they had when the counters were taken.
-MEASURED_TRAFFIC = {
-    # profiles/launches_single_seq.md: write_back_kernel 794,880 B + attention_tc_kernel
-    # 17,260,544 B + merge_kernel 3,208,448 B per call (medians of 21 launches; ncu empties
-    # the caches between kernels, so the merge reads its partials from DRAM; writes stay in L2)
-    ("single_seq", "attention"): {"sources": "1a8ff541fc1a3a54", "bytes": 21263872},
-}
+# the call's kernels, per launch).  Used only while the kernel sources hash to the
+# value they had when the counters were taken.
+MEASURED_TRAFFIC = {}
 
 
 def kernel_sources_hash() -> str:
@@ -97,13 +94,17 @@ def parse_args(argv=None):
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=20)
-    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                   choices=sorted(synth.WORKLOADS) + ["all"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--seed", type=int, default=0)
-    p.add_argument("--e2e-steps", type=int, default=300)
+    p.add_argument("--e2e-steps", type=int, default=200,
+                   help="timed end-to-end steps (at least 100 are always run)")
+    p.add_argument("--e2e-warmup", type=int, default=30,
+                   help="untimed end-to-end steps first (at least 20 are always run)")
     p.add_argument("--eager", action="store_true", help="time eager launches, not graph replays")
-    p.add_argument("--cpu-seconds", type=float, default=10.0,
-                   help="CPU time budget of the oracle baseline sample")
+    p.add_argument("--cpu-seconds", type=float, default=8.0,
+                   help="CPU time budget of each oracle baseline sample (one core, all cores)")
     return p.parse_args(argv)
 
 
@@ -319,8 +320,8 @@ def dist_setup(args):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        backend = "nccl" if _cuda_ok() else "gloo"
-        dist.init_process_group(backend)
+        if not dist.is_initialized():
+            dist.init_process_group("nccl" if _cuda_ok() else "gloo")
     return rank, world, local
 
 
@@ -355,14 +356,14 @@ def aggregate(per_rank_units: float, world: int, max_seconds: float) -> float:
     return per_rank_units * world / max_seconds
 
 
-def run_ours(args):
+def run_ours(args, workload=None):
     import torch
     rank, world, local = dist_setup(args)
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     from entropy_gated_kv_decode_b300 import _native as nat
     nat.lib()  # fails loudly when libec.so is missing: there is no other path
-    w = synth.WORKLOADS[args.workload]
+    w = synth.WORKLOADS[workload or args.workload]
     geo = workload_geometry(w)
     st, logits, att = host_inputs(w, args.seed)
     stream = torch.cuda.Stream(device)
@@ -375,50 +376,40 @@ def run_ours(args):
         flush()
         step.run()
     torch.cuda.synchronize(device)
-    # One step = one replay of a CUDA graph holding the three calls between two
-    # timing events, so host launch cost stays out of the device time and the calls
-    # chain as they do in use (each kernel's set-up overlaps its predecessor's
-    # tail).  A second graph puts events between the calls for the per-call
-    # breakdown; each of its parts includes one event node's gap.
-    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
-    graph = graph_parts = None
-    mode = "cuda-graph replay per step"
+    # Four CUDA graphs, each one call (or the whole step) between its own pair of
+    # timing events: host launch cost stays out of the device time, and within
+    # the step graph the calls chain as they do in use (each kernel's set-up
+    # overlaps its predecessor's tail).
+    parts = {"step": step.run, "attention": step.attention, "decode_gate": step.decode,
+             "recompute_set": step.recompute}
+    ev = {k: (torch.cuda.Event(enable_timing=True, external=True),
+              torch.cuda.Event(enable_timing=True, external=True)) for k in parts}
+    graphs = {}
+    mode = "cuda-graph replay per call"
 
-    def record_step():
-        ev[4].record()
-        step.run()
-        ev[5].record()
-
-    def record_parts():
-        ev[0].record()
-        step.attention()
-        ev[1].record()
-        step.decode()
-        ev[2].record()
-        step.recompute()
-        ev[3].record()
+    def record(name):
+        ev[name][0].record()
+        parts[name]()
+        ev[name][1].record()
 
     if args.eager:
         mode = "eager launches"
     else:
         try:
-            graph, graph_parts = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                record_step()
-            with torch.cuda.graph(graph_parts, stream=stream):
-                record_parts()
-            graph.replay()
-            graph_parts.replay()
+            for name in parts:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    record(name)
+                graphs[name] = g
+            for g in graphs.values():
+                g.replay()
             torch.cuda.synchronize(device)
         except Exception as exc:  # capture not possible: time eager launches instead
-            graph = graph_parts = None
+            graphs = {}
             mode = f"eager launches (graph capture failed: {type(exc).__name__})"
 
-    def one_step():
-        graph.replay() if graph is not None else record_step()
-
-    def one_parts():
-        graph_parts.replay() if graph_parts is not None else record_parts()
+    def replay(name):
+        graphs[name].replay() if graphs else record(name)
 
     uuid = None
     try:
@@ -431,48 +422,48 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize(device)
     t_wall = time.perf_counter()
-    t_step = 0.0
+    t = {name: 0.0 for name in parts}
     for _ in range(K):
-        flush()
-        one_step()
-        ev[5].synchronize()
-        t_step += ev[4].elapsed_time(ev[5]) / 1e3
+        for name in parts:
+            flush()
+            replay(name)
+        ev["recompute_set"][1].synchronize()
+        for name in parts:
+            t[name] += ev[name][0].elapsed_time(ev[name][1]) / 1e3
     torch.cuda.synchronize(device)
     barrier(world)
     wall = time.perf_counter() - t_wall
-    # per-call breakdown (same steps, events between the calls)
-    t_att = t_dec = t_rec = 0.0
-    for _ in range(K):
-        flush()
-        one_parts()
-        ev[3].synchronize()
-        t_att += ev[0].elapsed_time(ev[1]) / 1e3
-        t_dec += ev[1].elapsed_time(ev[2]) / 1e3
-        t_rec += ev[2].elapsed_time(ev[3]) / 1e3
     clocks = sampler.stop()
-    t_step_max = reduce_max(t_step, world)
+    t_max = {name: reduce_max(v, world) for name, v in t.items()}
     status = nat.ec_read_device_status(step.ws_dec) | nat.ec_read_device_status(step.ws_att)
 
-    e2e = run_e2e(step, geo, w, logits, att, min(args.e2e_steps, K), world)
+    e2e = run_e2e(step, geo, w, logits, att, max(100, args.e2e_steps),
+                  max(20, args.e2e_warmup), world)
 
     peaks, peak_kind = load_peaks()
     hbm = float(peaks["hbm_gbs"])
     tc = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    us = lambda t: t / K * 1e6  # noqa: E731
+    us = lambda x: x / K * 1e6  # noqa: E731
+    t_att, t_dec = t_max["attention"], t_max["decode_gate"]
     att_tflops = geo["attn_flops"] * K / t_att / 1e12
     att_gbs = geo["attn_bytes"] * K / t_att / 1e9
     att_ai = geo["attn_flops"] / geo["attn_bytes"]
     att_roof = min(tc, att_ai * hbm / 1e3)
-    parts = {
+    dec_gbs = geo["logits_bytes"] * K / t_dec / 1e9
+    n_launch = kernels_per_step(nat, w)
+    out_parts = {
+        "step": {"us": us(t_max["step"]),
+                 "logits_gbs": geo["logits_bytes"] * K / t_max["step"] / 1e9,
+                 "launches": sum(n_launch.values())},
         "attention": {"us": us(t_att), "tflops": att_tflops, "frac_tensor_peak": att_tflops / tc,
                       "gbs": att_gbs, "frac_hbm": att_gbs / hbm,
                       "frac_attainable": att_tflops / att_roof, "intensity_flop_per_byte": att_ai,
-                      "launches": kernels_per_step(nat, w)["attention"]},
-        "decode_gate": {"us": us(t_dec), "gbs": geo["logits_bytes"] * K / t_dec / 1e9,
-                        "frac_hbm": geo["logits_bytes"] * K / t_dec / 1e9 / hbm, "launches": 1},
-        "recompute_set": {"us": us(t_rec), "launches": 1},
+                      "launches": n_launch["attention"]},
+        "decode_gate": {"us": us(t_dec), "gbs": dec_gbs, "frac_hbm": dec_gbs / hbm,
+                        "launches": 1},
+        "recompute_set": {"us": us(t_max["recompute_set"]), "launches": 1},
     }
-    dominant = max(("attention", t_att), ("decode_gate", t_dec), key=lambda x: x[1])[0]
+    dominant = "attention" if t_att > t_dec else "decode_gate"
     if dominant == "attention":
         bound = "tensor" if att_ai > tc * 1e3 / hbm else "hbm"
         if bound == "hbm":
@@ -481,47 +472,47 @@ def run_ours(args):
         else:
             roof = {"bound": "tensor", "achieved": att_tflops, "peak": tc, "unit": "TFLOP/s",
                     "frac": att_tflops / tc}
-        roof["kernel"] = "ec_selective_attention (write-back + attention + merge)"
+        roof["kernel"] = "ec_selective_attention"
         roof["traffic"] = measured_traffic(w.name, "attention")
     else:
-        g = parts["decode_gate"]["gbs"]
-        roof = {"bound": "hbm", "achieved": g, "peak": hbm, "unit": "GB/s", "frac": g / hbm,
-                "kernel": "decode_gate_kernel", "traffic": measured_traffic(w.name, "decode")}
-    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+        roof = {"bound": "hbm", "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
+                "frac": dec_gbs / hbm, "kernel": "decode_gate_kernel",
+                "traffic": measured_traffic(w.name, "decode")}
+    roof["peak_source"] = ("measured burst (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                           else "fallback")
 
     cpu = None
     if rank == 0 and world == 1:
         cpu = cpu_baseline(w, st, logits, att, args.cpu_seconds, geo)
 
-    value = aggregate(geo["logits_bytes"] * K, world, t_step_max) / 1e9
+    value = aggregate(geo["logits_bytes"] * K, world, t_dec) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": W, "ms_per_step": t_step_max / K * 1e3, "higher_is_better": True,
+        "warmup": W, "ms_per_step": t_max["step"] / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.attn_dtype == synth.BF16 else "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seq_len, "vocab": w.vocab,
                    "n_rows": w.n_rows, "recompute_rows": w.r_max, "n_heads": w.n_heads,
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "n_unmask": w.n_unmask,
                    "k": w.k, "tau": w.tau, "accumulate": "f32",
-                   "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)", "launch": mode,
-                   "parallelism": f"replicas x{world}"},
-        "parts": parts,
-        "parts_note": "each call timed between its own events in a second graph (one event-node "
-                      "gap each); ms_per_step has events only around the whole step",
+                   "l2": "flushed before every timed replay (256 MiB write + 256 MiB read, untimed)",
+                   "launch": mode, "parallelism": f"replicas x{world}"},
+        "value_note": "decode-and-gate call: logits bytes / its own device time; "
+                      "ms_per_step is the whole step (attention, decode, recompute set)",
+        "parts": out_parts,
         "roofline": roof, "clocks": clocks, "e2e": e2e,
-        "gpu_launches": sum(kernels_per_step(nat, w).values()) * K,
+        "gpu_launches": (sum(n_launch.values()) * 2) * K,
         "cpu_baseline": cpu, "device_status": status, "wall_s_timed_region": wall,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
 
 
-def run_e2e(step: GpuStep, geo, w, logits, att, K, world):
+def run_e2e(step: GpuStep, geo, w, logits, att, K, W, world):
     """Same metric through the public calls, starting from pinned host buffers:
-    every step copies its inputs host->device and its results device->host."""
+    every step copies its inputs host->device and its results device->host.
+    W untimed steps first, then K steps each between its own events (L2 flushed
+    before each, outside the events); the value uses the median step time."""
     import torch
     dev = step.dev
 
@@ -544,7 +535,8 @@ def run_e2e(step: GpuStep, geo, w, logits, att, K, world):
         step.run()
         h_out.blob.copy_(step.results.blob, non_blocking=True)
 
-    for _ in range(3):
+    for _ in range(W):
+        flush()
         one()
     torch.cuda.synchronize(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -557,27 +549,44 @@ def run_e2e(step: GpuStep, geo, w, logits, att, K, world):
         ev[i][1].record()
     torch.cuda.synchronize(dev)
     barrier(world)
-    t = reduce_max(sum(a.elapsed_time(b) for a, b in ev) / 1e3, world)
-    return {"value": aggregate(geo["logits_bytes"] * K, world, t) / 1e9, "unit": "GB/s",
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": K,
-            "ms_per_step": t / K * 1e3}
+    per = sorted(a.elapsed_time(b) / 1e3 for a, b in ev)
+    med = reduce_max(per[len(per) // 2], world)
+    mean = reduce_max(sum(per) / len(per), world)
+    return {"value": aggregate(geo["logits_bytes"], world, med) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": K, "warmup": W,
+            "ms_per_step": med * 1e3, "ms_per_step_median": med * 1e3,
+            "ms_per_step_mean": mean * 1e3,
+            "note": "whole step (3 calls) plus one pinned copy each way; value from the median"}
 
 
 # ---------------------------------------------------------------------------
 # the float64 CPU oracle as the reported baseline / reference arm
 
 
-def oracle_step_seconds(orc, w, st, logits, att, budget_s, rng):
-    """Seconds the float64 oracle takes for one full step, measured on a bounded
-    sample: entropy rows and attention (row, head) outputs are each timed on as
-    many items as half the budget allows and scaled to the full count; the
-    unmask/gate, index-set and write-back stages run in full.
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def oracle_step_seconds(orc, w, st, logits, att, budget_s, rng, threads=1):
+    """Seconds the float64 oracle takes for one full step on `threads` host
+    threads, measured on a bounded sample: entropy rows and attention (row, head)
+    outputs are each timed on as many items as half the budget allows (at least
+    four per thread) and scaled to the full count; the unmask/gate, index-set
+    and write-back stages run in full.
     Returns (seconds per full step, description of the sample)."""
+    orc.set_threads(threads)
     N = w.n_rows
     t0 = time.perf_counter()
     orc.row_stats(logits[:1])
-    per_row = max(time.perf_counter() - t0, 1e-6)
-    n_rows = int(min(N, max(1, 0.5 * budget_s / per_row)))
+    per_row = max(time.perf_counter() - t0, 1e-6) / threads
+    n_rows = int(min(N, max(4 * threads, 0.5 * budget_s / per_row)))
     t0 = time.perf_counter()
     h, c, t = orc.row_stats(logits[:n_rows])
     t_rows = (time.perf_counter() - t0) / n_rows * N
@@ -593,7 +602,6 @@ def oracle_step_seconds(orc, w, st, logits, att, budget_s, rng):
     t_rest = time.perf_counter() - t0
     scale = 1.0 / math.sqrt(w.head_dim)
     total = int(cnt.sum()) * w.n_heads
-    flat = rng.choice(total, size=1, replace=False)
 
     def triples(ids):
         out = []
@@ -608,25 +616,33 @@ def oracle_step_seconds(orc, w, st, logits, att, budget_s, rng):
         return np.array(out, np.int32)
 
     t0 = time.perf_counter()
-    orc.attention(att.q, kc, vc, cnt, scale, samples=triples(flat))
-    per_out = max(time.perf_counter() - t0, 1e-6)
-    n_out = int(min(total, max(1, 0.5 * budget_s / per_out)))
+    orc.attention(att.q, kc, vc, cnt, scale, samples=triples(rng.choice(total, size=1)))
+    per_out = max(time.perf_counter() - t0, 1e-6) / threads
+    n_out = int(min(total, max(4 * threads, 0.5 * budget_s / per_out)))
     pick = triples(rng.choice(total, size=n_out, replace=False))
     t0 = time.perf_counter()
     orc.attention(att.q, kc, vc, cnt, scale, samples=pick)
     t_att = (time.perf_counter() - t0) / n_out * total
+    orc.set_threads(1)
     sample = (f"entropy on {n_rows}/{N} logits rows, attention on {n_out}/{total} (row, head) "
               f"outputs, each scaled to the full step; unmask, gate, index set, write-back in full")
     return t_rows + t_rest + t_att, sample
 
 
 def cpu_baseline(w, st, logits, att, budget_s, geo):
+    """The oracle timed on one host core and on every core this process may use."""
     import oracle as orc
     orc.build()
-    secs, sample = oracle_step_seconds(orc, w, st, logits, att, budget_s,
-                                       np.random.default_rng(1))
-    return {"value": geo["logits_bytes"] / secs / 1e9, "unit": "GB/s", "cores": 1,
-            "kind": "oracle", "sample": sample, "seconds_per_step": secs}
+    cores = orc.usable_cores()
+    one, sample1 = oracle_step_seconds(orc, w, st, logits, att, budget_s, np.random.default_rng(1), 1)
+    every, sample_n = oracle_step_seconds(orc, w, st, logits, att, budget_s,
+                                          np.random.default_rng(2), cores)
+    return {"value": geo["logits_bytes"] / every / 1e9, "unit": "GB/s", "cores": cores,
+            "kind": "oracle", "sample": sample_n, "seconds_per_step": every,
+            "single_core": {"value": geo["logits_bytes"] / one / 1e9, "unit": "GB/s", "cores": 1,
+                            "sample": sample1, "seconds_per_step": one},
+            "cpu_model": cpu_model(),
+            "note": "OpenMP over independent rows and (row, head) outputs; value = all cores"}
 
 
 def run_reference(args):
@@ -634,19 +650,22 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    w = synth.WORKLOADS[args.workload]
+    w = synth.WORKLOADS[DEFAULT_WORKLOAD if args.workload == "all" else args.workload]
+    if w.name == "trajectory":
+        w = synth.WORKLOADS[DEFAULT_WORKLOAD]
     geo = workload_geometry(w)
     st, logits, att = host_inputs(w, args.seed)
-    # the whole run (warm-up + K sampled steps) takes about --cpu-seconds x 12
-    budget = max(0.005, 12 * args.cpu_seconds / max(1, args.steps + args.warmup))
     import oracle as orc
     orc.build()
+    cores = orc.usable_cores()
+    # the whole run (warm-up + K sampled steps) takes about --cpu-seconds x 12
+    budget = max(0.005, 12 * args.cpu_seconds / max(1, args.steps + args.warmup))
     rng = np.random.default_rng(1)
     for _ in range(args.warmup):
-        oracle_step_seconds(orc, w, st, logits, att, budget, rng)
+        oracle_step_seconds(orc, w, st, logits, att, budget, rng, cores)
     times, sample = [], ""
     for _ in range(args.steps):
-        s, sample = oracle_step_seconds(orc, w, st, logits, att, budget, rng)
+        s, sample = oracle_step_seconds(orc, w, st, logits, att, budget, rng, cores)
         times.append(s)
     t = sum(times)
     value = geo["logits_bytes"] * len(times) / t / 1e9
@@ -658,8 +677,8 @@ def run_reference(args):
                    "n_rows": w.n_rows, "recompute_rows": w.r_max, "n_heads": w.n_heads,
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim},
         "impl": "reference",
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -689,6 +708,54 @@ def time_projection(nat, tr, rows, reps=20):
         e1.record()
     e1.synchronize()
     return e0.elapsed_time(e1) / 1e3 / reps
+
+
+def time_forward(tr, full: bool, reps=10):
+    """Mean device time (s) of one forward variant (graph replay), over reps
+    replays with the trajectory's buffers."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(tr.stream):
+        tr._forward(full)
+        e0.record()
+        for _ in range(reps):
+            tr._forward(full)
+        e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / reps
+
+
+def trajectory_cpu_baseline(w, seed, budget_s, total_bytes):
+    """The oracle's decision path (row statistics, unmasking, gate, index sets;
+    no layers) on one core and on all cores, over the first steps that fit the
+    budget, scaled to the whole trajectory by logits rows."""
+    import oracle as orc
+    import oracle.trajectory as otr
+    orc.build()
+    rows = synth.trajectory_rows_per_step(w)
+    cores = orc.usable_cores()
+    out = {}
+    for threads in (1, cores):
+        orc.set_threads(threads)
+        n = 1
+        while True:
+            t0 = time.perf_counter()
+            otr.run(w, seed, n_steps=n)
+            dt = time.perf_counter() - t0
+            if dt > 0.25 * budget_s or n >= w.n_steps:
+                break
+            n = min(w.n_steps, n * 2)
+        secs = dt * sum(rows) / max(1, sum(rows[:n]))
+        out[threads] = (secs, f"decision path of the first {n}/{w.n_steps} steps scaled by "
+                              f"logits rows; the layers' forward is not timed")
+    orc.set_threads(1)
+    secs, sample = out[cores]
+    one, sample1 = out[1]
+    return {"value": total_bytes / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": sample, "seconds_per_trajectory": secs,
+            "single_core": {"value": total_bytes / one / 1e9, "unit": "GB/s", "cores": 1,
+                            "sample": sample1, "seconds_per_trajectory": one},
+            "cpu_model": cpu_model()}
 
 
 def run_trajectory(args):
@@ -731,13 +798,32 @@ def run_trajectory(args):
     sel = [r for r in recs if not r.full]
     t_proj_full = time_projection(nat, tr, w.seq_len)
     t_proj_sel = time_projection(nat, tr, tr.r_sel)
+    t_fwd_full = time_forward(tr, True)
+    t_fwd_sel = time_forward(tr, False)
+    # end to end: each step's logits copied in from pinned host memory inside the
+    # step, the one-byte flag (and the next row count) read back every step
+    tr.use_host_logits(True)
+    tr.run()
+    torch.cuda.synchronize(device)
+    e2e_walls = []
+    for _ in range(max(2, min(K, 5))):
+        t0 = time.perf_counter()
+        tr.run()
+        tok = tr.tokens.cpu()
+        e2e_walls.append(time.perf_counter() - t0)
+    tr.use_host_logits(False)
+    del tok
+    e2e_wall = reduce_max(sorted(e2e_walls)[len(e2e_walls) // 2], world)
     peaks, peak_kind = load_peaks()
     tc = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hid = w.n_heads * w.head_dim
     flops_full = 2.0 * w.seq_len * hid * 3 * hid
     proj_tflops = flops_full / t_proj_full / 1e12
     wbytes = 3 * hid * hid * 2
-    value = aggregate(trajectory_bytes(w) * K, world, t_max) / 1e9
+    tbytes = trajectory_bytes(w)
+    value = aggregate(tbytes * K, world, t_max) / 1e9
+    cpu = trajectory_cpu_baseline(w, args.seed, args.cpu_seconds, tbytes) \
+        if rank == 0 and world == 1 else None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": t_max / K * 1e3, "higher_is_better": True,
@@ -748,6 +834,7 @@ def run_trajectory(args):
                    "tau": w.tau, "step": "one whole 128-step trajectory",
                    "l2": "inputs (3.2 GB of weights per step) exceed L2",
                    "parallelism": f"replicas x{world}"},
+        "value_note": "logits bytes of all 128 denoising steps / wall time of the trajectory",
         "parts": {
             "denoising_steps_per_s": n_steps / wall,
             "refresh_fraction": sum(r.refresh for r in recs) / len(recs),
@@ -755,6 +842,9 @@ def run_trajectory(args):
             "mean_rows": float(np.mean([r.rows for r in recs])),
             "full_forward_ms": float(np.mean([r.forward_ms for r in full])) if full else None,
             "partial_forward_ms": float(np.mean([r.forward_ms for r in sel])) if sel else None,
+            "full_forward_ms_replay": t_fwd_full * 1e3,
+            "partial_forward_ms_replay": t_fwd_sel * 1e3,
+            "partial_forward_rows": tr.r_sel,
             "decode_and_sets_ms": float(np.mean([r.decode_ms for r in recs])),
             "gate_share_of_device_time": dec / device_s,
             "host_overhead_share": max(0.0, 1 - device_s / wall),
@@ -768,13 +858,16 @@ def run_trajectory(args):
                      "peak_source": f"{peak_kind} sustained (MEASURED_PEAKS.json)"},
         "clocks": clocks,
         "gpu_launches": sum(1 + 2 * w.n_layers + 3 for _ in recs) * K,
-        "e2e": None, "cpu_baseline": None,
+        "e2e": {"value": aggregate(tbytes, world, e2e_wall) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": tbytes / w.n_steps,
+                "d2h_bytes_per_step": 5 + tr.tokens.numel() * 4 / w.n_steps,
+                "ms_per_trajectory": e2e_wall * 1e3,
+                "note": "each step's logits copied from pinned host memory inside the step; "
+                        "refresh flag and row count read back every step; tokens at the end"},
+        "cpu_baseline": cpu,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
 
 
 def main(argv=None):
@@ -783,8 +876,16 @@ def main(argv=None):
         run_reference(args)
     elif args.workload == "trajectory":
         run_trajectory(args)
+    elif args.workload == "all":
+        for name in ("tiny", "single_seq", "batched", "long_ctx"):
+            run_ours(args, name)
+        run_trajectory(args)
     else:
         run_ours(args)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
 
 
 if __name__ == "__main__":

@@ -172,7 +172,9 @@ def ec_read_device_status(workspace: torch.Tensor, stream=None) -> int:
 
 def _decode_args(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step, token_out,
                  conf_out, entropy_out, unmask_rows, max_entropy, refresh, is_masked, seq_tokens,
-                 decode_step, workspace):
+                 decode_step, workspace=None):
+    """Arguments of ec_decode_step (workspace given) or of ec_decode_step_noalloc
+    (workspace None: no workspace arguments)."""
     _cuda("logits", logits, contiguous=False)
     if logits.dim() != 2 or (logits.shape[0] > 0 and logits.stride(1) != 1):
         raise ValueError("logits must be [N, V] with unit stride along V")
@@ -192,12 +194,14 @@ def _decode_args(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step,
         _cuda(name, t, dt)
         _numel(t, n, name)
     _numel(row_pos, n_rows, "row_pos")
-    _cuda("workspace", workspace, torch.uint8)
-    return [_p(logits), _float_code(logits), logits.stride(0) if n_rows > 0 else vocab, n_rows,
+    args = [_p(logits), _float_code(logits), logits.stride(0) if n_rows > 0 else vocab, n_rows,
             vocab, _p(seq_row_offsets), _p(row_pos), batch, seq_len, n_unmask, float(tau),
             int(step), _p(token_out), _p(conf_out), _p(entropy_out), _p(unmask_rows),
-            _p(max_entropy), _p(refresh), _p(is_masked), _p(seq_tokens), _p(decode_step),
-            _p(workspace), workspace.numel()]
+            _p(max_entropy), _p(refresh), _p(is_masked), _p(seq_tokens), _p(decode_step)]
+    if workspace is not None:
+        _cuda("workspace", workspace, torch.uint8)
+        args += [_p(workspace), workspace.numel()]
+    return args
 
 
 def ec_decode_step(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step,
@@ -215,10 +219,9 @@ def ec_decode_step_noalloc(logits, seq_row_offsets, row_pos, seq_len, n_unmask, 
                            is_masked, seq_tokens, decode_step, stream=None):
     """ec_decode_step without a workspace, for callers that cannot allocate device
     memory: the scratch is a fixed 2 MiB array inside the library (see ec.h)."""
-    dummy = torch.empty(0, dtype=torch.uint8, device=logits.device)
     args = _decode_args(logits, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step,
                         token_out, conf_out, entropy_out, unmask_rows, max_entropy, refresh,
-                        is_masked, seq_tokens, decode_step, dummy)[:-2]
+                        is_masked, seq_tokens, decode_step)
     _check(lib().ec_decode_step_noalloc(*args, _stream(stream)), "ec_decode_step_noalloc")
 
 

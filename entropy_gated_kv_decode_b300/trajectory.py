@@ -132,6 +132,8 @@ class Trajectory:
         self.trace = trace
         self.traces: list[dict] = []
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        self.logits_host = None
+        self.copy_logits = False
         self.records: list[StepRecord] = []
         self.t = 0
         self.next_full = True
@@ -173,10 +175,22 @@ class Trajectory:
             self.graphs[key] = g
         g.replay()
 
+    def use_host_logits(self, on: bool = True):
+        """Keep every step's logits in pinned host memory and copy each step's rows
+        to the device inside the step, as a caller whose logits arrive from the
+        host would (the end-to-end measurement)."""
+        if on and self.logits_host is None:
+            self.logits_host = torch.empty(self.logits.shape, dtype=self.logits.dtype).pin_memory()
+            self.logits_host.copy_(self.logits)
+        self.copy_logits = on
+
     def _decode(self, t: int):
         """Unmask and gate with step t's logits, then build the next row set."""
         w = self.w
         n_rows = self.rows_per_step[t]
+        if self.copy_logits and n_rows:
+            a, b = int(self.row_off[t]), int(self.row_off[t + 1])
+            self.logits[a:b].copy_(self.logits_host[a:b], non_blocking=True)
         lo, hi = synth.trajectory_block(w, t)
         nat.ec_build_recompute_set(self.is_masked, self.decode_step, self.zero_flag, lo, hi, 0,
                                    self.idx_rows, self.count_rows, stream=self.stream)

@@ -25,9 +25,10 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile ``liboracle.so`` with plain ``-O2`` (no fast-math) if stale."""
+    """Compile ``liboracle.so`` with plain ``-O2`` (no fast-math) and OpenMP over
+    independent items, if stale."""
     if force or not os.path.exists(LIBRARY) or os.path.getmtime(LIBRARY) < os.path.getmtime(SOURCE):
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-Wall", "-fPIC", "-shared",
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-Wall", "-fPIC", "-fopenmp", "-shared",
                                "-o", LIBRARY, SOURCE, "-lm"])
     return LIBRARY
 
@@ -54,11 +55,33 @@ def lib():
         L.orc_embed_rows.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, i32, i32,
                                      i32, i32, vp]
         L.orc_projection.argtypes = [vp, vp, ctypes.c_int, i64, i32, i32, vp, i64, vp]
+        L.orc_set_threads.argtypes = [ctypes.c_int]
+        L.orc_set_threads.restype = None
+        L.orc_get_threads.argtypes = []
+        L.orc_get_threads.restype = ctypes.c_int
         for fn in (L.orc_row_stats, L.orc_unmask_gate, L.orc_recompute_set,
                    L.orc_scatter_kv, L.orc_attention, L.orc_embed_rows, L.orc_projection):
             fn.restype = ctypes.c_int
         _lib = L
     return _lib
+
+
+def set_threads(n: int) -> None:
+    """Host threads for the loops over independent rows / outputs (default 1).
+    Every item is computed by one thread, so results do not depend on n."""
+    lib().orc_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return lib().orc_get_threads()
+
+
+def usable_cores() -> int:
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 def _check(rc, what):

@@ -28,6 +28,11 @@
  *   - attention is bidirectional softmax(q K^T * scale) V over all L keys of the
  *     cache after the fresh K/V rows were written into it.
  *
+ * Parallelism: the loops over independent items (logits rows, attention outputs,
+ * projection rows) may run on several host threads (OpenMP, orc_set_threads);
+ * each item is still computed by one thread with the loop body below, so the
+ * result of every item is the same whatever the thread count.
+ *
  * Element types: 0 = float32, 1 = bfloat16 (raw uint16 bits), 2 = float64.
  * Every value is widened exactly to double before any arithmetic.
  * Return codes: 0 = ok, -2 = bad shape/argument, -3 = bad dtype, -9 = out of memory.
@@ -37,10 +42,28 @@
 #include <stdlib.h>
 #include <string.h>
 
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
 #define ORC_OK 0
 #define ORC_BAD_ARG (-2)
 #define ORC_BAD_DTYPE (-3)
 #define ORC_NOMEM (-9)
+
+/* Host threads the item loops use (1 unless set). */
+static int g_threads = 1;
+
+void orc_set_threads(int n) { g_threads = n > 0 ? n : 1; }
+
+int orc_get_threads(void)
+{
+#ifdef _OPENMP
+    return g_threads;
+#else
+    return 1;
+#endif
+}
 
 static int dtype_ok(int dtype) { return dtype == 0 || dtype == 1 || dtype == 2; }
 
@@ -70,6 +93,43 @@ static double load(const void *base, int dtype, int64_t i)
  *   conf[i]    = p_{i, token[i]}
  *   entropy[i] = -sum_j p_ij ln p_ij   (terms with p_ij = 0 contribute 0)
  */
+static void row_stats_one(const void *logits, int dtype, int64_t row_stride, int32_t vocab,
+                          int32_t i, double *x, double *p, double *entropy, double *conf,
+                          int32_t *token)
+{
+    const int64_t base = (int64_t)i * row_stride;
+    for (int32_t j = 0; j < vocab; ++j)
+        x[j] = load(logits, dtype, base + j);
+
+    /* greedy decode: the first index holding the maximum */
+    double m = x[0];
+    int32_t a = 0;
+    for (int32_t j = 1; j < vocab; ++j)
+        if (x[j] > m) {
+            m = x[j];
+            a = j;
+        }
+
+    /* softmax, shifted by the maximum for range */
+    double z = 0.0;
+    for (int32_t j = 0; j < vocab; ++j) {
+        p[j] = exp(x[j] - m);
+        z += p[j];
+    }
+    for (int32_t j = 0; j < vocab; ++j)
+        p[j] /= z;
+
+    /* Shannon entropy in nats */
+    double h = 0.0;
+    for (int32_t j = 0; j < vocab; ++j)
+        if (p[j] > 0.0)
+            h -= p[j] * log(p[j]);
+
+    entropy[i] = h;
+    conf[i] = p[a];
+    token[i] = a;
+}
+
 int orc_row_stats(const void *logits, int dtype, int64_t row_stride, int32_t n_rows,
                   int32_t vocab, double *entropy, double *conf, int32_t *token)
 {
@@ -77,49 +137,24 @@ int orc_row_stats(const void *logits, int dtype, int64_t row_stride, int32_t n_r
         return ORC_BAD_DTYPE;
     if (n_rows < 0 || vocab <= 0 || row_stride < vocab)
         return ORC_BAD_ARG;
-    double *x = (double *)malloc((size_t)vocab * sizeof(double));
-    double *p = (double *)malloc((size_t)vocab * sizeof(double));
-    if (!x || !p) {
+    int status = ORC_OK;
+#pragma omp parallel num_threads(g_threads)
+    {
+        double *x = (double *)malloc((size_t)vocab * sizeof(double));
+        double *p = (double *)malloc((size_t)vocab * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int32_t i = 0; i < n_rows; ++i) {
+            if (!x || !p) {
+#pragma omp atomic write
+                status = ORC_NOMEM;
+                continue;
+            }
+            row_stats_one(logits, dtype, row_stride, vocab, i, x, p, entropy, conf, token);
+        }
         free(x);
         free(p);
-        return ORC_NOMEM;
     }
-    for (int32_t i = 0; i < n_rows; ++i) {
-        const int64_t base = (int64_t)i * row_stride;
-        for (int32_t j = 0; j < vocab; ++j)
-            x[j] = load(logits, dtype, base + j);
-
-        /* greedy decode: the first index holding the maximum */
-        double m = x[0];
-        int32_t a = 0;
-        for (int32_t j = 1; j < vocab; ++j)
-            if (x[j] > m) {
-                m = x[j];
-                a = j;
-            }
-
-        /* softmax, shifted by the maximum for range */
-        double z = 0.0;
-        for (int32_t j = 0; j < vocab; ++j) {
-            p[j] = exp(x[j] - m);
-            z += p[j];
-        }
-        for (int32_t j = 0; j < vocab; ++j)
-            p[j] /= z;
-
-        /* Shannon entropy in nats */
-        double h = 0.0;
-        for (int32_t j = 0; j < vocab; ++j)
-            if (p[j] > 0.0)
-                h -= p[j] * log(p[j]);
-
-        entropy[i] = h;
-        conf[i] = p[a];
-        token[i] = a;
-    }
-    free(x);
-    free(p);
-    return ORC_OK;
+    return status;
 }
 
 /* ---- confidence-ranked unmasking, max entropy, gate, state update ---- */
@@ -328,6 +363,41 @@ int orc_scatter_kv(const void *k_new, const void *v_new, int dtype, const int32_
  * r >= count[b] are left untouched).  Otherwise samples holds n_samples triples
  * (b, r, h) and out[s, :] receives the output of triple s.
  */
+/* One output row (b, r, h) of the attention below, written to o[0 .. head_dim). */
+static void attention_one(const void *q, const void *k_cache, const void *v_cache, int dtype,
+                          int32_t seq_len, int32_t r_max, int32_t n_heads, int32_t n_kv_heads,
+                          int32_t head_dim, double scale, int32_t b, int32_t r, int32_t h,
+                          double *s, double *o)
+{
+    const int32_t group = n_heads / n_kv_heads;
+    const int32_t g = h / group;
+    const int64_t qoff = (((int64_t)b * r_max + r) * n_heads + h) * head_dim;
+
+    double m = -INFINITY;
+    for (int32_t j = 0; j < seq_len; ++j) {
+        const int64_t koff = (((int64_t)b * seq_len + j) * n_kv_heads + g) * head_dim;
+        double dot = 0.0;
+        for (int32_t e = 0; e < head_dim; ++e)
+            dot += load(q, dtype, qoff + e) * load(k_cache, dtype, koff + e);
+        s[j] = scale * dot;
+        if (s[j] > m)
+            m = s[j];
+    }
+    double z = 0.0;
+    for (int32_t j = 0; j < seq_len; ++j) {
+        s[j] = exp(s[j] - m);
+        z += s[j];
+    }
+    for (int32_t e = 0; e < head_dim; ++e)
+        o[e] = 0.0;
+    for (int32_t j = 0; j < seq_len; ++j) {
+        const int64_t voff = (((int64_t)b * seq_len + j) * n_kv_heads + g) * head_dim;
+        const double w = s[j] / z;
+        for (int32_t e = 0; e < head_dim; ++e)
+            o[e] += w * load(v_cache, dtype, voff + e);
+    }
+}
+
 int orc_attention(const void *q, const void *k_cache, const void *v_cache, int dtype,
                   const int32_t *count, int32_t batch, int32_t seq_len, int32_t r_max,
                   int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, double scale,
@@ -338,61 +408,42 @@ int orc_attention(const void *q, const void *k_cache, const void *v_cache, int d
     if (batch < 0 || seq_len <= 0 || r_max < 0 || n_heads <= 0 || n_kv_heads <= 0 ||
         head_dim <= 0 || n_heads % n_kv_heads != 0)
         return ORC_BAD_ARG;
-    const int32_t group = n_heads / n_kv_heads;
-    double *s = (double *)malloc((size_t)seq_len * sizeof(double));
-    if (!s)
-        return ORC_NOMEM;
-
-    const int64_t total = samples ? n_samples : (int64_t)batch * r_max * n_heads;
-    for (int64_t t = 0; t < total; ++t) {
-        int32_t b, r, h;
-        double *o;
-        if (samples) {
-            b = samples[3 * t];
-            r = samples[3 * t + 1];
-            h = samples[3 * t + 2];
-            o = out + t * head_dim;
-            if (b < 0 || b >= batch || r < 0 || r >= r_max || h < 0 || h >= n_heads) {
-                free(s);
+    if (samples)
+        for (int64_t t = 0; t < n_samples; ++t) {
+            const int32_t b = samples[3 * t], r = samples[3 * t + 1], h = samples[3 * t + 2];
+            if (b < 0 || b >= batch || r < 0 || r >= r_max || h < 0 || h >= n_heads)
                 return ORC_BAD_ARG;
+        }
+    const int64_t total = samples ? n_samples : (int64_t)batch * r_max * n_heads;
+    int status = ORC_OK;
+#pragma omp parallel num_threads(g_threads)
+    {
+        double *s = (double *)malloc((size_t)seq_len * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < total; ++t) {
+            int32_t b, r, h;
+            if (samples) {
+                b = samples[3 * t];
+                r = samples[3 * t + 1];
+                h = samples[3 * t + 2];
+            } else {
+                b = (int32_t)(t / ((int64_t)r_max * n_heads));
+                r = (int32_t)((t / n_heads) % r_max);
+                h = (int32_t)(t % n_heads);
+                if (r >= count[b])
+                    continue;
             }
-        } else {
-            b = (int32_t)(t / ((int64_t)r_max * n_heads));
-            r = (int32_t)((t / n_heads) % r_max);
-            h = (int32_t)(t % n_heads);
-            if (r >= count[b])
+            if (!s) {
+#pragma omp atomic write
+                status = ORC_NOMEM;
                 continue;
-            o = out + t * head_dim;
+            }
+            attention_one(q, k_cache, v_cache, dtype, seq_len, r_max, n_heads, n_kv_heads,
+                          head_dim, scale, b, r, h, s, out + t * head_dim);
         }
-        const int32_t g = h / group;
-        const int64_t qoff = (((int64_t)b * r_max + r) * n_heads + h) * head_dim;
-
-        double m = -INFINITY;
-        for (int32_t j = 0; j < seq_len; ++j) {
-            const int64_t koff = (((int64_t)b * seq_len + j) * n_kv_heads + g) * head_dim;
-            double dot = 0.0;
-            for (int32_t e = 0; e < head_dim; ++e)
-                dot += load(q, dtype, qoff + e) * load(k_cache, dtype, koff + e);
-            s[j] = scale * dot;
-            if (s[j] > m)
-                m = s[j];
-        }
-        double z = 0.0;
-        for (int32_t j = 0; j < seq_len; ++j) {
-            s[j] = exp(s[j] - m);
-            z += s[j];
-        }
-        for (int32_t e = 0; e < head_dim; ++e)
-            o[e] = 0.0;
-        for (int32_t j = 0; j < seq_len; ++j) {
-            const int64_t voff = (((int64_t)b * seq_len + j) * n_kv_heads + g) * head_dim;
-            const double w = s[j] / z;
-            for (int32_t e = 0; e < head_dim; ++e)
-                o[e] += w * load(v_cache, dtype, voff + e);
-        }
+        free(s);
     }
-    free(s);
-    return ORC_OK;
+    return status;
 }
 
 /*
@@ -446,25 +497,33 @@ int orc_projection(const void *x, const void *w, int dtype, int64_t n_rows, int3
         return ORC_BAD_DTYPE;
     if (n_rows < 0 || hidden <= 0 || n_out <= 0)
         return ORC_BAD_ARG;
-    double *xr = (double *)malloc((size_t)hidden * sizeof(double));
-    if (!xr)
-        return ORC_NOMEM;
     const int64_t total = rows ? n_sel : n_rows;
-    for (int64_t s = 0; s < total; ++s) {
-        const int64_t row = rows ? rows[s] : s;
-        if (row < 0 || row >= n_rows) {
-            free(xr);
-            return ORC_BAD_ARG;
-        }
-        for (int32_t e = 0; e < hidden; ++e)
-            xr[e] = load(x, dtype, row * hidden + e);
-        for (int32_t j = 0; j < n_out; ++j) {
-            double acc = 0.0;
+    if (rows)
+        for (int64_t s = 0; s < total; ++s)
+            if (rows[s] < 0 || rows[s] >= n_rows)
+                return ORC_BAD_ARG;
+    int status = ORC_OK;
+#pragma omp parallel num_threads(g_threads)
+    {
+        double *xr = (double *)malloc((size_t)hidden * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t s = 0; s < total; ++s) {
+            if (!xr) {
+#pragma omp atomic write
+                status = ORC_NOMEM;
+                continue;
+            }
+            const int64_t row = rows ? rows[s] : s;
             for (int32_t e = 0; e < hidden; ++e)
-                acc += xr[e] * load(w, dtype, (int64_t)j * hidden + e);
-            y[s * n_out + j] = acc;
+                xr[e] = load(x, dtype, row * hidden + e);
+            for (int32_t j = 0; j < n_out; ++j) {
+                double acc = 0.0;
+                for (int32_t e = 0; e < hidden; ++e)
+                    acc += xr[e] * load(w, dtype, (int64_t)j * hidden + e);
+                y[s * n_out + j] = acc;
+            }
         }
+        free(xr);
     }
-    free(xr);
-    return ORC_OK;
+    return status;
 }

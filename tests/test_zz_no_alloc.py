@@ -37,27 +37,38 @@ def _args(w, st, logits, o):
             o["refresh"], o["is_masked"], o["tokens"], o["decode_step"])
 
 
+def _compare_one_call(nat, w, seed, tag):
+    st = synth.make_state(np.random.default_rng(0), w)
+    rng = np.random.default_rng(seed)
+    logits = dev(synth.make_logits(rng, w.n_rows, w.vocab, w.logits_dtype, w.near_uniform_frac))
+    ref = _buffers(w, st)
+    ws = nat.new_workspace(nat.ec_decode_workspace_size(w.n_rows, w.batch))
+    nat.ec_decode_step(*_args(w, st, logits, ref), ws)
+    got = _buffers(w, st)
+    nat.ec_decode_step_noalloc(*_args(w, st, logits, got))
+    torch.cuda.synchronize()
+    for k in FIELDS:
+        a, b = host(ref[k]), host(got[k])
+        if k in ("conf", "entropy", "max_entropy"):
+            assert np.allclose(a, b, rtol=1e-6, atol=ENTROPY_ATOL, equal_nan=False), (tag, k)
+        else:
+            assert np.array_equal(a, b), (tag, k)
+
+
 @pytest.mark.parametrize("name", ["single_seq", "batched"])
 def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(name):
     nat = native()
     w = synth.WORKLOADS[name]
-    st = synth.make_state(np.random.default_rng(0), w)
     for call in range(2):  # the second call must not see the first call's leftovers
-        rng = np.random.default_rng(100 + call)
-        logits = dev(synth.make_logits(rng, w.n_rows, w.vocab, w.logits_dtype,
-                                       w.near_uniform_frac))
-        ref = _buffers(w, st)
-        ws = nat.new_workspace(nat.ec_decode_workspace_size(w.n_rows, w.batch))
-        nat.ec_decode_step(*_args(w, st, logits, ref), ws)
-        got = _buffers(w, st)
-        nat.ec_decode_step_noalloc(*_args(w, st, logits, got))
-        torch.cuda.synchronize()
-        for k in FIELDS:
-            a, b = host(ref[k]), host(got[k])
-            if k in ("conf", "entropy", "max_entropy"):
-                assert np.allclose(a, b, rtol=1e-6, atol=ENTROPY_ATOL, equal_nan=False), (call, k)
-            else:
-                assert np.array_equal(a, b), (call, k)
+        _compare_one_call(nat, w, 100 + call, call)
+
+
+def test_noalloc_alternating_shapes():
+    # the scratch layout moves with n_rows and batch: a call after a larger or a
+    # smaller one must still start from cleared counters
+    nat = native()
+    for i, name in enumerate(["batched", "single_seq", "tiny", "batched", "single_seq"]):
+        _compare_one_call(nat, synth.WORKLOADS[name], 200 + i, (i, name))
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch():
