@@ -25,7 +25,8 @@ DEV_BAD_COUNT = 0x4
 DEV_BAD_INDEX = 0x8
 DEV_TIMEOUT = 0x10
 
-EXPORTED = ("ec_status_str", "ec_abi_version", "ec_workspace_init", "ec_read_device_status",
+EXPORTED = ("ec_status_str", "ec_abi_version", "ec_debug_set_wait_limit", "ec_workspace_init",
+            "ec_read_device_status",
             "ec_decode_workspace_size", "ec_decode_step", "ec_decode_step_noalloc",
             "ec_build_recompute_set", "ec_attention_workspace_size", "ec_attention_kernel_count",
             "ec_selective_attention",
@@ -58,6 +59,7 @@ def lib() -> ctypes.CDLL:
         L.ec_status_str.restype = ctypes.c_char_p
         L.ec_abi_version.argtypes = []
         L.ec_abi_version.restype = ctypes.c_int
+        L.ec_debug_set_wait_limit.argtypes = [i64]
         L.ec_workspace_init.argtypes = [vp, sz, vp]
         L.ec_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         L.ec_decode_workspace_size.argtypes = [i32, i32]
@@ -76,7 +78,8 @@ def lib() -> ctypes.CDLL:
         L.ec_embed_rows.argtypes = [vp, i64, i32, vp, i64, vp, vp, vp, i32, i32, i32, i32, vp, vp,
                                     sz, vp]
         L.ec_qkv_projection.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, sz, vp]
-        for name in ("ec_workspace_init", "ec_read_device_status", "ec_decode_step",
+        for name in ("ec_debug_set_wait_limit", "ec_workspace_init", "ec_read_device_status",
+                     "ec_decode_step",
                      "ec_decode_step_noalloc", "ec_build_recompute_set", "ec_selective_attention",
                      "ec_embed_rows", "ec_qkv_projection"):
             getattr(L, name).restype = ctypes.c_int
@@ -146,6 +149,12 @@ def ec_attention_kernel_count(dtype, batch, seq_len, r_max, n_heads, n_kv_heads,
     code = {torch.bfloat16: EC_BF16, torch.float32: EC_F32}[dtype]
     return lib().ec_attention_kernel_count(code, batch, seq_len, r_max, n_heads, n_kv_heads,
                                            head_dim)
+
+
+def ec_debug_set_wait_limit(cycles: int):
+    """Test hook: the cycle limit of every in-kernel wait of later launches
+    (0 restores the default of about 2 s); see ec.h."""
+    _check(lib().ec_debug_set_wait_limit(int(cycles)), "ec_debug_set_wait_limit")
 
 
 def new_workspace(nbytes: int, device="cuda") -> torch.Tensor:

@@ -114,6 +114,7 @@ struct Params {
     int n_split;       // > 0: split-major items (see piece_at); 0: stream-K ranges
     float scale_log2;
     uint32_t *status;   // workspace status word
+    long long wait_limit;  // cycles one in-kernel wait may take
     float2 *part_ml;    // [n_units][slots][128] (m, l), m in raw score units
     float4 *part_o;     // [n_units][slots][D / 4][128] unnormalised O
 };
@@ -715,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 16);
-    Sync S{sbase + C::kOffBar, abort_flag, P.status};
+    Sync S{sbase + C::kOffBar, abort_flag, P.status, P.wait_limit};
 
     pdl_launch_dependents();
     if (threadIdx.x == 0) {
@@ -970,6 +971,7 @@ cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_
     size_t o_ml, o_o;
     partial_offsets(plan, head_dim, &o_ml, &o_o);
     p.status = reinterpret_cast<uint32_t *>(ws);
+    p.wait_limit = wait_limit_cycles();
     p.part_ml = reinterpret_cast<float2 *>(ws + o_ml);
     p.part_o = reinterpret_cast<float4 *>(ws + o_o);
     return head_dim == 128 ? launch_typed<128>(p, plan, q, stream)

@@ -337,6 +337,7 @@ struct Args {
     uint8_t *refresh, *is_masked;
     int32_t *seq_tokens, *decode_step;
     uint32_t *status;
+    long long wait_limit;  // cycles one in-kernel wait may take
     unsigned *row_ctr, *seq_ctr;
     Partial *parts;
 };
@@ -658,7 +659,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
     __shared__ Partial s_piece[kPieceSlots][kConsumerWarps];
     __shared__ Piece s_info[kPieceSlots];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    Sync S{ring_u32 + kStages * kChunk, reinterpret_cast<volatile int *>(&s_abort), A.status};
+    Sync S{ring_u32 + kStages * kChunk, reinterpret_cast<volatile int *>(&s_abort), A.status,
+           A.wait_limit};
 
     if (tid == 0) {
         s_abort = 0;
@@ -821,6 +823,7 @@ cudaError_t launch_decode_gate(const void *logits, int dtype, int64_t row_stride
     A.decode_step = decode_step;
     char *ws = static_cast<char *>(workspace);
     A.status = reinterpret_cast<uint32_t *>(ws);
+    A.wait_limit = wait_limit_cycles();
     size_t off = kWsHeader;
     A.row_ctr = reinterpret_cast<unsigned *>(ws + off);
     off = align_up(off + static_cast<size_t>(std::max(n_rows, 0)) * sizeof(unsigned), 16);

@@ -2,11 +2,21 @@
 // Every check here runs on the host before anything is enqueued.
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ec_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace ec {
+
+static std::atomic<long long> g_wait_limit{0};
+
+long long wait_limit_cycles()
+{
+    const long long v = g_wait_limit.load(std::memory_order_relaxed);
+    return v > 0 ? v : ptx::kWaitCycles;
+}
 
 cudaError_t configure_kernel(const void *kernel, int dynamic_smem)
 {
@@ -77,6 +87,13 @@ const char *ec_status_str(int s)
 }
 
 int ec_abi_version(void) { return EC_ABI_VERSION; }
+
+ec_status ec_debug_set_wait_limit(int64_t cycles)
+{
+    if (cycles < 0) return EC_ERR_SHAPE;
+    ec::g_wait_limit.store(static_cast<long long>(cycles), std::memory_order_relaxed);
+    return EC_OK;
+}
 
 ec_status ec_workspace_init(void *workspace, size_t workspace_bytes, ec_stream_t stream)
 {

@@ -44,6 +44,10 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
 
 int device_sm_count();  // SM count of the current device (cached per device)
 
+// Cycles one in-kernel wait may take before it gives up (kernels carry it in
+// their parameters): about 2 s, unless ec_debug_set_wait_limit lowered it.
+long long wait_limit_cycles();
+
 // ---- launches ----
 // Every kernel of the library is launched with programmatic dependent launch:
 // it may start while the previous kernel on the stream is still running.  Its

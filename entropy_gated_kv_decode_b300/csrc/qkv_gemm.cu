@@ -68,6 +68,7 @@ struct GemmParams {
     __nv_bfloat16 *out[3];
     int batch, r_max, hidden, width, n_mt, n_nt, n_tiles;
     uint32_t *status;
+    long long wait_limit;  // cycles one in-kernel wait may take
 };
 
 struct Tile {
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 16);
-    Sync S{sbase + C::kOffBar, abort_flag, P.status};
+    Sync S{sbase + C::kOffBar, abort_flag, P.status, P.wait_limit};
 
     pdl_launch_dependents();
     if (threadIdx.x == 0) {
@@ -371,6 +372,7 @@ cudaError_t launch_qkv_projection(const void *x, const int32_t *count, int32_t b
     p.width = width;
     p.n_mt = (r_max + kBM - 1) / kBM;
     p.status = status;
+    p.wait_limit = wait_limit_cycles();
     switch (choose_bn(batch, r_max, width)) {
     case 256: return launch_bn<256>(p, x, w_qkv, stream);
     case 128: return launch_bn<128>(p, x, w_qkv, stream);

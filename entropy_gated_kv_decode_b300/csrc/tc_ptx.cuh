@@ -56,6 +56,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of a phase's completion.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // As mbar_try_wait, but the thread sleeps in the barrier until the phase
 // completes or about `ns` nanoseconds pass, instead of returning at once: a
 // waiting warp then takes no issue slots from the warps doing the work.
@@ -266,39 +279,55 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // ---- bounded waits on a CTA's array of mbarriers ----
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s: a wait this long is a fault
+constexpr long long kShortWait = 1000000LL;      // limits below this are test limits
 constexpr uint32_t kSleepNs = 20000;              // longest sleep of one try_wait
 
-// mbarrier i lives at bars + 8 i.  wait() gives up after ~2 s (or as soon as
-// another role of the CTA gave up): it raises the CTA's abort flag, sets
+// mbarrier i lives at bars + 8 i.  wait() gives up after `limit` cycles (the
+// launch's wait limit, kWaitCycles unless a test lowered it) or as soon as
+// another role of the CTA gave up: it raises the CTA's abort flag, sets
 // EC_DEV_TIMEOUT in the status word and returns false, so every role unwinds.
+// A test limit (below kShortWait) polls without sleeping and checks the clock
+// on every poll, so a wait on data that cannot have arrived yet gives up.
 struct Sync {
     uint32_t bars;
     volatile int *abort_flag;
     uint32_t *status;
+    long long limit;
     __device__ uint32_t bar(int i) const { return bars + 8u * static_cast<uint32_t>(i); }
+    __device__ bool give_up() const
+    {
+        *abort_flag = 1;
+        flag_status(status, EC_DEV_TIMEOUT);
+        return false;
+    }
     __device__ bool wait(int i, uint32_t parity) const
     {
         const uint32_t b = bar(i);
-        if (mbar_try_wait(b, parity)) return true;
+        if (mbar_test_wait(b, parity)) return true;
         const long long t0 = clock64();
+        if (limit < kShortWait) {
+            while (clock64() - t0 <= limit) {
+                if (*abort_flag) return false;
+                if (mbar_test_wait(b, parity)) return true;
+            }
+            return give_up();
+        }
         for (uint32_t it = 1;; ++it) {
             if (mbar_try_wait_sleep(b, parity, kSleepNs)) return true;
             if ((it & 15u) == 0u) {
                 if (*abort_flag) return false;
-                if (clock64() - t0 > kWaitCycles) {
-                    *abort_flag = 1;
-                    flag_status(status, EC_DEV_TIMEOUT);
-                    return false;
-                }
+                if (clock64() - t0 > limit) return give_up();
             }
         }
     }
-    // Used after an abort, to let copies already in flight land (bounded too).
+    // Used after an abort, to let copies (or tensor-core operations) already in
+    // flight complete before the CTA exits or frees TMEM.  Always the full limit:
+    // it must outlast any copy, whatever limit the waits had.
     __device__ bool drain(int i, uint32_t parity) const
     {
         const long long t0 = clock64();
         while (!mbar_try_wait(bar(i), parity))
-            if (clock64() - t0 > kWaitCycles / 4) return false;
+            if (clock64() - t0 > kWaitCycles) return false;
         return true;
     }
 };

@@ -69,6 +69,21 @@ const char *ec_status_str(int status);
 #define EC_ABI_VERSION 1
 int ec_abi_version(void);
 
+/*
+ * Test hook for the device-side timeout path.  Every wait inside the kernels
+ * (a ring stage landing, a tensor-core product completing) is bounded: by
+ * default it gives up after about 2 s, sets EC_DEV_TIMEOUT in the workspace's
+ * status word, lets the copies and tensor-core operations it already started
+ * complete, releases its tensor memory and returns, leaving the context usable.
+ * This sets that limit, in SM clock cycles, for launches made afterwards by any
+ * thread of the process (0 restores the default); a limit of a few hundred
+ * cycles makes the first wait on data give up.  After a call that timed out,
+ * zero its workspace (ec_workspace_init) before the next call.  Not for use in
+ * production: it changes no result of a call that does not time out.
+ * Returns EC_ERR_SHAPE for a negative value.
+ */
+ec_status ec_debug_set_wait_limit(int64_t cycles);
+
 /* Alignment, in bytes, that every workspace pointer must have. */
 #define EC_WORKSPACE_ALIGN 256
 
