@@ -1,52 +1,54 @@
 // Selective-recompute bidirectional attention on the 5th-generation tensor
-// cores (tcgen05 + TMEM), fed by TMA, with the KV write-back in the same call.
+// cores (tcgen05 + TMEM), fed by TMA, with the KV write-back in the same kernel.
 //
 // "EntropyCache: Decoded Token Entropy Guided KV Caching for Diffusion Language
 // Models" — Italian summary, section "1. Il Problema" (dLLM attention is
 // bidirectional) and "Algoritmo di Funzionamento" step 2 (the partial forward
 // recomputes K/V only for the selected tokens; the cache supplies the rest).
 //
-// Up to three launches, chained by programmatic dependent launch (PDL):
-//   write_back_kernel   copies every fresh K/V row into the caches and at once
-//                       lets the attention grid start;
-//   attention_tc_kernel allocates TMEM, sets up its barriers and loads its first
-//                       Q tile while the write-back runs, and waits for it
-//                       (griddepcontrol.wait) only before its first K/V load;
-//   merge_kernel        (only when some unit is split over several CTAs)
-//                       combines the split units' partials into the output.
+// One launch.  Work is cut into
+//   units    up to 128 query rows of one (sequence b, KV head g): the
+//            (recomputed row r, head h of g's group) pairs packed r-major, so a
+//            GQA group shares each K/V tile; a (b, g) has n_mt units;
+//   groups   n_mt CTAs, one per unit of a (b, g).  The (b, g, 128-key tile)
+//            pairs, laid end to end, are cut into one equal contiguous range per
+//            group, and the n_mt CTAs of a group walk the same key tiles at the
+//            same time: each tile comes from HBM once and from L2 for the others.
+//   pieces   the (b, g)'s a range meets.  A piece that covers all of a unit's
+//            tiles writes its output.  A unit cut over several groups is merged
+//            in the kernel: the group holding its last tile owns it; the others
+//            contribute a partial (O, m, l) and release a flag.  Every CTA runs
+//            its pieces from the last (b, g) to the first, so a contribution
+//            (the first piece a group runs) is done long before its owner (the
+//            last piece of the next group) needs it.
+// Write-back: the fresh K/V rows of a tile are patched into the tile in shared
+// memory after its TMA load lands (so no CTA depends on another's global write),
+// and the group whose range holds the tile writes them to the cache from its
+// mt = 0 CTA.  A sequence that recomputes all L rows (count = L, so the index
+// set is 0 .. L-1) loads its tiles from the fresh K/V directly, and its mt = 0
+// CTAs store every tile to the cache with a TMA store.
 //
-// Attention kernel: persistent, one CTA per SM.
-//   units      up to 128 query rows of one (sequence b, KV head g): the
-//              (recomputed row r, head h of g's group) pairs packed r-major, so
-//              a GQA group shares each K/V tile.
-//   pieces     the units' 128-key tiles are laid end to end and cut into one
-//              equal contiguous range per CTA (stream-K), so every CTA does the
-//              same number of tiles.  A range covers pieces of one or more
-//              units.  A piece that is a whole unit writes its output directly;
-//              otherwise it stores a partial (O, m, l) and moves on: no CTA
-//              waits for another, and the merge kernel, spread over the whole
-//              GPU, combines the partials afterwards.
-//   warp 0     producer of Q (one tile per piece) and K tiles, warp 6 producer
-//              of V tiles: TMA, 128-byte swizzle, rings of stages; a K stage is
-//              released when its QK product completes, a V stage when its PV
-//              product does;
-//   warp 1     TMEM allocation; Q into TMEM (tcgen05.cp) and S = Q K^T into one
-//              of two TMEM S buffers (tcgen05.mma) once the PV product that read
-//              that buffer's P has completed;
+// Warp roles (320 threads):
+//   warp 0     TMA producer of Q (one tile per piece) and K tiles; warp 6 of V
+//              tiles (128-byte swizzle, rings of stages);
+//   warps 8, 9 patch the fresh rows into each landed K / V tile (or store the
+//              tile to the cache, full refresh), then release it to the MMAs;
+//   warp 1     TMEM allocation; Q into TMEM (tcgen05.cp) and S = Q K^T into one of
+//              two TMEM S buffers (tcgen05.mma) once the PV product that read that
+//              buffer's P has completed;
 //   warp 7     O += P V into the TMEM O accumulator: a second issuing thread, so
 //              the next tile's QK never queues behind this tile's PV;
 //   warps 2-5  one thread per query row: online softmax in the log2 domain on S
-//              read by tcgen05.ld (the reference maximum moves only when it
-//              grows by more than 8 in log2 units, rescaling O in TMEM when it
-//              does), P as bf16 over the first half of the same S buffer (the
-//              PV product takes its A operand from there), and the epilogue.
-//              With P in its own S buffer the softmax never waits for the
-//              previous tile's PV product, except to rescale O.
-// Every wait is bounded (~2 s); a timeout sets EC_DEV_TIMEOUT and unwinds.
+//              read by tcgen05.ld (the reference maximum moves only when it grows
+//              by more than 8 in log2 units, rescaling O in TMEM), P as bf16 over
+//              the first half of the same S buffer (the PV product reads its A
+//              operand there), and the piece's epilogue.
+// Every wait is bounded; a timeout sets EC_DEV_TIMEOUT and unwinds.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 
 #include "ec_internal.cuh"
@@ -59,8 +61,9 @@ using namespace ptx;
 
 constexpr int kBlockM = 128;   // query rows per unit = TMEM lanes
 constexpr int kBlockN = 128;   // keys per tile
-constexpr int kThreads = 256;  // 8 warps
-constexpr int kMaxContrib = 64;  // pieces a unit may be cut into
+constexpr int kThreads = 320;  // 10 warps
+constexpr int kSoftmaxBarrier = 1;  // named barrier of the 4 softmax warps
+constexpr int kMaxContrib = 8;      // contributors merged by one owner at most
 
 template <int D>
 struct Cfg {
@@ -74,7 +77,7 @@ struct Cfg {
     static constexpr uint32_t kOffK = kOffQ + kQBufs * kTile;
     static constexpr uint32_t kOffV = kOffK + kKStages * kTile;
     static constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
-    static constexpr uint32_t kOffMisc = kOffBar + 256;
+    static constexpr uint32_t kOffMisc = kOffBar + 512;
     static constexpr uint32_t kBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1 KB
     static constexpr uint32_t kTmemCols = 512;
     // two S buffers, columns [0, 128) and [128, 256); P (bf16 pairs) of a tile
@@ -85,19 +88,22 @@ struct Cfg {
 };
 
 enum : int {
-    B_KFULL = 0,    // [4] K tile landed
-    B_KEMPTY = 4,   // [4] K stage consumed (its QK done)
-    B_VFULL = 8,    // [4] V tile landed
-    B_VEMPTY = 12,  // [4] V stage consumed (its PV done)
-    B_QFULL = 16,   // [2] Q tile landed
-    B_QEMPTY = 18,  // [2] Q tile copied into TMEM
-    B_SFULL = 20,   // [2] S buffer written by its QK product
-    B_PFULL = 22,   // [2] P written over its S buffer (and O corrected): 4 softmax warps
-    B_SFREE = 24,   // [2] the PV product that read the buffer's P completed (O updated)
-    B_DRAIN = 26,   // QK issuer's products all complete
-    B_DRAIN2 = 27,  // PV issuer's products all complete
-    B_COUNT = 28
+    B_KFULL = 0,     // [4] K tile landed
+    B_KREADY = 4,    // [4] K tile patched (fresh rows in place): the QK product may read it
+    B_KEMPTY = 8,    // [4] K stage consumed (its QK done)
+    B_VFULL = 12,    // [4] V tile landed
+    B_VREADY = 16,   // [4] V tile patched
+    B_VEMPTY = 20,   // [4] V stage consumed (its PV done)
+    B_QFULL = 24,    // [2] Q tile landed
+    B_QEMPTY = 26,   // [2] Q tile copied into TMEM
+    B_SFULL = 28,    // [2] S buffer written by its QK product
+    B_PFULL = 30,    // [2] P written over its S buffer (and O corrected): 4 softmax warps
+    B_SFREE = 32,    // [2] the PV product that read the buffer's P completed (O updated)
+    B_DRAIN = 34,    // QK issuer's products all complete
+    B_DRAIN2 = 35,   // PV issuer's products all complete
+    B_COUNT = 36
 };
+static_assert(8 * B_COUNT <= 512, "barrier area");
 
 struct Params {
     const __nv_bfloat16 *k_new, *v_new;
@@ -109,110 +115,119 @@ struct Params {
     int tok_per_tile;  // recomputed rows per unit: floor(128 / G)
     int n_mt;          // units per (b, g)
     int n_units, n_tiles, grid;
-    int64_t total;     // n_units * n_tiles
-    int slots;         // partial slots per unit (most pieces a unit is cut into)
-    int n_split;       // > 0: split-major items (see piece_at); 0: stream-K ranges
+    int grouped;       // 1: groups of n_mt CTAs over (b, g, tile) ranges; 0: whole units round-robin
+    int n_groups;
+    int64_t total;     // B * Hkv * n_tiles
+    int slots;         // partial slots per unit (most contributors a unit can have)
     float scale_log2;
-    uint32_t *status;   // workspace status word
-    long long wait_limit;  // cycles one in-kernel wait may take
-    float2 *part_ml;    // [n_units][slots][128] (m, l), m in raw score units
-    float4 *part_o;     // [n_units][slots][D / 4][128] unnormalised O
+    uint32_t *status;     // workspace status word
+    long long wait_limit; // cycles one in-kernel wait may take
+    uint32_t *flags;      // [n_units] contributions released (the owner resets it to 0)
+    float2 *part_ml;      // [n_units][slots][128] (m, l), m in raw score units
+    float4 *part_o;       // [n_units][slots][D / 4][128] unnormalised O
 };
 
-// A piece: tiles [t0, t1) of one unit, processed by this CTA.
+enum : int { ROLE_WHOLE = 0, ROLE_CONTRIB = 1, ROLE_OWNER = 2 };
+
+// A piece: tiles [t0, t1) of unit (b, g, mt), processed by this CTA.
 struct Piece {
-    int unit, b, g, mt, t0, t1, cnt, slot, n_contrib;
+    int unit, b, g, mt, t0, t1, cnt, role, slot, n_contrib;
 };
 
-__device__ __forceinline__ int64_t range_begin(const Params &P, int c)
+__device__ __forceinline__ int group_of(const Params &P, int64_t w)
 {
-    return static_cast<int64_t>(c) * P.total / P.grid;
-}
-__device__ __forceinline__ int cta_of(const Params &P, int64_t w)
-{
-    return static_cast<int>(((w + 1) * P.grid - 1) / P.total);
+    return static_cast<int>(((w + 1) * P.n_groups - 1) / P.total);
 }
 
-// The pieces of CTA blockIdx.x, in order.
-//   stream-K (n_split == 0): the units' tiles laid end to end, one equal
-//     contiguous range per CTA; the pieces are the units that range meets.
-//   split-major items (n_split > 0): item i = ((b, g, split), mt) with mt
-//     varying fastest is tiles [split * n_tiles / n_split, ...) of unit
-//     (b, g, mt); items are dealt round-robin.  The CTAs working on the row
-//     tiles of one KV head then read the same K/V tiles at the same time, so
-//     each tile comes from HBM once and from L2 for the others (used when the
-//     caches do not fit in L2).
+// This CTA's share: `count` pieces, piece_at(k) for k in [0, count) in processing order.
 struct Range {
     int64_t w0, w1;
-    int u_first, count;
+    int bg_first, count, mt, group;
 };
 __device__ __forceinline__ Range my_range(const Params &P)
 {
     Range r;
-    if (P.n_split > 0) {
-        const int n_items = P.n_units * P.n_split;
-        r.w0 = r.w1 = 0;
-        r.u_first = 0;
-        r.count = static_cast<int>(blockIdx.x) < n_items
-                      ? (n_items - 1 - static_cast<int>(blockIdx.x)) / P.grid + 1
+    r.w0 = r.w1 = 0;
+    r.bg_first = 0;
+    r.group = 0;
+    r.mt = 0;
+    r.count = 0;
+    if (!P.grouped) {  // whole units dealt round-robin
+        r.count = static_cast<int>(blockIdx.x) < P.n_units
+                      ? (P.n_units - 1 - static_cast<int>(blockIdx.x)) / P.grid + 1
                       : 0;
         return r;
     }
-    r.w0 = range_begin(P, blockIdx.x);
-    r.w1 = range_begin(P, blockIdx.x + 1);
-    r.u_first = static_cast<int>(r.w0 / P.n_tiles);
-    r.count = r.w1 > r.w0 ? static_cast<int>((r.w1 - 1) / P.n_tiles) - r.u_first + 1 : 0;
+    r.group = static_cast<int>(blockIdx.x) / P.n_mt;
+    r.mt = static_cast<int>(blockIdx.x) % P.n_mt;
+    if (r.group >= P.n_groups) return r;
+    r.w0 = static_cast<int64_t>(r.group) * P.total / P.n_groups;
+    r.w1 = static_cast<int64_t>(r.group + 1) * P.total / P.n_groups;
+    if (r.w1 <= r.w0) return r;
+    r.bg_first = static_cast<int>(r.w0 / P.n_tiles);
+    r.count = static_cast<int>((r.w1 - 1) / P.n_tiles) - r.bg_first + 1;
     return r;
 }
 
 __device__ __forceinline__ Piece piece_at(const Params &P, const Range &r, int k)
 {
     Piece p;
-    if (P.n_split > 0) {
-        const int i = static_cast<int>(blockIdx.x) + k * P.grid;
-        p.mt = i % P.n_mt;
-        const int split = (i / P.n_mt) % P.n_split;
-        const int bg = i / (P.n_mt * P.n_split);
-        p.unit = bg * P.n_mt + p.mt;
+    if (!P.grouped) {
+        p.unit = static_cast<int>(blockIdx.x) + k * P.grid;
+        p.mt = p.unit % P.n_mt;
+        const int bg = p.unit / P.n_mt;
         p.g = bg % P.Hkv;
         p.b = bg / P.Hkv;
-        p.t0 = static_cast<int>(static_cast<int64_t>(P.n_tiles) * split / P.n_split);
-        p.t1 = static_cast<int>(static_cast<int64_t>(P.n_tiles) * (split + 1) / P.n_split);
-        p.slot = split;
-        p.n_contrib = P.n_split;
+        p.t0 = 0;
+        p.t1 = P.n_tiles;
+        p.role = ROLE_WHOLE;
+        p.slot = p.n_contrib = 0;
     } else {
-        const int u = r.u_first + k;
-        p.unit = u;
-        p.mt = u % P.n_mt;
-        p.g = (u / P.n_mt) % P.Hkv;
-        p.b = u / (P.n_mt * P.Hkv);
-        const int64_t base = static_cast<int64_t>(u) * P.n_tiles;
+        const int bg = r.bg_first + r.count - 1 - k;  // the last (b, g) first
+        p.mt = r.mt;
+        p.unit = bg * P.n_mt + r.mt;
+        p.g = bg % P.Hkv;
+        p.b = bg / P.Hkv;
+        const int64_t base = static_cast<int64_t>(bg) * P.n_tiles;
         p.t0 = static_cast<int>(max(r.w0, base) - base);
         p.t1 = static_cast<int>(min(r.w1, base + P.n_tiles) - base);
-        const int c0 = cta_of(P, base), c1 = cta_of(P, base + P.n_tiles - 1);
-        p.slot = static_cast<int>(blockIdx.x) - c0;
-        p.n_contrib = c1 - c0 + 1;
+        const int k_first = group_of(P, base), k_last = group_of(P, base + P.n_tiles - 1);
+        p.n_contrib = k_last - k_first;
+        if (k_first == k_last) {
+            p.role = ROLE_WHOLE;
+            p.slot = 0;
+        } else if (r.group == k_last) {
+            p.role = ROLE_OWNER;
+            p.slot = 0;
+        } else {
+            p.role = ROLE_CONTRIB;
+            p.slot = r.group - k_first;
+        }
     }
     p.cnt = max(0, min(__ldg(P.count + p.b), P.r_max));
     return p;
 }
 
 // Units with no recomputed rows (mt beyond the sequence's count) are skipped by
-// every role alike.
+// every role alike (contributors and owner agree: count is one value).
 __device__ __forceinline__ bool piece_active(const Params &P, const Piece &p)
 {
     return p.mt * P.tok_per_tile < p.cnt && p.t1 > p.t0;
 }
+
+// Every position of sequence b is recomputed: the index set is 0 .. L-1.
+__device__ __forceinline__ bool piece_dense(const Params &P, const Piece &p) { return p.cnt == P.L; }
 
 static_assert(Cfg<128>::kColS + 2 * kBlockN <= Cfg<128>::kColO, "TMEM columns overlap");
 static_assert(Cfg<128>::kColO + 128 <= Cfg<128>::kColQ, "TMEM columns overlap");
 static_assert(Cfg<128>::kColQ + 128 / 2 <= Cfg<128>::kTmemCols, "TMEM columns overflow");
 static_assert(Cfg<128>::kBytes <= 227 * 1024 && Cfg<64>::kBytes <= 227 * 1024, "shared memory");
 
-// Q and K producer (one thread): per piece its Q tile, then its K tiles.
+// Q and K producer (one thread): per piece its Q tile, then its K tiles (from the
+// fresh K of a fully recomputed sequence, else from the cache).
 template <int D>
 __device__ void producer_qk(const Params &P, const Sync &S, uint32_t sbase, const CUtensorMap *tm_q,
-                            const CUtensorMap *tm_k)
+                            const CUtensorMap *tm_k, const CUtensorMap *tm_kn)
 {
     using C = Cfg<D>;
     const uint32_t q_bytes = static_cast<uint32_t>(P.tok_per_tile * P.G) * D * 2;
@@ -222,6 +237,7 @@ __device__ void producer_qk(const Params &P, const Sync &S, uint32_t sbase, cons
     for (int k = 0; k < r.count && ok; ++k) {
         const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
+        const CUtensorMap *src = piece_dense(P, w) ? tm_kn : tm_k;
         const int qb = it % C::kQBufs;
         if (it >= static_cast<uint32_t>(C::kQBufs))
             ok = S.wait(B_QEMPTY + qb, ((it / C::kQBufs) - 1) & 1);
@@ -240,8 +256,7 @@ __device__ void producer_qk(const Params &P, const Sync &S, uint32_t sbase, cons
             const uint32_t kdst = sbase + C::kOffK + s * C::kTile;
             mbar_expect_tx(S.bar(B_KFULL + s), C::kTile);
             for (int c = 0; c < D / 64; ++c)
-                tma_load_4d(kdst + c * C::kCol, tm_k, S.bar(B_KFULL + s), c * 64, w.g, t * kBlockN,
-                            w.b);
+                tma_load_4d(kdst + c * C::kCol, src, S.bar(B_KFULL + s), c * 64, w.g, t * kBlockN, w.b);
         }
     }
     if (!ok) {  // let every copy this thread started land before the CTA exits
@@ -254,7 +269,8 @@ __device__ void producer_qk(const Params &P, const Sync &S, uint32_t sbase, cons
 
 // V producer (one thread): the V tiles of every piece, in the same order.
 template <int D>
-__device__ void producer_v(const Params &P, const Sync &S, uint32_t sbase, const CUtensorMap *tm_v)
+__device__ void producer_v(const Params &P, const Sync &S, uint32_t sbase, const CUtensorMap *tm_v,
+                           const CUtensorMap *tm_vn)
 {
     using C = Cfg<D>;
     const Range r = my_range(P);
@@ -263,6 +279,7 @@ __device__ void producer_v(const Params &P, const Sync &S, uint32_t sbase, const
     for (int k = 0; k < r.count && ok; ++k) {
         const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
+        const CUtensorMap *src = piece_dense(P, w) ? tm_vn : tm_v;
         for (int t = w.t0; t < w.t1 && ok; ++t, ++T) {
             const int s = T % C::kVStages;
             if (T >= static_cast<uint32_t>(C::kVStages))
@@ -271,8 +288,7 @@ __device__ void producer_v(const Params &P, const Sync &S, uint32_t sbase, const
             const uint32_t vdst = sbase + C::kOffV + s * C::kTile;
             mbar_expect_tx(S.bar(B_VFULL + s), C::kTile);
             for (int c = 0; c < D / 64; ++c)
-                tma_load_4d(vdst + c * C::kCol, tm_v, S.bar(B_VFULL + s), c * 64, w.g, t * kBlockN,
-                            w.b);
+                tma_load_4d(vdst + c * C::kCol, src, S.bar(B_VFULL + s), c * 64, w.g, t * kBlockN, w.b);
         }
     }
     if (!ok)
@@ -280,10 +296,161 @@ __device__ void producer_v(const Params &P, const Sync &S, uint32_t sbase, const
             S.drain(B_VFULL + u % C::kVStages, (u / C::kVStages) & 1);
 }
 
+// TMA store of one 64-column block of a tile (rows past L are not stored).
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t src, int c0, int c1,
+                                             int c2, int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+        : "memory");
+}
+// Wait until every bulk store this thread issued has finished reading shared memory.
+__device__ __forceinline__ void bulk_commit_and_wait_read()
+{
+    asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until every bulk store this thread issued is complete (before the CTA exits).
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// First r in [0, cnt) with idx[r] >= key (cnt when none), by the whole warp:
+// 32 samples per round.  idx ascending; a non-ascending set still yields an
+// index in [0, cnt].
+__device__ __forceinline__ int lower_bound_warp(const int32_t *idx, int cnt, int key)
+{
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = cnt;  // the answer lies in [lo, hi]
+    while (hi - lo > 32) {
+        const int step = (hi - lo + 31) / 32;
+        const int j = lo + lane * step;
+        const bool below = j < hi && __ldg(idx + j) < key;
+        const int n = __popc(__ballot_sync(0xffffffffu, below));  // samples below the key
+        const int nlo = n > 0 ? lo + (n - 1) * step + 1 : lo;
+        hi = min(hi, lo + n * step);
+        lo = nlo;
+    }
+    const int j = lo + lane;
+    const bool below = j < hi && __ldg(idx + j) < key;
+    return lo + __popc(__ballot_sync(0xffffffffu, below));
+}
+
+// Patch warp (warps 8 and 9: K and V): after each tile of a piece lands, put
+// the fresh rows that fall in it into the tile in shared memory (and, from the
+// group's mt = 0 CTA, into the cache), or for a fully recomputed sequence store
+// the landed tile to the cache; then release the tile to the MMA issuer.
+template <int D>
+__device__ void patcher(const Params &P, const Sync &S, uint32_t sbase, bool is_v,
+                        const CUtensorMap *tm_cache)
+{
+    using C = Cfg<D>;
+    constexpr int kChunks = D / 8;          // 16-byte chunks per row and head
+    const int lane = threadIdx.x & 31;
+    const int stages = is_v ? C::kVStages : C::kKStages;
+    const int full0 = is_v ? B_VFULL : B_KFULL, ready0 = is_v ? B_VREADY : B_KREADY;
+    const uint32_t off0 = sbase + (is_v ? C::kOffV : C::kOffK);
+    const __nv_bfloat16 *fresh = is_v ? P.v_new : P.k_new;
+    __nv_bfloat16 *cache = is_v ? P.v_cache : P.k_cache;
+    const Range r = my_range(P);
+    uint32_t T = 0;
+    bool stored = false;
+    for (int k = 0; k < r.count; ++k) {
+        const Piece w = piece_at(P, r, k);
+        if (!piece_active(P, w)) continue;
+        const bool dense = piece_dense(P, w);
+        const bool writer = w.mt == 0;
+        const int32_t *idx = P.idx + static_cast<int64_t>(w.b) * P.idx_stride;
+        // One CTA per sequence checks the count and the whole index set.
+        if (!is_v && writer && w.g == 0 && w.t0 == 0) {
+            const int c_raw = __ldg(P.count + w.b);
+            if (lane == 0 && (c_raw < 0 || c_raw > P.r_max)) flag_status(P.status, EC_DEV_BAD_COUNT);
+            bool bad = false;
+            for (int j = lane; j < w.cnt; j += 32) {
+                const int p = __ldg(idx + j);
+                bad |= p < 0 || p >= P.L || (j > 0 && __ldg(idx + j - 1) >= p);
+            }
+            if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(P.status, EC_DEV_BAD_INDEX);
+        }
+        // cursor into the index set, and a window of 32 of its entries in registers
+        int cur = dense ? 0 : lower_bound_warp(idx, w.cnt, w.t0 * kBlockN);
+        int vbase = cur;
+        int v = !dense && cur + lane < w.cnt ? __ldg(idx + cur + lane) : INT_MAX;
+        for (int t = w.t0; t < w.t1; ++t, ++T) {
+            const int s = T % stages;
+            if (!__all_sync(0xffffffffu, S.wait(full0 + s, (T / stages) & 1))) {
+                if (stored && lane == 0) bulk_wait_all();
+                return;
+            }
+            const uint32_t tile = off0 + s * C::kTile;
+            if (dense) {
+                if (writer && lane == 0) {  // the landed tile is the cache's new content
+                    fence_async_smem();
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_store_4d(tm_cache, tile + c * C::kCol, c * 64, w.g, t * kBlockN, w.b);
+                    bulk_commit_and_wait_read();
+                    stored = true;
+                }
+            } else {
+                const int tile_end = (t + 1) * kBlockN;
+                for (;;) {
+                    // the rows cur .. cur + n - 1 of the window fall in this tile
+                    const int j = vbase + lane;
+                    const bool in = j >= cur && v < tile_end;
+                    const int n = __popc(__ballot_sync(0xffffffffu, in));
+                    if (n > 0) {
+                        // every 16-byte chunk of those rows in flight at once (one
+                        // round trip), then the write-back reads them from the tile
+                        const int first = cur - vbase;
+                        const int total = n * kChunks;
+                        for (int k0 = 0; k0 < total; k0 += 32) {
+                            const int k = k0 + lane, q = min(k / kChunks, n - 1), c = k % kChunks;
+                            const int rit = __shfl_sync(0xffffffffu, v, first + q) - t * kBlockN;
+                            if (k < total && rit >= 0 && rit < kBlockN && rit + t * kBlockN < P.L) {
+                                const int64_t src =
+                                    ((static_cast<int64_t>(w.b) * P.r_max + cur + q) * P.Hkv + w.g) * D + c * 8;
+                                cp_async_16(tile + (c / 8) * C::kCol + rit * 128 + (((c % 8) ^ (rit & 7)) << 4),
+                                            fresh + src);
+                            }
+                        }
+                        cp_async_wait_all();
+                        __syncwarp();
+                        if (writer) {
+                            for (int k0 = 0; k0 < total; k0 += 32) {
+                                const int k = k0 + lane, q = min(k / kChunks, n - 1), c = k % kChunks;
+                                const int p = __shfl_sync(0xffffffffu, v, first + q);
+                                const int rit = p - t * kBlockN;
+                                if (k < total && rit >= 0 && rit < kBlockN && p < P.L) {
+                                    const uint4 x = ld_shared_v4(tile + (c / 8) * C::kCol + rit * 128 +
+                                                                 (((c % 8) ^ (rit & 7)) << 4));
+                                    const int64_t at =
+                                        ((static_cast<int64_t>(w.b) * P.L + p) * P.Hkv + w.g) * D + c * 8;
+                                    *reinterpret_cast<uint4 *>(cache + at) = x;
+                                }
+                            }
+                        }
+                        cur += n;
+                    }
+                    // window used up and the index set goes on: slide it, the tile
+                    // may hold more rows
+                    if (cur - vbase < 32 || cur >= w.cnt) break;
+                    vbase = cur;
+                    v = cur + lane < w.cnt ? __ldg(idx + cur + lane) : INT_MAX;
+                }
+                fence_async_smem();  // the patched rows are visible to the tensor core
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(S.bar(ready0 + s));
+        }
+    }
+    if (stored && lane == 0) bulk_wait_all();
+}
+
 // QK issuer (one thread): per piece Q into TMEM, then S = Q K^T for each tile
-// into one of the two S buffers as soon as its K tile landed and the PV product
-// of the tile two back (which read its P from that buffer) completed.  The next
-// tile's scores are then ready while the softmax warps still work on this one.
+// into one of the two S buffers as soon as its K tile is ready and the PV product
+// of the tile two back (which read its P from that buffer) completed.
 template <int D>
 __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem)
 {
@@ -309,7 +476,7 @@ __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
         umma_commit(S.bar(B_QEMPTY + qb));
         for (int t = w.t0; t < w.t1; ++t, ++T) {
             const int s = T % C::kKStages, sb = T & 1;
-            ok = S.wait(B_KFULL + s, (T / C::kKStages) & 1);
+            ok = S.wait(B_KREADY + s, (T / C::kKStages) & 1);
             if (ok && T >= 2) ok = S.wait(B_SFREE + sb, ((T >> 1) - 1) & 1);
             if (!ok) break;
             tc_fence_after();
@@ -331,7 +498,7 @@ __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
 }
 
 // PV issuer (one thread): O (+)= P V for each tile once the softmax warps wrote
-// P over its S buffer and its V tile landed; the first tile of a piece
+// P over its S buffer and its V tile is ready; the first tile of a piece
 // overwrites O.  Its completion frees the V stage and the S buffer.
 template <int D>
 __device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem)
@@ -346,7 +513,7 @@ __device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
         if (!piece_active(P, w)) continue;
         for (int t = w.t0; t < w.t1; ++t, ++T) {
             const int s = T % C::kVStages, sb = T & 1;
-            ok = S.wait(B_PFULL + sb, (T >> 1) & 1) && S.wait(B_VFULL + s, (T / C::kVStages) & 1);
+            ok = S.wait(B_PFULL + sb, (T >> 1) & 1) && S.wait(B_VREADY + s, (T / C::kVStages) & 1);
             if (!ok) break;
             tc_fence_after();
             const uint32_t vbase = sbase + C::kOffV + s * C::kTile;
@@ -393,6 +560,63 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
 }
+__device__ __forceinline__ void softmax_sync()
+{
+    asm volatile("bar.sync %0, %1;" ::"n"(kSoftmaxBarrier), "n"(128) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ float4 ld_cg_v4(const float4 *p)
+{
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float2 ld_cg_v2(const float2 *p)
+{
+    float2 v;
+    asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
+}
+
+// The owner of a split unit waits until its contributors released their
+// partials (bounded; a timeout aborts the CTA like any other wait).  All four
+// softmax warps call it, whatever their own state (`ok` false: a wait of this
+// warp already gave up), so all of them reach the named barrier.
+__device__ bool wait_contributions(const Params &P, const Sync &S, int unit, int n, bool ok_in)
+{
+    __shared__ int s_ok;
+    if (threadIdx.x == 64) {
+        const uint32_t *f = P.flags + unit;
+        const long long t0 = clock64();
+        bool ok = ok_in && !*S.abort_flag;
+        while (ok && ld_acquire(f) < static_cast<uint32_t>(n)) {
+            if (*S.abort_flag) {
+                ok = false;
+                break;
+            }
+            if (clock64() - t0 > P.wait_limit) {
+                ok = S.give_up();
+                break;
+            }
+            __nanosleep(64);
+        }
+        s_ok = ok;
+        if (ok) P.flags[unit] = 0;  // ready for the next launch (no contributor touches it again)
+    }
+    softmax_sync();
+    __threadfence();  // every thread reads the partials after the acquire
+    return s_ok != 0;
+}
 
 template <int D>
 __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
@@ -419,33 +643,29 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
             if (ok) ok = __all_sync(0xffffffffu, S.wait(B_SFULL + sb, (T >> 1) & 1));
             if (!ok) continue;
             tc_fence_after();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                tmem_ld32(tmem + lane_off + C::kColS + sb * kBlockN + cc * 32, sr[cc]);
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_wait_ld(sr[cc]);
-
-            if (t == P.n_tiles - 1 && kv_tail < kBlockN) {  // keys past L do not exist
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (cc * 32 + j >= kv_tail) sr[cc][j] = __float_as_uint(-INFINITY);
-            }
-            // row maximum of the raw scores (scale > 0 keeps the order)
-            float mx4[4];
+            const uint32_t scol = tmem + lane_off + C::kColS + sb * kBlockN;
+            const int live = (t == P.n_tiles - 1) ? kv_tail : kBlockN;  // keys past L do not exist
+            // pass 1: the row maximum of the raw scores (scale > 0 keeps the order),
+            // 32 columns at a time
+            float mx = -INFINITY;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                float a = __uint_as_float(sr[cc][0]), b = __uint_as_float(sr[cc][1]);
+                uint32_t sr[32];
+                tmem_ld32(scol + cc * 32, sr);
+                tmem_wait_ld(sr);
+                if (live < kBlockN) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (cc * 32 + j >= live) sr[j] = __float_as_uint(-INFINITY);
+                }
+                float a = __uint_as_float(sr[0]), b = __uint_as_float(sr[1]);
 #pragma unroll
                 for (int j = 2; j < 32; j += 4) {
-                    a = fmax3(a, __uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1]));
-                    b = fmax3(b, __uint_as_float(sr[cc][j + 2]), __uint_as_float(sr[cc][j + 3]));
+                    a = fmax3(a, __uint_as_float(sr[j]), __uint_as_float(sr[j + 1]));
+                    b = fmax3(b, __uint_as_float(sr[j + 2]), __uint_as_float(sr[j + 3]));
                 }
-                mx4[cc] = fmaxf(a, b);
+                mx = fmax3(mx, a, b);
             }
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             float m_use = m_run, alpha = 1.f;
             bool rescale = false;
             if (mx > m_run + move) {  // p would exceed 2^8: move the reference
@@ -453,25 +673,40 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
                 alpha = ex2((m_run - mx) * c);
                 rescale = t > w.t0;
             }
-            // p = 2^{(s - m) c}; two-wide FMA and adds, four partial sums
+            // pass 2: p = 2^{(s - m) c} (two-wide FMA and adds, four partial sums),
+            // P as bf16 pairs over the first half of this S buffer, 64 columns of S
+            // (32 of P) at a time: P never overwrites a column not yet read
             const uint64_t c2 = f2x2(c, c);
             const float nmc = -m_use * c;
             const uint64_t nmc2 = f2x2(nmc, nmc);
             uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-            uint32_t pk[64];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const uint64_t y2 = ffma2(f2x2(__uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1])),
-                                              c2, nmc2);
-                    float y0, y1;
-                    x2f(y2, y0, y1);
-                    const float p0 = ex2(y0), p1 = ex2(y1);
-                    const uint64_t p2 = f2x2(p0, p1);
-                    acc2[(j >> 1) & 3] = fadd2(acc2[(j >> 1) & 3], p2);
-                    pk[(cc * 32 + j) >> 1] = pack_bf16x2(p0, p1);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int cc = 2 * half + h2;
+                    uint32_t sr[32];
+                    tmem_ld32(scol + cc * 32, sr);
+                    tmem_wait_ld(sr);
+                    if (live < kBlockN) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (cc * 32 + j >= live) sr[j] = __float_as_uint(-INFINITY);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const uint64_t y2 = ffma2(f2x2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])),
+                                                  c2, nmc2);
+                        float y0, y1;
+                        x2f(y2, y0, y1);
+                        const float p0 = ex2(y0), p1 = ex2(y1);
+                        acc2[(j >> 1) & 3] = fadd2(acc2[(j >> 1) & 3], f2x2(p0, p1));
+                        pk[h2 * 16 + (j >> 1)] = pack_bf16x2(p0, p1);
+                    }
                 }
+                tmem_st32(scol + half * 32, pk);
+            }
             float rs0, rs1, rs2, rs3, rs4, rs5, rs6, rs7;
             x2f(acc2[0], rs0, rs1);
             x2f(acc2[1], rs2, rs3);
@@ -488,7 +723,7 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
                 ok = __all_sync(0xffffffffu, S.wait(B_SFREE + (Tp & 1), (Tp >> 1) & 1));
                 if (!ok) continue;
                 tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
                     const uint32_t ta = tmem + lane_off + C::kColO + cc * 32;
@@ -500,11 +735,7 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
                 }
                 tmem_wait_st();
             }
-            // P (bf16 pairs) over the first half of this S buffer, in this row's
-            // TMEM lane; the PV product reads it there
-            const uint32_t pcol = tmem + lane_off + C::kColS + sb * kBlockN;
-            tmem_st32(pcol, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-            tmem_st32(pcol + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+            // the P stores (and any O correction) complete before the PV product reads them
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -520,185 +751,99 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
         const bool valid = row < P.tok_per_tile * P.G && tok < w.cnt;
         const int h = w.g * P.G + row % P.G;
         __nv_bfloat16 *orow = P.out + ((static_cast<int64_t>(w.b) * P.r_max + tok) * P.H + h) * D;
-        if (w.n_contrib == 1) {
-            if (!ok) continue;
-            const float inv = 1.f / l_run;
+        if (w.role == ROLE_CONTRIB) {
+            // a partial for the unit's owner: unnormalised O and (m, l), then the flag
+            if (ok) {
+                float4 *po = P.part_o + (static_cast<int64_t>(w.unit) * P.slots + w.slot) * (D / 4) * kBlockM;
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
+                    tmem_wait_ld(o);
+                    if (valid) {
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
-                tmem_wait_ld(o);
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-                        v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-                        v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-                        v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-                        dst[q] = v;
+                        for (int q = 0; q < 8; ++q)
+                            __stcg(po + (cc * 8 + q) * kBlockM + row,
+                                   make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                               __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3])));
                     }
                 }
+                if (valid)
+                    __stcg(P.part_ml + (static_cast<int64_t>(w.unit) * P.slots + w.slot) * kBlockM + row,
+                           make_float2(m_run, l_run));
+                __threadfence();
             }
             tc_fence_before();
+            softmax_sync();
+            // released only when every softmax warp wrote its rows: a warp that gave
+            // up raised the CTA's abort flag before the barrier
+            if (ok && threadIdx.x == 64 && !*S.abort_flag) red_release_add(P.flags + w.unit, 1u);
             continue;
         }
-        // part of a unit: store the partial (the merge kernel combines them)
+        // whole unit or owner: out = (wo O + sum_s ws_s O_s) / (wo l + sum_s ws_s l_s),
+        // every term scaled to M, the largest of the maxima
+        int n = 0;
+        if (w.role == ROLE_OWNER) {
+            ok = wait_contributions(P, S, w.unit, w.n_contrib, ok);  // every softmax warp
+            n = min(w.n_contrib, kMaxContrib);
+        }
         if (!ok) continue;
-        float4 *po = P.part_o + (static_cast<int64_t>(w.unit) * P.slots + w.slot) * (D / 4) * kBlockM;
-#pragma unroll
+        const float2 *mlp = P.part_ml + static_cast<int64_t>(w.unit) * P.slots * kBlockM + row;
+        const float4 *pop = P.part_o + static_cast<int64_t>(w.unit) * P.slots * (D / 4) * kBlockM + row;
+        auto weight = [&](int s, float M, float &ls) {  // contributor s's scale and its l
+            const float2 v = valid ? ld_cg_v2(mlp + static_cast<int64_t>(s) * kBlockM)
+                                   : make_float2(-INFINITY, 0.f);
+            ls = v.y;
+            return v.y > 0.f ? ex2((v.x - M) * c) : 0.f;
+        };
+        float M = m_run;
+        for (int s = 0; s < n; ++s)
+            if (valid) M = fmaxf(M, ld_cg_v2(mlp + static_cast<int64_t>(s) * kBlockM).x);
+        const float wo = l_run > 0.f ? ex2((m_run - M) * c) : 0.f;
+        float l = wo * l_run;
+        for (int s = 0; s < n; ++s) {
+            float ls;
+            const float ws = weight(s, M, ls);
+            l = fmaf(ws, ls, l);
+        }
+        const float inv = 1.f / l;
+#pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t o[32];
             tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
             tmem_wait_ld(o);
-            if (valid) {
+            float acc[32];
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    __stcg(po + (cc * 8 + q) * kBlockM + row,
-                           make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
-                                       __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3])));
+            for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(o[j]) * wo;
+            for (int s = 0; s < n; ++s) {
+                float ls;
+                const float ws = weight(s, M, ls);
+                const float4 *po = pop + (static_cast<int64_t>(s) * (D / 4) + cc * 8) * kBlockM;
+                if (valid) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 x = ld_cg_v4(po + q * kBlockM);
+                        acc[4 * q] = fmaf(ws, x.x, acc[4 * q]);
+                        acc[4 * q + 1] = fmaf(ws, x.y, acc[4 * q + 1]);
+                        acc[4 * q + 2] = fmaf(ws, x.z, acc[4 * q + 2]);
+                        acc[4 * q + 3] = fmaf(ws, x.w, acc[4 * q + 3]);
+                    }
+                }
+            }
+            if (valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 v;
+                    v.x = pack_bf16x2(acc[8 * q] * inv, acc[8 * q + 1] * inv);
+                    v.y = pack_bf16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv);
+                    v.z = pack_bf16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv);
+                    v.w = pack_bf16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv);
+                    dst[q] = v;
+                }
             }
         }
         tc_fence_before();
-        if (valid)
-            __stcg(P.part_ml + (static_cast<int64_t>(w.unit) * P.slots + w.slot) * kBlockM + row,
-                   make_float2(m_run, l_run));
-    }
-}
-
-// Merge of the split units, a grid of its own after the attention grid.  For
-// every valid row of a unit cut into n >= 2 pieces with partials (O_s, m_s, l_s):
-//   out = sum_s 2^{(m_s - M) c} O_s / sum_s 2^{(m_s - M) c} l_s,   M = max_s m_s,
-// the standard combination of softmax partials (m in raw score units, c the
-// scale in log2 units).  Block (unit, 32-row group), thread (row, 8-column
-// group): the partials keep rows innermost, so a warp reads 512 contiguous bytes
-// per load.  Slots are taken eight at a time and every load of a batch, the
-// sequence's row count included, is issued (volatile, in order) before any is
-// used: a unit cut into up to eight pieces costs one round trip to L2.
-__device__ __forceinline__ float4 ld_cg_v4(const float4 *p)
-{
-    float4 v;
-    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ float2 ld_cg_v2(const float2 *p)
-{
-    float2 v;
-    asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
-    return v;
-}
-
-template <int D>
-__global__ void __launch_bounds__(D * 4) merge_kernel(const Params P)
-{
-    constexpr int kBatch = 8;
-    pdl_launch_dependents();
-    pdl_wait();
-    const int unit = blockIdx.x;
-    const int row = blockIdx.y * 32 + (threadIdx.x & 31);
-    const int grp = threadIdx.x >> 5;  // columns [8 grp, 8 grp + 8)
-    const int mt = unit % P.n_mt, bg = unit / P.n_mt;
-    const int g = bg % P.Hkv, b = bg / P.Hkv;
-    int n = P.n_split;
-    if (n == 0) {
-        const int64_t base = static_cast<int64_t>(unit) * P.n_tiles;
-        n = cta_of(P, base + P.n_tiles - 1) - cta_of(P, base) + 1;
-    }
-    // whole units were written by their piece; rows past r_max hold no token
-    if (n < 2 || row >= P.tok_per_tile * P.G || mt * P.tok_per_tile + row / P.G >= P.r_max) return;
-    const int count_b = __ldg(P.count + b);
-    const float c = P.scale_log2;
-    const int64_t s_base = static_cast<int64_t>(unit) * P.slots;
-    float M = -INFINITY, l_sum = 0.f, acc[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-    // rows past the sequence's count hold no partials; their loads stay inside the
-    // workspace and their results are dropped below
-    for (int s0 = 0; s0 < n; s0 += kBatch) {
-        float2 ml[kBatch];
-        float4 o[kBatch][2];
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            ml[k] = make_float2(-INFINITY, 0.f);
-            o[k][0] = o[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (s0 + k < n) {  // uniform over the block
-                const int64_t sl = s_base + s0 + k;
-                ml[k] = ld_cg_v2(P.part_ml + sl * kBlockM + row);
-#pragma unroll
-                for (int q = 0; q < 2; ++q)
-                    o[k][q] = ld_cg_v4(P.part_o + (sl * (D / 4) + grp * 2 + q) * kBlockM + row);
-            }
-        }
-        float mb = M;
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k)
-            if (s0 + k < n) mb = fmaxf(mb, ml[k].x);
-        const float alpha = ex2((M - mb) * c);  // 0 on the first batch
-        l_sum *= alpha;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] *= alpha;
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            const float e = s0 + k < n ? ex2((ml[k].x - mb) * c) : 0.f;
-            l_sum = fmaf(e, ml[k].y, l_sum);
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                acc[4 * q] = fmaf(e, o[k][q].x, acc[4 * q]);
-                acc[4 * q + 1] = fmaf(e, o[k][q].y, acc[4 * q + 1]);
-                acc[4 * q + 2] = fmaf(e, o[k][q].z, acc[4 * q + 2]);
-                acc[4 * q + 3] = fmaf(e, o[k][q].w, acc[4 * q + 3]);
-            }
-        }
-        M = mb;
-    }
-    const int cnt = max(0, min(count_b, P.r_max));
-    const int tok = mt * P.tok_per_tile + row / P.G;
-    if (tok >= cnt) return;
-    const float inv = 1.f / l_sum;
-    const int h = g * P.G + row % P.G;
-    uint4 v;
-    v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-    v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    *reinterpret_cast<uint4 *>(P.out + ((static_cast<int64_t>(b) * P.r_max + tok) * P.H + h) * D +
-                               grp * 8) = v;
-}
-
-// Fresh K/V rows into the caches.  Lets the attention grid launch at once.
-template <int D>
-__global__ void __launch_bounds__(256) write_back_kernel(const Params P)
-{
-    pdl_launch_dependents();
-    pdl_wait();
-    constexpr int kChunks = D / 8;
-    const int64_t total = static_cast<int64_t>(P.B) * P.r_max * P.Hkv * kChunks;
-    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
-         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int ch = static_cast<int>(e % kChunks);
-        const int64_t rg = e / kChunks;  // (b, r, g) flattened
-        const int g = static_cast<int>(rg % P.Hkv);
-        const int64_t br = rg / P.Hkv;
-        const int r = static_cast<int>(br % P.r_max);
-        const int b = static_cast<int>(br / P.r_max);
-        const int c = __ldg(P.count + b);
-        if (ch == 0 && g == 0 && r == 0 && (c < 0 || c > P.r_max))
-            flag_status(P.status, EC_DEV_BAD_COUNT);
-        if (r >= min(max(c, 0), P.r_max)) continue;
-        const int32_t *idx = P.idx + static_cast<int64_t>(b) * P.idx_stride;
-        const int p = __ldg(idx + r);
-        if (p < 0 || p >= P.L) {
-            if (ch == 0 && g == 0) flag_status(P.status, EC_DEV_BAD_INDEX);
-            continue;
-        }
-        if (ch == 0 && g == 0 && r > 0 && __ldg(idx + r - 1) >= p)
-            flag_status(P.status, EC_DEV_BAD_INDEX);
-        const int64_t src = (br * P.Hkv + g) * D + ch * 8;
-        const int64_t dst = ((static_cast<int64_t>(b) * P.L + p) * P.Hkv + g) * D + ch * 8;
-        *reinterpret_cast<uint4 *>(P.k_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(P.k_new + src));
-        *reinterpret_cast<uint4 *>(P.v_cache + dst) = __ldg(reinterpret_cast<const uint4 *>(P.v_new + src));
     }
 }
 
@@ -706,7 +851,9 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_tc_kernel(const Params P, const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v)
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_kn,
+                        const __grid_constant__ CUtensorMap tm_vn)
 {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -737,18 +884,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_kn);
+        prefetch_tmap(&tm_vn);
     }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    pdl_wait();  // the write-back grid (and everything before it) has completed
+    pdl_wait();  // inputs and outputs belong to the previous kernel until here
 
     if (warp == 0 || warp == 6) {
         if ((threadIdx.x & 31) == 0) {
             if (warp == 0)
-                producer_qk<D>(P, S, sbase, &tm_q, &tm_k);
+                producer_qk<D>(P, S, sbase, &tm_q, &tm_k, &tm_kn);
             else
-                producer_v<D>(P, S, sbase, &tm_v);
+                producer_v<D>(P, S, sbase, &tm_v, &tm_vn);
         }
         __syncwarp();
     } else if (warp == 1 || warp == 7) {
@@ -759,6 +908,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pv_issuer<D>(P, S, sbase, tmem);
         }
         __syncwarp();
+    } else if (warp == 8 || warp == 9) {
+        patcher<D>(P, S, sbase, warp == 9, warp == 9 ? &tm_v : &tm_k);
     } else {
         softmax_epilogue<D>(P, S, tmem);
     }
@@ -783,9 +934,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// [B, rows, heads, D] bf16 viewed as 4-D {D, heads, rows, B}; box {64, box_heads,
-// box_rows, 1}, 128-byte swizzle, out-of-range elements read as zero.
-bool encode_4d(CUtensorMap *map, const void *base, int B, int rows, int heads, int D,
+// [B, rows_alloc, heads, D] bf16 viewed as 4-D {D, heads, rows, B} with only the
+// first `rows` rows of every batch entry addressable; box {64, box_heads,
+// box_rows, 1}, 128-byte swizzle; out-of-range elements load as zero and are not
+// stored.
+bool encode_4d(CUtensorMap *map, const void *base, int B, int rows, int rows_alloc, int heads, int D,
                int box_heads, int box_rows)
 {
     auto fn = encode_fn();
@@ -794,7 +947,7 @@ bool encode_4d(CUtensorMap *map, const void *base, int B, int rows, int heads, i
                                 static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
                                    static_cast<cuuint64_t>(heads) * D * 2,
-                                   static_cast<cuuint64_t>(rows) * heads * D * 2};
+                                   static_cast<cuuint64_t>(rows_alloc) * heads * D * 2};
     const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_heads),
                                static_cast<cuuint32_t>(box_rows), 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
@@ -804,111 +957,73 @@ bool encode_4d(CUtensorMap *map, const void *base, int B, int rows, int heads, i
 }
 
 struct Plan {
-    int G, tok_per_tile, n_mt, n_units, n_tiles, grid, slots, n_split;
+    int G, tok_per_tile, n_mt, n_units, n_tiles, grid, slots, grouped, n_groups;
     int64_t total;
-    bool split;  // some unit is cut into several pieces: the merge kernel runs
 };
 
-// The work split, chosen by a cost model counted in tile times (one 128 x 128
-// tile is about 1 us per SM at steady state):
-//   whole units      split-major items with one split: no partials, no merge;
-//   stream-K         equal contiguous tile ranges on every SM, plus the merge;
-//   split-major      items of n_tiles / sp tiles dealt round-robin, plus the merge.
-// A piece's epilogue costs about one tile and the merge kernel about five (its
-// CTAs become resident while the attention grid runs; after it, one round trip
-// to L2 and the writes).  Calibrated on whole decode steps: the single-sequence
-// step (32 units of 8 tiles) is faster cut into 4 splits than in whole units.
-// With several row tiles per KV head and caches larger than half of L2, stream-K
-// would read each K/V tile from HBM once per row tile and is not taken.
+// The work split.  Groups of n_mt CTAs (one per unit of a (b, g)) take equal
+// contiguous ranges of the (b, g, key tile) pairs, so every CTA does the same
+// number of tiles and a group's CTAs share each K/V tile through L2.  When a
+// (b, g) has more units than half the SMs, or a unit would need more than
+// kMaxContrib contributors, whole units are dealt round-robin instead.
 Plan make_plan(int B, int L, int r_max, int H, int Hkv)
 {
-    constexpr double kPiece = 1.0, kMerge = 5.0;
     Plan p;
     p.G = H / Hkv;
     p.tok_per_tile = kBlockM / p.G;
     p.n_mt = (r_max + p.tok_per_tile - 1) / p.tok_per_tile;
     p.n_units = B * Hkv * p.n_mt;
     p.n_tiles = (L + kBlockN - 1) / kBlockN;
-    p.total = static_cast<int64_t>(p.n_units) * p.n_tiles;
+    p.total = static_cast<int64_t>(B) * Hkv * p.n_tiles;
     const int n_sm = device_sm_count();
-    auto ceil_div = [](int64_t a, int64_t b) { return (a + b - 1) / b; };
-
-    // whole units
-    double best = static_cast<double>(ceil_div(p.n_units, n_sm)) * (p.n_tiles + kPiece);
-    p.n_split = 1;
-    // split-major items
-    for (int sp = 2; sp <= std::min(kMaxContrib, p.n_tiles / 2); ++sp) {
-        const int64_t rounds = ceil_div(static_cast<int64_t>(p.n_units) * sp, n_sm);
-        const double cost =
-            static_cast<double>(rounds) * (ceil_div(p.n_tiles, sp) + kPiece) + kMerge;
-        if (cost < best - 1e-9) {
-            best = cost;
-            p.n_split = sp;
+    p.slots = 0;
+    p.grouped = 0;
+    p.n_groups = 0;
+    if (p.n_mt >= 1 && 2 * p.n_mt <= n_sm) {
+        const int n_groups = static_cast<int>(std::min<int64_t>(n_sm / p.n_mt, p.total));
+        // most contributors of one (b, g): groups meeting it, its owner excluded
+        auto grp = [&](int64_t w) { return ((w + 1) * n_groups - 1) / p.total; };
+        int64_t worst = 0;
+        for (int64_t bg = 0; bg < static_cast<int64_t>(B) * Hkv; ++bg)
+            worst = std::max<int64_t>(worst, grp(bg * p.n_tiles + p.n_tiles - 1) - grp(bg * p.n_tiles));
+        if (worst <= kMaxContrib) {
+            p.grouped = 1;
+            p.n_groups = n_groups;
+            p.slots = static_cast<int>(worst);  // 0: no unit is cut, no partials
         }
     }
-    // stream-K
-    const int64_t kv_bytes = 2LL * B * L * Hkv * 128 * 2;
-    int64_t g = std::min<int64_t>(n_sm, p.total);
-    g = std::max<int64_t>(1, std::min<int64_t>(g, static_cast<int64_t>(p.n_units) * (kMaxContrib - 2)));
-    if (!(p.n_mt > 1 && kv_bytes > (64LL << 20))) {
-        const int64_t per_cta = ceil_div(p.total, g);
-        const double cost = static_cast<double>(per_cta) +
-                            kPiece * static_cast<double>(ceil_div(per_cta, p.n_tiles) + 1) + kMerge;
-        if (cost < best - 1e-9) {
-            best = cost;
-            p.n_split = 0;
-        }
-    }
-    if (p.n_split == 0) {
-        p.grid = static_cast<int>(g);
-        // a unit of n_tiles tiles meets at most ceil(n_tiles * grid / total) + 1 ranges
-        p.slots = static_cast<int>(std::min<int64_t>(
-            kMaxContrib, ceil_div(static_cast<int64_t>(p.n_tiles) * p.grid, p.total) + 1));
-        // a unit is split when a range boundary falls inside it
-        auto cta = [&](int64_t w) { return ((w + 1) * p.grid - 1) / p.total; };
-        p.split = false;
-        for (int64_t u = 0; u < p.n_units && !p.split; ++u)
-            p.split = cta(u * p.n_tiles) != cta(u * p.n_tiles + p.n_tiles - 1);
-    } else {
-        p.grid = static_cast<int>(std::min<int64_t>(n_sm, static_cast<int64_t>(p.n_units) * p.n_split));
-        p.slots = p.n_split;
-        p.split = p.n_split > 1;
-    }
+    p.grid = p.grouped ? p.n_groups * p.n_mt : std::max(1, std::min(n_sm, p.n_units));
     return p;
 }
 
-size_t partial_offsets(const Plan &p, int D, size_t *off_ml, size_t *off_o)
+void partial_offsets(const Plan &p, int D, size_t *off_flags, size_t *off_ml, size_t *off_o,
+                     size_t *end)
 {
     size_t off = kWsHeader;
+    *off_flags = off;
+    off = align_up(off + static_cast<size_t>(p.n_units) * sizeof(uint32_t), 256);
     *off_ml = off;
-    const size_t parts = p.split ? static_cast<size_t>(p.n_units) * p.slots : 0;
+    const size_t parts = p.grouped ? static_cast<size_t>(p.n_units) * p.slots : 0;
     off = align_up(off + parts * kBlockM * sizeof(float2), 256);
     *off_o = off;
-    return off + parts * kBlockM * static_cast<size_t>(D) * sizeof(float);
+    *end = off + parts * kBlockM * static_cast<size_t>(D) * sizeof(float);
 }
 
 template <int D>
 cudaError_t launch_typed(const Params &p, const Plan &plan, const void *q, cudaStream_t stream)
 {
-    CUtensorMap tq, tk, tv;
-    if (!encode_4d(&tq, q, p.B, p.r_max, p.H, D, p.G, p.tok_per_tile) ||
-        !encode_4d(&tk, p.k_cache, p.B, p.L, p.Hkv, D, 1, kBlockN) ||
-        !encode_4d(&tv, p.v_cache, p.B, p.L, p.Hkv, D, 1, kBlockN))
+    CUtensorMap tq, tk, tv, tkn, tvn;
+    // the fresh K/V are viewed with at most L rows, so that rows at or past L
+    // (present only when r_max > L) read as zero
+    const int fresh_rows = std::min(p.L, p.r_max);
+    if (!encode_4d(&tq, q, p.B, p.r_max, p.r_max, p.H, D, p.G, p.tok_per_tile) ||
+        !encode_4d(&tk, p.k_cache, p.B, p.L, p.L, p.Hkv, D, 1, kBlockN) ||
+        !encode_4d(&tv, p.v_cache, p.B, p.L, p.L, p.Hkv, D, 1, kBlockN) ||
+        !encode_4d(&tkn, p.k_new, p.B, fresh_rows, p.r_max, p.Hkv, D, 1, kBlockN) ||
+        !encode_4d(&tvn, p.v_new, p.B, fresh_rows, p.r_max, p.Hkv, D, 1, kBlockN))
         return cudaErrorInvalidValue;
-    // 1. write-back: a few CTAs per SM over the fresh rows
-    const int64_t chunks = static_cast<int64_t>(p.B) * p.r_max * p.Hkv * (D / 8);
-    const int wb_grid = static_cast<int>(std::max<int64_t>(
-        1, std::min<int64_t>((chunks + 255) / 256, 4 * static_cast<int64_t>(device_sm_count()))));
-    cudaError_t e = launch(write_back_kernel<D>, dim3(wb_grid), dim3(256), 0, stream, p);
-    if (e != cudaSuccess) return e;
-    // 2. attention; its set-up overlaps the write-back (programmatic dependent launch)
-    e = launch(attention_tc_kernel<D>, dim3(plan.grid), dim3(kThreads), Cfg<D>::kBytes, stream, p,
-               tq, tk, tv);
-    if (e != cudaSuccess || !plan.split) return e;
-    // 3. merge of the split units: (unit, 32-row group) blocks over the rows a unit
-    //    can hold (at most r_max tokens)
-    const int row_groups = (std::min(kBlockM, std::min(p.tok_per_tile, p.r_max) * p.G) + 31) / 32;
-    return launch(merge_kernel<D>, dim3(p.n_units, row_groups), dim3(D * 4), 0, stream, p);
+    return launch(attention_tc_kernel<D>, dim3(plan.grid), dim3(kThreads), Cfg<D>::kBytes, stream, p,
+                  tq, tk, tv, tkn, tvn);
 }
 
 }  // namespace
@@ -918,11 +1033,7 @@ bool attention_tc_supported(int dtype, int32_t seq_len, int32_t head_dim)
     return dtype == EC_BF16 && (head_dim == 64 || head_dim == 128) && seq_len >= 1;
 }
 
-int32_t attention_tc_kernel_count(int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
-                                  int32_t n_kv_heads)
-{
-    return make_plan(batch, seq_len, r_max, n_heads, n_kv_heads).split ? 3 : 2;
-}
+int32_t attention_tc_kernel_count(int32_t, int32_t, int32_t, int32_t, int32_t) { return 1; }
 
 size_t attention_tc_workspace_bytes(int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
                                     int32_t n_kv_heads, int32_t head_dim)
@@ -930,8 +1041,9 @@ size_t attention_tc_workspace_bytes(int32_t batch, int32_t seq_len, int32_t r_ma
     if (batch < 1 || seq_len < 1 || r_max < 1 || n_kv_heads < 1 || n_heads < n_kv_heads)
         return kWsHeader;
     const Plan p = make_plan(batch, seq_len, r_max, n_heads, n_kv_heads);
-    size_t a, b;
-    return partial_offsets(p, head_dim, &a, &b);
+    size_t a, b, c, end;
+    partial_offsets(p, head_dim, &a, &b, &c, &end);
+    return end;
 }
 
 cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_new,
@@ -963,15 +1075,17 @@ cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_
     p.n_units = plan.n_units;
     p.n_tiles = plan.n_tiles;
     p.grid = plan.grid;
+    p.grouped = plan.grouped;
+    p.n_groups = plan.n_groups;
     p.total = plan.total;
     p.slots = plan.slots;
-    p.n_split = plan.n_split;
     p.scale_log2 = scale * kLog2e;
     char *ws = static_cast<char *>(workspace);
-    size_t o_ml, o_o;
-    partial_offsets(plan, head_dim, &o_ml, &o_o);
+    size_t o_f, o_ml, o_o, end;
+    partial_offsets(plan, head_dim, &o_f, &o_ml, &o_o, &end);
     p.status = reinterpret_cast<uint32_t *>(ws);
     p.wait_limit = wait_limit_cycles();
+    p.flags = reinterpret_cast<uint32_t *>(ws + o_f);
     p.part_ml = reinterpret_cast<float2 *>(ws + o_ml);
     p.part_o = reinterpret_cast<float4 *>(ws + o_o);
     return head_dim == 128 ? launch_typed<128>(p, plan, q, stream)

@@ -69,23 +69,26 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
         : "memory");
     return ok != 0;
 }
-// As mbar_try_wait, but the thread sleeps in the barrier until the phase
-// completes or about `ns` nanoseconds pass, instead of returning at once: a
-// waiting warp then takes no issue slots from the warps doing the work.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
 
 // ---- proxies / fences ----
+// 16 bytes global -> shared without a register round trip (L2 only); many may be
+// in flight per thread.  cp_async_wait_all makes the thread's copies visible to it.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
 __device__ __forceinline__ void fence_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -280,7 +283,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // ---- bounded waits on a CTA's array of mbarriers ----
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s: a wait this long is a fault
 constexpr long long kShortWait = 1000000LL;      // limits below this are test limits
-constexpr uint32_t kSleepNs = 20000;              // longest sleep of one try_wait
 
 // mbarrier i lives at bars + 8 i.  wait() gives up after `limit` cycles (the
 // launch's wait limit, kWaitCycles unless a test lowered it) or as soon as
@@ -303,7 +305,6 @@ struct Sync {
     __device__ bool wait(int i, uint32_t parity) const
     {
         const uint32_t b = bar(i);
-        if (mbar_test_wait(b, parity)) return true;
         const long long t0 = clock64();
         if (limit < kShortWait) {
             while (clock64() - t0 <= limit) {
@@ -312,8 +313,10 @@ struct Sync {
             }
             return give_up();
         }
+        // try_wait suspends the thread for a short hardware-defined window while
+        // the phase is incomplete and resumes it as soon as the phase completes
         for (uint32_t it = 1;; ++it) {
-            if (mbar_try_wait_sleep(b, parity, kSleepNs)) return true;
+            if (mbar_try_wait(b, parity)) return true;
             if ((it & 15u) == 0u) {
                 if (*abort_flag) return false;
                 if (clock64() - t0 > limit) return give_up();

@@ -16,4 +16,5 @@ def pytest_configure(config):
 def orc():
     import oracle
     oracle.build()
+    oracle.set_threads(oracle.usable_cores())  # results do not depend on the thread count
     return oracle

@@ -2,7 +2,8 @@
 against the oracle.  The write-back must be bit-exact; outputs within 1e-4 for
 float32 and 2e-2 relative / 1e-2 absolute for bf16 (plus a per-row relative
 Frobenius bound, since the workloads' N(0, 1/sqrt(d)) operands give outputs of
-magnitude ~1e-2).  Large workloads are checked on sampled (b, r, h) rows."""
+magnitude ~1e-2).  Every output row is compared, at every workload's full size
+(the oracle runs its rows on all host cores)."""
 import math
 
 import numpy as np
@@ -15,7 +16,7 @@ from gpu_helpers import attention_close, dev, host, native
 pytestmark = pytest.mark.gpu
 
 
-def run_case(orc, w, idx, cnt, r_max, std=None, n_samples=None, seed=0):
+def run_case(orc, w, idx, cnt, r_max, std=None, seed=0):
     nat = native()
     rng = np.random.default_rng(seed)
     a = synth.make_attention(rng, w, r_max, std)
@@ -35,17 +36,9 @@ def run_case(orc, w, idx, cnt, r_max, std=None, n_samples=None, seed=0):
     got64 = synth.bf16_bits_to_f32(got).astype(np.float64) if bf16 else got.astype(np.float64)
     for b in range(w.batch):  # rows past count are left untouched
         assert not got64[b, cnt[b]:].any()
-    if n_samples is None:
-        ref = orc.attention(a.q, kc_ref, vc_ref, cnt, scale)
-        for b in range(w.batch):
-            attention_close(got64[b, :cnt[b]], ref[b, :cnt[b]], bf16)
-    else:
-        valid = [(b, r) for b in range(w.batch) for r in range(cnt[b])]
-        pick = rng.choice(len(valid), size=min(n_samples, len(valid)), replace=False)
-        samples = np.array([(valid[i][0], valid[i][1], rng.integers(w.n_heads)) for i in pick])
-        ref = orc.attention(a.q, kc_ref, vc_ref, cnt, scale, samples=samples)
-        gs = np.stack([got64[b, r, h] for b, r, h in samples])
-        attention_close(gs, ref, bf16)
+    ref = orc.attention(a.q, kc_ref, vc_ref, cnt, scale)
+    for b in range(w.batch):
+        attention_close(got64[b, :cnt[b]], ref[b, :cnt[b]], bf16)
 
 
 def _workload_index_set(orc, w):
@@ -54,14 +47,13 @@ def _workload_index_set(orc, w):
                              st.block_lo, st.block_hi, w.k)
 
 
-@pytest.mark.parametrize("name,samples", [("tiny", None), ("single_seq", None),
-                                          ("batched", 384), ("long_ctx", 256)])
+@pytest.mark.parametrize("name", ["tiny", "single_seq", "batched", "long_ctx"])
 @pytest.mark.parametrize("sharp", [False, True])
-def test_workloads(orc, name, samples, sharp):
+def test_workloads(orc, name, sharp):
     w = synth.WORKLOADS[name]
     idx, cnt = _workload_index_set(orc, w)
     assert (cnt == w.r_max).all()
-    run_case(orc, w, idx, cnt, w.r_max, std=1.0 if sharp else None, n_samples=samples)
+    run_case(orc, w, idx, cnt, w.r_max, std=1.0 if sharp else None)
 
 
 @pytest.mark.parametrize("L,H,Hkv,d", [(1, 4, 4, 64), (129, 8, 2, 128), (300, 7, 1, 64),
@@ -83,7 +75,7 @@ def test_full_refresh_every_row_recomputed(orc):
     L = w.seq_len
     idx = np.arange(L, dtype=np.int32)[None, :]
     cnt = np.array([L], np.int32)
-    run_case(orc, w, idx, cnt, L, n_samples=300)
+    run_case(orc, w, idx, cnt, L)
 
 
 def test_zero_rows(orc):

@@ -160,6 +160,44 @@ def test_repeated_calls_split_rows(orc):
     check_decode(runs[0], ref, st, w.n_unmask, w.tau, st.step)
 
 
+@pytest.mark.parametrize("dt", [synth.BF16, synth.F32])
+def test_long_rows_with_neg_inf_ties_and_signed_zeros(orc, dt):
+    # rows long enough to be split into a head and pool chunks (>= 64 KB): -inf
+    # logits anywhere (the bf16 fold's guarded refold), maxima placed in the
+    # head, in a pool chunk and in the last elements after the final whole
+    # vector, exact ties across pieces, and +0 / -0 maxima
+    nat = native()
+    V = 70003 if dt == synth.BF16 else 40001
+    w = synth.scaled(synth.WORKLOADS["batched"], vocab=V, logits_dtype=dt, batch=2, block=8,
+                     seq_len=256, prompt_len=64, active_block=2, n_unmask=3)
+    rng = np.random.default_rng(77)
+    st = synth.make_state(rng, w)
+    x = rng.standard_normal((w.n_rows, V)).astype(np.float32)
+    x[0, ::3] = -np.inf                       # a third banned, max in the head
+    x[0, 17] = 6.0
+    x[1, V - 2] = 7.0                         # max among the last elements
+    x[1, 1000:1100] = -np.inf
+    x[2, [5, V // 2, V - 900]] = 8.0          # tie: head, middle, pool chunk -> 5
+    x[3, :] = -np.inf                         # one-hot at the very end of the row
+    x[3, V - 1] = 0.0
+    x[4, :] = -1.0                            # -0 before +0: the maximum is 0, first at -0
+    x[4, V // 3] = -0.0
+    x[4, V - 3] = 0.0
+    x[5, V - 5000] = 9.0                      # max in a pool chunk
+    x[6, :V // 2] = -np.inf                   # the first half banned
+    x[7, :] = 0.25                            # uniform
+    logits = synth.f32_to_bf16_bits(x) if dt == synth.BF16 else x
+    per_vec = 8 if dt == synth.BF16 else 4
+    stride = -(-V // per_vec) * per_vec
+    gpu = run_decode_gpu(nat, logits, st, w.n_unmask, w.tau, st.step, row_stride=stride)
+    ref = run_decode_oracle(orc, logits, st, w.n_unmask, w.tau, st.step)
+    check_decode(gpu, ref, st, w.n_unmask, w.tau, st.step)
+    assert gpu["token"][0] == 17 and gpu["token"][1] == V - 2 and gpu["token"][2] == 5
+    assert gpu["token"][3] == V - 1 and gpu["entropy"][3] == 0.0
+    assert gpu["token"][4] == V // 3 and gpu["token"][5] == V - 5000
+    assert abs(gpu["entropy"][7] - np.log(V)) < 1e-4
+
+
 def test_report_exclusions():
     for name, seed, excl in REPORT:
         if excl:

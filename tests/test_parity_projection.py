@@ -52,7 +52,7 @@ def run_projection(orc, batch, r_max, hidden, width, counts, seed=0, sample_rows
 
 def test_trajectory_full_refresh_shape(orc):
     # every position of a 1024-token sequence through a 4096 -> 3 x 4096 projection
-    run_projection(orc, 1, 1024, 4096, 4096, [1024], sample_rows=12)
+    run_projection(orc, 1, 1024, 4096, 4096, [1024])
 
 
 def test_trajectory_selective_shape(orc):
