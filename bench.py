@@ -103,6 +103,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-warmup", type=int, default=30,
                    help="untimed end-to-end steps first (at least 20 are always run)")
     p.add_argument("--eager", action="store_true", help="time eager launches, not graph replays")
+    p.add_argument("--no-lmhead", action="store_true",
+                   help="skip the LM-head fused decode-and-gate part")
     p.add_argument("--cpu-seconds", type=float, default=8.0,
                    help="CPU time budget of each oracle baseline sample (one core, all cores)")
     return p.parse_args(argv)
@@ -304,9 +306,9 @@ class GpuStep:
 
 
 def kernels_per_step(nat, w: synth.Workload):
-    """Launches of our kernels per step, as the library reports them: the attention
-    call runs a write-back, the attention kernel and (when some unit is split over
-    several CTAs) a merge kernel."""
+    """Launches of our kernels per step, as the library reports them (the bf16
+    attention call is one kernel; float32 runs a write-back and the CUDA-core
+    kernel)."""
     import torch
     dt = torch.bfloat16 if w.attn_dtype == synth.BF16 else torch.float32
     n_att = nat.ec_attention_kernel_count(dt, w.batch, w.seq_len, w.r_max, w.n_heads,
@@ -481,6 +483,10 @@ def run_ours(args, workload=None):
     roof["peak_source"] = ("measured burst (MEASURED_PEAKS.json)" if peak_kind == "measured"
                            else "fallback")
 
+    if w.logits_dtype == synth.BF16 and not args.no_lmhead:
+        out_parts["lmhead_gate"] = lmhead_part(nat, w, st, device, stream, flush, min(K, 50), tc,
+                                               hbm, args.seed)
+
     cpu = None
     if rank == 0 and world == 1:
         cpu = cpu_baseline(w, st, logits, att, args.cpu_seconds, geo)
@@ -506,6 +512,76 @@ def run_ours(args, workload=None):
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+LMHEAD_HIDDEN = 4096
+
+
+def lmhead_part(nat, w: synth.Workload, st, device, stream, flush, K, tc_peak, hbm_peak, seed):
+    """The LM-head fused decode-and-gate call on this workload's rows (hidden size
+    4096, Gaussian bf16 inputs), against the unfused pair it replaces: a cuBLAS
+    GEMM writing bf16 logits, then the decode-and-gate call reading them."""
+    import torch
+    N, V, Hd, B = w.n_rows, w.vocab, LMHEAD_HIDDEN, w.batch
+    x, wl = synth.make_lmhead(np.random.default_rng(seed + 101), N, V, Hd, exact=False)
+    as_bf16 = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)  # noqa: E731
+    xd, wd = as_bf16(x), as_bf16(wl)
+    del x, wl
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+    off, pos = up(st.seq_row_offsets), up(st.row_pos)
+    state = [up(st.is_masked), up(st.tokens), up(st.decode_step)]
+    outs = [torch.empty(N, dtype=torch.int32, device=device), torch.empty(N, device=device),
+            torch.empty(N, device=device),
+            torch.empty(B * w.n_unmask, dtype=torch.int32, device=device),
+            torch.empty(B, device=device), torch.empty(B, dtype=torch.uint8, device=device)]
+    ws = nat.new_workspace(nat.ec_lmhead_workspace_size(N, V, B), device)
+    fused = nat.prepare_lmhead_decode_step(xd, wd, off, pos, w.seq_len, w.n_unmask, w.tau, st.step,
+                                           *outs, *state, ws, stream=stream)
+    logits = torch.empty((N, V), dtype=torch.bfloat16, device=device)
+    ws_dec = nat.new_workspace(nat.ec_decode_workspace_size(N, B), device)
+    decode = nat.prepare_decode_step(logits, off, pos, w.seq_len, w.n_unmask, w.tau, st.step,
+                                     *outs, *state, ws_dec, stream=stream)
+
+    def unfused_gemm():
+        torch.matmul(xd, wd.t(), out=logits)
+
+    unfused_gemm()  # cuBLAS creates its handle and workspace outside the graph capture
+    torch.cuda.synchronize(device)
+
+    def timed(fns, reps):
+        ev = [(torch.cuda.Event(enable_timing=True, external=True),
+               torch.cuda.Event(enable_timing=True, external=True)) for _ in fns]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for f, (e0, e1) in zip(fns, ev):
+                e0.record()
+                f()
+                e1.record()
+        for _ in range(3):
+            flush()
+            g.replay()
+        tot = [0.0] * len(fns)
+        for _ in range(reps):
+            flush()
+            g.replay()
+            ev[-1][1].synchronize()
+            for i, (e0, e1) in enumerate(ev):
+                tot[i] += e0.elapsed_time(e1) / 1e3
+        return [t / reps * 1e6 for t in tot]
+
+    (t_fused,) = timed([fused], K)
+    t_gemm, t_dec = timed([unfused_gemm, decode], K)
+    status = nat.ec_read_device_status(ws) | nat.ec_read_device_status(ws_dec)
+    flops = 2.0 * N * V * Hd
+    w_bytes = V * Hd * 2 + N * Hd * 2
+    tflops = flops / t_fused / 1e6
+    del xd, wd, logits
+    return {"us": t_fused, "hidden": Hd, "tflops": tflops, "frac_tensor_peak": tflops / tc_peak,
+            "weight_gbs": w_bytes / t_fused / 1e3, "frac_hbm": w_bytes / t_fused / 1e3 / hbm_peak,
+            "logits_bytes_not_moved": 2 * N * V * 2,
+            "unfused_us": {"cublas_gemm": t_gemm, "decode_gate": t_dec, "total": t_gemm + t_dec},
+            "speedup_vs_unfused": (t_gemm + t_dec) / t_fused, "launches": 1,
+            "device_status": status, "inputs": "Gaussian bf16 (hidden N(0,1), W_lm N(0, 4/hidden))"}
 
 
 def run_e2e(step: GpuStep, geo, w, logits, att, K, W, world):

@@ -28,6 +28,7 @@ DEV_TIMEOUT = 0x10
 EXPORTED = ("ec_status_str", "ec_abi_version", "ec_debug_set_wait_limit", "ec_workspace_init",
             "ec_read_device_status",
             "ec_decode_workspace_size", "ec_decode_step", "ec_decode_step_noalloc",
+            "ec_decode_noalloc_read_status", "ec_lmhead_workspace_size", "ec_lmhead_decode_step",
             "ec_build_recompute_set", "ec_attention_workspace_size", "ec_attention_kernel_count",
             "ec_selective_attention",
             "ec_embed_rows", "ec_qkv_projection")
@@ -68,6 +69,11 @@ def lib() -> ctypes.CDLL:
                                      i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ec_decode_step_noalloc.argtypes = [vp, ctypes.c_int, i64, i32, i32, vp, vp, i32, i32, i32,
                                              f32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.ec_decode_noalloc_read_status.argtypes = [vp, vp]
+        L.ec_lmhead_workspace_size.argtypes = [i32, i32, i32]
+        L.ec_lmhead_workspace_size.restype = sz
+        L.ec_lmhead_decode_step.argtypes = [vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, f32, i32,
+                                            vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ec_build_recompute_set.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
         L.ec_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         L.ec_attention_workspace_size.restype = sz
@@ -80,7 +86,9 @@ def lib() -> ctypes.CDLL:
         L.ec_qkv_projection.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, sz, vp]
         for name in ("ec_debug_set_wait_limit", "ec_workspace_init", "ec_read_device_status",
                      "ec_decode_step",
-                     "ec_decode_step_noalloc", "ec_build_recompute_set", "ec_selective_attention",
+                     "ec_decode_step_noalloc", "ec_decode_noalloc_read_status",
+                     "ec_lmhead_decode_step", "ec_build_recompute_set",
+                     "ec_selective_attention",
                      "ec_embed_rows", "ec_qkv_projection"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -234,6 +242,60 @@ def ec_decode_step_noalloc(logits, seq_row_offsets, row_pos, seq_len, n_unmask, 
     _check(lib().ec_decode_step_noalloc(*args, _stream(stream)), "ec_decode_step_noalloc")
 
 
+def ec_decode_noalloc_read_status(stream=None) -> int:
+    """Device status bits of the last ec_decode_step_noalloc call on this device."""
+    bits = ctypes.c_uint32(0)
+    _check(lib().ec_decode_noalloc_read_status(ctypes.byref(bits), _stream(stream)),
+           "ec_decode_noalloc_read_status")
+    return bits.value
+
+
+def ec_lmhead_workspace_size(n_rows: int, vocab: int, batch: int) -> int:
+    return lib().ec_lmhead_workspace_size(n_rows, vocab, batch)
+
+
+def _lmhead_args(hidden, w_lm, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step, token_out,
+                 conf_out, entropy_out, unmask_rows, max_entropy, refresh, is_masked, seq_tokens,
+                 decode_step, workspace):
+    _cuda("hidden", hidden, torch.bfloat16)
+    _cuda("w_lm", w_lm, torch.bfloat16)
+    if hidden.dim() != 2 or w_lm.dim() != 2 or hidden.shape[1] != w_lm.shape[1]:
+        raise ValueError("hidden must be [N, hidden_dim] and w_lm [vocab, hidden_dim]")
+    n_rows, hidden_dim = hidden.shape
+    vocab = w_lm.shape[0]
+    batch = seq_row_offsets.numel() - 1
+    _cuda("seq_row_offsets", seq_row_offsets, torch.int32)
+    _cuda("row_pos", row_pos, torch.int32)
+    for name, t, dt, n in (("token_out", token_out, torch.int32, n_rows),
+                           ("conf_out", conf_out, torch.float32, n_rows),
+                           ("entropy_out", entropy_out, torch.float32, n_rows),
+                           ("unmask_rows", unmask_rows, torch.int32, batch * n_unmask),
+                           ("max_entropy", max_entropy, torch.float32, batch),
+                           ("refresh", refresh, torch.uint8, batch),
+                           ("is_masked", is_masked, torch.uint8, batch * seq_len),
+                           ("seq_tokens", seq_tokens, torch.int32, batch * seq_len),
+                           ("decode_step", decode_step, torch.int32, batch * seq_len)):
+        _cuda(name, t, dt)
+        _numel(t, n, name)
+    _numel(row_pos, n_rows, "row_pos")
+    _cuda("workspace", workspace, torch.uint8)
+    return [_p(hidden), _p(w_lm), n_rows, hidden_dim, vocab, _p(seq_row_offsets), _p(row_pos),
+            batch, seq_len, n_unmask, float(tau), int(step), _p(token_out), _p(conf_out),
+            _p(entropy_out), _p(unmask_rows), _p(max_entropy), _p(refresh), _p(is_masked),
+            _p(seq_tokens), _p(decode_step), _p(workspace), workspace.numel()]
+
+
+def ec_lmhead_decode_step(hidden, w_lm, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step,
+                          token_out, conf_out, entropy_out, unmask_rows, max_entropy, refresh,
+                          is_masked, seq_tokens, decode_step, workspace, stream=None):
+    """hidden [N, hidden_dim] and w_lm [vocab, hidden_dim] bf16; the decode-and-gate
+    step on the logits hidden @ w_lm.T, which are never materialised (see ec.h)."""
+    args = _lmhead_args(hidden, w_lm, seq_row_offsets, row_pos, seq_len, n_unmask, tau, step,
+                        token_out, conf_out, entropy_out, unmask_rows, max_entropy, refresh,
+                        is_masked, seq_tokens, decode_step, workspace)
+    _check(lib().ec_lmhead_decode_step(*args, _stream(stream)), "ec_lmhead_decode_step")
+
+
 def _recompute_args(is_masked, decode_step, refresh, block_lo, block_hi, k, idx, count):
     _cuda("is_masked", is_masked, torch.uint8)
     _cuda("decode_step", decode_step, torch.int32)
@@ -364,6 +426,10 @@ def prepare_decode_step(*args, stream=None, **kwargs):
     p = Prepared("ec_decode_step", _decode_args(*args, **kwargs), stream)
     p.set_step = lambda t: p.set_arg(11, int(t))
     return p
+
+
+def prepare_lmhead_decode_step(*args, stream=None, **kwargs):
+    return Prepared("ec_lmhead_decode_step", _lmhead_args(*args, **kwargs), stream)
 
 
 def prepare_build_recompute_set(*args, stream=None, **kwargs):

@@ -149,6 +149,38 @@ ec_status ec_decode_step(const void *logits, ec_dtype dtype, int64_t row_stride,
         is_masked, seq_tokens, decode_step, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t ec_lmhead_workspace_size(int32_t n_rows, int32_t vocab, int32_t batch)
+{
+    return ec::lmhead_workspace_bytes(n_rows, vocab, batch);
+}
+
+ec_status ec_lmhead_decode_step(const void *hidden, const void *w_lm, int32_t n_rows,
+                                int32_t hidden_dim, int32_t vocab, const int32_t *seq_row_offsets,
+                                const int32_t *row_pos, int32_t batch, int32_t seq_len,
+                                int32_t n_unmask, float tau, int32_t step, int32_t *token_out,
+                                float *conf_out, float *entropy_out, int32_t *unmask_rows,
+                                float *max_entropy, uint8_t *refresh, uint8_t *is_masked,
+                                int32_t *seq_tokens, int32_t *decode_step, void *workspace,
+                                size_t workspace_bytes, ec_stream_t stream)
+{
+    if (batch < 1 || seq_len < 1 || n_unmask < 1 || n_unmask > 1024 || !isfinite(tau) ||
+        !ec::lmhead_shape_ok(n_rows, hidden_dim, vocab))
+        return EC_ERR_SHAPE;
+    if (!seq_row_offsets || !unmask_rows || !max_entropy || !refresh || !is_masked ||
+        !seq_tokens || !decode_step || !workspace)
+        return EC_ERR_NULL;
+    if (n_rows > 0 && (!hidden || !w_lm || !row_pos || !token_out || !conf_out || !entropy_out))
+        return EC_ERR_NULL;
+    if ((hidden && !aligned(hidden, 16)) || (w_lm && !aligned(w_lm, 16))) return EC_ERR_ALIGN;
+    if (!aligned(workspace, EC_WORKSPACE_ALIGN) ||
+        workspace_bytes < ec::lmhead_workspace_bytes(n_rows, vocab, batch))
+        return EC_ERR_WORKSPACE;
+    return launched(ec::launch_lmhead_gate(
+        hidden, w_lm, n_rows, hidden_dim, vocab, seq_row_offsets, row_pos, batch, seq_len, n_unmask,
+        tau, step, token_out, conf_out, entropy_out, unmask_rows, max_entropy, refresh, is_masked,
+        seq_tokens, decode_step, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 ec_status ec_build_recompute_set(const uint8_t *is_masked, const int32_t *decode_step,
                                  const uint8_t *refresh, int32_t batch, int32_t seq_len,
                                  int32_t block_lo, int32_t block_hi, int32_t k, int32_t *idx,

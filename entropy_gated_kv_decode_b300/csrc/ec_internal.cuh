@@ -98,6 +98,18 @@ cudaError_t launch_decode_gate(const void *logits, int dtype, int64_t row_stride
                                int32_t *seq_tokens, int32_t *decode_step, void *workspace,
                                cudaStream_t stream);
 
+// lmhead_gate.cu
+bool lmhead_shape_ok(int32_t n_rows, int32_t hidden, int32_t vocab);
+size_t lmhead_workspace_bytes(int32_t n_rows, int32_t vocab, int32_t batch);
+cudaError_t launch_lmhead_gate(const void *hidden, const void *w_lm, int32_t n_rows,
+                               int32_t hidden_dim, int32_t vocab, const int32_t *seq_row_offsets,
+                               const int32_t *row_pos, int32_t batch, int32_t seq_len,
+                               int32_t n_unmask, float tau, int32_t step, int32_t *token_out,
+                               float *conf_out, float *entropy_out, int32_t *unmask_rows,
+                               float *max_entropy, uint8_t *refresh, uint8_t *is_masked,
+                               int32_t *seq_tokens, int32_t *decode_step, void *workspace,
+                               cudaStream_t stream);
+
 // recompute_set.cu
 cudaError_t launch_recompute_set(const uint8_t *is_masked, const int32_t *decode_step,
                                  const uint8_t *refresh, int32_t batch, int32_t seq_len,

@@ -19,6 +19,18 @@ Recipe (one seeded ``numpy.random.Generator`` per call, PCG64):
   after the other; every block before the active one is fully decoded, in a
   seeded random order, ``n_unmask`` tokens per denoising step.  The active block
   and everything after it is masked (token id = vocab, the [MASK] id).
+* LM-head operands (hidden states ``[N, hidden]`` and W_lm ``[V, hidden]``,
+  bf16).  The "exact" recipe uses small integers times powers of two, so every
+  logit is exactly representable and every float32 partial sum is exact in any
+  order: ``W_lm = 2^-6 * U{-3..3}``; hidden row i is
+  ``U{-3..3} * 2^a_i + spike_i * 2^b_i``, where ``spike_i`` is the integer
+  pattern of W_lm row ``t_i`` on ``m = max(1, hidden / 8)`` random coordinates.
+  ``a_i`` sets the spread of the row's logits, about
+  ``sigma_i = 4 sqrt(hidden) 2^(a_i - 6)``, to 1/8, 1/4, 1/2 or 1; ``b_i`` sets
+  the spike's size, about ``4 m 2^(b_i - 6)``, to 0 (no spike), 2, 4, 8 or 16
+  with probabilities .5, .15, .15, .15, .05 (exponents rounded, and
+  |a_i - b_i| <= 5 so that every hidden value stays a bf16 integer multiple).
+  The "gauss" recipe: hidden ``N(0, 1)``, W_lm ``N(0, (2 / sqrt(hidden))^2)``.
 * Attention operands.  Q, the pre-step K/V caches and the freshly projected
   K/V rows are i.i.d. ``N(0, std^2)``.
 """
@@ -236,6 +248,41 @@ def make_attention(rng: np.random.Generator, w: Workload, r_max: int,
     k_cache = draw(B, L, Hkv, d)
     v_cache = draw(B, L, Hkv, d)
     return AttentionInputs(q, k_new, v_new, k_cache, v_cache, w.attn_dtype)
+
+
+def make_lmhead(rng: np.random.Generator, n_rows: int, vocab: int, hidden: int,
+                exact: bool = True) -> tuple[np.ndarray, np.ndarray]:
+    """(hidden bf16 bits ``[n_rows, hidden]``, W_lm bf16 bits ``[vocab, hidden]``)
+    of the LM-head recipes above."""
+    w = np.empty((vocab, hidden), np.uint16)
+    if exact:
+        w_int = np.empty((vocab, hidden), np.int8)
+        for r0 in range(0, vocab, 8192):
+            r1 = min(vocab, r0 + 8192)
+            w_int[r0:r1] = rng.integers(-3, 4, size=(r1 - r0, hidden), dtype=np.int8)
+            w[r0:r1] = f32_to_bf16_bits(w_int[r0:r1].astype(np.float32) * np.float32(2.0 ** -6))
+        m = max(1, hidden // 8)
+        sigma = rng.choice(np.array([0.125, 0.25, 0.5, 1.0]), size=n_rows)
+        spike = rng.choice(np.array([0.0, 2.0, 4.0, 8.0, 16.0]), size=n_rows,
+                           p=[0.5, 0.15, 0.15, 0.15, 0.05])
+        target = rng.integers(0, vocab, size=n_rows)
+        x = np.empty((n_rows, hidden), np.uint16)
+        for i in range(n_rows):
+            a = int(round(6 + math.log2(sigma[i] / (4 * math.sqrt(hidden)))))
+            row = rng.integers(-3, 4, size=hidden).astype(np.float64) * 2.0 ** a
+            if spike[i] > 0:
+                b = int(round(6 + math.log2(spike[i] / (4 * m))))
+                b = min(max(b, a - 5), a + 5)
+                on = rng.choice(hidden, size=m, replace=False)
+                row[on] += w_int[target[i], on].astype(np.float64) * 2.0 ** b
+            x[i] = f32_to_bf16_bits(row.astype(np.float32))
+        return x, w
+    std = np.float32(2.0 / math.sqrt(hidden))
+    for r0 in range(0, vocab, 8192):
+        r1 = min(vocab, r0 + 8192)
+        w[r0:r1] = f32_to_bf16_bits(rng.standard_normal((r1 - r0, hidden), dtype=np.float32) * std)
+    x = f32_to_bf16_bits(rng.standard_normal((n_rows, hidden), dtype=np.float32))
+    return x, w
 
 
 def random_index_set(rng: np.random.Generator, batch: int, seq_len: int,

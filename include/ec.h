@@ -175,8 +175,10 @@ ec_status ec_decode_step(const void *logits, ec_dtype dtype, int64_t row_stride,
  *     start at zero, on `stream`.  Calls whose kernels can overlap on the GPU
  *     (different streams, no ordering between them) race on the array and give
  *     undefined results; serialise them.
- *   - Device-side index checks still keep every access in bounds, but their status
- *     bits are not reported by this entry point.
+ *   - The call's device status bits (bad offsets or positions, EC_DEV_TIMEOUT when
+ *     a bounded wait ran out and the step was left unfinished) stay in the array:
+ *     read them with ec_decode_noalloc_read_status.  The return value of this call
+ *     reports only what the host checks and the launch found.
  */
 ec_status ec_decode_step_noalloc(const void *logits, ec_dtype dtype, int64_t row_stride,
                                  int32_t n_rows, int32_t vocab, const int32_t *seq_row_offsets,
@@ -185,6 +187,48 @@ ec_status ec_decode_step_noalloc(const void *logits, ec_dtype dtype, int64_t row
                                  float *conf_out, float *entropy_out, int32_t *unmask_rows,
                                  float *max_entropy, uint8_t *refresh, uint8_t *is_masked,
                                  int32_t *seq_tokens, int32_t *decode_step, ec_stream_t stream);
+
+/*
+ * Status bits (EC_DEV_* flags, 0 = clean) of the last ec_decode_step_noalloc call
+ * on the current device: synchronizes `stream` (the stream of that call), then
+ * copies the status word out of the library's scratch array, allocating nothing.
+ * The next ec_decode_step_noalloc call clears it.  EC_ERR_NULL for a null `bits`.
+ */
+ec_status ec_decode_noalloc_read_status(uint32_t *bits, ec_stream_t stream);
+
+/* Bytes of device workspace ec_lmhead_decode_step needs (depends on the
+ * current device's SM count). */
+size_t ec_lmhead_workspace_size(int32_t n_rows, int32_t vocab, int32_t batch);
+
+/*
+ * The decode-and-gate step with the logits computed inside it: the LM head's
+ * product hidden x W_lm^T on the tensor cores, each row's logits folded into its
+ * softmax statistics as they leave the accumulator, so the [n_rows, vocab] logits
+ * are never written to memory ([EC-it] section 2, observation 1: the decision is
+ * an O(V) operation per decoded token; "Algoritmo di Funzionamento" point 3 and
+ * section 4: it costs a constant, negligible share of inference).
+ *
+ *   logits[i, j] = sum_e hidden[i, e] * w_lm[j, e]   (float32 accumulation of the
+ *   bf16 products), then everything ec_decode_step computes from those logits.
+ *
+ * hidden  bf16 device [n_rows, hidden_dim], rows contiguous, 16-byte aligned;
+ * w_lm    bf16 device [vocab, hidden_dim] (one vocabulary entry's weights per row,
+ *         as a linear layer stores them), 16-byte aligned.
+ * hidden_dim a multiple of 64; n_rows at most 128 x the SM count (18944 on a
+ * B300).  Every other argument, output and state buffer is as in
+ * ec_decode_step; the token is the first index of the largest float32 logit.
+ * Workspace: ec_lmhead_workspace_size bytes, EC_WORKSPACE_ALIGN-aligned, zeroed
+ * before first use (counters return to zero after every call; zero it again
+ * after a call whose status reports EC_DEV_TIMEOUT).
+ */
+ec_status ec_lmhead_decode_step(const void *hidden, const void *w_lm, int32_t n_rows,
+                                int32_t hidden_dim, int32_t vocab, const int32_t *seq_row_offsets,
+                                const int32_t *row_pos, int32_t batch, int32_t seq_len,
+                                int32_t n_unmask, float tau, int32_t step, int32_t *token_out,
+                                float *conf_out, float *entropy_out, int32_t *unmask_rows,
+                                float *max_entropy, uint8_t *refresh, uint8_t *is_masked,
+                                int32_t *seq_tokens, int32_t *decode_step, void *workspace,
+                                size_t workspace_bytes, ec_stream_t stream);
 
 /*
  * Recompute index set of the next forward ([EC-it] step 2; [EC-ar] phase 1 and

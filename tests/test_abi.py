@@ -164,3 +164,32 @@ def test_noalloc_decode_rejects_bad_arguments(L):
     assert call(0, 0x1008) == -4      # logits not 16-byte aligned
     # a request whose scratch exceeds the fixed 2 MiB array (checked before any CUDA call)
     assert call(3, 1 << 20) == -8     # EC_ERR_SCRATCH_LIMIT
+
+
+def test_noalloc_status_reader_rejects_null(L):
+    assert L.ec_decode_noalloc_read_status(None, None) == -1
+
+
+def test_lmhead_rejects_bad_arguments(L):
+    f = L.ec_lmhead_decode_step
+    #       hidden  w_lm    N    hid   V       offsets row_pos B  L     n  tau  step tok     conf    ent     unmask  emax    refresh masked  tokens  dstep   ws      ws_bytes stream
+    base = [0x1000, 0x2000, 32, 4096, 126464, 0x3000, 0x4000, 1, 1024, 2, 0.5, 0,   0x5000, 0x6000, 0x7000, 0x8000, 0x9000, 0xa000, 0xb000, 0xc000, 0xd000, 0x10000, 1 << 24, None]
+
+    def call(i, v):
+        args = list(base)
+        args[i] = v
+        return f(*args)
+
+    assert call(3, 100) == -2         # hidden size not a multiple of 64
+    assert call(3, 0) == -2
+    assert call(4, 0) == -2           # vocab
+    assert call(2, 148 * 128 + 1) == -2  # more rows than 128 per SM
+    assert call(9, 0) == -2           # n_unmask
+    assert call(10, float("nan")) == -2  # tau
+    assert call(5, None) == -1        # offsets
+    assert call(0, None) == -1        # hidden with rows
+    assert call(21, None) == -1       # workspace
+    assert call(0, 0x1008) == -4      # hidden not 16-byte aligned
+    assert call(1, 0x2004) == -4      # w_lm not 16-byte aligned
+    assert call(22, 64) == -5         # workspace too small
+    assert call(21, 0x10010) == -5    # workspace misaligned

@@ -134,3 +134,24 @@ def test_projection_timeout_unwinds_and_recovers(orc):
         r = ref[..., j * width:(j + 1) * width]
         for b in range(B):
             assert np.all(np.abs(g[b, :cnt[b]] - r[b, :cnt[b]]) <= 2e-2 * np.abs(r[b, :cnt[b]]) + 2e-2)
+
+
+def test_lmhead_timeout_unwinds_and_recovers(orc):
+    from test_parity_lmhead import run_lmhead_gpu
+    nat = native()
+    w = synth.scaled(synth.WORKLOADS["batched"], batch=3, block=50, seq_len=512, prompt_len=128,
+                     active_block=2, vocab=9000)
+    rng = np.random.default_rng(29)
+    st = synth.make_state(rng, w)
+    x, wl = synth.make_lmhead(rng, w.n_rows, w.vocab, 256)
+    ws = nat.new_workspace(nat.ec_lmhead_workspace_size(w.n_rows, w.vocab, w.batch))
+    with short_waits(nat):
+        got = run_lmhead_gpu(nat, x, wl, st, w.n_unmask, w.tau, st.step, workspace=ws)
+    assert got["status"] & nat.DEV_TIMEOUT, f"status {got['status']:#x}"
+    ref = run_decode_oracle(orc, orc.projection(x, wl), st, w.n_unmask, w.tau, st.step)
+    tok_ok = (got["token"] == -7) | (got["token"] == ref["token"])
+    ent_ok = np.isnan(got["entropy"]) | (np.abs(got["entropy"] - ref["entropy"]) <= 1e-4)
+    assert tok_ok.all() and ent_ok.all()
+    nat.ec_workspace_init(ws)
+    again = run_lmhead_gpu(nat, x, wl, st, w.n_unmask, w.tau, st.step, workspace=ws)
+    check_decode(again, ref, st, w.n_unmask, w.tau, st.step)

@@ -81,3 +81,25 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
                                     0xa000, 0xb000, 0xc000, None)
     assert rc == -8
     assert "scratch" in nat.status_str(rc)
+
+
+def test_noalloc_status_reports_a_timeout_and_clears():
+    # the allocation-free call's device status: clean after a normal call,
+    # EC_DEV_TIMEOUT after a call whose waits were made to run out, clean again
+    # after the next normal call
+    nat = native()
+    w = synth.scaled(synth.WORKLOADS["batched"], batch=4, block=16, seq_len=512, prompt_len=128,
+                     active_block=2, vocab=20000)
+    st = synth.make_state(np.random.default_rng(0), w)
+    logits = dev(synth.make_logits(np.random.default_rng(3), w.n_rows, w.vocab, w.logits_dtype))
+    nat.ec_decode_step_noalloc(*_args(w, st, logits, _buffers(w, st)))
+    assert nat.ec_decode_noalloc_read_status() == 0
+    nat.ec_debug_set_wait_limit(300)
+    try:
+        nat.ec_decode_step_noalloc(*_args(w, st, logits, _buffers(w, st)))
+        bits = nat.ec_decode_noalloc_read_status()
+    finally:
+        nat.ec_debug_set_wait_limit(0)
+    assert bits & nat.DEV_TIMEOUT, f"status {bits:#x}"
+    _compare_one_call(nat, w, 3, "after timeout")
+    assert nat.ec_decode_noalloc_read_status() == 0
