@@ -313,7 +313,7 @@ def kernels_per_step(nat, w: synth.Workload):
     dt = torch.bfloat16 if w.attn_dtype == synth.BF16 else torch.float32
     n_att = nat.ec_attention_kernel_count(dt, w.batch, w.seq_len, w.r_max, w.n_heads,
                                           w.n_kv_heads, w.head_dim)
-    return {"attention": n_att, "decode": 1, "recompute": 1}
+    return {"attention": n_att, "decode": 2 if w.n_rows > 0 else 1, "recompute": 1}
 
 
 def dist_setup(args):
@@ -462,7 +462,7 @@ def run_ours(args, workload=None):
                       "frac_attainable": att_tflops / att_roof, "intensity_flop_per_byte": att_ai,
                       "launches": n_launch["attention"]},
         "decode_gate": {"us": us(t_dec), "gbs": dec_gbs, "frac_hbm": dec_gbs / hbm,
-                        "launches": 1},
+                        "launches": n_launch["decode"]},
         "recompute_set": {"us": us(t_max["recompute_set"]), "launches": 1},
     }
     dominant = "attention" if t_att > t_dec else "decode_gate"
@@ -933,7 +933,7 @@ def run_trajectory(args):
                      "kernel": "qkv_gemm_kernel (full-refresh shape 1024 x 12288 x 4096)",
                      "peak_source": f"{peak_kind} sustained (MEASURED_PEAKS.json)"},
         "clocks": clocks,
-        "gpu_launches": sum(1 + 2 * w.n_layers + 3 for _ in recs) * K,
+        "gpu_launches": sum(1 + 2 * w.n_layers + 4 for _ in recs) * K,
         "e2e": {"value": aggregate(tbytes, world, e2e_wall) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": tbytes / w.n_steps,
                 "d2h_bytes_per_step": 5 + tr.tokens.numel() * 4 / w.n_steps,

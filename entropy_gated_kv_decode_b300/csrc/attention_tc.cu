@@ -28,20 +28,23 @@
 // set is 0 .. L-1) loads its tiles from the fresh K/V directly, and its mt = 0
 // CTAs store every tile to the cache with a TMA store.
 //
-// Warp roles (320 threads):
+// Warp roles (256 threads):
 //   warp 0     TMA producer of Q (one tile per piece) and K tiles; warp 6 of V
 //              tiles (128-byte swizzle, rings of stages);
-//   warps 8, 9 patch the fresh rows into each landed K / V tile (or store the
-//              tile to the cache, full refresh), then release it to the MMAs;
-//   warp 1     TMEM allocation; Q into TMEM (tcgen05.cp) and S = Q K^T into one of
-//              two TMEM S buffers (tcgen05.mma) once the PV product that read that
-//              buffer's P has completed;
-//   warp 7     O += P V into the TMEM O accumulator: a second issuing thread, so
-//              the next tile's QK never queues behind this tile's PV;
+//   warp 1     TMEM allocation; Q into TMEM (tcgen05.cp); per K tile the whole
+//              warp patches the fresh rows into it (cp.async, one round trip)
+//              and writes them back to the cache, or stores the tile for a full
+//              refresh; then one thread issues S = Q K^T (tcgen05.mma) into one
+//              of two TMEM S buffers once the PV product that read that buffer's
+//              P has completed;
+//   warp 7     the same patching for each V tile, then O += P V into the TMEM O
+//              accumulator: a second issuing thread, so the next tile's QK never
+//              queues behind this tile's PV;
 //   warps 2-5  one thread per query row: online softmax in the log2 domain on S
-//              read by tcgen05.ld (the reference maximum moves only when it grows
-//              by more than 8 in log2 units, rescaling O in TMEM), P as bf16 over
-//              the first half of the same S buffer (the PV product reads its A
+//              read by tcgen05.ld (the whole row in registers, one round trip
+//              per tile; the reference maximum moves only when it grows by more
+//              than 8 in log2 units, rescaling O in TMEM), P as bf16 over the
+//              first half of the same S buffer (the PV product reads its A
 //              operand there), and the piece's epilogue.
 // Every wait is bounded; a timeout sets EC_DEV_TIMEOUT and unwinds.
 #include <cuda_bf16.h>
@@ -61,7 +64,7 @@ using namespace ptx;
 
 constexpr int kBlockM = 128;   // query rows per unit = TMEM lanes
 constexpr int kBlockN = 128;   // keys per tile
-constexpr int kThreads = 320;  // 10 warps
+constexpr int kThreads = 256;  // 8 warps
 constexpr int kSoftmaxBarrier = 1;  // named barrier of the 4 softmax warps
 constexpr int kMaxContrib = 8;      // contributors merged by one owner at most
 
@@ -89,19 +92,17 @@ struct Cfg {
 
 enum : int {
     B_KFULL = 0,     // [4] K tile landed
-    B_KREADY = 4,    // [4] K tile patched (fresh rows in place): the QK product may read it
-    B_KEMPTY = 8,    // [4] K stage consumed (its QK done)
-    B_VFULL = 12,    // [4] V tile landed
-    B_VREADY = 16,   // [4] V tile patched
-    B_VEMPTY = 20,   // [4] V stage consumed (its PV done)
-    B_QFULL = 24,    // [2] Q tile landed
-    B_QEMPTY = 26,   // [2] Q tile copied into TMEM
-    B_SFULL = 28,    // [2] S buffer written by its QK product
-    B_PFULL = 30,    // [2] P written over its S buffer (and O corrected): 4 softmax warps
-    B_SFREE = 32,    // [2] the PV product that read the buffer's P completed (O updated)
-    B_DRAIN = 34,    // QK issuer's products all complete
-    B_DRAIN2 = 35,   // PV issuer's products all complete
-    B_COUNT = 36
+    B_KEMPTY = 4,    // [4] K stage consumed (its QK done)
+    B_VFULL = 8,     // [4] V tile landed
+    B_VEMPTY = 12,   // [4] V stage consumed (its PV done)
+    B_QFULL = 16,    // [2] Q tile landed
+    B_QEMPTY = 18,   // [2] Q tile copied into TMEM
+    B_SFULL = 20,    // [2] S buffer written by its QK product
+    B_PFULL = 22,    // [2] P written over its S buffer (and O corrected): 4 softmax warps
+    B_SFREE = 24,    // [2] the PV product that read the buffer's P completed (O updated)
+    B_DRAIN = 26,    // QK issuer's products all complete
+    B_DRAIN2 = 27,   // PV issuer's products all complete
+    B_COUNT = 28
 };
 static_assert(8 * B_COUNT <= 512, "barrier area");
 
@@ -338,33 +339,21 @@ __device__ __forceinline__ int lower_bound_warp(const int32_t *idx, int cnt, int
     return lo + __popc(__ballot_sync(0xffffffffu, below));
 }
 
-// Patch warp (warps 8 and 9: K and V): after each tile of a piece lands, put
-// the fresh rows that fall in it into the tile in shared memory (and, from the
-// group's mt = 0 CTA, into the cache), or for a fully recomputed sequence store
-// the landed tile to the cache; then release the tile to the MMA issuer.
+// The fresh K or V rows of one piece, put into each landed tile by an MMA
+// issuer warp before its product reads the tile.  The cursor walks the piece's
+// ascending index set; a window of 32 of its entries stays in registers.
 template <int D>
-__device__ void patcher(const Params &P, const Sync &S, uint32_t sbase, bool is_v,
-                        const CUtensorMap *tm_cache)
-{
-    using C = Cfg<D>;
-    constexpr int kChunks = D / 8;          // 16-byte chunks per row and head
-    const int lane = threadIdx.x & 31;
-    const int stages = is_v ? C::kVStages : C::kKStages;
-    const int full0 = is_v ? B_VFULL : B_KFULL, ready0 = is_v ? B_VREADY : B_KREADY;
-    const uint32_t off0 = sbase + (is_v ? C::kOffV : C::kOffK);
-    const __nv_bfloat16 *fresh = is_v ? P.v_new : P.k_new;
-    __nv_bfloat16 *cache = is_v ? P.v_cache : P.k_cache;
-    const Range r = my_range(P);
-    uint32_t T = 0;
-    bool stored = false;
-    for (int k = 0; k < r.count; ++k) {
-        const Piece w = piece_at(P, r, k);
-        if (!piece_active(P, w)) continue;
-        const bool dense = piece_dense(P, w);
-        const bool writer = w.mt == 0;
+struct Patch {
+    int cur, vbase, v;
+    bool stored;  // a TMA store to the cache is in flight (full refresh)
+
+    // Whole warp, at a piece start.  The K side of one CTA per sequence also
+    // checks the count and the whole index set.
+    __device__ void start(const Params &P, const Piece &w, bool check)
+    {
+        const int lane = threadIdx.x & 31;
         const int32_t *idx = P.idx + static_cast<int64_t>(w.b) * P.idx_stride;
-        // One CTA per sequence checks the count and the whole index set.
-        if (!is_v && writer && w.g == 0 && w.t0 == 0) {
+        if (check && w.mt == 0 && w.g == 0 && w.t0 == 0) {
             const int c_raw = __ldg(P.count + w.b);
             if (lane == 0 && (c_raw < 0 || c_raw > P.r_max)) flag_status(P.status, EC_DEV_BAD_COUNT);
             bool bad = false;
@@ -374,162 +363,212 @@ __device__ void patcher(const Params &P, const Sync &S, uint32_t sbase, bool is_
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(P.status, EC_DEV_BAD_INDEX);
         }
-        // cursor into the index set, and a window of 32 of its entries in registers
-        int cur = dense ? 0 : lower_bound_warp(idx, w.cnt, w.t0 * kBlockN);
-        int vbase = cur;
-        int v = !dense && cur + lane < w.cnt ? __ldg(idx + cur + lane) : INT_MAX;
-        for (int t = w.t0; t < w.t1; ++t, ++T) {
-            const int s = T % stages;
-            if (!__all_sync(0xffffffffu, S.wait(full0 + s, (T / stages) & 1))) {
-                if (stored && lane == 0) bulk_wait_all();
-                return;
-            }
-            const uint32_t tile = off0 + s * C::kTile;
-            if (dense) {
-                if (writer && lane == 0) {  // the landed tile is the cache's new content
-                    fence_async_smem();
-                    for (int c = 0; c < D / 64; ++c)
-                        tma_store_4d(tm_cache, tile + c * C::kCol, c * 64, w.g, t * kBlockN, w.b);
-                    bulk_commit_and_wait_read();
-                    stored = true;
-                }
-            } else {
-                const int tile_end = (t + 1) * kBlockN;
-                for (;;) {
-                    // the rows cur .. cur + n - 1 of the window fall in this tile
-                    const int j = vbase + lane;
-                    const bool in = j >= cur && v < tile_end;
-                    const int n = __popc(__ballot_sync(0xffffffffu, in));
-                    if (n > 0) {
-                        // every 16-byte chunk of those rows in flight at once (one
-                        // round trip), then the write-back reads them from the tile
-                        const int first = cur - vbase;
-                        const int total = n * kChunks;
-                        for (int k0 = 0; k0 < total; k0 += 32) {
-                            const int k = k0 + lane, q = min(k / kChunks, n - 1), c = k % kChunks;
-                            const int rit = __shfl_sync(0xffffffffu, v, first + q) - t * kBlockN;
-                            if (k < total && rit >= 0 && rit < kBlockN && rit + t * kBlockN < P.L) {
-                                const int64_t src =
-                                    ((static_cast<int64_t>(w.b) * P.r_max + cur + q) * P.Hkv + w.g) * D + c * 8;
-                                cp_async_16(tile + (c / 8) * C::kCol + rit * 128 + (((c % 8) ^ (rit & 7)) << 4),
-                                            fresh + src);
-                            }
-                        }
-                        cp_async_wait_all();
-                        __syncwarp();
-                        if (writer) {
-                            for (int k0 = 0; k0 < total; k0 += 32) {
-                                const int k = k0 + lane, q = min(k / kChunks, n - 1), c = k % kChunks;
-                                const int p = __shfl_sync(0xffffffffu, v, first + q);
-                                const int rit = p - t * kBlockN;
-                                if (k < total && rit >= 0 && rit < kBlockN && p < P.L) {
-                                    const uint4 x = ld_shared_v4(tile + (c / 8) * C::kCol + rit * 128 +
-                                                                 (((c % 8) ^ (rit & 7)) << 4));
-                                    const int64_t at =
-                                        ((static_cast<int64_t>(w.b) * P.L + p) * P.Hkv + w.g) * D + c * 8;
-                                    *reinterpret_cast<uint4 *>(cache + at) = x;
-                                }
-                            }
-                        }
-                        cur += n;
-                    }
-                    // window used up and the index set goes on: slide it, the tile
-                    // may hold more rows
-                    if (cur - vbase < 32 || cur >= w.cnt) break;
-                    vbase = cur;
-                    v = cur + lane < w.cnt ? __ldg(idx + cur + lane) : INT_MAX;
-                }
-                fence_async_smem();  // the patched rows are visible to the tensor core
+        const bool dense = piece_dense(P, w);
+        cur = dense ? 0 : lower_bound_warp(idx, w.cnt, w.t0 * kBlockN);
+        vbase = cur;
+        v = !dense && cur + lane < w.cnt ? __ldg(idx + cur + lane) : INT_MAX;
+    }
+
+    // Whole warp, tile t of piece w landed at `tile`: the fresh rows that fall in
+    // it into it (and, from the group's mt = 0 CTA, into the cache), or for a
+    // fully recomputed sequence the tile stored to the cache as it is.  Returns
+    // with the tile visible to the tensor core.
+    __device__ void tile(const Params &P, const Piece &w, int t, uint32_t tile, bool is_v,
+                         const CUtensorMap *tm_cache)
+    {
+        using C = Cfg<D>;
+        constexpr int kChunks = D / 8;  // 16-byte chunks per row and head
+        const int lane = threadIdx.x & 31;
+        const bool writer = w.mt == 0;
+        if (piece_dense(P, w)) {
+            if (writer && lane == 0) {  // the landed tile is the cache's new content
+                fence_async_smem();
+                for (int c = 0; c < D / 64; ++c)
+                    tma_store_4d(tm_cache, tile + c * C::kCol, c * 64, w.g, t * kBlockN, w.b);
+                bulk_commit_and_wait_read();  // read before the stage can be reused
+                stored = true;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(S.bar(ready0 + s));
+            return;
         }
+        const __nv_bfloat16 *fresh = is_v ? P.v_new : P.k_new;
+        __nv_bfloat16 *cache = is_v ? P.v_cache : P.k_cache;
+        const int32_t *idx = P.idx + static_cast<int64_t>(w.b) * P.idx_stride;
+        const int tile_end = (t + 1) * kBlockN;
+        bool patched = false;
+        for (;;) {
+            // the rows cur .. cur + n - 1 of the window fall in this tile
+            const int j = vbase + lane;
+            const bool in = j >= cur && v < tile_end;
+            const int n = __popc(__ballot_sync(0xffffffffu, in));
+            if (n > 0) {
+                // every 16-byte chunk of those rows in flight at once (one round
+                // trip); the write-back then reads them from the tile
+                const int first = cur - vbase;
+                const int total = n * kChunks;
+                for (int k0 = 0; k0 < total; k0 += 32) {
+                    const int k = k0 + lane, q = min(k / kChunks, n - 1), c = k % kChunks;
+                    const int rit = __shfl_sync(0xffffffffu, v, first + q) - t * kBlockN;
+                    if (k < total && rit >= 0 && rit < kBlockN && rit + t * kBlockN < P.L) {
+                        const int64_t src =
+                            ((static_cast<int64_t>(w.b) * P.r_max + cur + q) * P.Hkv + w.g) * D + c * 8;
+                        cp_async_16(tile + (c / 8) * C::kCol + rit * 128 + (((c % 8) ^ (rit & 7)) << 4),
+                                    fresh + src);
+                    }
+                }
+                cp_async_wait_all();
+                __syncwarp();
+                if (writer) {
+                    for (int k0 = 0; k0 < total; k0 += 32) {
+                        const int k = k0 + lane, q = min(k / kChunks, n - 1), c = k % kChunks;
+                        const int p = __shfl_sync(0xffffffffu, v, first + q);
+                        const int rit = p - t * kBlockN;
+                        if (k < total && rit >= 0 && rit < kBlockN && p < P.L) {
+                            const uint4 x = ld_shared_v4(tile + (c / 8) * C::kCol + rit * 128 +
+                                                         (((c % 8) ^ (rit & 7)) << 4));
+                            const int64_t at =
+                                ((static_cast<int64_t>(w.b) * P.L + p) * P.Hkv + w.g) * D + c * 8;
+                            *reinterpret_cast<uint4 *>(cache + at) = x;
+                        }
+                    }
+                }
+                cur += n;
+                patched = true;
+            }
+            // window used up and the index set goes on: slide it, the tile may
+            // hold more rows
+            if (cur - vbase < 32 || cur >= w.cnt) break;
+            vbase = cur;
+            v = cur + lane < w.cnt ? __ldg(idx + cur + lane) : INT_MAX;
+        }
+        if (patched) fence_async_smem();  // the patched rows are visible to the tensor core
+        __syncwarp();
     }
-    if (stored && lane == 0) bulk_wait_all();
-}
+};
 
-// QK issuer (one thread): per piece Q into TMEM, then S = Q K^T for each tile
-// into one of the two S buffers as soon as its K tile is ready and the PV product
-// of the tile two back (which read its P from that buffer) completed.
+// QK issuer warp: per piece Q into TMEM; then per tile, once its K tile landed,
+// the whole warp patches the fresh K rows into it, and one thread issues
+// S = Q K^T into one of the two S buffers once the PV product of the tile two
+// back (which read its P from that buffer) completed.
 template <int D>
-__device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem)
+__device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem,
+                          const CUtensorMap *tm_k)
 {
     using C = Cfg<D>;
     constexpr uint32_t kIdescQK = idesc_bf16(kBlockM, kBlockN, false, false);
+    const int lane = threadIdx.x & 31;
     const Range r = my_range(P);
+    Patch<D> pt;
+    pt.stored = false;
     uint32_t T = 0, it = 0;
     bool ok = true;
     for (int k = 0; k < r.count && ok; ++k) {
         const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
         const int qb = it % C::kQBufs;
-        ok = S.wait(B_QFULL + qb, (it / C::kQBufs) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        // Q into TMEM once per piece (after the previous piece's last QK, in issue
-        // order); its shared-memory buffer is free for the next piece's Q after that
-        const uint32_t qbase = sbase + C::kOffQ + qb * C::kTile;
+        if (lane == 0) {
+            ok = S.wait(B_QFULL + qb, (it / C::kQBufs) & 1);
+            if (ok) {
+                tc_fence_after();
+                // Q into TMEM once per piece (after the previous piece's last QK, in
+                // issue order); its shared-memory buffer is free for the next
+                // piece's Q after that
+                const uint32_t qbase = sbase + C::kOffQ + qb * C::kTile;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-            tmem_copy_128x256b(tmem + C::kColQ + kk * 8,
-                               desc_sw128(qbase + (kk >> 2) * C::kCol + (kk & 3) * 32, 16, 1024));
-        umma_commit(S.bar(B_QEMPTY + qb));
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tmem_copy_128x256b(tmem + C::kColQ + kk * 8,
+                                       desc_sw128(qbase + (kk >> 2) * C::kCol + (kk & 3) * 32, 16, 1024));
+                umma_commit(S.bar(B_QEMPTY + qb));
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        pt.start(P, w, true);
         for (int t = w.t0; t < w.t1; ++t, ++T) {
             const int s = T % C::kKStages, sb = T & 1;
-            ok = S.wait(B_KREADY + s, (T / C::kKStages) & 1);
-            if (ok && T >= 2) ok = S.wait(B_SFREE + sb, ((T >> 1) - 1) & 1);
+            ok = __all_sync(0xffffffffu, S.wait(B_KFULL + s, (T / C::kKStages) & 1));
             if (!ok) break;
-            tc_fence_after();
             const uint32_t kbase = sbase + C::kOffK + s * C::kTile;
+            pt.tile(P, w, t, kbase, false, tm_k);
+            if (lane == 0) {
+                if (T >= 2) ok = S.wait(B_SFREE + sb, ((T >> 1) - 1) & 1);
+                if (ok) {
+                    tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // Q from TMEM, K from shared memory
-                const uint32_t off = (kk >> 2) * C::kCol + (kk & 3) * 32;
-                umma_bf16_ts(tmem + C::kColS + sb * kBlockN, tmem + C::kColQ + kk * 8,
-                             desc_sw128(kbase + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {  // Q from TMEM, K from shared memory
+                        const uint32_t off = (kk >> 2) * C::kCol + (kk & 3) * 32;
+                        umma_bf16_ts(tmem + C::kColS + sb * kBlockN, tmem + C::kColQ + kk * 8,
+                                     desc_sw128(kbase + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(S.bar(B_SFULL + sb));
+                    umma_commit(S.bar(B_KEMPTY + s));
+                }
             }
-            umma_commit(S.bar(B_SFULL + sb));
-            umma_commit(S.bar(B_KEMPTY + s));
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
         }
         ++it;
     }
-    // everything issued has completed before TMEM is released
-    umma_commit(S.bar(B_DRAIN));
-    S.drain(B_DRAIN, 0);
+    if (lane == 0) {
+        // everything issued has completed before TMEM is released
+        umma_commit(S.bar(B_DRAIN));
+        S.drain(B_DRAIN, 0);
+        if (pt.stored) bulk_wait_all();
+    }
+    __syncwarp();
 }
 
-// PV issuer (one thread): O (+)= P V for each tile once the softmax warps wrote
-// P over its S buffer and its V tile is ready; the first tile of a piece
-// overwrites O.  Its completion frees the V stage and the S buffer.
+// PV issuer warp: per tile, once its V tile landed the whole warp patches the
+// fresh V rows into it, and one thread issues O (+)= P V once the softmax warps
+// wrote P over its S buffer; the first tile of a piece overwrites O.  The
+// product's completion frees the V stage and the S buffer.
 template <int D>
-__device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem)
+__device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem,
+                          const CUtensorMap *tm_v)
 {
     using C = Cfg<D>;
     constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, false, true);
+    const int lane = threadIdx.x & 31;
     const Range r = my_range(P);
+    Patch<D> pt;
+    pt.stored = false;
     uint32_t T = 0;
     bool ok = true;
     for (int k = 0; k < r.count && ok; ++k) {
         const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
+        pt.start(P, w, false);
         for (int t = w.t0; t < w.t1; ++t, ++T) {
             const int s = T % C::kVStages, sb = T & 1;
-            ok = S.wait(B_PFULL + sb, (T >> 1) & 1) && S.wait(B_VREADY + s, (T / C::kVStages) & 1);
+            ok = __all_sync(0xffffffffu, S.wait(B_VFULL + s, (T / C::kVStages) & 1));
             if (!ok) break;
-            tc_fence_after();
             const uint32_t vbase = sbase + C::kOffV + s * C::kTile;
-            const uint32_t pcol = tmem + C::kColS + sb * kBlockN;
+            pt.tile(P, w, t, vbase, true, tm_v);
+            if (lane == 0) {
+                ok = S.wait(B_PFULL + sb, (T >> 1) & 1);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t pcol = tmem + C::kColS + sb * kBlockN;
 #pragma unroll
-            for (int kk = 0; kk < kBlockN / 16; ++kk) {  // P from TMEM, V from shared memory
-                const uint64_t bd = desc_sw128(vbase + kk * 16 * 128, C::kCol, 1024);
-                umma_bf16_ts(tmem + C::kColO, pcol + kk * 8, bd, kIdescPV,
-                             (t > w.t0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBlockN / 16; ++kk) {  // P from TMEM, V from shared memory
+                        const uint64_t bd = desc_sw128(vbase + kk * 16 * 128, C::kCol, 1024);
+                        umma_bf16_ts(tmem + C::kColO, pcol + kk * 8, bd, kIdescPV,
+                                     (t > w.t0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(S.bar(B_VEMPTY + s));
+                    umma_commit(S.bar(B_SFREE + sb));
+                }
             }
-            umma_commit(S.bar(B_VEMPTY + s));
-            umma_commit(S.bar(B_SFREE + sb));
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
         }
     }
-    umma_commit(S.bar(B_DRAIN2));
-    S.drain(B_DRAIN2, 0);
+    if (lane == 0) {
+        umma_commit(S.bar(B_DRAIN2));
+        S.drain(B_DRAIN2, 0);
+        if (pt.stored) bulk_wait_all();
+    }
+    __syncwarp();
 }
 
 __device__ __forceinline__ uint64_t f2x2(float lo, float hi)
@@ -644,28 +683,32 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
             if (!ok) continue;
             tc_fence_after();
             const uint32_t scol = tmem + lane_off + C::kColS + sb * kBlockN;
-            const int live = (t == P.n_tiles - 1) ? kv_tail : kBlockN;  // keys past L do not exist
-            // pass 1: the row maximum of the raw scores (scale > 0 keeps the order),
-            // 32 columns at a time
-            float mx = -INFINITY;
+            // the whole row of S in registers: one round trip to TMEM per tile
+            uint32_t sr[4][32];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t sr[32];
-                tmem_ld32(scol + cc * 32, sr);
-                tmem_wait_ld(sr);
-                if (live < kBlockN) {
+            for (int cc = 0; cc < 4; ++cc) tmem_ld32(scol + cc * 32, sr[cc]);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) tmem_wait_ld(sr[cc]);
+            if (t == P.n_tiles - 1 && kv_tail < kBlockN) {  // keys past L do not exist
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (cc * 32 + j >= live) sr[j] = __float_as_uint(-INFINITY);
-                }
-                float a = __uint_as_float(sr[0]), b = __uint_as_float(sr[1]);
+                        if (cc * 32 + j >= kv_tail) sr[cc][j] = __float_as_uint(-INFINITY);
+            }
+            // row maximum of the raw scores (scale > 0 keeps the order)
+            float mx4[4];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float a = __uint_as_float(sr[cc][0]), b = __uint_as_float(sr[cc][1]);
 #pragma unroll
                 for (int j = 2; j < 32; j += 4) {
-                    a = fmax3(a, __uint_as_float(sr[j]), __uint_as_float(sr[j + 1]));
-                    b = fmax3(b, __uint_as_float(sr[j + 2]), __uint_as_float(sr[j + 3]));
+                    a = fmax3(a, __uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1]));
+                    b = fmax3(b, __uint_as_float(sr[cc][j + 2]), __uint_as_float(sr[cc][j + 3]));
                 }
-                mx = fmax3(mx, a, b);
+                mx4[cc] = fmaxf(a, b);
             }
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             float m_use = m_run, alpha = 1.f;
             bool rescale = false;
             if (mx > m_run + move) {  // p would exceed 2^8: move the reference
@@ -673,40 +716,27 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
                 alpha = ex2((m_run - mx) * c);
                 rescale = t > w.t0;
             }
-            // pass 2: p = 2^{(s - m) c} (two-wide FMA and adds, four partial sums),
-            // P as bf16 pairs over the first half of this S buffer, 64 columns of S
-            // (32 of P) at a time: P never overwrites a column not yet read
+            // p = 2^{(s - m) c}: two-wide FMA and adds, four partial sums; P as bf16
+            // pairs over the first half of this S buffer, where the PV product reads it
             const uint64_t c2 = f2x2(c, c);
             const float nmc = -m_use * c;
             const uint64_t nmc2 = f2x2(nmc, nmc);
             uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+            uint32_t pk[64];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
+            for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int cc = 2 * half + h2;
-                    uint32_t sr[32];
-                    tmem_ld32(scol + cc * 32, sr);
-                    tmem_wait_ld(sr);
-                    if (live < kBlockN) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (cc * 32 + j >= live) sr[j] = __float_as_uint(-INFINITY);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        const uint64_t y2 = ffma2(f2x2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])),
-                                                  c2, nmc2);
-                        float y0, y1;
-                        x2f(y2, y0, y1);
-                        const float p0 = ex2(y0), p1 = ex2(y1);
-                        acc2[(j >> 1) & 3] = fadd2(acc2[(j >> 1) & 3], f2x2(p0, p1));
-                        pk[h2 * 16 + (j >> 1)] = pack_bf16x2(p0, p1);
-                    }
+                for (int j = 0; j < 32; j += 2) {
+                    const uint64_t y2 = ffma2(f2x2(__uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1])),
+                                              c2, nmc2);
+                    float y0, y1;
+                    x2f(y2, y0, y1);
+                    const float p0 = ex2(y0), p1 = ex2(y1);
+                    acc2[(j >> 1) & 3] = fadd2(acc2[(j >> 1) & 3], f2x2(p0, p1));
+                    pk[(cc * 32 + j) >> 1] = pack_bf16x2(p0, p1);
                 }
-                tmem_st32(scol + half * 32, pk);
-            }
+            tmem_st32(scol, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+            tmem_st32(scol + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
             float rs0, rs1, rs2, rs3, rs4, rs5, rs6, rs7;
             x2f(acc2[0], rs0, rs1);
             x2f(acc2[1], rs2, rs3);
@@ -900,16 +930,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 producer_v<D>(P, S, sbase, &tm_v, &tm_vn);
         }
         __syncwarp();
-    } else if (warp == 1 || warp == 7) {
-        if ((threadIdx.x & 31) == 0) {
-            if (warp == 1)
-                qk_issuer<D>(P, S, sbase, tmem);
-            else
-                pv_issuer<D>(P, S, sbase, tmem);
-        }
-        __syncwarp();
-    } else if (warp == 8 || warp == 9) {
-        patcher<D>(P, S, sbase, warp == 9, warp == 9 ? &tm_v : &tm_k);
+    } else if (warp == 1) {
+        qk_issuer<D>(P, S, sbase, tmem, &tm_k);
+    } else if (warp == 7) {
+        pv_issuer<D>(P, S, sbase, tmem, &tm_v);
     } else {
         softmax_epilogue<D>(P, S, tmem);
     }

@@ -1,4 +1,5 @@
-// Decode-and-gate step of EntropyCache in one kernel launch.
+// Decode-and-gate step of EntropyCache: a streaming kernel and a finishing
+// kernel, chained by programmatic dependent launch.
 //
 // "EntropyCache: Decoded Token Entropy Guided KV Caching for Diffusion Language
 // Models" — Italian summary, "Algoritmo di Funzionamento" steps 1-2, and the
@@ -7,8 +8,9 @@
 //
 // One pass over the logits folds every row into an online softmax state
 //     m = max x,   S = sum 2^{y},  T = sum 2^{y} y,   y = x log2(e) - fl(m log2(e)),
-// so that for the whole row  H = ln S - ln2 * T / S  and  conf = p_a = 2^{y_a} / S.
-// States merge associatively (rescaling by 2^{difference of the references}).
+// so that for the whole row  H = ln S - ln2 * T / S  and  conf = p_a = 2^{y_a} / S,
+// a = the first index of m.  States merge associatively (rescaling by
+// 2^{difference of the references}; on equal maxima the earlier index wins).
 //
 // Work split.  A row's 16-byte vectors form a head (about 80 %) and, for rows
 // of 64 KB or more, a few tail chunks of at most 32 KB.  The heads of all rows,
@@ -19,26 +21,26 @@
 // contiguous run of one row a CTA processes is a piece; a row's pieces fill
 // fixed partial slots (its head pieces in CTA order, then its tail chunks), so
 // the merge order, hence every result, is deterministic.
+// Streaming kernel:
 //   producer warp   one thread streams each piece into a ring of 16 KB stages
 //                   with bulk asynchronous copies (evict-first in L2), a stage
 //                   never crossing a row end, and writes a header per stage;
 //   8 consumer warps each thread folds 4 contiguous vectors of every stage
 //                   (64 bytes; read in a rotated order, free of bank conflicts)
 //                   into its running state, which lives across the stages of a
-//                   piece.  The maximum's position is kept only to the 64-byte
-//                   batch it lies in.  At a piece end each warp reduces its
-//                   lanes (maximum first, then rescaled sums) and hands its
-//                   partial to the finisher;
-//   finisher warp   merges the 8 warp partials of a piece, publishes it to the
-//                   row's slot, and takes the row's ticket (an acq_rel atomic;
-//                   no CTA ever waits for another).  The row's last piece merges
-//                   the slots in order, finds the first index of the maximum in
-//                   the batch that holds it (one 64-byte read), and writes
-//                   token / conf / entropy.  The last row of a sequence to finish
-//                   ranks the sequence's rows by (confidence desc, position asc),
-//                   takes the first n_unmask, E = max entropy over them,
-//                   refresh = E > tau, and updates is_masked / tokens / the
-//                   decode-time log at their positions.
+//                   piece.  When the running maximum grows, the first index of
+//                   the new maximum in the thread's batch is found at once.  At
+//                   a piece end each warp reduces its lanes (maximum first, then
+//                   rescaled sums) and hands its partial to the finisher;
+//   finisher warp   merges the 8 warp partials of a piece into the piece's slot.
+// Finishing kernel, one block per sequence: its rows' slots merged in parallel
+// (token / conf / entropy written, ranking keys staged in shared memory), then
+// one warp ranks the rows by (confidence desc, position asc), takes the first
+// n_unmask, E = max entropy over them, refresh = E > tau, and updates
+// is_masked / tokens / the decode-time log at their positions.  Finishing after
+// the stream, all sequences at once, keeps the rows' last pieces, which all
+// complete near the end of the stream, from queueing behind one another, and
+// needs no ticket between blocks.
 // The bf16 fold has no per-element guard for -inf: a -inf logit makes T NaN
 // (0 * -inf), and the thread then refolds its share of that piece from global
 // memory with -inf mapped to -1e30 (weight exactly 0), so rows without -inf pay
@@ -74,13 +76,13 @@ constexpr int kCtasPerSm = 3;
 constexpr uint32_t kStageBytes = 16384;      // bytes per ring stage
 constexpr int kStages = 3;
 constexpr int kVecPerStage = kStageBytes / 16;   // 1024 vectors
-constexpr int kVecPerThread = 4;                 // contiguous: one 64-byte batch
 constexpr int kPieceSlots = 4;               // finished pieces queued for the finisher
 constexpr int kMaxSplits = 64;               // partial slots per row
 constexpr int kTailMinBytes = 65536;         // rows this long get a tail pool
 constexpr int kTailPercent = 20;             // share of such a row in the pool
 constexpr int kTailChunkVecs = 2048;         // 32 KB per pool chunk at most
 constexpr int kMaxUnmask = gate::kMaxUnmask;
+constexpr int kFinishThreads = 512;          // threads of a finishing block (one per sequence)
 
 enum : int {
     D_FULL = 0,                        // [kStages] stage landed (and its header written)
@@ -149,7 +151,8 @@ struct Fold {
         s = t = 0.f;
         a = INT_MAX;
     }
-    // A new maximum cm >= everything folded so far: shift the sums to it.
+    // A new maximum cm > everything folded so far, first seen in the 64-byte
+    // batch starting at 16-byte vector `batch`: shift the sums to it.
     __device__ __forceinline__ void raise(float cm, int batch)
     {
         float s_lo, s_hi, t_lo, t_hi;
@@ -169,7 +172,7 @@ struct Fold {
         m = cm;
         a = batch;
     }
-    // One guarded element (-inf has weight exactly 0).
+    // One guarded element of the batch at vector `batch` (-inf has weight exactly 0).
     __device__ __forceinline__ void add_guarded(float x, int batch)
     {
         if (x > m) raise(x, batch);
@@ -179,8 +182,9 @@ struct Fold {
         s += e;
         t = fmaf(e, y, t);
     }
-    // A batch of bf16 pairs, the first nw of them valid (the others are -inf
-    // fill and do not enter the sums).  No guard for -inf: see the file header.
+    // A batch of bf16 pairs (the thread's 64-byte batch starting at 16-byte
+    // vector `batch`), the first nw of them valid (the others are -inf fill and
+    // do not enter the sums).  No guard for -inf: see the file header.
     template <int N>
     __device__ __forceinline__ void add_bf16(const uint32_t (&w)[N], int nw, int batch)
     {
@@ -257,7 +261,7 @@ struct Args {
     gate::GateArgs g;    // outputs, decode state, sequences
     uint32_t *status;
     long long wait_limit;  // cycles one in-kernel wait may take
-    unsigned *row_ctr, *pool_ctr;  // pool_ctr[0] claims, pool_ctr[1] producers done
+    unsigned *pool_ctr;  // [0] pool claims, [1] producers done
     Partial *parts;
 };
 
@@ -289,55 +293,18 @@ __device__ __forceinline__ const char *row_ptr(const Args &A, int i)
     return static_cast<const char *>(A.logits) + static_cast<int64_t>(i) * A.row_stride * sizeof(T);
 }
 
-// First index of the row maximum M inside the 64-byte batch starting at
-// 16-byte vector a (or, for a = nvec, among the elements after the last whole
-// vector).  Whole warp; elements past the vocabulary are not read.
+// First index of the maximum M inside the 64-byte batch starting at 16-byte
+// vector a (for a = nvec: among the elements after the last whole vector).
+// Whole warp, one element per lane; elements past the vocabulary are not read.
 template <typename T>
 __device__ __forceinline__ int first_index_of(const Args &A, int row, int a, float M)
 {
     constexpr int E = Elem<T>::kPerVec;
     const int lane = threadIdx.x & 31;
     const int64_t j = static_cast<int64_t>(a) * E + lane;
-    const bool hit = lane < kVecPerThread * E && j < A.vocab &&
-                     Elem<T>::at(row_ptr<T>(A, row), j) == M;
+    const bool hit = lane < 4 * E && j < A.vocab && Elem<T>::at(row_ptr<T>(A, row), j) == M;
     const unsigned mask = __ballot_sync(0xffffffffu, hit);
     return mask ? static_cast<int>(j - lane) + __ffs(mask) - 1 : a * E;
-}
-
-// Finisher warp, one finished piece (its CTA partial p, the same in every lane):
-// publish it; the row's last piece merges every slot and writes token / conf /
-// entropy; the sequence's last row ranks and gates.
-template <typename T>
-__device__ void finish_piece(const Args &A, int i, int slot, Partial p)
-{
-    const int lane = threadIdx.x & 31;
-    const int n = row_slots(A, i);
-    if (n > 1) {
-        int last = 0;
-        if (lane == 0) {
-            __stcg(reinterpret_cast<float4 *>(A.parts + static_cast<int64_t>(i) * kMaxSplits + slot),
-                   make_float4(p.m, p.s, p.t, __int_as_float(p.a)));
-            last = ticket(A.row_ctr + i, static_cast<unsigned>(n - 1)) == static_cast<unsigned>(n - 1);
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (!last) return;
-        __threadfence();  // every lane reads the other pieces' partials after the acquire
-        // the last piece merges every slot in slot order
-        p = empty_partial();
-        for (int k = lane; k < n; k += 32) {
-            const float4 q4 = __ldcg(
-                reinterpret_cast<const float4 *>(A.parts + static_cast<int64_t>(i) * kMaxSplits + k));
-            Partial q;
-            q.m = q4.x;
-            q.s = q4.y;
-            q.t = q4.z;
-            q.a = __float_as_int(q4.w);
-            merge(p, q);
-        }
-        warp_merge(p);
-    }
-    const int token = p.s > 0.f ? first_index_of<T>(A, i, p.a, p.m) : 0;
-    gate::finish_row(A.g, i, p, token);
 }
 
 // ---- the consumer side ----
@@ -580,8 +547,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
     }
 
     if (warp == kConsumerWarps + 1) {
-        // ---- finisher: empty sequences (CTA 0), then every piece of this CTA ----
-        if (blockIdx.x == 0) gate::empty_sequences(A.g);
+        // ---- finisher: the 8 warp partials of each piece merged into its slot ----
         for (uint32_t pc = 0;; ++pc) {
             const int slot = pc % kPieceSlots;
             if (!S.wait(D_PFULL + slot, (pc / kPieceSlots) & 1)) break;
@@ -592,9 +558,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
             if (info.x < 0) break;  // the consumers' end marker
 #pragma unroll
             for (int off = 4; off; off >>= 1) merge(p, shfl_xor(p, off));
+            // the piece's maximum to its exact first index (the fold kept only
+            // the 64-byte batch), off the consumers' path
             p = Partial{__shfl_sync(0xffffffffu, p.m, 0), __shfl_sync(0xffffffffu, p.s, 0),
                         __shfl_sync(0xffffffffu, p.t, 0), __shfl_sync(0xffffffffu, p.a, 0)};
-            finish_piece<T>(A, info.x, info.y, p);
+            if (p.s > 0.f) p.a = first_index_of<T>(A, info.x, p.a, p.m);
+            if (lane == 0)
+                __stcg(reinterpret_cast<float4 *>(A.parts + static_cast<int64_t>(info.x) * kMaxSplits + info.y),
+                       gate::to_f4(p));
         }
         return;
     }
@@ -651,6 +622,58 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
     }
 }
 
+// Second kernel, one block per sequence: groups of g lanes (g = 32 for short
+// sequences, down to 1 for long ones) each merge one row's slots, write its
+// token / conf / entropy and stage its ranking key in shared memory; then one
+// warp ranks the sequence's rows, takes the first n_unmask, E = max entropy over
+// them, refresh = E > tau, and updates the decode state.  No block waits for
+// another.  A stream kernel that gave up a wait left some slots unwritten: then
+// nothing is finished (the status word reports the timeout).
+__global__ void __launch_bounds__(kFinishThreads) decode_finish_kernel(const Args A)
+{
+    __shared__ gate::SeqStage st;
+    pdl_wait();  // the stream kernel's slots are complete and visible
+    pdl_launch_dependents();
+    if (ld_status(A.status) & EC_DEV_TIMEOUT) return;  // the whole block alike
+    const int b = static_cast<int>(blockIdx.x), tid = static_cast<int>(threadIdx.x);
+    const int lo = __ldg(A.g.offsets + b), hi = __ldg(A.g.offsets + b + 1);
+    if (lo < 0 || hi > A.n_rows || lo > hi) {
+        if (tid == 0) flag_status(A.status, EC_DEV_BAD_OFFSETS);
+        return;
+    }
+    const int cnt = hi - lo;
+    int g = 32;  // lanes per row: as many as the block holds for this sequence
+    while (g > 1 && g * cnt > kFinishThreads) g >>= 1;
+    const int j = tid % g;
+    for (int r0 = 0; r0 < cnt; r0 += kFinishThreads / g) {
+        const int r = r0 + tid / g;
+        const bool live = r < cnt;
+        const int i = lo + r;
+        Partial p = empty_partial();
+        if (live) {
+            const float4 *slots =
+                reinterpret_cast<const float4 *>(A.parts + static_cast<int64_t>(i) * kMaxSplits);
+            const int n = row_slots(A, i);
+            for (int k = j; k < n; k += g) merge(p, gate::from_f4(__ldcg(slots + k)));
+        }
+        for (int off = g >> 1; off; off >>= 1) merge(p, shfl_xor(p, off));
+        if (live && j == 0) {
+            float conf, entropy;
+            const int token = p.s > 0.f ? p.a : 0;
+            gate::store_row(A.g, i, p, token, conf, entropy);
+            const int pos = __ldg(A.g.row_pos + i);
+            if (pos < 0 || pos >= A.g.seq_len) flag_status(A.status, EC_DEV_BAD_ROW_POS);
+            if (r < gate::kMaxStagedRows) {
+                st.key[r] = gate::select_key(conf, pos);
+                st.ent[r] = entropy;
+                st.tok[r] = token;
+            }
+        }
+    }
+    __syncthreads();  // every row's outputs written and staged
+    if (tid < 32) gate::rank_and_gate(A.g, b, lo, cnt, st);
+}
+
 }  // namespace
 
 // Pool chunks per row of `nvec` 16-byte vectors and the row's head length.
@@ -669,10 +692,7 @@ static void row_split(int nvec, int *head, int *n_tc)
 size_t decode_workspace_bytes(int32_t n_rows, int32_t batch)
 {
     const size_t rows = n_rows > 0 ? static_cast<size_t>(n_rows) : 0;
-    const size_t seqs = batch > 0 ? static_cast<size_t>(batch) : 0;
     size_t off = kWsHeader;
-    off = align_up(off + rows * sizeof(unsigned), 16);
-    off = align_up(off + seqs * sizeof(unsigned), 16);
     off = align_up(off + 2 * sizeof(unsigned), 256);  // pool claims, producers done
     return off + rows * kMaxSplits * sizeof(Partial);
 }
@@ -740,18 +760,20 @@ cudaError_t launch_decode_gate(const void *logits, int dtype, int64_t row_stride
     g.status = A.status;
     A.wait_limit = wait_limit_cycles();
     size_t off = kWsHeader;
-    A.row_ctr = reinterpret_cast<unsigned *>(ws + off);
-    off = align_up(off + static_cast<size_t>(std::max(n_rows, 0)) * sizeof(unsigned), 16);
-    g.seq_ctr = reinterpret_cast<unsigned *>(ws + off);
-    off = align_up(off + static_cast<size_t>(batch) * sizeof(unsigned), 16);
+    g.seq_ctr = nullptr;  // the finishing kernel takes a block per sequence: no tickets
     A.pool_ctr = reinterpret_cast<unsigned *>(ws + off);
     off = align_up(off + 2 * sizeof(unsigned), 256);
     A.parts = reinterpret_cast<Partial *>(ws + off);
 
-    const dim3 grid(static_cast<unsigned>(A.grid));
-    if (dtype == EC_BF16)
-        return launch(decode_gate_kernel<uint16_t>, grid, dim3(kThreads), kSmemDyn, stream, A);
-    return launch(decode_gate_kernel<float>, grid, dim3(kThreads), kSmemDyn, stream, A);
+    if (n_rows > 0) {
+        const dim3 grid(static_cast<unsigned>(A.grid));
+        const cudaError_t e =
+            dtype == EC_BF16 ? launch(decode_gate_kernel<uint16_t>, grid, dim3(kThreads), kSmemDyn, stream, A)
+                             : launch(decode_gate_kernel<float>, grid, dim3(kThreads), kSmemDyn, stream, A);
+        if (e != cudaSuccess) return e;
+    }
+    return launch(decode_finish_kernel, dim3(static_cast<unsigned>(batch)), dim3(kFinishThreads), 0,
+                  stream, A);
 }
 
 }  // namespace ec
@@ -819,9 +841,9 @@ extern "C" ec_status ec_decode_step_noalloc(
     void *scratch = nullptr;
     if (ec::decode_scratch_address(&scratch) != cudaSuccess) return EC_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // The array keeps the previous call's contents: clear the status word, the
-    // tickets and the pool counters, which must start at zero (the partial slots
-    // are always written before they are read).
+    // The array keeps the previous call's contents: clear the status word and the
+    // pool counters, which must start at zero (the partial slots are always
+    // written before they are read).
     const size_t zeroed = ec::decode_workspace_zeroed_bytes(n_rows, batch);
     if (cudaMemsetAsync(scratch, 0, zeroed, s) != cudaSuccess) return EC_ERR_CUDA;
     const cudaError_t e = ec::launch_decode_gate(

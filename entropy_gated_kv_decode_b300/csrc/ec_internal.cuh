@@ -19,6 +19,7 @@ constexpr size_t kWsHeader = 256;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+__device__ __forceinline__ uint32_t ld_status(const uint32_t *status) { return __ldcg(status); }
 __device__ __forceinline__ void flag_status(uint32_t *status, uint32_t bits)
 {
     if (status) atomicOr(status, bits);

@@ -208,40 +208,52 @@ __device__ __forceinline__ int sequence_of(const GateArgs &A, int i, int &lo, in
     return a;
 }
 
-// Rank, gate and state update for sequence b, by one warp.  Every row's
-// confidence, position, entropy and token are loaded in one round trip.
-__device__ __forceinline__ void finish_sequence(const GateArgs &A, int b, int r0, int cnt)
+// The ranking's view of a sequence's rows in shared memory (rows beyond
+// kMaxStagedRows are read from the outputs in global memory instead).
+struct SeqStage {
+    unsigned long long key[kMaxStagedRows];
+    float ent[kMaxStagedRows];
+    int tok[kMaxStagedRows];
+    int sel[kMaxUnmask];
+};
+
+// Stages sequence rows [r0, r0 + cnt) from the outputs in global memory, by one
+// warp: every row's confidence, position, entropy and token in one round trip.
+__device__ __forceinline__ void stage_sequence(const GateArgs &A, int r0, int cnt, SeqStage &st)
 {
-    __shared__ unsigned long long s_key[kMaxStagedRows];
-    __shared__ float s_ent[kMaxStagedRows];
-    __shared__ int s_tok[kMaxStagedRows];
-    __shared__ int s_sel[kMaxUnmask];
     const int lane = threadIdx.x & 31;
-    const bool staged = cnt <= kMaxStagedRows;
-    if (staged)  // eight rows per lane per round, every load issued before any is used
-        for (int i0 = 0; i0 < cnt; i0 += 32 * 8) {
-            float cf[8], en[8];
-            int ps[8], tk[8];
+    if (cnt > kMaxStagedRows) return;
+    for (int i0 = 0; i0 < cnt; i0 += 32 * 8) {  // eight rows per lane per round
+        float cf[8], en[8];
+        int ps[8], tk[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int i = i0 + u * 32 + lane;
-                cf[u] = i < cnt ? __ldcg(A.conf_out + r0 + i) : 0.f;
-                en[u] = i < cnt ? __ldcg(A.entropy_out + r0 + i) : 0.f;
-                tk[u] = i < cnt ? __ldcg(A.token_out + r0 + i) : 0;
-                ps[u] = i < cnt ? __ldg(A.row_pos + r0 + i) : 0;
-            }
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * 32 + lane;
+            cf[u] = i < cnt ? __ldcg(A.conf_out + r0 + i) : 0.f;
+            en[u] = i < cnt ? __ldcg(A.entropy_out + r0 + i) : 0.f;
+            tk[u] = i < cnt ? __ldcg(A.token_out + r0 + i) : 0;
+            ps[u] = i < cnt ? __ldg(A.row_pos + r0 + i) : 0;
+        }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int i = i0 + u * 32 + lane;
-                if (i < cnt) {
-                    s_key[i] = select_key(cf[u], ps[u]);
-                    s_ent[i] = en[u];
-                    s_tok[i] = tk[u];
-                }
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * 32 + lane;
+            if (i < cnt) {
+                st.key[i] = select_key(cf[u], ps[u]);
+                st.ent[i] = en[u];
+                st.tok[i] = tk[u];
             }
         }
+    }
     __syncwarp();
+}
 
+// Rank, gate and state update for sequence b (rows [r0, r0 + cnt), staged in
+// `st` when cnt <= kMaxStagedRows), by one warp.  A sequence with no rows gets
+// no unmasked rows, E = -inf and no refresh.
+__device__ __forceinline__ void rank_and_gate(const GateArgs &A, int b, int r0, int cnt, SeqStage &st)
+{
+    const int lane = threadIdx.x & 31;
+    const bool staged = cnt <= kMaxStagedRows;
     const int take = min(A.n_unmask, cnt);
     unsigned long long prev = ~0ull;
     int nsel = 0;
@@ -250,7 +262,7 @@ __device__ __forceinline__ void finish_sequence(const GateArgs &A, int b, int r0
         int bi = INT_MAX;
         for (int i = lane; i < cnt; i += 32) {
             const unsigned long long k =
-                staged ? s_key[i]
+                staged ? st.key[i]
                        : select_key(__ldcg(A.conf_out + r0 + i), __ldg(A.row_pos + r0 + i));
             if (k < prev && k > best) {
                 best = k;
@@ -267,7 +279,7 @@ __device__ __forceinline__ void finish_sequence(const GateArgs &A, int b, int r0
             }
         }
         if (best == 0ull) break;  // only with duplicate positions (invalid input)
-        if (lane == 0) s_sel[s] = bi;
+        if (lane == 0) st.sel[s] = bi;
         prev = best;
         ++nsel;
     }
@@ -277,10 +289,10 @@ __device__ __forceinline__ void finish_sequence(const GateArgs &A, int b, int r0
     for (int s = lane; s < A.n_unmask; s += 32) {
         int32_t *slot = A.unmask_rows + static_cast<int64_t>(b) * A.n_unmask + s;
         if (s < nsel) {
-            const int i = s_sel[s];
+            const int i = st.sel[s];
             const int r = r0 + i;
-            h = fmaxf(h, staged ? s_ent[i] : __ldcg(A.entropy_out + r));
-            const int tok = staged ? s_tok[i] : __ldcg(A.token_out + r);
+            h = fmaxf(h, staged ? st.ent[i] : __ldcg(A.entropy_out + r));
+            const int tok = staged ? st.tok[i] : __ldcg(A.token_out + r);
             const int p = __ldg(A.row_pos + r);
             *slot = r;
             if (p >= 0 && p < A.seq_len) {
@@ -302,38 +314,30 @@ __device__ __forceinline__ void finish_sequence(const GateArgs &A, int b, int r0
     __syncwarp();  // the staged arrays are reused by the next call
 }
 
-// The row's outputs from its merged state p (the same in every lane) and its
-// token; the sequence's last row to finish then ranks and gates.  Whole warp.
-__device__ __forceinline__ void finish_row(const GateArgs &A, int i, const Partial &p, int token)
+// Stage, then rank and gate, sequence b from the rows' outputs in global memory.
+__device__ __forceinline__ void finish_sequence(const GateArgs &A, int b, int r0, int cnt, SeqStage &st)
 {
-    const int lane = threadIdx.x & 31;
-    int lo = 0, cnt = 0, last_row = 0;
-    const int b = sequence_of(A, i, lo, cnt);
-    if (lane == 0) {
-        // Sums are relative to mb = fl(m log2 e); for any reference point
-        // H = ln S - ln2 * T / S, and the argmax's own term is 2^{m log2 e - mb}.
-        const float S = p.s;
-        const float H = logf(S) - kLn2 * (p.t / S);
-        const float top = ex2(fmaf(p.m, kLog2e, -(p.m * kLog2e)));
-        __stcg(A.entropy_out + i, fmaxf(H, 0.f));
-        __stcg(A.conf_out + i, top / S);
-        __stcg(A.token_out + i, token);
-        if (b < 0)
-            flag_status(A.status, EC_DEV_BAD_OFFSETS);
-        else
-            last_row = ticket(A.seq_ctr + b, static_cast<unsigned>(cnt - 1)) ==
-                       static_cast<unsigned>(cnt - 1);
-    } else if (lane == 1) {
-        const int pos = __ldg(A.row_pos + i);
-        if (pos < 0 || pos >= A.seq_len) flag_status(A.status, EC_DEV_BAD_ROW_POS);
-    }
-    last_row = __shfl_sync(0xffffffffu, last_row, 0);
-    if (!last_row) return;
-    __threadfence();  // every lane reads the other rows' outputs after the acquire
-    finish_sequence(A, b, lo, cnt);
+    stage_sequence(A, r0, cnt, st);
+    rank_and_gate(A, b, r0, cnt, st);
 }
 
-// One thread's version of finish_row for row i: the outputs, the row-position
+// The outputs of row i from its merged state p: entropy, confidence and token.
+__device__ __forceinline__ void store_row(const GateArgs &A, int i, const Partial &p, int token,
+                                          float &conf, float &entropy)
+{
+    // Sums are relative to mb = fl(m log2 e); for any reference point
+    // H = ln S - ln2 * T / S, and the argmax's own term is 2^{m log2 e - mb}.
+    const float S = p.s;
+    const float H = logf(S) - kLn2 * (p.t / S);
+    const float top = ex2(fmaf(p.m, kLog2e, -(p.m * kLog2e)));
+    entropy = fmaxf(H, 0.f);
+    conf = top / S;
+    __stcg(A.entropy_out + i, entropy);
+    __stcg(A.conf_out + i, conf);
+    __stcg(A.token_out + i, token);
+}
+
+// One thread, row i from its merged state p: the outputs, the row-position
 // check and the sequence ticket.  Returns the sequence when this row was its
 // last to finish (the caller then runs finish_sequence with a whole warp), else
 // -1.  The sequence is found by a binary search over the offsets.
@@ -350,12 +354,8 @@ __device__ __forceinline__ int row_outputs(const GateArgs &A, int i, const Parti
     }
     const int o0 = __ldg(A.offsets + a), o1 = __ldg(A.offsets + a + 1);
     const bool ok = !(o0 < 0 || o1 > A.n_rows || o0 > i || i >= o1);
-    const float S = p.s;
-    const float H = logf(S) - kLn2 * (p.t / S);
-    const float top = ex2(fmaf(p.m, kLog2e, -(p.m * kLog2e)));
-    __stcg(A.entropy_out + i, fmaxf(H, 0.f));
-    __stcg(A.conf_out + i, top / S);
-    __stcg(A.token_out + i, token);
+    float conf, entropy;
+    store_row(A, i, p, token, conf, entropy);
     const int pos = __ldg(A.row_pos + i);
     if (pos < 0 || pos >= A.seq_len) flag_status(A.status, EC_DEV_BAD_ROW_POS);
     if (!ok) {

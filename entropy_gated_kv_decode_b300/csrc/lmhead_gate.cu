@@ -253,6 +253,7 @@ __device__ void lm_epilogue(const LmParams &P, const Sync &S, uint32_t tmem)
     // its row tile is left unfinished (the status word reports the timeout).
     __shared__ int s_last, s_n_done;
     __shared__ int s_done[kBM];
+    __shared__ gate::SeqStage s_stage;
     const int slot = static_cast<int>(blockIdx.x) / P.n_mt;
     if (ok && valid)
         __stcg(P.parts + static_cast<int64_t>(row) * P.per_mt + slot, gate::to_f4(f.partial()));
@@ -281,7 +282,7 @@ __device__ void lm_epilogue(const LmParams &P, const Sync &S, uint32_t tmem)
     for (int k = 0; k < s_n_done; ++k) {
         const int b = s_done[k];
         const int lo = __ldg(P.g.offsets + b);
-        gate::finish_sequence(P.g, b, lo, __ldg(P.g.offsets + b + 1) - lo);
+        gate::finish_sequence(P.g, b, lo, __ldg(P.g.offsets + b + 1) - lo, s_stage);
     }
 }
 

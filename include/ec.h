@@ -142,8 +142,14 @@ size_t ec_decode_workspace_size(int32_t n_rows, int32_t batch);
  *   decode_step   int32: receives `step` at every unmasked position (the
  *                 decode-time log of [EC-ar] phase 3; -1 = never decoded).
  * Workspace: device, EC_WORKSPACE_ALIGN-aligned, at least
- *   ec_decode_workspace_size(n_rows, batch) bytes, zeroed before first use.
+ *   ec_decode_workspace_size(n_rows, batch) bytes, zeroed before first use (its
+ *   counters return to zero after every call).
  * Calls on the same workspace must not overlap in time.
+ * Launches: a streaming kernel and a finishing kernel chained by programmatic
+ * dependent launch (the finishing kernel alone when n_rows == 0).  When the
+ * status word reports EC_DEV_TIMEOUT (a bounded wait ran out) no per-row output
+ * of that call is written; zero the workspace again (ec_workspace_init) before
+ * reusing it.
  */
 ec_status ec_decode_step(const void *logits, ec_dtype dtype, int64_t row_stride,
                          int32_t n_rows, int32_t vocab, const int32_t *seq_row_offsets,
@@ -260,10 +266,10 @@ size_t ec_attention_workspace_size(int32_t batch, int32_t seq_len, int32_t r_max
                                    int32_t n_heads, int32_t n_kv_heads, int32_t head_dim);
 
 /* Kernels one ec_selective_attention call with these arguments launches on the
- * current device (for launch accounting): bf16 with head_dim 64/128 runs the
- * KV write-back, the tensor-core attention and, when the keys of some unit are
- * split over several CTAs, a merge kernel; float32 runs a write-back and the
- * CUDA-core attention.  0 when r_max == 0; -1 for arguments the call rejects. */
+ * current device (for launch accounting): bf16 with head_dim 64/128 runs one
+ * tensor-core kernel (the KV write-back and the merge of units split over
+ * several CTAs happen inside it); float32 runs a write-back and the CUDA-core
+ * attention.  0 when r_max == 0; -1 for arguments the call rejects. */
 int32_t ec_attention_kernel_count(ec_dtype dtype, int32_t batch, int32_t seq_len, int32_t r_max,
                                   int32_t n_heads, int32_t n_kv_heads, int32_t head_dim);
 
