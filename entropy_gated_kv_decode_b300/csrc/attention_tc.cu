@@ -81,7 +81,8 @@ struct Cfg {
     static constexpr uint32_t kOffV = kOffK + kKStages * kTile;
     static constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
     static constexpr uint32_t kOffMisc = kOffBar + 512;
-    static constexpr uint32_t kBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1 KB
+    static constexpr uint32_t kOffPos = kOffMisc + 64;  // [2][128] positions of a tile's fresh rows
+    static constexpr uint32_t kBytes = kOffPos + 2 * 128 * 4 + 1024;  // + slack to align the base to 1 KB
     static constexpr uint32_t kTmemCols = 512;
     // two S buffers, columns [0, 128) and [128, 256); P (bf16 pairs) of a tile
     // overwrites the first 64 columns of its own S buffer
@@ -341,18 +342,34 @@ __device__ __forceinline__ int lower_bound_warp(const int32_t *idx, int cnt, int
 
 // The fresh K or V rows of one piece, put into each landed tile by an MMA
 // issuer warp before its product reads the tile.  The cursor walks the piece's
-// ascending index set; a window of 32 of its entries stays in registers.
+// ascending index set; a window of 128 of its entries (4 per lane) stays in
+// registers and is refilled, off the critical path, after a tile used some.
 template <int D>
 struct Patch {
-    int cur, vbase, v;
-    bool stored;  // a TMA store to the cache is in flight (full refresh)
+    int cur, vbase, cnt;
+    int v0, v1, v2, v3;  // entries vbase + lane + 32 k, INT_MAX past the set
+    bool stored;         // a TMA store to the cache is in flight (full refresh)
+    const int32_t *idx;
+    int *pos;            // shared [128]: positions of the current tile's fresh rows
+
+    __device__ void load_window(int at)
+    {
+        const int lane = threadIdx.x & 31;
+        vbase = at;
+        v0 = at + lane < cnt ? __ldg(idx + at + lane) : INT_MAX;
+        v1 = at + 32 + lane < cnt ? __ldg(idx + at + 32 + lane) : INT_MAX;
+        v2 = at + 64 + lane < cnt ? __ldg(idx + at + 64 + lane) : INT_MAX;
+        v3 = at + 96 + lane < cnt ? __ldg(idx + at + 96 + lane) : INT_MAX;
+    }
 
     // Whole warp, at a piece start.  The K side of one CTA per sequence also
     // checks the count and the whole index set.
-    __device__ void start(const Params &P, const Piece &w, bool check)
+    __device__ void start(const Params &P, const Piece &w, bool check, int *pos_smem)
     {
         const int lane = threadIdx.x & 31;
-        const int32_t *idx = P.idx + static_cast<int64_t>(w.b) * P.idx_stride;
+        idx = P.idx + static_cast<int64_t>(w.b) * P.idx_stride;
+        cnt = w.cnt;
+        pos = pos_smem;
         if (check && w.mt == 0 && w.g == 0 && w.t0 == 0) {
             const int c_raw = __ldg(P.count + w.b);
             if (lane == 0 && (c_raw < 0 || c_raw > P.r_max)) flag_status(P.status, EC_DEV_BAD_COUNT);
@@ -363,10 +380,13 @@ struct Patch {
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(P.status, EC_DEV_BAD_INDEX);
         }
-        const bool dense = piece_dense(P, w);
-        cur = dense ? 0 : lower_bound_warp(idx, w.cnt, w.t0 * kBlockN);
-        vbase = cur;
-        v = !dense && cur + lane < w.cnt ? __ldg(idx + cur + lane) : INT_MAX;
+        if (piece_dense(P, w)) {
+            cur = vbase = 0;
+            v0 = v1 = v2 = v3 = INT_MAX;
+            return;
+        }
+        cur = lower_bound_warp(idx, w.cnt, w.t0 * kBlockN);
+        load_window(cur);
     }
 
     // Whole warp, tile t of piece w landed at `tile`: the fresh rows that fall in
@@ -393,23 +413,33 @@ struct Patch {
         }
         const __nv_bfloat16 *fresh = is_v ? P.v_new : P.k_new;
         __nv_bfloat16 *cache = is_v ? P.v_cache : P.k_cache;
-        const int32_t *idx = P.idx + static_cast<int64_t>(w.b) * P.idx_stride;
         const int tile_end = (t + 1) * kBlockN;
         bool patched = false;
         for (;;) {
-            // the rows cur .. cur + n - 1 of the window fall in this tile
-            const int j = vbase + lane;
-            const bool in = j >= cur && v < tile_end;
-            const int n = __popc(__ballot_sync(0xffffffffu, in));
+            // the entries cur .. cur + n - 1 of the window fall in this tile: their
+            // positions to shared memory, in order
+            int n = 0;
+            {
+                const int vv[4] = {v0, v1, v2, v3};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int e = vbase + 32 * k + lane;
+                    const bool in = e >= cur && vv[k] < tile_end;
+                    const unsigned m = __ballot_sync(0xffffffffu, in);
+                    if (in) pos[e - cur] = vv[k];
+                    n += __popc(m);
+                }
+            }
+            __syncwarp();
             if (n > 0) {
                 // every 16-byte chunk of those rows in flight at once (one round
                 // trip); the write-back then reads them from the tile
-                const int first = cur - vbase;
                 const int total = n * kChunks;
-                for (int k0 = 0; k0 < total; k0 += 32) {
-                    const int k = k0 + lane, q = min(k / kChunks, n - 1), c = k % kChunks;
-                    const int rit = __shfl_sync(0xffffffffu, v, first + q) - t * kBlockN;
-                    if (k < total && rit >= 0 && rit < kBlockN && rit + t * kBlockN < P.L) {
+                for (int k = lane; k < total; k += 32) {
+                    const int q = k / kChunks, c = k % kChunks;
+                    const int p = pos[q];
+                    const int rit = p - t * kBlockN;
+                    if (rit >= 0 && rit < kBlockN && p < P.L) {
                         const int64_t src =
                             ((static_cast<int64_t>(w.b) * P.r_max + cur + q) * P.Hkv + w.g) * D + c * 8;
                         cp_async_16(tile + (c / 8) * C::kCol + rit * 128 + (((c % 8) ^ (rit & 7)) << 4),
@@ -419,11 +449,11 @@ struct Patch {
                 cp_async_wait_all();
                 __syncwarp();
                 if (writer) {
-                    for (int k0 = 0; k0 < total; k0 += 32) {
-                        const int k = k0 + lane, q = min(k / kChunks, n - 1), c = k % kChunks;
-                        const int p = __shfl_sync(0xffffffffu, v, first + q);
+                    for (int k = lane; k < total; k += 32) {
+                        const int q = k / kChunks, c = k % kChunks;
+                        const int p = pos[q];
                         const int rit = p - t * kBlockN;
-                        if (k < total && rit >= 0 && rit < kBlockN && p < P.L) {
+                        if (rit >= 0 && rit < kBlockN && p < P.L) {
                             const uint4 x = ld_shared_v4(tile + (c / 8) * C::kCol + rit * 128 +
                                                          (((c % 8) ^ (rit & 7)) << 4));
                             const int64_t at =
@@ -432,16 +462,21 @@ struct Patch {
                         }
                     }
                 }
+                __syncwarp();  // pos is rewritten by the next tile
                 cur += n;
                 patched = true;
             }
-            // window used up and the index set goes on: slide it, the tile may
-            // hold more rows
-            if (cur - vbase < 32 || cur >= w.cnt) break;
-            vbase = cur;
-            v = cur + lane < w.cnt ? __ldg(idx + cur + lane) : INT_MAX;
+            // the window ran out inside this tile and the index set goes on: refill
+            // it here and look again
+            if (cur < vbase + 128 || cur >= cnt) break;
+            load_window(cur);
         }
-        if (patched) fence_async_smem();  // the patched rows are visible to the tensor core
+        if (patched) {
+            fence_async_smem();  // the patched rows are visible to the tensor core
+            // refill the window at the cursor for the next tiles; its loads travel
+            // while this tile's product runs
+            if (cur < cnt && cur > vbase) load_window(cur);
+        }
         __syncwarp();
     }
 };
@@ -452,7 +487,7 @@ struct Patch {
 // back (which read its P from that buffer) completed.
 template <int D>
 __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem,
-                          const CUtensorMap *tm_k)
+                          const CUtensorMap *tm_k, int *pos)
 {
     using C = Cfg<D>;
     constexpr uint32_t kIdescQK = idesc_bf16(kBlockM, kBlockN, false, false);
@@ -483,7 +518,7 @@ __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        pt.start(P, w, true);
+        pt.start(P, w, true, pos);
         for (int t = w.t0; t < w.t1; ++t, ++T) {
             const int s = T % C::kKStages, sb = T & 1;
             ok = __all_sync(0xffffffffu, S.wait(B_KFULL + s, (T / C::kKStages) & 1));
@@ -524,7 +559,7 @@ __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
 // product's completion frees the V stage and the S buffer.
 template <int D>
 __device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem,
-                          const CUtensorMap *tm_v)
+                          const CUtensorMap *tm_v, int *pos)
 {
     using C = Cfg<D>;
     constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, false, true);
@@ -537,7 +572,7 @@ __device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
     for (int k = 0; k < r.count && ok; ++k) {
         const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
-        pt.start(P, w, false);
+        pt.start(P, w, false, pos);
         for (int t = w.t0; t < w.t1; ++t, ++T) {
             const int s = T % C::kVStages, sb = T & 1;
             ok = __all_sync(0xffffffffu, S.wait(B_VFULL + s, (T / C::kVStages) & 1));
@@ -931,9 +966,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        qk_issuer<D>(P, S, sbase, tmem, &tm_k);
+        qk_issuer<D>(P, S, sbase, tmem, &tm_k, reinterpret_cast<int *>(smem + C::kOffPos));
     } else if (warp == 7) {
-        pv_issuer<D>(P, S, sbase, tmem, &tm_v);
+        pv_issuer<D>(P, S, sbase, tmem, &tm_v, reinterpret_cast<int *>(smem + C::kOffPos) + 128);
     } else {
         softmax_epilogue<D>(P, S, tmem);
     }

@@ -624,36 +624,46 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_gate_kernel(const
 
 // Second kernel, one block per sequence: groups of g lanes (g = 32 for short
 // sequences, down to 1 for long ones) each merge one row's slots, write its
-// token / conf / entropy and stage its ranking key in shared memory; then one
-// warp ranks the sequence's rows, takes the first n_unmask, E = max entropy over
-// them, refresh = E > tau, and updates the decode state.  No block waits for
-// another.  A stream kernel that gave up a wait left some slots unwritten: then
+// token / conf / entropy and stage its ranking key in shared memory; then every
+// row's rank is counted in parallel (one thread per row; sequences longer than
+// the block are ranked by one warp, n_unmask selection rounds), the first
+// n_unmask are unmasked, E = max entropy over them, refresh = E > tau, and the
+// decode state is updated.  No block waits for another.  A stream kernel that gave up a wait left some slots unwritten: then
 // nothing is finished (the status word reports the timeout).
 __global__ void __launch_bounds__(kFinishThreads) decode_finish_kernel(const Args A)
 {
     __shared__ gate::SeqStage st;
-    pdl_wait();  // the stream kernel's slots are complete and visible
-    pdl_launch_dependents();
-    if (ld_status(A.status) & EC_DEV_TIMEOUT) return;  // the whole block alike
     const int b = static_cast<int>(blockIdx.x), tid = static_cast<int>(threadIdx.x);
+    // The offsets, positions and slot counts are inputs, complete before the
+    // streaming kernel began: read them while it still runs.
     const int lo = __ldg(A.g.offsets + b), hi = __ldg(A.g.offsets + b + 1);
-    if (lo < 0 || hi > A.n_rows || lo > hi) {
-        if (tid == 0) flag_status(A.status, EC_DEV_BAD_OFFSETS);
-        return;
-    }
-    const int cnt = hi - lo;
+    const bool seq_ok = !(lo < 0 || hi > A.n_rows || lo > hi);
+    const int cnt = seq_ok ? hi - lo : 0;
     int g = 32;  // lanes per row: as many as the block holds for this sequence
     while (g > 1 && g * cnt > kFinishThreads) g >>= 1;
     const int j = tid % g;
+    const int r_first = tid / g;
+    const bool first_live = r_first < cnt;
+    const int n_first = first_live ? row_slots(A, lo + r_first) : 0;
+    const int pos_first = first_live ? __ldg(A.g.row_pos + lo + r_first) : 0;
+    pdl_wait();  // the stream kernel's slots are complete and visible
+    pdl_launch_dependents();
+    if (ld_status(A.status) & EC_DEV_TIMEOUT) return;  // the whole block alike
+    if (!seq_ok) {
+        if (tid == 0) flag_status(A.status, EC_DEV_BAD_OFFSETS);
+        return;
+    }
     for (int r0 = 0; r0 < cnt; r0 += kFinishThreads / g) {
-        const int r = r0 + tid / g;
+        const int r = r0 + r_first;
         const bool live = r < cnt;
         const int i = lo + r;
         Partial p = empty_partial();
+        int pos = 0;
         if (live) {
             const float4 *slots =
                 reinterpret_cast<const float4 *>(A.parts + static_cast<int64_t>(i) * kMaxSplits);
-            const int n = row_slots(A, i);
+            const int n = r0 == 0 ? n_first : row_slots(A, i);
+            pos = r0 == 0 ? pos_first : __ldg(A.g.row_pos + i);
             for (int k = j; k < n; k += g) merge(p, gate::from_f4(__ldcg(slots + k)));
         }
         for (int off = g >> 1; off; off >>= 1) merge(p, shfl_xor(p, off));
@@ -661,7 +671,6 @@ __global__ void __launch_bounds__(kFinishThreads) decode_finish_kernel(const Arg
             float conf, entropy;
             const int token = p.s > 0.f ? p.a : 0;
             gate::store_row(A.g, i, p, token, conf, entropy);
-            const int pos = __ldg(A.g.row_pos + i);
             if (pos < 0 || pos >= A.g.seq_len) flag_status(A.status, EC_DEV_BAD_ROW_POS);
             if (r < gate::kMaxStagedRows) {
                 st.key[r] = gate::select_key(conf, pos);
@@ -671,7 +680,45 @@ __global__ void __launch_bounds__(kFinishThreads) decode_finish_kernel(const Arg
         }
     }
     __syncthreads();  // every row's outputs written and staged
-    if (tid < 32) gate::rank_and_gate(A.g, b, lo, cnt, st);
+    if (cnt > kFinishThreads || cnt > gate::kMaxStagedRows) {
+        if (tid < 32) gate::rank_and_gate(A.g, b, lo, cnt, st);
+        return;
+    }
+    // Every row's rank by counting the rows ahead of it (confidence desc, then
+    // position asc; equal keys, which only duplicate positions give, by row):
+    // the n_unmask first are unmasked, in rank order.
+    __shared__ int s_emax;  // max entropy of the unmasked rows, as bits (entropy >= 0)
+    if (tid == 0) s_emax = INT_MIN;
+    __syncthreads();
+    const int take = min(A.g.n_unmask, cnt);
+    if (tid < cnt) {
+        const unsigned long long key = st.key[tid];
+        int rank = 0;
+        for (int q = 0; q < cnt; ++q) {
+            const unsigned long long kq = st.key[q];
+            rank += kq > key || (kq == key && q < tid);
+        }
+        if (rank < take) {
+            const int r = lo + tid;
+            const int p = static_cast<int>(0xffffffffu - static_cast<uint32_t>(key));
+            A.g.unmask_rows[static_cast<int64_t>(b) * A.g.n_unmask + rank] = r;
+            if (p >= 0 && p < A.g.seq_len) {
+                const int64_t at = static_cast<int64_t>(b) * A.g.seq_len + p;
+                A.g.is_masked[at] = 0;
+                A.g.seq_tokens[at] = st.tok[tid];
+                A.g.decode_step[at] = A.g.step;
+            }
+            atomicMax(&s_emax, __float_as_int(st.ent[tid]));
+        }
+    }
+    for (int s2 = take + tid; s2 < A.g.n_unmask; s2 += kFinishThreads)
+        A.g.unmask_rows[static_cast<int64_t>(b) * A.g.n_unmask + s2] = -1;
+    __syncthreads();
+    if (tid == 0) {
+        const float h = take > 0 ? __int_as_float(s_emax) : -INFINITY;
+        A.g.max_entropy[b] = h;
+        A.g.refresh[b] = h > A.g.tau ? 1 : 0;
+    }
 }
 
 }  // namespace

@@ -293,7 +293,8 @@ __device__ __forceinline__ void rank_and_gate(const GateArgs &A, int b, int r0, 
             const int r = r0 + i;
             h = fmaxf(h, staged ? st.ent[i] : __ldcg(A.entropy_out + r));
             const int tok = staged ? st.tok[i] : __ldcg(A.token_out + r);
-            const int p = __ldg(A.row_pos + r);
+            const int p = staged ? static_cast<int>(0xffffffffu - static_cast<uint32_t>(st.key[i]))
+                                 : __ldg(A.row_pos + r);
             *slot = r;
             if (p >= 0 && p < A.seq_len) {
                 const int64_t at = static_cast<int64_t>(b) * A.seq_len + p;
