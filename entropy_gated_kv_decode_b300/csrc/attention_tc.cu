@@ -103,7 +103,9 @@ enum : int {
     B_SFREE = 24,    // [2] the PV product that read the buffer's P completed (O updated)
     B_DRAIN = 26,    // QK issuer's products all complete
     B_DRAIN2 = 27,   // PV issuer's products all complete
-    B_COUNT = 28
+    B_KPATCH = 28,   // fresh K granules landed in the current K tile
+    B_VPATCH = 29,   // fresh V granules landed in the current V tile
+    B_COUNT = 30
 };
 static_assert(8 * B_COUNT <= 512, "barrier area");
 
@@ -344,13 +346,29 @@ __device__ __forceinline__ int lower_bound_warp(const int32_t *idx, int cnt, int
 // issuer warp before its product reads the tile.  The cursor walks the piece's
 // ascending index set; a window of 128 of its entries (4 per lane) stays in
 // registers and is refilled, off the critical path, after a tile used some.
+// A tile made only of fresh rows comes in as one TMA box per column block; the
+// rows of other tiles are copied by cp.async.  (Writing them back to the cache
+// is done separately, see write_back_share.)
 template <int D>
 struct Patch {
     int cur, vbase, cnt;
     int v0, v1, v2, v3;  // entries vbase + lane + 32 k, INT_MAX past the set
     bool stored;         // a TMA store to the cache is in flight (full refresh)
+    int bar;             // index of this warp's mbarrier for the granule loads
+    uint32_t uses;       // its phases used so far
     const int32_t *idx;
     int *pos;            // shared [128]: positions of the current tile's fresh rows
+    const CUtensorMap *fresh128, *cache128;
+
+    __device__ void init(int bar_, int *pos_smem, const CUtensorMap *f128, const CUtensorMap *c128)
+    {
+        stored = false;
+        bar = bar_;
+        uses = 0;
+        pos = pos_smem;
+        fresh128 = f128;
+        cache128 = c128;
+    }
 
     __device__ void load_window(int at)
     {
@@ -364,12 +382,11 @@ struct Patch {
 
     // Whole warp, at a piece start.  The K side of one CTA per sequence also
     // checks the count and the whole index set.
-    __device__ void start(const Params &P, const Piece &w, bool check, int *pos_smem)
+    __device__ void start(const Params &P, const Piece &w, bool check)
     {
         const int lane = threadIdx.x & 31;
         idx = P.idx + static_cast<int64_t>(w.b) * P.idx_stride;
         cnt = w.cnt;
-        pos = pos_smem;
         if (check && w.mt == 0 && w.g == 0 && w.t0 == 0) {
             const int c_raw = __ldg(P.count + w.b);
             if (lane == 0 && (c_raw < 0 || c_raw > P.r_max)) flag_status(P.status, EC_DEV_BAD_COUNT);
@@ -390,29 +407,27 @@ struct Patch {
     }
 
     // Whole warp, tile t of piece w landed at `tile`: the fresh rows that fall in
-    // it into it (and, from the group's mt = 0 CTA, into the cache), or for a
-    // fully recomputed sequence the tile stored to the cache as it is.  Returns
-    // with the tile visible to the tensor core.
-    __device__ void tile(const Params &P, const Piece &w, int t, uint32_t tile, bool is_v,
-                         const CUtensorMap *tm_cache)
+    // it into it, or for a fully recomputed sequence the tile stored to the cache
+    // as it is (from the group's mt = 0 CTA).  Returns with the tile visible to
+    // the tensor core, or false when a wait gave up.
+    __device__ bool tile(const Params &P, const Sync &S, const Piece &w, int t, uint32_t tile, bool is_v)
     {
         using C = Cfg<D>;
         constexpr int kChunks = D / 8;  // 16-byte chunks per row and head
+        constexpr int step = 32 / kChunks;
         const int lane = threadIdx.x & 31;
-        const bool writer = w.mt == 0;
         if (piece_dense(P, w)) {
-            if (writer && lane == 0) {  // the landed tile is the cache's new content
+            if (w.mt == 0 && lane == 0) {  // the landed tile is the cache's new content
                 fence_async_smem();
                 for (int c = 0; c < D / 64; ++c)
-                    tma_store_4d(tm_cache, tile + c * C::kCol, c * 64, w.g, t * kBlockN, w.b);
+                    tma_store_4d(cache128, tile + c * C::kCol, c * 64, w.g, t * kBlockN, w.b);
                 bulk_commit_and_wait_read();  // read before the stage can be reused
                 stored = true;
             }
             __syncwarp();
-            return;
+            return true;
         }
         const __nv_bfloat16 *fresh = is_v ? P.v_new : P.k_new;
-        __nv_bfloat16 *cache = is_v ? P.v_cache : P.k_cache;
         const int tile_end = (t + 1) * kBlockN;
         bool patched = false;
         for (;;) {
@@ -432,35 +447,43 @@ struct Patch {
             }
             __syncwarp();
             if (n > 0) {
-                // every 16-byte chunk of those rows in flight at once (one round
-                // trip); the write-back then reads them from the tile
-                const int total = n * kChunks;
-                for (int k = lane; k < total; k += 32) {
-                    const int q = k / kChunks, c = k % kChunks;
-                    const int p = pos[q];
-                    const int rit = p - t * kBlockN;
-                    if (rit >= 0 && rit < kBlockN && p < P.L) {
-                        const int64_t src =
-                            ((static_cast<int64_t>(w.b) * P.r_max + cur + q) * P.Hkv + w.g) * D + c * 8;
-                        cp_async_16(tile + (c / 8) * C::kCol + rit * 128 + (((c % 8) ^ (rit & 7)) << 4),
-                                    fresh + src);
+                if (n == kBlockN) {
+                    // a whole tile of fresh rows (128 distinct positions inside it,
+                    // so 128 consecutive fresh rows): one TMA box per column block
+                    if (lane == 0) {
+                        mbar_expect_tx(S.bar(bar), C::kTile);
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_load_4d(tile + c * C::kCol, fresh128, S.bar(bar), c * 64, w.g, cur, w.b);
                     }
-                }
-                cp_async_wait_all();
-                __syncwarp();
-                if (writer) {
-                    for (int k = lane; k < total; k += 32) {
-                        const int q = k / kChunks, c = k % kChunks;
-                        const int p = pos[q];
-                        const int rit = p - t * kBlockN;
-                        if (rit >= 0 && rit < kBlockN && p < P.L) {
-                            const uint4 x = ld_shared_v4(tile + (c / 8) * C::kCol + rit * 128 +
-                                                         (((c % 8) ^ (rit & 7)) << 4));
-                            const int64_t at =
-                                ((static_cast<int64_t>(w.b) * P.L + p) * P.Hkv + w.g) * D + c * 8;
-                            *reinterpret_cast<uint4 *>(cache + at) = x;
+                    const bool ok = __all_sync(0xffffffffu, S.wait(bar, uses & 1));
+                    ++uses;
+                    if (!ok) {
+                        pending = true;  // the load may still land: drained on exit
+                        return false;
+                    }
+                } else {
+                    // every 16-byte chunk of those rows in flight at once (one round
+                    // trip).  A lane always moves the same chunk c of rows q0,
+                    // q0 + step, ..., four rows per step so that their addresses are
+                    // computed together.
+                    const int c = lane % kChunks, q0 = lane / kChunks;
+                    const uint32_t col = tile + (c / 8) * C::kCol;
+                    const int64_t row_elems = static_cast<int64_t>(P.Hkv) * D;
+                    const int64_t src0 =
+                        (static_cast<int64_t>(w.b) * P.r_max + cur) * row_elems + w.g * D + c * 8;
+                    for (int qb = q0; qb < n; qb += 4 * step) {
+                        int pq[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) pq[u] = qb + u * step < n ? pos[qb + u * step] : -1;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int rit = pq[u] - t * kBlockN;
+                            if (pq[u] >= 0 && rit >= 0 && rit < kBlockN && pq[u] < P.L)
+                                cp_async_16(col + rit * 128 + (((c % 8) ^ (rit & 7)) << 4),
+                                            fresh + src0 + (qb + u * step) * row_elems);
                         }
                     }
+                    cp_async_wait_all();
                 }
                 __syncwarp();  // pos is rewritten by the next tile
                 cur += n;
@@ -478,23 +501,80 @@ struct Patch {
             if (cur < cnt && cur > vbase) load_window(cur);
         }
         __syncwarp();
+        return true;
     }
+
+    // One thread, when the warp unwinds: let granule loads still in flight land.
+    __device__ void drain(const Sync &S) const
+    {
+        if (pending) S.drain(bar, (uses - 1) & 1);
+    }
+    bool pending = false;
 };
+
+// Whole warp, at the start of the kernel while the first tiles are in flight:
+// this CTA's share of the KV write-back.  The CTAs of a group cover the same key
+// tiles; the fresh rows whose positions fall in those tiles are written to the
+// cache by the group's CTA mt = (row's rank mod n_mt), 16 bytes per lane, four
+// rows per step.  Nothing in this kernel reads a fresh row from the cache (each
+// landed tile is patched from the fresh tensor), so the copies need no ordering
+// against the loads.  A fully recomputed sequence is written back from its
+// tiles instead (see Patch::tile).
+template <int D>
+__device__ void write_back_share(const Params &P, bool is_v)
+{
+    constexpr int kChunks = D / 8;
+    constexpr int step = 32 / kChunks;
+    const int lane = threadIdx.x & 31;
+    const int c = lane % kChunks, q0 = lane / kChunks;
+    const __nv_bfloat16 *fresh = is_v ? P.v_new : P.k_new;
+    __nv_bfloat16 *cache = is_v ? P.v_cache : P.k_cache;
+    const int64_t row_elems = static_cast<int64_t>(P.Hkv) * D;
+    const Range r = my_range(P);
+    for (int k = 0; k < r.count; ++k) {
+        const Piece w = piece_at(P, r, k);  // inactive pieces included: their rows are shared too
+        if (w.t1 <= w.t0 || w.cnt == 0 || piece_dense(P, w)) continue;
+        const int32_t *idx = P.idx + static_cast<int64_t>(w.b) * P.idx_stride;
+        const int j0 = lower_bound_warp(idx, w.cnt, w.t0 * kBlockN);
+        const int j1 = lower_bound_warp(idx, w.cnt, w.t1 * kBlockN);
+        const int64_t src0 = static_cast<int64_t>(w.b) * P.r_max * row_elems + w.g * D + c * 8;
+        const int64_t dst0 = static_cast<int64_t>(w.b) * P.L * row_elems + w.g * D + c * 8;
+        // rows j0 + mt, j0 + mt + n_mt, ... of this CTA; lane group q0 takes every step-th
+        for (int jb = j0 + w.mt + q0 * P.n_mt; jb < j1; jb += 4 * step * P.n_mt) {
+            int jj[4], pp[4];
+            uint4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                jj[u] = jb + u * step * P.n_mt;
+                pp[u] = jj[u] < j1 ? __ldg(idx + jj[u]) : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (pp[u] >= 0 && pp[u] < P.L)
+                    x[u] = __ldg(reinterpret_cast<const uint4 *>(fresh + src0 + jj[u] * row_elems));
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (pp[u] >= 0 && pp[u] < P.L)
+                    *reinterpret_cast<uint4 *>(cache + dst0 + static_cast<int64_t>(pp[u]) * row_elems) = x[u];
+        }
+    }
+}
 
 // QK issuer warp: per piece Q into TMEM; then per tile, once its K tile landed,
 // the whole warp patches the fresh K rows into it, and one thread issues
 // S = Q K^T into one of the two S buffers once the PV product of the tile two
 // back (which read its P from that buffer) completed.
 template <int D>
-__device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem,
-                          const CUtensorMap *tm_k, int *pos)
+__device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem, int *pos,
+                          const CUtensorMap *tm_kn, const CUtensorMap *tm_k)
 {
     using C = Cfg<D>;
     constexpr uint32_t kIdescQK = idesc_bf16(kBlockM, kBlockN, false, false);
     const int lane = threadIdx.x & 31;
     const Range r = my_range(P);
     Patch<D> pt;
-    pt.stored = false;
+    pt.init(B_KPATCH, pos, tm_kn, tm_k);
+    write_back_share<D>(P, false);
     uint32_t T = 0, it = 0;
     bool ok = true;
     for (int k = 0; k < r.count && ok; ++k) {
@@ -518,13 +598,14 @@ __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        pt.start(P, w, true, pos);
+        pt.start(P, w, true);
         for (int t = w.t0; t < w.t1; ++t, ++T) {
             const int s = T % C::kKStages, sb = T & 1;
             ok = __all_sync(0xffffffffu, S.wait(B_KFULL + s, (T / C::kKStages) & 1));
             if (!ok) break;
             const uint32_t kbase = sbase + C::kOffK + s * C::kTile;
-            pt.tile(P, w, t, kbase, false, tm_k);
+            ok = pt.tile(P, S, w, t, kbase, false);
+            if (!ok) break;
             if (lane == 0) {
                 if (T >= 2) ok = S.wait(B_SFREE + sb, ((T >> 1) - 1) & 1);
                 if (ok) {
@@ -548,6 +629,7 @@ __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
         // everything issued has completed before TMEM is released
         umma_commit(S.bar(B_DRAIN));
         S.drain(B_DRAIN, 0);
+        pt.drain(S);
         if (pt.stored) bulk_wait_all();
     }
     __syncwarp();
@@ -558,27 +640,29 @@ __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
 // wrote P over its S buffer; the first tile of a piece overwrites O.  The
 // product's completion frees the V stage and the S buffer.
 template <int D>
-__device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem,
-                          const CUtensorMap *tm_v, int *pos)
+__device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem, int *pos,
+                          const CUtensorMap *tm_vn, const CUtensorMap *tm_v)
 {
     using C = Cfg<D>;
     constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, false, true);
     const int lane = threadIdx.x & 31;
     const Range r = my_range(P);
     Patch<D> pt;
-    pt.stored = false;
+    pt.init(B_VPATCH, pos, tm_vn, tm_v);
+    write_back_share<D>(P, true);
     uint32_t T = 0;
     bool ok = true;
     for (int k = 0; k < r.count && ok; ++k) {
         const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
-        pt.start(P, w, false, pos);
+        pt.start(P, w, false);
         for (int t = w.t0; t < w.t1; ++t, ++T) {
             const int s = T % C::kVStages, sb = T & 1;
             ok = __all_sync(0xffffffffu, S.wait(B_VFULL + s, (T / C::kVStages) & 1));
             if (!ok) break;
             const uint32_t vbase = sbase + C::kOffV + s * C::kTile;
-            pt.tile(P, w, t, vbase, true, tm_v);
+            ok = pt.tile(P, S, w, t, vbase, true);
+            if (!ok) break;
             if (lane == 0) {
                 ok = S.wait(B_PFULL + sb, (T >> 1) & 1);
                 if (ok) {
@@ -601,6 +685,7 @@ __device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
     if (lane == 0) {
         umma_commit(S.bar(B_DRAIN2));
         S.drain(B_DRAIN2, 0);
+        pt.drain(S);
         if (pt.stored) bulk_wait_all();
     }
     __syncwarp();
@@ -662,6 +747,46 @@ __device__ __forceinline__ float2 ld_cg_v2(const float2 *p)
     return v;
 }
 
+// Row maximum of a tile's 128 raw scores (eight independent chains).
+__device__ __forceinline__ float row_max(const uint32_t (&sr)[4][32])
+{
+    float mx4[4];
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        float a = __uint_as_float(sr[cc][0]), b = __uint_as_float(sr[cc][1]);
+#pragma unroll
+        for (int j = 2; j < 32; j += 4) {
+            a = fmax3(a, __uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1]));
+            b = fmax3(b, __uint_as_float(sr[cc][j + 2]), __uint_as_float(sr[cc][j + 3]));
+        }
+        mx4[cc] = fmaxf(a, b);
+    }
+    return fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+}
+
+// p = 2^{y}, y = s c - m c, for a tile's 128 scores: two-wide FMA and adds into
+// four partial sums, P packed as bf16 pairs.
+__device__ __forceinline__ void exp_tile(const uint32_t (&sr)[4][32], uint64_t c2, float nmc,
+                                          uint64_t (&acc2)[4], uint32_t (&pk)[64])
+{
+    const uint64_t nmc2 = f2x2(nmc, nmc);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc2[k] = 0ull;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            const uint64_t y2 =
+                ffma2(f2x2(__uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1])), c2, nmc2);
+            float y0, y1;
+            x2f(y2, y0, y1);
+            const float p0 = ex2(y0), p1 = ex2(y1);
+            acc2[(j >> 1) & 3] = fadd2(acc2[(j >> 1) & 3], f2x2(p0, p1));
+            pk[(cc * 32 + j) >> 1] = pack_bf16x2(p0, p1);
+        }
+    }
+}
+
 // The owner of a split unit waits until its contributors released their
 // partials (bounded; a timeout aborts the CTA like any other wait).  All four
 // softmax warps call it, whatever their own state (`ok` false: a wait of this
@@ -701,7 +826,6 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = P.scale_log2;           // log2 units per raw score unit
-    const float move = 8.f / c;             // raw-score growth that moves the reference
     const int kv_tail = P.L - (P.n_tiles - 1) * kBlockN;  // keys in the last tile
     const Range r = my_range(P);
     uint32_t T = 0;
@@ -731,45 +855,22 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
                     for (int j = 0; j < 32; ++j)
                         if (cc * 32 + j >= kv_tail) sr[cc][j] = __float_as_uint(-INFINITY);
             }
-            // row maximum of the raw scores (scale > 0 keeps the order)
-            float mx4[4];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                float a = __uint_as_float(sr[cc][0]), b = __uint_as_float(sr[cc][1]);
-#pragma unroll
-                for (int j = 2; j < 32; j += 4) {
-                    a = fmax3(a, __uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1]));
-                    b = fmax3(b, __uint_as_float(sr[cc][j + 2]), __uint_as_float(sr[cc][j + 3]));
-                }
-                mx4[cc] = fmaxf(a, b);
-            }
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            // The reference m moves only when a score exceeds it by more than 8 in
+            // log2 units (then O is rescaled once the previous PV product is done).
+            const float mx = row_max(sr);  // scale > 0 keeps the order
             float m_use = m_run, alpha = 1.f;
             bool rescale = false;
-            if (mx > m_run + move) {  // p would exceed 2^8: move the reference
+            if ((mx - m_run) * c > 8.f) {
                 m_use = mx;
                 alpha = ex2((m_run - mx) * c);
                 rescale = t > w.t0;
             }
-            // p = 2^{(s - m) c}: two-wide FMA and adds, four partial sums; P as bf16
-            // pairs over the first half of this S buffer, where the PV product reads it
             const uint64_t c2 = f2x2(c, c);
-            const float nmc = -m_use * c;
-            const uint64_t nmc2 = f2x2(nmc, nmc);
-            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+            uint64_t acc2[4];
             uint32_t pk[64];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const uint64_t y2 = ffma2(f2x2(__uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1])),
-                                              c2, nmc2);
-                    float y0, y1;
-                    x2f(y2, y0, y1);
-                    const float p0 = ex2(y0), p1 = ex2(y1);
-                    acc2[(j >> 1) & 3] = fadd2(acc2[(j >> 1) & 3], f2x2(p0, p1));
-                    pk[(cc * 32 + j) >> 1] = pack_bf16x2(p0, p1);
-                }
+            exp_tile(sr, c2, -m_use * c, acc2, pk);
+            // P (bf16 pairs) over the first half of this S buffer, where the PV
+            // product reads it
             tmem_st32(scol, *reinterpret_cast<const uint32_t(*)[32]>(pk));
             tmem_st32(scol + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
             float rs0, rs1, rs2, rs3, rs4, rs5, rs6, rs7;
@@ -966,9 +1067,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        qk_issuer<D>(P, S, sbase, tmem, &tm_k, reinterpret_cast<int *>(smem + C::kOffPos));
+        qk_issuer<D>(P, S, sbase, tmem, reinterpret_cast<int *>(smem + C::kOffPos), &tm_kn, &tm_k);
     } else if (warp == 7) {
-        pv_issuer<D>(P, S, sbase, tmem, &tm_v, reinterpret_cast<int *>(smem + C::kOffPos) + 128);
+        pv_issuer<D>(P, S, sbase, tmem, reinterpret_cast<int *>(smem + C::kOffPos) + 128, &tm_vn, &tm_v);
     } else {
         softmax_epilogue<D>(P, S, tmem);
     }

@@ -72,10 +72,12 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
 
 // ---- proxies / fences ----
 // 16 bytes global -> shared without a register round trip (L2 only); many may be
-// in flight per thread.  cp_async_wait_all makes the thread's copies visible to it.
+// in flight per thread.  cp_async_wait_all (a compiler memory barrier) makes the
+// thread's copies visible to it; the copies themselves do not fence other
+// memory accesses, so the compiler may overlap their address arithmetic.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src));
 }
 __device__ __forceinline__ void cp_async_wait_all()
 {
@@ -84,7 +86,7 @@ __device__ __forceinline__ void cp_async_wait_all()
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
 {
     uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr));
     return v;
