@@ -28,24 +28,25 @@
 // set is 0 .. L-1) loads its tiles from the fresh K/V directly, and its mt = 0
 // CTAs store every tile to the cache with a TMA store.
 //
-// Warp roles (256 threads):
+// Warp roles (384 threads):
 //   warp 0     TMA producer of Q (one tile per piece) and K tiles; warp 6 of V
 //              tiles (128-byte swizzle, rings of stages);
-//   warp 1     TMEM allocation; Q into TMEM (tcgen05.cp); per K tile the whole
-//              warp patches the fresh rows into it (cp.async, one round trip)
-//              and writes them back to the cache, or stores the tile for a full
-//              refresh; then one thread issues S = Q K^T (tcgen05.mma) into one
-//              of two TMEM S buffers once the PV product that read that buffer's
-//              P has completed;
-//   warp 7     the same patching for each V tile, then O += P V into the TMEM O
+//   warp 1     TMEM allocation; at the start its share of the K write-back;
+//              Q into TMEM (tcgen05.cp); per K tile the whole warp patches the
+//              fresh rows into it (a TMA box for a tile of fresh rows, else
+//              cp.async), or stores the tile for a full refresh; then one thread
+//              issues S = Q K^T (tcgen05.mma) into one of two TMEM S buffers once
+//              the PV product that read that buffer's P has completed;
+//   warp 7     the same for V (write-back share, patching), then O += P V into the TMEM O
 //              accumulator: a second issuing thread, so the next tile's QK never
 //              queues behind this tile's PV;
-//   warps 2-5  one thread per query row: online softmax in the log2 domain on S
-//              read by tcgen05.ld (the whole row in registers, one round trip
-//              per tile; the reference maximum moves only when it grows by more
-//              than 8 in log2 units, rescaling O in TMEM), P as bf16 over the
-//              first half of the same S buffer (the PV product reads its A
-//              operand there), and the piece's epilogue.
+//   warps 2-5, 8-11  softmax, two warps per quarter of the TMEM lanes: one row per
+//              thread and half a tile's score columns per warp (the two halves
+//              agree on the row maximum through shared memory); online softmax in
+//              the log2 domain on S read by tcgen05.ld (the reference maximum moves
+//              only when it grows by more than 8 in log2 units, rescaling O in
+//              TMEM), P as bf16 over the first half of the same S buffer (the PV
+//              product reads its A operand there), and the piece's epilogue.
 // Every wait is bounded; a timeout sets EC_DEV_TIMEOUT and unwinds.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -64,8 +65,10 @@ using namespace ptx;
 
 constexpr int kBlockM = 128;   // query rows per unit = TMEM lanes
 constexpr int kBlockN = 128;   // keys per tile
-constexpr int kThreads = 256;  // 8 warps
-constexpr int kSoftmaxBarrier = 1;  // named barrier of the 4 softmax warps
+constexpr int kThreads = 384;  // 12 warps
+constexpr int kSoftmaxThreads = 256;  // 8 softmax warps
+constexpr int kSoftmaxBarrier = 1;  // named barrier of the softmax warps
+constexpr int kPairBarrier0 = 2;    // named barriers 2-5: the two softmax warps of a TMEM lane quarter
 constexpr int kMaxContrib = 8;      // contributors merged by one owner at most
 
 template <int D>
@@ -80,9 +83,10 @@ struct Cfg {
     static constexpr uint32_t kOffK = kOffQ + kQBufs * kTile;
     static constexpr uint32_t kOffV = kOffK + kKStages * kTile;
     static constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
-    static constexpr uint32_t kOffMisc = kOffBar + 512;
-    static constexpr uint32_t kOffPos = kOffMisc + 64;  // [2][128] positions of a tile's fresh rows
-    static constexpr uint32_t kBytes = kOffPos + 2 * 128 * 4 + 1024;  // + slack to align the base to 1 KB
+    static constexpr uint32_t kOffMisc = kOffBar + 256;
+    static constexpr uint32_t kOffRows = kOffMisc + 64;   // [2][128] tile rows of a tile's fresh rows (K, V)
+    static constexpr uint32_t kOffXchg = kOffRows + 256;  // [2][128] row maxima / sums of the two column halves
+    static constexpr uint32_t kBytes = kOffXchg + 2 * 128 * 4 + 1024;  // + slack to align the base to 1 KB
     static constexpr uint32_t kTmemCols = 512;
     // two S buffers, columns [0, 128) and [128, 256); P (bf16 pairs) of a tile
     // overwrites the first 64 columns of its own S buffer
@@ -99,7 +103,7 @@ enum : int {
     B_QFULL = 16,    // [2] Q tile landed
     B_QEMPTY = 18,   // [2] Q tile copied into TMEM
     B_SFULL = 20,    // [2] S buffer written by its QK product
-    B_PFULL = 22,    // [2] P written over its S buffer (and O corrected): 4 softmax warps
+    B_PFULL = 22,    // [2] P written over its S buffer (and O corrected): 8 softmax warps
     B_SFREE = 24,    // [2] the PV product that read the buffer's P completed (O updated)
     B_DRAIN = 26,    // QK issuer's products all complete
     B_DRAIN2 = 27,   // PV issuer's products all complete
@@ -107,7 +111,7 @@ enum : int {
     B_VPATCH = 29,   // fresh V granules landed in the current V tile
     B_COUNT = 30
 };
-static_assert(8 * B_COUNT <= 512, "barrier area");
+static_assert(8 * B_COUNT <= 256, "barrier area");
 
 struct Params {
     const __nv_bfloat16 *k_new, *v_new;
@@ -357,15 +361,15 @@ struct Patch {
     int bar;             // index of this warp's mbarrier for the granule loads
     uint32_t uses;       // its phases used so far
     const int32_t *idx;
-    int *pos;            // shared [128]: positions of the current tile's fresh rows
+    uint8_t *rows;       // shared [128]: tile rows of the current tile's fresh rows (255: none)
     const CUtensorMap *fresh128, *cache128;
 
-    __device__ void init(int bar_, int *pos_smem, const CUtensorMap *f128, const CUtensorMap *c128)
+    __device__ void init(int bar_, uint8_t *rows_smem, const CUtensorMap *f128, const CUtensorMap *c128)
     {
         stored = false;
         bar = bar_;
         uses = 0;
-        pos = pos_smem;
+        rows = rows_smem;
         fresh128 = f128;
         cache128 = c128;
     }
@@ -432,7 +436,7 @@ struct Patch {
         bool patched = false;
         for (;;) {
             // the entries cur .. cur + n - 1 of the window fall in this tile: their
-            // positions to shared memory, in order
+            // rows in the tile to shared memory, in order
             int n = 0;
             {
                 const int vv[4] = {v0, v1, v2, v3};
@@ -441,7 +445,10 @@ struct Patch {
                     const int e = vbase + 32 * k + lane;
                     const bool in = e >= cur && vv[k] < tile_end;
                     const unsigned m = __ballot_sync(0xffffffffu, in);
-                    if (in) pos[e - cur] = vv[k];
+                    if (in) {
+                        const int rit = vv[k] - t * kBlockN;
+                        rows[e - cur] = rit >= 0 && rit < kBlockN ? static_cast<uint8_t>(rit) : uint8_t(255);
+                    }
                     n += __popc(m);
                 }
             }
@@ -472,20 +479,20 @@ struct Patch {
                     const int64_t src0 =
                         (static_cast<int64_t>(w.b) * P.r_max + cur) * row_elems + w.g * D + c * 8;
                     for (int qb = q0; qb < n; qb += 4 * step) {
-                        int pq[4];
+                        int rq[4];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) pq[u] = qb + u * step < n ? pos[qb + u * step] : -1;
+                        for (int u = 0; u < 4; ++u) rq[u] = qb + u * step < n ? rows[qb + u * step] : 255;
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            const int rit = pq[u] - t * kBlockN;
-                            if (pq[u] >= 0 && rit >= 0 && rit < kBlockN && pq[u] < P.L)
+                            const int rit = rq[u];
+                            if (rit < kBlockN && t * kBlockN + rit < P.L)
                                 cp_async_16(col + rit * 128 + (((c % 8) ^ (rit & 7)) << 4),
                                             fresh + src0 + (qb + u * step) * row_elems);
                         }
                     }
                     cp_async_wait_all();
                 }
-                __syncwarp();  // pos is rewritten by the next tile
+                __syncwarp();  // rows is rewritten by the next tile
                 cur += n;
                 patched = true;
             }
@@ -565,7 +572,7 @@ __device__ void write_back_share(const Params &P, bool is_v)
 // S = Q K^T into one of the two S buffers once the PV product of the tile two
 // back (which read its P from that buffer) completed.
 template <int D>
-__device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem, int *pos,
+__device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem, uint8_t *rows,
                           const CUtensorMap *tm_kn, const CUtensorMap *tm_k)
 {
     using C = Cfg<D>;
@@ -573,7 +580,7 @@ __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
     const int lane = threadIdx.x & 31;
     const Range r = my_range(P);
     Patch<D> pt;
-    pt.init(B_KPATCH, pos, tm_kn, tm_k);
+    pt.init(B_KPATCH, rows, tm_kn, tm_k);
     write_back_share<D>(P, false);
     uint32_t T = 0, it = 0;
     bool ok = true;
@@ -640,7 +647,7 @@ __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
 // wrote P over its S buffer; the first tile of a piece overwrites O.  The
 // product's completion frees the V stage and the S buffer.
 template <int D>
-__device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem, int *pos,
+__device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem, uint8_t *rows,
                           const CUtensorMap *tm_vn, const CUtensorMap *tm_v)
 {
     using C = Cfg<D>;
@@ -648,7 +655,7 @@ __device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
     const int lane = threadIdx.x & 31;
     const Range r = my_range(P);
     Patch<D> pt;
-    pt.init(B_VPATCH, pos, tm_vn, tm_v);
+    pt.init(B_VPATCH, rows, tm_vn, tm_v);
     write_back_share<D>(P, true);
     uint32_t T = 0;
     bool ok = true;
@@ -721,7 +728,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
 }
 __device__ __forceinline__ void softmax_sync()
 {
-    asm volatile("bar.sync %0, %1;" ::"n"(kSoftmaxBarrier), "n"(128) : "memory");
+    asm volatile("bar.sync %0, %1;" ::"n"(kSoftmaxBarrier), "n"(kSoftmaxThreads) : "memory");
 }
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
 {
@@ -745,46 +752,6 @@ __device__ __forceinline__ float2 ld_cg_v2(const float2 *p)
     float2 v;
     asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
     return v;
-}
-
-// Row maximum of a tile's 128 raw scores (eight independent chains).
-__device__ __forceinline__ float row_max(const uint32_t (&sr)[4][32])
-{
-    float mx4[4];
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-        float a = __uint_as_float(sr[cc][0]), b = __uint_as_float(sr[cc][1]);
-#pragma unroll
-        for (int j = 2; j < 32; j += 4) {
-            a = fmax3(a, __uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1]));
-            b = fmax3(b, __uint_as_float(sr[cc][j + 2]), __uint_as_float(sr[cc][j + 3]));
-        }
-        mx4[cc] = fmaxf(a, b);
-    }
-    return fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-}
-
-// p = 2^{y}, y = s c - m c, for a tile's 128 scores: two-wide FMA and adds into
-// four partial sums, P packed as bf16 pairs.
-__device__ __forceinline__ void exp_tile(const uint32_t (&sr)[4][32], uint64_t c2, float nmc,
-                                          uint64_t (&acc2)[4], uint32_t (&pk)[64])
-{
-    const uint64_t nmc2 = f2x2(nmc, nmc);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) acc2[k] = 0ull;
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-            const uint64_t y2 =
-                ffma2(f2x2(__uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1])), c2, nmc2);
-            float y0, y1;
-            x2f(y2, y0, y1);
-            const float p0 = ex2(y0), p1 = ex2(y1);
-            acc2[(j >> 1) & 3] = fadd2(acc2[(j >> 1) & 3], f2x2(p0, p1));
-            pk[(cc * 32 + j) >> 1] = pack_bf16x2(p0, p1);
-        }
-    }
 }
 
 // The owner of a split unit waits until its contributors released their
@@ -817,47 +784,114 @@ __device__ bool wait_contributions(const Params &P, const Sync &S, int unit, int
     return s_ok != 0;
 }
 
+// Softmax warps: 8 of them, two per quarter of the 128 TMEM lanes.  The warp of
+// half 0 (warps 2-5) takes score columns 0-63 of its 32 rows, the warp of half 1
+// (warps 8-11) columns 64-127, so two warps of each SM sub-partition share the
+// exponentials and hide each other's latencies.  The two halves of a row agree on
+// the row maximum through shared memory (one pair barrier per tile) and so keep
+// the same reference m; each keeps its own partial row sum and its own half of
+// O's columns, and the halves' sums are added at the end of a piece.
+__device__ __forceinline__ void pair_sync(int quarter)
+{
+    asm volatile("bar.sync %0, 64;" ::"r"(kPairBarrier0 + quarter) : "memory");
+}
+
+// Row maximum of half a tile's raw scores (four independent chains).
+__device__ __forceinline__ float row_max64(const uint32_t (&sr)[2][32])
+{
+    float mx2[2];
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        float a = __uint_as_float(sr[cc][0]), b = __uint_as_float(sr[cc][1]);
+#pragma unroll
+        for (int j = 2; j < 32; j += 4) {
+            a = fmax3(a, __uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1]));
+            b = fmax3(b, __uint_as_float(sr[cc][j + 2]), __uint_as_float(sr[cc][j + 3]));
+        }
+        mx2[cc] = fmaxf(a, b);
+    }
+    return fmaxf(mx2[0], mx2[1]);
+}
+
+// p = 2^{y}, y = s c - m c, for half a tile's 64 scores: two-wide FMA and adds
+// into four partial sums, P packed as bf16 pairs.
+__device__ __forceinline__ void exp_half(const uint32_t (&sr)[2][32], uint64_t c2, float nmc,
+                                         uint64_t (&acc2)[4], uint32_t (&pk)[32])
+{
+    const uint64_t nmc2 = f2x2(nmc, nmc);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc2[k] = 0ull;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            const uint64_t y2 =
+                ffma2(f2x2(__uint_as_float(sr[cc][j]), __uint_as_float(sr[cc][j + 1])), c2, nmc2);
+            float y0, y1;
+            x2f(y2, y0, y1);
+            const float p0 = ex2(y0), p1 = ex2(y1);
+            acc2[(j >> 1) & 3] = fadd2(acc2[(j >> 1) & 3], f2x2(p0, p1));
+            pk[(cc * 32 + j) >> 1] = pack_bf16x2(p0, p1);
+        }
+    }
+}
+
 template <int D>
-__device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
+__device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, float *xchg)
 {
     using C = Cfg<D>;
+    constexpr int kOChunks = D / 64;  // 32-column chunks of O per half
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = warp >= 8 ? 1 : 0;
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const float c = P.scale_log2;           // log2 units per raw score unit
+    float *x_own = xchg + half * kBlockM + row;
+    const float *x_other = xchg + (1 - half) * kBlockM + row;
+    const float c = P.scale_log2;  // log2 units per raw score unit
     const int kv_tail = P.L - (P.n_tiles - 1) * kBlockN;  // keys in the last tile
     const Range r = my_range(P);
     uint32_t T = 0;
     bool ok = true;
     // After a failed (timed-out) wait a warp skips all further work; every later
-    // wait of any role returns at once (the abort flag is set).
+    // wait of any role returns at once (the abort flag is set).  Both warps of a
+    // pair always reach the same pair barriers.
     for (int k = 0; k < r.count; ++k) {
         const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
-        float m_run = -INFINITY, l_run = 0.f;  // m in raw score units
+        float m_run = -INFINITY, l_run = 0.f;  // m in raw score units; l of this half
         for (int t = w.t0; t < w.t1; ++t, ++T) {
             const int sb = T & 1;
             if (ok) ok = __all_sync(0xffffffffu, S.wait(B_SFULL + sb, (T >> 1) & 1));
-            if (!ok) continue;
             tc_fence_after();
-            const uint32_t scol = tmem + lane_off + C::kColS + sb * kBlockN;
-            // the whole row of S in registers: one round trip to TMEM per tile
-            uint32_t sr[4][32];
+            const uint32_t scol = tmem + lane_off + C::kColS + sb * kBlockN + half * 64;
+            uint32_t sr[2][32];
+            float pmax = -INFINITY;
+            if (ok) {
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_ld32(scol + cc * 32, sr[cc]);
+                for (int cc = 0; cc < 2; ++cc) tmem_ld32(scol + cc * 32, sr[cc]);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_wait_ld(sr[cc]);
-            if (t == P.n_tiles - 1 && kv_tail < kBlockN) {  // keys past L do not exist
+                for (int cc = 0; cc < 2; ++cc) tmem_wait_ld(sr[cc]);
+                const int live = kv_tail - half * 64;  // keys of this half in the last tile
+                if (t == P.n_tiles - 1 && live < 64) {  // keys past L do not exist
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
+                    for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (cc * 32 + j >= kv_tail) sr[cc][j] = __float_as_uint(-INFINITY);
+                        for (int j = 0; j < 32; ++j)
+                            if (cc * 32 + j >= live) sr[cc][j] = __float_as_uint(-INFINITY);
+                }
+                pmax = row_max64(sr);  // scale > 0 keeps the order
             }
+            // the row maximum from both halves (the partner read our previous value
+            // before the first barrier)
+            pair_sync(quarter);
+            *x_own = pmax;
+            pair_sync(quarter);
+            const float mx = fmaxf(pmax, *x_other);
+            if (!ok) continue;
             // The reference m moves only when a score exceeds it by more than 8 in
-            // log2 units (then O is rescaled once the previous PV product is done).
-            const float mx = row_max(sr);  // scale > 0 keeps the order
+            // log2 units (then O is rescaled once the previous PV product is done);
+            // both halves take the same decision.
             float m_use = m_run, alpha = 1.f;
             bool rescale = false;
             if ((mx - m_run) * c > 8.f) {
@@ -865,14 +899,12 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
                 alpha = ex2((m_run - mx) * c);
                 rescale = t > w.t0;
             }
-            const uint64_t c2 = f2x2(c, c);
             uint64_t acc2[4];
-            uint32_t pk[64];
-            exp_tile(sr, c2, -m_use * c, acc2, pk);
+            uint32_t pk[32];
+            exp_half(sr, f2x2(c, c), -m_use * c, acc2, pk);
             // P (bf16 pairs) over the first half of this S buffer, where the PV
-            // product reads it
-            tmem_st32(scol, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-            tmem_st32(scol + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+            // product reads it: this half's 64 probabilities in 32 columns
+            tmem_st32(tmem + lane_off + C::kColS + sb * kBlockN + half * 32, pk);
             float rs0, rs1, rs2, rs3, rs4, rs5, rs6, rs7;
             x2f(acc2[0], rs0, rs1);
             x2f(acc2[1], rs2, rs3);
@@ -883,23 +915,22 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
             m_run = m_use;
 
             // O may be rescaled only after the previous tile's PV product completed
-            // (the completion that freed the other S buffer)
+            // (the completion that freed the other S buffer); each half its columns
             if (rescale) {
                 const uint32_t Tp = T - 1;
                 ok = __all_sync(0xffffffffu, S.wait(B_SFREE + (Tp & 1), (Tp >> 1) & 1));
                 if (!ok) continue;
                 tc_fence_after();
 #pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
+                for (int cc = 0; cc < kOChunks; ++cc) {
                     uint32_t o[32];
-                    const uint32_t ta = tmem + lane_off + C::kColO + cc * 32;
+                    const uint32_t ta = tmem + lane_off + C::kColO + (half * kOChunks + cc) * 32;
                     tmem_ld32(ta, o);
                     tmem_wait_ld(o);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
                     tmem_st32(ta, o);
                 }
-                tmem_wait_st();
             }
             // the P stores (and any O correction) complete before the PV product reads them
             tmem_wait_st();
@@ -913,6 +944,11 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
             ok = __all_sync(0xffffffffu, S.wait(B_SFREE + (Tp & 1), (Tp >> 1) & 1));
         }
         tc_fence_after();
+        // the row sum of both halves (same reference m)
+        pair_sync(quarter);
+        *x_own = l_run;
+        pair_sync(quarter);
+        const float l_row = l_run + *x_other;
         const int tok = w.mt * P.tok_per_tile + row / P.G;
         const bool valid = row < P.tok_per_tile * P.G && tok < w.cnt;
         const int h = w.g * P.G + row % P.G;
@@ -922,7 +958,7 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
             if (ok) {
                 float4 *po = P.part_o + (static_cast<int64_t>(w.unit) * P.slots + w.slot) * (D / 4) * kBlockM;
 #pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
+                for (int cc = half * kOChunks; cc < (half + 1) * kOChunks; ++cc) {
                     uint32_t o[32];
                     tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
                     tmem_wait_ld(o);
@@ -934,9 +970,9 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
                                                __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3])));
                     }
                 }
-                if (valid)
+                if (valid && half == 0)
                     __stcg(P.part_ml + (static_cast<int64_t>(w.unit) * P.slots + w.slot) * kBlockM + row,
-                           make_float2(m_run, l_run));
+                           make_float2(m_run, l_row));
                 __threadfence();
             }
             tc_fence_before();
@@ -947,7 +983,7 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
             continue;
         }
         // whole unit or owner: out = (wo O + sum_s ws_s O_s) / (wo l + sum_s ws_s l_s),
-        // every term scaled to M, the largest of the maxima
+        // every term scaled to M, the largest of the maxima; each half its columns
         int n = 0;
         if (w.role == ROLE_OWNER) {
             ok = wait_contributions(P, S, w.unit, w.n_contrib, ok);  // every softmax warp
@@ -965,8 +1001,8 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
         float M = m_run;
         for (int s = 0; s < n; ++s)
             if (valid) M = fmaxf(M, ld_cg_v2(mlp + static_cast<int64_t>(s) * kBlockM).x);
-        const float wo = l_run > 0.f ? ex2((m_run - M) * c) : 0.f;
-        float l = wo * l_run;
+        const float wo = l_row > 0.f ? ex2((m_run - M) * c) : 0.f;
+        float l = wo * l_row;
         for (int s = 0; s < n; ++s) {
             float ls;
             const float ws = weight(s, M, ls);
@@ -974,7 +1010,7 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem)
         }
         const float inv = 1.f / l;
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = half * kOChunks; cc < (half + 1) * kOChunks; ++cc) {
             uint32_t o[32];
             tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
             tmem_wait_ld(o);
@@ -1035,7 +1071,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         for (int i = 0; i < B_COUNT; ++i)
-            mbar_init(S.bar(i), (i == B_PFULL || i == B_PFULL + 1) ? 4u : 1u);
+            mbar_init(S.bar(i), (i == B_PFULL || i == B_PFULL + 1) ? 8u : 1u);
         fence_mbar_init();
     }
     // Q rows past tok_per_tile * G are never loaded: keep them zero
@@ -1067,11 +1103,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        qk_issuer<D>(P, S, sbase, tmem, reinterpret_cast<int *>(smem + C::kOffPos), &tm_kn, &tm_k);
+        qk_issuer<D>(P, S, sbase, tmem, smem + C::kOffRows, &tm_kn, &tm_k);
     } else if (warp == 7) {
-        pv_issuer<D>(P, S, sbase, tmem, reinterpret_cast<int *>(smem + C::kOffPos) + 128, &tm_vn, &tm_v);
+        pv_issuer<D>(P, S, sbase, tmem, smem + C::kOffRows + 128, &tm_vn, &tm_v);
     } else {
-        softmax_epilogue<D>(P, S, tmem);
+        softmax_epilogue<D>(P, S, tmem, reinterpret_cast<float *>(smem + C::kOffXchg));
     }
     __syncthreads();
     if (warp == 1) {
