@@ -52,6 +52,8 @@ def lib():
                                      i32, i32, i32, i32, i32]
         L.orc_attention.argtypes = [vp, vp, vp, ctypes.c_int, vp, i32, i32, i32, i32, i32, i32,
                                     f64, vp, i64, vp]
+        L.orc_attention_simsd.argtypes = [vp, vp, vp, ctypes.c_int, vp, i64, vp, vp, vp, i32, i32,
+                                          i32, i32, i32, i32, f64, vp, i64, vp]
         L.orc_embed_rows.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, i32, i32,
                                      i32, i32, vp]
         L.orc_projection.argtypes = [vp, vp, ctypes.c_int, i64, i32, i32, vp, i64, vp]
@@ -60,7 +62,8 @@ def lib():
         L.orc_get_threads.argtypes = []
         L.orc_get_threads.restype = ctypes.c_int
         for fn in (L.orc_row_stats, L.orc_unmask_gate, L.orc_recompute_set,
-                   L.orc_scatter_kv, L.orc_attention, L.orc_embed_rows, L.orc_projection):
+                   L.orc_scatter_kv, L.orc_attention, L.orc_attention_simsd, L.orc_embed_rows,
+                   L.orc_projection):
             fn.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -184,6 +187,35 @@ def attention(q, k_cache, v_cache, count, scale, samples=None):
         out = np.empty((ns, d), np.float64)
     _check(lib().orc_attention(_p(qq), _p(kc), _p(vc), dt, _p(cnt), batch, seq_len, r_max, h,
                                hkv, d, float(scale), _p(sp), ns, _p(out)), "attention")
+    return out
+
+
+def attention_simsd(q, k_cache, v_cache, idx, count, section, tau, scale, samples=None):
+    """float64 attention under SimSD's temporal causal mask (``oracle.c``,
+    ``orc_attention_simsd``).  ``idx`` [B, >= r_max] gives each query row's
+    position, ``section`` uint8 and ``tau`` int32 [B, L] the layout.  Same output
+    shapes as :func:`attention`."""
+    qq = np.ascontiguousarray(q)
+    kc = np.ascontiguousarray(k_cache)
+    vc = np.ascontiguousarray(v_cache)
+    ix = np.ascontiguousarray(idx, np.int32)
+    cnt = np.ascontiguousarray(count, np.int32)
+    sec = np.ascontiguousarray(section, np.uint8)
+    tl = np.ascontiguousarray(tau, np.int32)
+    batch, r_max, h, d = qq.shape
+    seq_len, hkv = kc.shape[1], kc.shape[2]
+    assert sec.shape == (batch, seq_len) and tl.shape == (batch, seq_len)
+    dt = _dtype_of(qq)
+    if samples is None:
+        out = np.full((batch, r_max, h, d), np.nan, np.float64)
+        sp, ns = None, 0
+    else:
+        sp = np.ascontiguousarray(samples, np.int32).reshape(-1, 3)
+        ns = sp.shape[0]
+        out = np.empty((ns, d), np.float64)
+    _check(lib().orc_attention_simsd(_p(qq), _p(kc), _p(vc), dt, _p(ix), ix.shape[-1], _p(cnt),
+                                     _p(sec), _p(tl), batch, seq_len, r_max, h, hkv, d,
+                                     float(scale), _p(sp), ns, _p(out)), "attention_simsd")
     return out
 
 

@@ -527,3 +527,147 @@ int orc_projection(const void *x, const void *w, int dtype, int64_t n_rows, int3
     }
     return status;
 }
+
+/*
+ * Attention under SimSD's token-level temporal causal mask ("SimSD - Simple
+ * Speculative Decoding in Diffusion Language Models", Italian technical summary
+ * (gist.science/it/paper/2606.02544), section "Metodologia: SimSD", items
+ * 1 "Layout di Input" and 2 "Maschera di Attenzione Temporale").
+ *
+ * Each position j of a sequence lies in one section: 0 = prompt, 1 = data
+ * section D (reference tokens), 2 = mask section (prediction slots); data and
+ * mask positions carry a step label tau[j] >= 1 (the step map; a data position
+ * and its paired mask slot share one label).  Key j is visible to the query at
+ * position i when
+ *   - j is in the prompt (every query), or
+ *   - i is a mask slot and either j is a data position with tau[j] < tau[i]
+ *     (revealed at an earlier step) or j is a mask slot with tau[j] >= tau[i]
+ *     (the page's two rules), or
+ *   - i is a data position and j a data position with tau[j] <= tau[i]
+ *     (reading: reference tokens see the prompt and the references revealed
+ *     no later than themselves, no prediction slot), or
+ *   - nothing else: a prompt query sees the prompt only (reading).
+ * The output is softmax over the visible keys only; a query with no visible
+ * key gets a zero row (reading; the rules above never leave one empty).
+ *
+ * The query row r of sequence b sits at position idx[b*idx_stride + r]; the
+ * caches already hold the fresh rows.  Layouts as in orc_attention; section
+ * and tau are [batch, seq_len].
+ */
+static int simsd_visible(uint8_t sec_i, int32_t tau_i, uint8_t sec_j, int32_t tau_j)
+{
+    if (sec_j == 0)
+        return 1;
+    if (sec_i == 2)
+        return sec_j == 1 ? tau_j < tau_i : tau_j >= tau_i;
+    if (sec_i == 1)
+        return sec_j == 1 && tau_j <= tau_i;
+    return 0;
+}
+
+static void attention_simsd_one(const void *q, const void *k_cache, const void *v_cache,
+                                int dtype, const uint8_t *section, const int32_t *tau,
+                                int32_t pos, int32_t seq_len, int32_t r_max, int32_t n_heads,
+                                int32_t n_kv_heads, int32_t head_dim, double scale, int32_t b,
+                                int32_t r, int32_t h, double *s, double *o)
+{
+    const int32_t group = n_heads / n_kv_heads;
+    const int32_t g = h / group;
+    const int64_t qoff = (((int64_t)b * r_max + r) * n_heads + h) * head_dim;
+    const uint8_t *sec = section + (int64_t)b * seq_len;
+    const int32_t *tl = tau + (int64_t)b * seq_len;
+
+    double m = -INFINITY;
+    for (int32_t j = 0; j < seq_len; ++j) {
+        s[j] = -INFINITY;
+        if (!simsd_visible(sec[pos], tl[pos], sec[j], tl[j]))
+            continue;
+        const int64_t koff = (((int64_t)b * seq_len + j) * n_kv_heads + g) * head_dim;
+        double dot = 0.0;
+        for (int32_t e = 0; e < head_dim; ++e)
+            dot += load(q, dtype, qoff + e) * load(k_cache, dtype, koff + e);
+        s[j] = scale * dot;
+        if (s[j] > m)
+            m = s[j];
+    }
+    for (int32_t e = 0; e < head_dim; ++e)
+        o[e] = 0.0;
+    if (m == -INFINITY)
+        return;
+    double z = 0.0;
+    for (int32_t j = 0; j < seq_len; ++j) {
+        s[j] = s[j] == -INFINITY ? 0.0 : exp(s[j] - m);
+        z += s[j];
+    }
+    for (int32_t j = 0; j < seq_len; ++j) {
+        if (s[j] == 0.0)
+            continue;
+        const int64_t voff = (((int64_t)b * seq_len + j) * n_kv_heads + g) * head_dim;
+        const double w = s[j] / z;
+        for (int32_t e = 0; e < head_dim; ++e)
+            o[e] += w * load(v_cache, dtype, voff + e);
+    }
+}
+
+int orc_attention_simsd(const void *q, const void *k_cache, const void *v_cache, int dtype,
+                        const int32_t *idx, int64_t idx_stride, const int32_t *count,
+                        const uint8_t *section, const int32_t *tau, int32_t batch,
+                        int32_t seq_len, int32_t r_max, int32_t n_heads, int32_t n_kv_heads,
+                        int32_t head_dim, double scale, const int32_t *samples,
+                        int64_t n_samples, double *out)
+{
+    if (!dtype_ok(dtype))
+        return ORC_BAD_DTYPE;
+    if (batch < 0 || seq_len <= 0 || r_max < 0 || idx_stride < r_max || n_heads <= 0 ||
+        n_kv_heads <= 0 || head_dim <= 0 || n_heads % n_kv_heads != 0)
+        return ORC_BAD_ARG;
+    for (int64_t j = 0; j < (int64_t)batch * seq_len; ++j)
+        if (section[j] > 2 || (section[j] != 0 && tau[j] < 1))
+            return ORC_BAD_ARG;
+    for (int32_t b = 0; b < batch; ++b) {
+        if (count[b] < 0 || count[b] > r_max)
+            return ORC_BAD_ARG;
+        for (int32_t r = 0; r < count[b]; ++r) {
+            const int32_t p = idx[b * idx_stride + r];
+            if (p < 0 || p >= seq_len)
+                return ORC_BAD_ARG;
+        }
+    }
+    if (samples)
+        for (int64_t t = 0; t < n_samples; ++t) {
+            const int32_t b = samples[3 * t], r = samples[3 * t + 1], h = samples[3 * t + 2];
+            if (b < 0 || b >= batch || r < 0 || r >= count[b] || h < 0 || h >= n_heads)
+                return ORC_BAD_ARG;
+        }
+    const int64_t total = samples ? n_samples : (int64_t)batch * r_max * n_heads;
+    int status = ORC_OK;
+#pragma omp parallel num_threads(g_threads)
+    {
+        double *s = (double *)malloc((size_t)seq_len * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < total; ++t) {
+            int32_t b, r, h;
+            if (samples) {
+                b = samples[3 * t];
+                r = samples[3 * t + 1];
+                h = samples[3 * t + 2];
+            } else {
+                b = (int32_t)(t / ((int64_t)r_max * n_heads));
+                r = (int32_t)((t / n_heads) % r_max);
+                h = (int32_t)(t % n_heads);
+                if (r >= count[b])
+                    continue;
+            }
+            if (!s) {
+#pragma omp atomic write
+                status = ORC_NOMEM;
+                continue;
+            }
+            attention_simsd_one(q, k_cache, v_cache, dtype, section, tau,
+                                idx[b * idx_stride + r], seq_len, r_max, n_heads, n_kv_heads,
+                                head_dim, scale, b, r, h, s, out + t * head_dim);
+        }
+        free(s);
+    }
+    return status;
+}
