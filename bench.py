@@ -53,7 +53,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # the same bench command (dram__bytes_read.sum + dram__bytes_write.sum summed over
 # the call's kernels, per launch).  Used only while the kernel sources hash to the
 # value they had when the counters were taken.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {
+    # `bench.py --steps 20 --warmup 3 --e2e-steps 100 --cpu-seconds 0.1 --no-lmhead
+    # --no-simsd`, mean of two launches; the decode call is both of its kernels
+    ("batched", "attention"): {"bytes": 39198208, "sources": "058d5b051c9f9f86"},
+    ("batched", "decode"): {"bytes": 156044032, "sources": "058d5b051c9f9f86"},
+}
 
 
 def kernel_sources_hash() -> str:
@@ -105,6 +110,8 @@ def parse_args(argv=None):
     p.add_argument("--eager", action="store_true", help="time eager launches, not graph replays")
     p.add_argument("--no-lmhead", action="store_true",
                    help="skip the LM-head fused decode-and-gate part")
+    p.add_argument("--no-simsd", action="store_true",
+                   help="leave out the SimSD masked-attention part")
     p.add_argument("--cpu-seconds", type=float, default=8.0,
                    help="CPU time budget of each oracle baseline sample (one core, all cores)")
     return p.parse_args(argv)
@@ -487,6 +494,10 @@ def run_ours(args, workload=None):
         out_parts["lmhead_gate"] = lmhead_part(nat, w, st, device, stream, flush, min(K, 50), tc,
                                                hbm, args.seed)
 
+    if w.attn_dtype == synth.BF16 and not args.no_simsd:
+        out_parts["simsd_attention"] = simsd_part(nat, device, stream, flush, min(K, 200), tc, hbm,
+                                                  args.seed)
+
     cpu = None
     if rank == 0 and world == 1:
         cpu = cpu_baseline(w, st, logits, att, args.cpu_seconds, geo)
@@ -582,6 +593,62 @@ def lmhead_part(nat, w: synth.Workload, st, device, stream, flush, K, tc_peak, h
             "unfused_us": {"cublas_gemm": t_gemm, "decode_gate": t_dec, "total": t_gemm + t_dec},
             "speedup_vs_unfused": (t_gemm + t_dec) / t_fused, "launches": 1,
             "device_status": status, "inputs": "Gaussian bf16 (hidden N(0,1), W_lm N(0, 4/hidden))"}
+
+
+def simsd_part(nat, device, stream, flush, K, tc_peak, hbm_peak, seed):
+    """The attention call under SimSD's temporal causal mask on its verification
+    workload (32 sequences, 1024-token prompt, data and mask sections of 8), and
+    the unmasked call on the same inputs for the cost of the mask."""
+    import torch
+    w = synth.SIMSD
+    r = 2 * w.block
+    rng = np.random.default_rng(seed + 202)
+    section, tau, idx, cnt = synth.make_simsd_layout(rng, w.batch, w.prompt_len, w.block)
+    a = synth.make_attention(rng, w, r)
+    up = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(device)  # noqa: E731
+    as_bf16 = lambda x: up(x.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    q, kn, vn, kc, vc = (as_bf16(x) for x in (a.q, a.k_new, a.v_new, a.k_cache, a.v_cache))
+    out = torch.empty_like(q)
+    ws = nat.new_workspace(nat.ec_attention_workspace_size(w.batch, w.seq_len, r, w.n_heads,
+                                                           w.n_kv_heads, w.head_dim), device)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    # the prepared calls hold raw pointers: every tensor they use stays referenced here
+    idx_d, cnt_d, sec_d, tau_d = up(idx), up(cnt), up(section), up(tau)
+    masked = nat.prepare_selective_attention_simsd(q, kn, vn, idx_d, cnt_d, sec_d, tau_d, kc, vc,
+                                                   out, scale, ws, stream=stream)
+    plain = nat.prepare_selective_attention(q, kn, vn, idx_d, cnt_d, kc, vc, out, scale, ws,
+                                            stream=stream)
+
+    def timed(fn):
+        e0 = torch.cuda.Event(enable_timing=True, external=True)
+        e1 = torch.cuda.Event(enable_timing=True, external=True)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            e0.record()
+            fn()
+            e1.record()
+        for _ in range(3):
+            flush()
+            g.replay()
+        tot = 0.0
+        for _ in range(K):
+            flush()
+            g.replay()
+            e1.synchronize()
+            tot += e0.elapsed_time(e1) / 1e3
+        return tot / K * 1e6
+
+    t_m = timed(masked)
+    t_p = timed(plain)
+    status = nat.ec_read_device_status(ws)
+    B, L, H, Hkv, d = w.batch, w.seq_len, w.n_heads, w.n_kv_heads, w.head_dim
+    nbytes = (2 * B * L * Hkv * d + 2 * B * r * H * d + 4 * B * r * Hkv * d) * 2
+    gbs = nbytes / t_m / 1e3
+    return {"us": t_m, "gbs": gbs, "frac_hbm": gbs / hbm_peak, "algorithmic_bytes": nbytes,
+            "tflops": 4.0 * B * r * L * H * d / t_m / 1e6, "unmasked_us": t_p,
+            "launches": 1, "device_status": status,
+            "config": {"batch": B, "prompt": w.prompt_len, "sections": w.block, "seq_len": L,
+                       "query_rows": r, "n_heads": H, "n_kv_heads": Hkv, "head_dim": d}}
 
 
 def run_e2e(step: GpuStep, geo, w, logits, att, K, W, world):

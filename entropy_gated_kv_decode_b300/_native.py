@@ -24,13 +24,14 @@ DEV_BAD_ROW_POS = 0x2
 DEV_BAD_COUNT = 0x4
 DEV_BAD_INDEX = 0x8
 DEV_TIMEOUT = 0x10
+DEV_BAD_LABEL = 0x20
 
 EXPORTED = ("ec_status_str", "ec_abi_version", "ec_debug_set_wait_limit", "ec_workspace_init",
             "ec_read_device_status",
             "ec_decode_workspace_size", "ec_decode_step", "ec_decode_step_noalloc",
             "ec_decode_noalloc_read_status", "ec_lmhead_workspace_size", "ec_lmhead_decode_step",
             "ec_build_recompute_set", "ec_attention_workspace_size", "ec_attention_kernel_count",
-            "ec_selective_attention",
+            "ec_selective_attention", "ec_selective_attention_simsd",
             "ec_embed_rows", "ec_qkv_projection")
 
 
@@ -81,6 +82,9 @@ def lib() -> ctypes.CDLL:
         L.ec_attention_kernel_count.restype = i32
         L.ec_selective_attention.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, ctypes.c_int,
                                              i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
+        L.ec_selective_attention_simsd.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp,
+                                                   ctypes.c_int, i32, i32, i32, i32, i32, i32, f32,
+                                                   vp, sz, vp]
         L.ec_embed_rows.argtypes = [vp, i64, i32, vp, i64, vp, vp, vp, i32, i32, i32, i32, vp, vp,
                                     sz, vp]
         L.ec_qkv_projection.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, sz, vp]
@@ -88,7 +92,7 @@ def lib() -> ctypes.CDLL:
                      "ec_decode_step",
                      "ec_decode_step_noalloc", "ec_decode_noalloc_read_status",
                      "ec_lmhead_decode_step", "ec_build_recompute_set",
-                     "ec_selective_attention",
+                     "ec_selective_attention", "ec_selective_attention_simsd",
                      "ec_embed_rows", "ec_qkv_projection"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -344,6 +348,26 @@ def ec_selective_attention(q, k_new, v_new, idx, count, k_cache, v_cache, out, s
     _check(lib().ec_selective_attention(*args, _stream(stream)), "ec_selective_attention")
 
 
+def _simsd_args(q, k_new, v_new, idx, count, section, tau, k_cache, v_cache, out, scale,
+                workspace):
+    a = _attention_args(q, k_new, v_new, idx, count, k_cache, v_cache, out, scale, workspace)
+    _cuda("section", section, torch.uint8)
+    _cuda("tau", tau, torch.int32)
+    if section.shape != k_cache.shape[:2] or tau.shape != k_cache.shape[:2]:
+        raise ValueError("section and tau must be [batch, seq_len]")
+    return a[:6] + [_p(section), _p(tau)] + a[6:]
+
+
+def ec_selective_attention_simsd(q, k_new, v_new, idx, count, section, tau, k_cache, v_cache,
+                                 out, scale, workspace, stream=None):
+    """ec_selective_attention under SimSD's temporal causal mask: section uint8 and
+    tau int32 [B, L] (0 prompt, 1 data, 2 mask slot; step labels >= 1)."""
+    args = _simsd_args(q, k_new, v_new, idx, count, section, tau, k_cache, v_cache, out, scale,
+                       workspace)
+    _check(lib().ec_selective_attention_simsd(*args, _stream(stream)),
+           "ec_selective_attention_simsd")
+
+
 def _embed_args(table, idx, count, seq_tokens, is_masked, mask_id, x, workspace):
     _cuda("table", table, torch.bfloat16)
     _cuda("idx", idx, torch.int32)
@@ -401,10 +425,13 @@ def ec_qkv_projection(x, count, w_qkv, q, k, v, workspace, stream=None):
 
 
 class Prepared:
-    """A C-ABI call whose arguments are already validated and converted."""
+    """A C-ABI call whose arguments are already validated and converted.  It holds
+    raw device pointers, so it also keeps a reference to every object it was
+    prepared from (``keep``): the tensors cannot be freed while the call lives."""
 
-    def __init__(self, name, args, stream):
+    def __init__(self, name, args, stream, keep=()):
         self.name = name
+        self._keep = tuple(keep)
         self.fn = getattr(lib(), name)
         args = list(args) + [_stream(stream)]
         # pre-convert every argument to its ctypes type so a call converts nothing
@@ -423,26 +450,37 @@ class Prepared:
 
 def prepare_decode_step(*args, stream=None, **kwargs):
     """ec_decode_step bound to fixed buffers; ``.set_step(t)`` changes the step index."""
-    p = Prepared("ec_decode_step", _decode_args(*args, **kwargs), stream)
+    p = Prepared("ec_decode_step", _decode_args(*args, **kwargs), stream,
+                 keep=(args, kwargs))
     p.set_step = lambda t: p.set_arg(11, int(t))
     return p
 
 
 def prepare_lmhead_decode_step(*args, stream=None, **kwargs):
-    return Prepared("ec_lmhead_decode_step", _lmhead_args(*args, **kwargs), stream)
+    return Prepared("ec_lmhead_decode_step", _lmhead_args(*args, **kwargs), stream,
+                    keep=(args, kwargs))
 
 
 def prepare_build_recompute_set(*args, stream=None, **kwargs):
-    return Prepared("ec_build_recompute_set", _recompute_args(*args, **kwargs), stream)
+    return Prepared("ec_build_recompute_set", _recompute_args(*args, **kwargs), stream,
+                    keep=(args, kwargs))
 
 
 def prepare_selective_attention(*args, stream=None, **kwargs):
-    return Prepared("ec_selective_attention", _attention_args(*args, **kwargs), stream)
+    return Prepared("ec_selective_attention", _attention_args(*args, **kwargs), stream,
+                    keep=(args, kwargs))
+
+
+def prepare_selective_attention_simsd(*args, stream=None, **kwargs):
+    return Prepared("ec_selective_attention_simsd", _simsd_args(*args, **kwargs), stream,
+                    keep=(args, kwargs))
 
 
 def prepare_embed_rows(*args, stream=None, **kwargs):
-    return Prepared("ec_embed_rows", _embed_args(*args, **kwargs), stream)
+    return Prepared("ec_embed_rows", _embed_args(*args, **kwargs), stream,
+                    keep=(args, kwargs))
 
 
 def prepare_qkv_projection(*args, stream=None, **kwargs):
-    return Prepared("ec_qkv_projection", _projection_args(*args, **kwargs), stream)
+    return Prepared("ec_qkv_projection", _projection_args(*args, **kwargs), stream,
+                    keep=(args, kwargs))

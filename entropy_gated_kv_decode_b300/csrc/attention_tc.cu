@@ -133,6 +133,10 @@ struct Params {
     uint32_t *flags;      // [n_units] contributions released (the owner resets it to 0)
     float2 *part_ml;      // [n_units][slots][128] (m, l), m in raw score units
     float4 *part_o;       // [n_units][slots][D / 4][128] unnormalised O
+    // SimSD's temporal causal mask (null without it): section (0 prompt, 1 data,
+    // 2 mask slot) and step label of every position, [B, L] each
+    const uint8_t *section;
+    const int32_t *tau;
 };
 
 enum : int { ROLE_WHOLE = 0, ROLE_CONTRIB = 1, ROLE_OWNER = 2 };
@@ -836,7 +840,46 @@ __device__ __forceinline__ void exp_half(const uint32_t (&sr)[2][32], uint64_t c
     }
 }
 
-template <int D>
+// SimSD's temporal causal mask as label windows.  Every key gets one integer
+// label and every query a closed window; the key is visible to the query when
+// its label lies in the window:
+//   key   prompt 0          data tau            mask slot tau - 2^30
+//   query prompt [0, 0]      data [0, tau]       mask slot [tau - 2^30, tau - 1]
+// A mask slot's window holds the prompt, the data labels below its own step and
+// the slot labels of its step and later ones; a data token's holds the prompt and
+// the data labels up to its own step; a prompt token's only the prompt.  Labels
+// must lie in [1, 2^30): anything else marks the key hidden (and the query's
+// window empty) and raises EC_DEV_BAD_LABEL.
+constexpr int kSlotBase = 1 << 30;
+
+__device__ __forceinline__ int simsd_key_label(const Params &P, int b, int j, bool &bad)
+{
+    const int64_t o = static_cast<int64_t>(b) * P.L + j;
+    const int sec = __ldg(P.section + o);
+    if (sec == 0) return 0;
+    const int t = __ldg(P.tau + o);
+    if (sec > 2 || t < 1 || t >= kSlotBase) {
+        bad = true;
+        return INT_MIN;
+    }
+    return sec == 1 ? t : t - kSlotBase;
+}
+
+__device__ __forceinline__ int2 simsd_window(const Params &P, int b, int pos, bool &bad)
+{
+    if (pos < 0 || pos >= P.L) return make_int2(1, 0);  // an index the K side flags
+    const int64_t o = static_cast<int64_t>(b) * P.L + pos;
+    const int sec = __ldg(P.section + o);
+    if (sec == 0) return make_int2(0, 0);
+    const int t = __ldg(P.tau + o);
+    if (sec > 2 || t < 1 || t >= kSlotBase) {
+        bad = true;
+        return make_int2(1, 0);
+    }
+    return sec == 1 ? make_int2(0, t) : make_int2(t - kSlotBase, t - 1);
+}
+
+template <int D, bool kMasked>
 __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, float *xchg)
 {
     using C = Cfg<D>;
@@ -860,8 +903,26 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, 
         const Piece w = piece_at(P, r, k);
         if (!piece_active(P, w)) continue;
         float m_run = -INFINITY, l_run = 0.f;  // m in raw score units; l of this half
+        int2 win = make_int2(INT_MIN, INT_MAX);  // rows past the unit's tokens see all
+        bool bad_label = false;
+        if constexpr (kMasked) {
+            const int tok = w.mt * P.tok_per_tile + row / P.G;
+            if (row < P.tok_per_tile * P.G && tok < w.cnt)
+                win = simsd_window(P, w.b, __ldg(P.idx + w.b * P.idx_stride + tok), bad_label);
+        }
         for (int t = w.t0; t < w.t1; ++t, ++T) {
             const int sb = T & 1;
+            // the labels of this half's 64 keys (two per lane) and their range,
+            // loaded while the product runs
+            int lab0 = 0, lab1 = 0, lab_lo = 0, lab_hi = 0;
+            if constexpr (kMasked) {
+                const int j0 = t * kBlockN + half * 64 + lane;
+                const bool in0 = j0 < P.L, in1 = j0 + 32 < P.L;
+                if (in0) lab0 = simsd_key_label(P, w.b, j0, bad_label);
+                if (in1) lab1 = simsd_key_label(P, w.b, j0 + 32, bad_label);
+                lab_lo = __reduce_min_sync(0xffffffffu, min(in0 ? lab0 : INT_MAX, in1 ? lab1 : INT_MAX));
+                lab_hi = __reduce_max_sync(0xffffffffu, max(in0 ? lab0 : INT_MIN, in1 ? lab1 : INT_MIN));
+            }
             if (ok) ok = __all_sync(0xffffffffu, S.wait(B_SFULL + sb, (T >> 1) & 1));
             tc_fence_after();
             const uint32_t scol = tmem + lane_off + C::kColS + sb * kBlockN + half * 64;
@@ -879,6 +940,20 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, 
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             if (cc * 32 + j >= live) sr[cc][j] = __float_as_uint(-INFINITY);
+                }
+                if constexpr (kMasked) {
+                    // a row whose window misses part of the keys' label range
+                    // hides those keys; the labels go round the warp
+                    const bool all_in = win.x <= lab_lo && lab_hi <= win.y;
+                    if (__any_sync(0xffffffffu, !all_in)) {
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const int lab = __shfl_sync(0xffffffffu, cc ? lab1 : lab0, j);
+                                if (lab < win.x || lab > win.y) sr[cc][j] = __float_as_uint(-INFINITY);
+                            }
+                    }
                 }
                 pmax = row_max64(sr);  // scale > 0 keeps the order
             }
@@ -901,7 +976,10 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, 
             }
             uint64_t acc2[4];
             uint32_t pk[32];
-            exp_half(sr, f2x2(c, c), -m_use * c, acc2, pk);
+            float nmc = -m_use * c;
+            if constexpr (kMasked)
+                if (m_use == -INFINITY) nmc = 0.f;  // every key so far hidden: all p = 0
+            exp_half(sr, f2x2(c, c), nmc, acc2, pk);
             // P (bf16 pairs) over the first half of this S buffer, where the PV
             // product reads it: this half's 64 probabilities in 32 columns
             tmem_st32(tmem + lane_off + C::kColS + sb * kBlockN + half * 32, pk);
@@ -944,6 +1022,8 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, 
             ok = __all_sync(0xffffffffu, S.wait(B_SFREE + (Tp & 1), (Tp >> 1) & 1));
         }
         tc_fence_after();
+        if constexpr (kMasked)
+            if (__any_sync(0xffffffffu, bad_label) && lane == 0) flag_status(P.status, EC_DEV_BAD_LABEL);
         // the row sum of both halves (same reference m)
         pair_sync(quarter);
         *x_own = l_run;
@@ -1008,7 +1088,7 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, 
             const float ws = weight(s, M, ls);
             l = fmaf(ws, ls, l);
         }
-        const float inv = 1.f / l;
+        const float inv = kMasked ? (l > 0.f ? 1.f / l : 0.f) : 1.f / l;  // no visible key: zeros
 #pragma unroll 1
         for (int cc = half * kOChunks; cc < (half + 1) * kOChunks; ++cc) {
             uint32_t o[32];
@@ -1049,7 +1129,7 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, 
     }
 }
 
-template <int D>
+template <int D, bool kMasked>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_tc_kernel(const Params P, const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -1107,7 +1187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 7) {
         pv_issuer<D>(P, S, sbase, tmem, smem + C::kOffRows + 128, &tm_vn, &tm_v);
     } else {
-        softmax_epilogue<D>(P, S, tmem, reinterpret_cast<float *>(smem + C::kOffXchg));
+        softmax_epilogue<D, kMasked>(P, S, tmem, reinterpret_cast<float *>(smem + C::kOffXchg));
     }
     __syncthreads();
     if (warp == 1) {
@@ -1218,8 +1298,11 @@ cudaError_t launch_typed(const Params &p, const Plan &plan, const void *q, cudaS
         !encode_4d(&tkn, p.k_new, p.B, fresh_rows, p.r_max, p.Hkv, D, 1, kBlockN) ||
         !encode_4d(&tvn, p.v_new, p.B, fresh_rows, p.r_max, p.Hkv, D, 1, kBlockN))
         return cudaErrorInvalidValue;
-    return launch(attention_tc_kernel<D>, dim3(plan.grid), dim3(kThreads), Cfg<D>::kBytes, stream, p,
-                  tq, tk, tv, tkn, tvn);
+    if (p.section)
+        return launch(attention_tc_kernel<D, true>, dim3(plan.grid), dim3(kThreads), Cfg<D>::kBytes,
+                      stream, p, tq, tk, tv, tkn, tvn);
+    return launch(attention_tc_kernel<D, false>, dim3(plan.grid), dim3(kThreads), Cfg<D>::kBytes,
+                  stream, p, tq, tk, tv, tkn, tvn);
 }
 
 }  // namespace
@@ -1247,7 +1330,8 @@ cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_
                                 void *k_cache, void *v_cache, void *out, int32_t batch,
                                 int32_t seq_len, int32_t r_max, int32_t n_heads,
                                 int32_t n_kv_heads, int32_t head_dim, float scale,
-                                void *workspace, cudaStream_t stream)
+                                void *workspace, cudaStream_t stream, const uint8_t *section,
+                                const int32_t *tau)
 {
     if (r_max == 0) return cudaSuccess;  // nothing to recompute, nothing to write back
     const Plan plan = make_plan(batch, seq_len, r_max, n_heads, n_kv_heads);
@@ -1284,6 +1368,8 @@ cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_
     p.flags = reinterpret_cast<uint32_t *>(ws + o_f);
     p.part_ml = reinterpret_cast<float2 *>(ws + o_ml);
     p.part_o = reinterpret_cast<float4 *>(ws + o_o);
+    p.section = section;
+    p.tau = tau;
     return head_dim == 128 ? launch_typed<128>(p, plan, q, stream)
                            : launch_typed<64>(p, plan, q, stream);
 }

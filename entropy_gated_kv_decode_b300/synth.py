@@ -125,6 +125,38 @@ WORKLOADS = {
 }
 
 
+# SimSD verification under its temporal causal mask: 32 sequences, each a
+# 1024-token prompt followed by a data section and a mask section of B = 8
+# positions (L = 1040); the 16 data and mask positions are the recomputed query
+# rows; GQA 32/8 heads, d = 128, bf16 N(0, 1/sqrt(d)).  The decode fields are
+# unused.
+SIMSD = Workload("simsd", batch=32, seq_len=1040, prompt_len=1024, block=8, active_block=0,
+                 vocab=151936, logits_dtype=BF16, near_uniform_frac=0.0, n_unmask=1, k=0,
+                 tau=0.5, n_heads=32, n_kv_heads=8, head_dim=128, attn_dtype=BF16,
+                 qkv_std=_INV_SQRT_128)
+
+
+def make_simsd_layout(rng: np.random.Generator, batch: int, prompt_len: int,
+                      blk: int) -> tuple[np.ndarray, np.ndarray, np.ndarray, np.ndarray]:
+    """SimSD's input layout: ``(section, tau, idx, count)``.  Each sequence is a
+    prompt of ``prompt_len`` positions (section 0), a data section and a mask
+    section of ``blk`` positions each (sections 1 and 2); one random step map (a
+    permutation of 1..blk) per sequence labels both the k-th data position and the
+    k-th mask slot.  The query rows are the ``2 blk`` data and mask positions."""
+    L = prompt_len + 2 * blk
+    section = np.zeros((batch, L), np.uint8)
+    tau = np.zeros((batch, L), np.int32)
+    for b in range(batch):
+        mu = (rng.permutation(blk) + 1).astype(np.int32)
+        section[b, prompt_len:prompt_len + blk] = 1
+        section[b, prompt_len + blk:] = 2
+        tau[b, prompt_len:prompt_len + blk] = mu
+        tau[b, prompt_len + blk:] = mu
+    idx = np.tile(np.arange(prompt_len, L, dtype=np.int32), (batch, 1))
+    count = np.full(batch, 2 * blk, np.int32)
+    return section, tau, idx, count
+
+
 def scaled(w: Workload, **changes) -> Workload:
     """A copy of ``w`` with some fields replaced (smaller parity cases)."""
     return dataclasses.replace(w, **changes)

@@ -61,6 +61,7 @@ typedef enum { EC_F32 = 0, EC_BF16 = 1 } ec_dtype;
 #define EC_DEV_BAD_COUNT 0x4u    /* a recompute count above r_max or seq_len */
 #define EC_DEV_BAD_INDEX 0x8u    /* an index outside [0, seq_len) or not ascending */
 #define EC_DEV_TIMEOUT 0x10u     /* a bounded wait inside a kernel gave up */
+#define EC_DEV_BAD_LABEL 0x20u   /* a SimSD section or step label out of range */
 
 /* Human-readable name of a status code (static string). */
 const char *ec_status_str(int status);
@@ -300,6 +301,42 @@ ec_status ec_selective_attention(const void *q, const void *k_new, const void *v
                                  int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
                                  int32_t n_kv_heads, int32_t head_dim, float scale,
                                  void *workspace, size_t workspace_bytes, ec_stream_t stream);
+
+/*
+ * ec_selective_attention under SimSD's token-level temporal causal mask
+ * ("SimSD - Simple Speculative Decoding in Diffusion Language Models", Italian
+ * technical summary, section "Metodologia: SimSD", items 1 and 2).
+ *
+ * The sequence is a prompt followed by a data section D of reference tokens and
+ * a mask section of prediction slots; section[b, j] is 0 (prompt), 1 (data) or 2
+ * (mask slot) and tau[b, j] the step label of a data or mask position (the step
+ * map; a data token and its paired slot carry the same label; ignored for the
+ * prompt).  The write-back and the attention are those of ec_selective_attention
+ * except that the softmax of query row r (position i = idx[b*idx_stride + r])
+ * runs over the keys j visible to it:
+ *   - every prompt key;
+ *   - for a mask slot i: data keys with tau[j] < tau[i] and slots with
+ *     tau[j] >= tau[i] (the page's rule);
+ *   - for a data token i: data keys with tau[j] <= tau[i] (reading: no slot);
+ *   - for a prompt token i: nothing more (reading).
+ * A row that sees no key is written as zeros.
+ *
+ * section uint8 and tau int32, device, [batch, seq_len] contiguous; labels of data
+ * and mask positions in [1, 2^30).  A label out of range (or a section above 2)
+ * hides that key, empties the window of a query at that position and sets
+ * EC_DEV_BAD_LABEL.  Every other argument, the workspace (same size as
+ * ec_attention_workspace_size) and the errors are those of ec_selective_attention,
+ * but only bf16 with head_dim 64 or 128 is implemented (EC_ERR_UNSUPPORTED
+ * otherwise); one kernel launch.
+ */
+ec_status ec_selective_attention_simsd(const void *q, const void *k_new, const void *v_new,
+                                       const int32_t *idx, int64_t idx_stride,
+                                       const int32_t *count, const uint8_t *section,
+                                       const int32_t *tau, void *k_cache, void *v_cache,
+                                       void *out, ec_dtype dtype, int32_t batch, int32_t seq_len,
+                                       int32_t r_max, int32_t n_heads, int32_t n_kv_heads,
+                                       int32_t head_dim, float scale, void *workspace,
+                                       size_t workspace_bytes, ec_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* the forward that produces the recomputed rows' queries, keys and values    */

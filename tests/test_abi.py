@@ -107,6 +107,29 @@ def test_recompute_set_and_attention_reject_bad_arguments(L):
     assert call(ws=0x10040) == -5
     assert call(wsb=8) == -5
 
+    # the SimSD variant: the same checks, its two label arrays, and bf16 only
+    m = L.ec_selective_attention_simsd
+
+    def call_m(**kw):
+        args = list(base)
+        names = ["q", "kn", "vn", "idx", "stride", "count", "kc", "vc", "out", "dtype", "batch",
+                 "L", "r", "H", "Hkv", "d", "scale", "ws", "wsb", "stream"]
+        for k, v in kw.items():
+            if k in names:
+                args[names.index(k)] = v
+        sec, tau = kw.get("section", 0x20000), kw.get("tau", 0x30000)
+        return m(*args[:6], sec, tau, *args[6:])
+
+    assert call_m(d=96) == -2
+    assert call_m(stride=40) == -2
+    assert call_m(dtype=3) == -3
+    assert call_m(section=None) == -1
+    assert call_m(tau=None) == -1
+    assert call_m(kc=None) == -1
+    assert call_m(dtype=0) == -7  # float32: not implemented for the masked variant
+    assert call_m(q=0x1004) == -4
+    assert call_m(wsb=8) == -5
+
 
 def test_projection_and_gather_reject_bad_arguments(L):
     p = L.ec_qkv_projection
