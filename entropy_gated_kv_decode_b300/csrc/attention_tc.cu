@@ -389,29 +389,52 @@ struct Patch {
     }
 
     // Whole warp, at a piece start.  The K side of one CTA per sequence also
-    // checks the count and the whole index set.
+    // checks the count and the whole index set.  The window starts as the set's
+    // first 128 entries; the cursor (the first entry at or past the piece's first
+    // key) is counted in it when it lies there, so a set of at most 128 entries
+    // costs one round trip to global memory.
     __device__ void start(const Params &P, const Piece &w, bool check)
     {
         const int lane = threadIdx.x & 31;
         idx = P.idx + static_cast<int64_t>(w.b) * P.idx_stride;
         cnt = w.cnt;
-        if (check && w.mt == 0 && w.g == 0 && w.t0 == 0) {
+        const bool checker = check && w.mt == 0 && w.g == 0 && w.t0 == 0;
+        const bool dense = piece_dense(P, w);
+        if (!dense || checker) load_window(0);
+        if (checker) {
             const int c_raw = __ldg(P.count + w.b);
             if (lane == 0 && (c_raw < 0 || c_raw > P.r_max)) flag_status(P.status, EC_DEV_BAD_COUNT);
+            // the window's entries against their predecessors, the rest by loads
             bool bad = false;
-            for (int j = lane; j < w.cnt; j += 32) {
+            const int vv[4] = {v0, v1, v2, v3};
+            int carry = INT_MIN;  // entry 32 k - 1
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int up = __shfl_up_sync(0xffffffffu, vv[k], 1);
+                const int prev = lane == 0 ? carry : up;
+                const int e = 32 * k + lane;
+                if (e < cnt) bad |= vv[k] < 0 || vv[k] >= P.L || (e > 0 && prev >= vv[k]);
+                carry = __shfl_sync(0xffffffffu, vv[k], 31);
+            }
+            for (int j = 128 + lane; j < cnt; j += 32) {
                 const int p = __ldg(idx + j);
-                bad |= p < 0 || p >= P.L || (j > 0 && __ldg(idx + j - 1) >= p);
+                bad |= p < 0 || p >= P.L || __ldg(idx + j - 1) >= p;
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(P.status, EC_DEV_BAD_INDEX);
         }
-        if (piece_dense(P, w)) {
+        if (dense) {
             cur = vbase = 0;
             v0 = v1 = v2 = v3 = INT_MAX;
             return;
         }
-        cur = lower_bound_warp(idx, w.cnt, w.t0 * kBlockN);
-        load_window(cur);
+        const int lo = w.t0 * kBlockN;
+        if (cnt <= 128 || __shfl_sync(0xffffffffu, v3, 31) >= lo) {  // entries are ascending
+            cur = __popc(__ballot_sync(0xffffffffu, v0 < lo)) + __popc(__ballot_sync(0xffffffffu, v1 < lo)) +
+                  __popc(__ballot_sync(0xffffffffu, v2 < lo)) + __popc(__ballot_sync(0xffffffffu, v3 < lo));
+        } else {
+            cur = lower_bound_warp(idx, w.cnt, lo);
+            load_window(cur);
+        }
     }
 
     // Whole warp, tile t of piece w landed at `tile`: the fresh rows that fall in
@@ -523,50 +546,67 @@ struct Patch {
     bool pending = false;
 };
 
-// Whole warp, at the start of the kernel while the first tiles are in flight:
-// this CTA's share of the KV write-back.  The CTAs of a group cover the same key
+// Candidate rows of piece w for this CTA's write-back share: its rows
+// j = mt, mt + n_mt, ... of the index set (none for a fully recomputed sequence,
+// whose tiles are stored whole, see Patch::tile).
+__device__ __forceinline__ int share_rows(const Params &P, const Piece &w)
+{
+    if (w.t1 <= w.t0 || w.cnt <= w.mt || piece_dense(P, w)) return 0;
+    return (w.cnt - w.mt + P.n_mt - 1) / P.n_mt;
+}
+
+// Warps `part` of `n_parts` (whole warps), at the start of the kernel while the
+// first tiles are in flight and before the first scores exist: this CTA's share
+// of the KV write-back, both caches.  The CTAs of a group cover the same key
 // tiles; the fresh rows whose positions fall in those tiles are written to the
-// cache by the group's CTA mt = (row's rank mod n_mt), 16 bytes per lane, four
-// rows per step.  Nothing in this kernel reads a fresh row from the cache (each
-// landed tile is patched from the fresh tensor), so the copies need no ordering
-// against the loads.  A fully recomputed sequence is written back from its
-// tiles instead (see Patch::tile).
+// cache by the group's CTA mt = (row's rank mod n_mt).  The candidate rows of all
+// pieces are laid end to end and dealt one per lane, so a round costs two round
+// trips (the index, then the K and V rows, 16-byte chunks, a whole row per lane).
+// Nothing in this kernel reads a fresh row from the cache (each landed tile is
+// patched from the fresh tensor), so the copies need no ordering against the
+// loads.
 template <int D>
-__device__ void write_back_share(const Params &P, bool is_v)
+__device__ void write_back_share(const Params &P, int part, int n_parts)
 {
     constexpr int kChunks = D / 8;
-    constexpr int step = 32 / kChunks;
     const int lane = threadIdx.x & 31;
-    const int c = lane % kChunks, q0 = lane / kChunks;
-    const __nv_bfloat16 *fresh = is_v ? P.v_new : P.k_new;
-    __nv_bfloat16 *cache = is_v ? P.v_cache : P.k_cache;
     const int64_t row_elems = static_cast<int64_t>(P.Hkv) * D;
     const Range r = my_range(P);
-    for (int k = 0; k < r.count; ++k) {
-        const Piece w = piece_at(P, r, k);  // inactive pieces included: their rows are shared too
-        if (w.t1 <= w.t0 || w.cnt == 0 || piece_dense(P, w)) continue;
-        const int32_t *idx = P.idx + static_cast<int64_t>(w.b) * P.idx_stride;
-        const int j0 = lower_bound_warp(idx, w.cnt, w.t0 * kBlockN);
-        const int j1 = lower_bound_warp(idx, w.cnt, w.t1 * kBlockN);
-        const int64_t src0 = static_cast<int64_t>(w.b) * P.r_max * row_elems + w.g * D + c * 8;
-        const int64_t dst0 = static_cast<int64_t>(w.b) * P.L * row_elems + w.g * D + c * 8;
-        // rows j0 + mt, j0 + mt + n_mt, ... of this CTA; lane group q0 takes every step-th
-        for (int jb = j0 + w.mt + q0 * P.n_mt; jb < j1; jb += 4 * step * P.n_mt) {
-            int jj[4], pp[4];
-            uint4 x[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                jj[u] = jb + u * step * P.n_mt;
-                pp[u] = jj[u] < j1 ? __ldg(idx + jj[u]) : -1;
+    for (int f0 = part * 32;; f0 += n_parts * 32) {
+        // this lane's candidate: piece k, row j
+        int f = f0 + lane, j = -1, k = 0;
+        Piece w;
+        for (; k < r.count; ++k) {
+            w = piece_at(P, r, k);  // inactive pieces included: their rows are shared too
+            const int n = share_rows(P, w);
+            if (f < n) {
+                j = w.mt + f * P.n_mt;
+                break;
             }
+            f -= n;
+        }
+        if (!__any_sync(0xffffffffu, j >= 0)) break;
+        int p = -1;
+        if (j >= 0) {
+            p = __ldg(P.idx + static_cast<int64_t>(w.b) * P.idx_stride + j);
+            if (p < w.t0 * kBlockN || p >= min(w.t1 * kBlockN, P.L)) p = -1;
+        }
+        if (p >= 0) {
+            const int64_t src = (static_cast<int64_t>(w.b) * P.r_max + j) * row_elems + w.g * D;
+            const int64_t dst = (static_cast<int64_t>(w.b) * P.L + p) * row_elems + w.g * D;
+            const uint4 *ks = reinterpret_cast<const uint4 *>(P.k_new + src);
+            const uint4 *vs = reinterpret_cast<const uint4 *>(P.v_new + src);
+            uint4 xk[kChunks], xv[kChunks];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (pp[u] >= 0 && pp[u] < P.L)
-                    x[u] = __ldg(reinterpret_cast<const uint4 *>(fresh + src0 + jj[u] * row_elems));
+            for (int c = 0; c < kChunks; ++c) xk[c] = __ldg(ks + c);
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (pp[u] >= 0 && pp[u] < P.L)
-                    *reinterpret_cast<uint4 *>(cache + dst0 + static_cast<int64_t>(pp[u]) * row_elems) = x[u];
+            for (int c = 0; c < kChunks; ++c) xv[c] = __ldg(vs + c);
+            uint4 *kd = reinterpret_cast<uint4 *>(P.k_cache + dst);
+            uint4 *vd = reinterpret_cast<uint4 *>(P.v_cache + dst);
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) kd[c] = xk[c];
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) vd[c] = xv[c];
         }
     }
 }
@@ -585,7 +625,6 @@ __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
     const Range r = my_range(P);
     Patch<D> pt;
     pt.init(B_KPATCH, rows, tm_kn, tm_k);
-    write_back_share<D>(P, false);
     uint32_t T = 0, it = 0;
     bool ok = true;
     for (int k = 0; k < r.count && ok; ++k) {
@@ -660,7 +699,6 @@ __device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
     const Range r = my_range(P);
     Patch<D> pt;
     pt.init(B_VPATCH, rows, tm_vn, tm_v);
-    write_back_share<D>(P, true);
     uint32_t T = 0;
     bool ok = true;
     for (int k = 0; k < r.count && ok; ++k) {
@@ -1187,6 +1225,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 7) {
         pv_issuer<D>(P, S, sbase, tmem, smem + C::kOffRows + 128, &tm_vn, &tm_v);
     } else {
+        // the eight softmax warps: the write-back share while the first scores are
+        // being produced, then the softmax
+        write_back_share<D>(P, warp < 8 ? warp - 2 : warp - 4, 8);
         softmax_epilogue<D, kMasked>(P, S, tmem, reinterpret_cast<float *>(smem + C::kOffXchg));
     }
     __syncthreads();
