@@ -54,6 +54,8 @@ def lib():
                                     f64, vp, i64, vp]
         L.orc_attention_simsd.argtypes = [vp, vp, vp, ctypes.c_int, vp, i64, vp, vp, vp, i32, i32,
                                           i32, i32, i32, i32, f64, vp, i64, vp]
+        L.orc_attention_cover.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp, i64, vp, vp, i32,
+                                          i32, i32, i32, i32, i32, f64, vp]
         L.orc_embed_rows.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, i32, i32,
                                      i32, i32, vp]
         L.orc_projection.argtypes = [vp, vp, ctypes.c_int, i64, i32, i32, vp, i64, vp]
@@ -62,8 +64,8 @@ def lib():
         L.orc_get_threads.argtypes = []
         L.orc_get_threads.restype = ctypes.c_int
         for fn in (L.orc_row_stats, L.orc_unmask_gate, L.orc_recompute_set,
-                   L.orc_scatter_kv, L.orc_attention, L.orc_attention_simsd, L.orc_embed_rows,
-                   L.orc_projection):
+                   L.orc_scatter_kv, L.orc_attention, L.orc_attention_simsd,
+                   L.orc_attention_cover, L.orc_embed_rows, L.orc_projection):
             fn.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -217,6 +219,30 @@ def attention_simsd(q, k_cache, v_cache, idx, count, section, tau, scale, sample
                                      _p(sec), _p(tl), batch, seq_len, r_max, h, hkv, d,
                                      float(scale), _p(sp), ns, _p(out)), "attention_simsd")
     return out
+
+
+def attention_cover(q, k_new, v_new, k_cache, v_cache, idx, count, seed, scale):
+    """COVER's dual-view attention (``oracle.c``, ``orc_attention_cover``):
+    returns ``(k_cache', v_cache', out)``: the caches after the write-back of the
+    non-seed rows and the float64 outputs ``[B, r_max, H, d]`` (rows past count
+    NaN).  ``seed`` uint8 ``[B, r_max]`` flags the recomputed rows that are seeds."""
+    qq = np.ascontiguousarray(q)
+    kn = np.ascontiguousarray(k_new)
+    vn = np.ascontiguousarray(v_new)
+    kc = np.array(k_cache, copy=True, order="C")
+    vc = np.array(v_cache, copy=True, order="C")
+    ix = np.ascontiguousarray(idx, np.int32)
+    cnt = np.ascontiguousarray(count, np.int32)
+    sd = np.ascontiguousarray(seed, np.uint8)
+    batch, r_max, h, d = qq.shape
+    seq_len, hkv = kc.shape[1], kc.shape[2]
+    assert sd.shape == (batch, r_max)
+    dt = _dtype_of(qq)
+    out = np.empty((batch, r_max, h, d), np.float64)
+    _check(lib().orc_attention_cover(_p(qq), _p(kn), _p(vn), _p(kc), _p(vc), dt, _p(ix),
+                                     ix.shape[-1], _p(cnt), _p(sd), batch, seq_len, r_max, h, hkv,
+                                     d, float(scale), _p(out)), "attention_cover")
+    return kc, vc, out
 
 
 def embed_rows(table, idx, count, tokens, is_masked, mask_id, r_max):

@@ -671,3 +671,119 @@ int orc_attention_simsd(const void *q, const void *k_cache, const void *v_cache,
     }
     return status;
 }
+
+/*
+ * COVER's dual-view attention with the KV-cache override and the diagonal
+ * correction ("Stop the Flip-Flop: Verifica Preservante il Contesto per una
+ * Decodifica di Diffusione Veloce e Revocabile", Italian technical summary
+ * (gist.science/it/paper/2602.06161), section "Metodologia: COVER", item 1
+ * "Dual-View Feed Forward tramite KV Cache Override").
+ *
+ * The recomputed rows r < count[b] of sequence b sit at positions
+ * p_r = idx[b*idx_stride + r]; seed[b*r_max + r] != 0 marks a seed (a decoded
+ * token under verification: its input was [MASK], so k_new / v_new of that row
+ * are the masked-input K/V).  The cache holds the K/V of the previous step.
+ *   - Cache: every non-seed row is written back, cache[p_r] = new[r]; a seed's
+ *     position keeps the previous step's K/V (the override).
+ *   - Attention of row r, head h (kv head g): softmax over all keys j < seq_len of
+ *     the cache after that write-back, except that for a seed row the key at its
+ *     own position p_r is its masked-input k_new[r] / v_new[r] (the diagonal
+ *     correction: no self-leakage of the stored token).
+ * Writes the caches in place (k_cache, v_cache) and the outputs to out
+ * ([batch, r_max, n_heads, head_dim] float64, rows past count NaN).
+ */
+int orc_attention_cover(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                        void *v_cache, int dtype, const int32_t *idx, int64_t idx_stride,
+                        const int32_t *count, const uint8_t *seed, int32_t batch,
+                        int32_t seq_len, int32_t r_max, int32_t n_heads, int32_t n_kv_heads,
+                        int32_t head_dim, double scale, double *out)
+{
+    if (!dtype_ok(dtype))
+        return ORC_BAD_DTYPE;
+    if (batch < 0 || seq_len <= 0 || r_max < 0 || idx_stride < r_max || n_heads <= 0 ||
+        n_kv_heads <= 0 || head_dim <= 0 || n_heads % n_kv_heads != 0)
+        return ORC_BAD_ARG;
+    const size_t esz = dtype_size(dtype);
+    const size_t row_bytes = (size_t)head_dim * esz;
+    for (int32_t b = 0; b < batch; ++b) {
+        if (count[b] < 0 || count[b] > r_max)
+            return ORC_BAD_ARG;
+        for (int32_t r = 0; r < count[b]; ++r) {
+            const int32_t p = idx[b * idx_stride + r];
+            if (p < 0 || p >= seq_len)
+                return ORC_BAD_ARG;
+        }
+    }
+    /* the write-back of the non-seed rows */
+    for (int32_t b = 0; b < batch; ++b)
+        for (int32_t r = 0; r < count[b]; ++r) {
+            if (seed[(int64_t)b * r_max + r])
+                continue;
+            const int32_t p = idx[b * idx_stride + r];
+            for (int32_t g = 0; g < n_kv_heads; ++g) {
+                const int64_t src = (((int64_t)b * r_max + r) * n_kv_heads + g) * head_dim;
+                const int64_t dst = (((int64_t)b * seq_len + p) * n_kv_heads + g) * head_dim;
+                memcpy((char *)k_cache + dst * esz, (const char *)k_new + src * esz, row_bytes);
+                memcpy((char *)v_cache + dst * esz, (const char *)v_new + src * esz, row_bytes);
+            }
+        }
+    const int64_t total = (int64_t)batch * r_max * n_heads;
+    int status = ORC_OK;
+#pragma omp parallel num_threads(g_threads)
+    {
+        double *s = (double *)malloc((size_t)seq_len * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < total; ++t) {
+            const int32_t b = (int32_t)(t / ((int64_t)r_max * n_heads));
+            const int32_t r = (int32_t)((t / n_heads) % r_max);
+            const int32_t h = (int32_t)(t % n_heads);
+            double *o = out + t * head_dim;
+            if (r >= count[b]) {
+                for (int32_t e = 0; e < head_dim; ++e)
+                    o[e] = NAN;
+                continue;
+            }
+            if (!s) {
+#pragma omp atomic write
+                status = ORC_NOMEM;
+                continue;
+            }
+            const int32_t g = h / (n_heads / n_kv_heads);
+            const int is_seed = seed[(int64_t)b * r_max + r] != 0;
+            const int32_t own = idx[b * idx_stride + r];
+            const int64_t qoff = (((int64_t)b * r_max + r) * n_heads + h) * head_dim;
+            const int64_t own_new = (((int64_t)b * r_max + r) * n_kv_heads + g) * head_dim;
+            double m = -INFINITY;
+            for (int32_t j = 0; j < seq_len; ++j) {
+                const int diag = is_seed && j == own;
+                const void *kb = diag ? k_new : k_cache;
+                const int64_t koff =
+                    diag ? own_new : (((int64_t)b * seq_len + j) * n_kv_heads + g) * head_dim;
+                double dot = 0.0;
+                for (int32_t e = 0; e < head_dim; ++e)
+                    dot += load(q, dtype, qoff + e) * load(kb, dtype, koff + e);
+                s[j] = scale * dot;
+                if (s[j] > m)
+                    m = s[j];
+            }
+            double z = 0.0;
+            for (int32_t j = 0; j < seq_len; ++j) {
+                s[j] = exp(s[j] - m);
+                z += s[j];
+            }
+            for (int32_t e = 0; e < head_dim; ++e)
+                o[e] = 0.0;
+            for (int32_t j = 0; j < seq_len; ++j) {
+                const int diag = is_seed && j == own;
+                const void *vb = diag ? v_new : v_cache;
+                const int64_t voff =
+                    diag ? own_new : (((int64_t)b * seq_len + j) * n_kv_heads + g) * head_dim;
+                const double w = s[j] / z;
+                for (int32_t e = 0; e < head_dim; ++e)
+                    o[e] += w * load(vb, dtype, voff + e);
+            }
+        }
+        free(s);
+    }
+    return status;
+}
