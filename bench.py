@@ -110,6 +110,8 @@ def parse_args(argv=None):
     p.add_argument("--eager", action="store_true", help="time eager launches, not graph replays")
     p.add_argument("--no-lmhead", action="store_true",
                    help="skip the LM-head fused decode-and-gate part")
+    p.add_argument("--no-cover", action="store_true",
+                   help="leave out the COVER dual-view attention part")
     p.add_argument("--no-simsd", action="store_true",
                    help="leave out the SimSD masked-attention part")
     p.add_argument("--cpu-seconds", type=float, default=8.0,
@@ -494,6 +496,9 @@ def run_ours(args, workload=None):
         out_parts["lmhead_gate"] = lmhead_part(nat, w, st, device, stream, flush, min(K, 50), tc,
                                                hbm, args.seed)
 
+    if w.attn_dtype == synth.BF16 and not args.no_cover:
+        out_parts["cover_attention"] = cover_part(nat, step, st, w, flush, min(K, 200), hbm, tc,
+                                                  args.seed)
     if w.attn_dtype == synth.BF16 and not args.no_simsd:
         out_parts["simsd_attention"] = simsd_part(nat, device, stream, flush, min(K, 200), tc, hbm,
                                                   args.seed)
@@ -649,6 +654,58 @@ def simsd_part(nat, device, stream, flush, K, tc_peak, hbm_peak, seed):
             "launches": 1, "device_status": status,
             "config": {"batch": B, "prompt": w.prompt_len, "sections": w.block, "seq_len": L,
                        "query_rows": r, "n_heads": H, "n_kv_heads": Hkv, "head_dim": d}}
+
+
+def cover_part(nat, step, st, w, flush, K, hbm_peak, tc_peak, seed, n_seeds=8):
+    """The attention call with COVER's dual view on this workload's recompute set,
+    ``n_seeds`` seeds per sequence among its decoded rows, and the plain call on
+    the same inputs for the cost of the override."""
+    import torch
+    torch.cuda.synchronize()
+    idx_h, cnt_h = step.idx.cpu().numpy(), step.count.cpu().numpy()
+    r = w.r_max
+    seeds = synth.cover_seeds(np.random.default_rng(seed + 303), st.is_masked, idx_h, cnt_h, r,
+                              n_seeds)
+    dev = step.dev
+    seed_d = torch.from_numpy(seeds).to(dev)
+    kc, vc = step.k_cache.clone(), step.v_cache.clone()
+    out = torch.empty_like(step.out)
+    ws = nat.new_workspace(nat.ec_attention_workspace_size(w.batch, w.seq_len, r, w.n_heads,
+                                                           w.n_kv_heads, w.head_dim), dev)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    cover = nat.prepare_selective_attention_cover(step.q, step.k_new, step.v_new, step.idx,
+                                                  step.count, seed_d, kc, vc, out, scale, ws,
+                                                  stream=step.stream)
+    plain = nat.prepare_selective_attention(step.q, step.k_new, step.v_new, step.idx, step.count,
+                                            kc, vc, out, scale, ws, stream=step.stream)
+
+    def timed(fn):
+        e0 = torch.cuda.Event(enable_timing=True, external=True)
+        e1 = torch.cuda.Event(enable_timing=True, external=True)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=step.stream):
+            e0.record()
+            fn()
+            e1.record()
+        for _ in range(3):
+            flush()
+            g.replay()
+        tot = 0.0
+        for _ in range(K):
+            flush()
+            g.replay()
+            e1.synchronize()
+            tot += e0.elapsed_time(e1) / 1e3
+        return tot / K * 1e6
+
+    t_c = timed(cover)
+    t_p = timed(plain)
+    geo = workload_geometry(w)
+    tflops = geo["attn_flops"] / t_c / 1e6
+    return {"us": t_c, "tflops": tflops, "frac_tensor_peak": tflops / tc_peak,
+            "gbs": geo["attn_bytes"] / t_c / 1e3, "frac_hbm": geo["attn_bytes"] / t_c / 1e3 / hbm_peak,
+            "plain_us": t_p, "seeds_per_sequence": n_seeds, "launches": 1,
+            "device_status": nat.ec_read_device_status(ws)}
 
 
 def run_e2e(step: GpuStep, geo, w, logits, att, K, W, world):

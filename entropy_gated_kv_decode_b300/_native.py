@@ -32,7 +32,7 @@ EXPORTED = ("ec_status_str", "ec_abi_version", "ec_debug_set_wait_limit", "ec_wo
             "ec_decode_noalloc_read_status", "ec_lmhead_workspace_size", "ec_lmhead_decode_step",
             "ec_build_recompute_set", "ec_attention_workspace_size", "ec_attention_kernel_count",
             "ec_selective_attention", "ec_selective_attention_simsd",
-            "ec_embed_rows", "ec_qkv_projection")
+            "ec_selective_attention_cover", "ec_embed_rows", "ec_qkv_projection")
 
 
 class NativeLibraryMissing(RuntimeError):
@@ -85,6 +85,9 @@ def lib() -> ctypes.CDLL:
         L.ec_selective_attention_simsd.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp,
                                                    ctypes.c_int, i32, i32, i32, i32, i32, i32, f32,
                                                    vp, sz, vp]
+        L.ec_selective_attention_cover.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, vp,
+                                                   ctypes.c_int, i32, i32, i32, i32, i32, i32, f32,
+                                                   vp, sz, vp]
         L.ec_embed_rows.argtypes = [vp, i64, i32, vp, i64, vp, vp, vp, i32, i32, i32, i32, vp, vp,
                                     sz, vp]
         L.ec_qkv_projection.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, sz, vp]
@@ -93,7 +96,7 @@ def lib() -> ctypes.CDLL:
                      "ec_decode_step_noalloc", "ec_decode_noalloc_read_status",
                      "ec_lmhead_decode_step", "ec_build_recompute_set",
                      "ec_selective_attention", "ec_selective_attention_simsd",
-                     "ec_embed_rows", "ec_qkv_projection"):
+                     "ec_selective_attention_cover", "ec_embed_rows", "ec_qkv_projection"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -368,6 +371,23 @@ def ec_selective_attention_simsd(q, k_new, v_new, idx, count, section, tau, k_ca
            "ec_selective_attention_simsd")
 
 
+def _cover_args(q, k_new, v_new, idx, count, seed, k_cache, v_cache, out, scale, workspace):
+    a = _attention_args(q, k_new, v_new, idx, count, k_cache, v_cache, out, scale, workspace)
+    _cuda("seed", seed, torch.uint8)
+    if seed.shape != q.shape[:2]:
+        raise ValueError("seed must be [batch, r_max]")
+    return a[:6] + [_p(seed)] + a[6:]
+
+
+def ec_selective_attention_cover(q, k_new, v_new, idx, count, seed, k_cache, v_cache, out,
+                                 scale, workspace, stream=None):
+    """ec_selective_attention with COVER's dual view: seed uint8 [B, R] flags the
+    recomputed rows that are seeds (masked-input K/V, not written back)."""
+    args = _cover_args(q, k_new, v_new, idx, count, seed, k_cache, v_cache, out, scale, workspace)
+    _check(lib().ec_selective_attention_cover(*args, _stream(stream)),
+           "ec_selective_attention_cover")
+
+
 def _embed_args(table, idx, count, seq_tokens, is_masked, mask_id, x, workspace):
     _cuda("table", table, torch.bfloat16)
     _cuda("idx", idx, torch.int32)
@@ -473,6 +493,11 @@ def prepare_selective_attention(*args, stream=None, **kwargs):
 
 def prepare_selective_attention_simsd(*args, stream=None, **kwargs):
     return Prepared("ec_selective_attention_simsd", _simsd_args(*args, **kwargs), stream,
+                    keep=(args, kwargs))
+
+
+def prepare_selective_attention_cover(*args, stream=None, **kwargs):
+    return Prepared("ec_selective_attention_cover", _cover_args(*args, **kwargs), stream,
                     keep=(args, kwargs))
 
 

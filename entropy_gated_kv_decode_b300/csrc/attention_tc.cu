@@ -137,7 +137,25 @@ struct Params {
     // 2 mask slot) and step label of every position, [B, L] each
     const uint8_t *section;
     const int32_t *tau;
+    // COVER's dual view (null without it): seed flag of every recomputed row,
+    // [B, r_max]; the queries, read directly for the seeds' diagonal terms
+    const uint8_t *seed;
+    const __nv_bfloat16 *q;
 };
+
+enum : int { MODE_PLAIN = 0, MODE_SIMSD = 1, MODE_COVER = 2 };
+
+// bf16 pairs (low half first) widened exactly to float, and a pair's dot product
+// added to an accumulator
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t x)
+{
+    return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
+__device__ __forceinline__ float fmaf_bf16x2(uint32_t a, uint32_t b, float acc)
+{
+    const float2 fa = bf16x2_to_f2(a), fb = bf16x2_to_f2(b);
+    return fmaf(fa.y, fb.y, fmaf(fa.x, fb.x, acc));
+}
 
 enum : int { ROLE_WHOLE = 0, ROLE_CONTRIB = 1, ROLE_OWNER = 2 };
 
@@ -227,8 +245,12 @@ __device__ __forceinline__ bool piece_active(const Params &P, const Piece &p)
     return p.mt * P.tok_per_tile < p.cnt && p.t1 > p.t0;
 }
 
-// Every position of sequence b is recomputed: the index set is 0 .. L-1.
-__device__ __forceinline__ bool piece_dense(const Params &P, const Piece &p) { return p.cnt == P.L; }
+// Every position of sequence b is recomputed: the index set is 0 .. L-1.  (Not
+// used with seeds, whose positions keep the cached K/V.)
+__device__ __forceinline__ bool piece_dense(const Params &P, const Piece &p)
+{
+    return p.cnt == P.L && P.seed == nullptr;
+}
 
 static_assert(Cfg<128>::kColS + 2 * kBlockN <= Cfg<128>::kColO, "TMEM columns overlap");
 static_assert(Cfg<128>::kColO + 128 <= Cfg<128>::kColQ, "TMEM columns overlap");
@@ -357,7 +379,7 @@ __device__ __forceinline__ int lower_bound_warp(const int32_t *idx, int cnt, int
 // A tile made only of fresh rows comes in as one TMA box per column block; the
 // rows of other tiles are copied by cp.async.  (Writing them back to the cache
 // is done separately, see write_back_share.)
-template <int D>
+template <int D, bool kSeeds>
 struct Patch {
     int cur, vbase, cnt;
     int v0, v1, v2, v3;  // entries vbase + lane + 32 k, INT_MAX past the set
@@ -365,6 +387,8 @@ struct Patch {
     int bar;             // index of this warp's mbarrier for the granule loads
     uint32_t uses;       // its phases used so far
     const int32_t *idx;
+    const uint8_t *sd;   // seed flags of the sequence's rows (null: no seeds)
+    unsigned sflags;     // bit k: entry vbase + lane + 32 k is a seed (not patched)
     uint8_t *rows;       // shared [128]: tile rows of the current tile's fresh rows (255: none)
     const CUtensorMap *fresh128, *cache128;
 
@@ -386,6 +410,11 @@ struct Patch {
         v1 = at + 32 + lane < cnt ? __ldg(idx + at + 32 + lane) : INT_MAX;
         v2 = at + 64 + lane < cnt ? __ldg(idx + at + 64 + lane) : INT_MAX;
         v3 = at + 96 + lane < cnt ? __ldg(idx + at + 96 + lane) : INT_MAX;
+        sflags = 0;
+        if constexpr (kSeeds)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (at + 32 * k + lane < cnt && __ldg(sd + at + 32 * k + lane)) sflags |= 1u << k;
     }
 
     // Whole warp, at a piece start.  The K side of one CTA per sequence also
@@ -397,6 +426,7 @@ struct Patch {
     {
         const int lane = threadIdx.x & 31;
         idx = P.idx + static_cast<int64_t>(w.b) * P.idx_stride;
+        sd = kSeeds ? P.seed + static_cast<int64_t>(w.b) * P.r_max : nullptr;
         cnt = w.cnt;
         const bool checker = check && w.mt == 0 && w.g == 0 && w.t0 == 0;
         const bool dense = piece_dense(P, w);
@@ -425,6 +455,7 @@ struct Patch {
         if (dense) {
             cur = vbase = 0;
             v0 = v1 = v2 = v3 = INT_MAX;
+            sflags = 0;
             return;
         }
         const int lo = w.t0 * kBlockN;
@@ -465,23 +496,27 @@ struct Patch {
             // the entries cur .. cur + n - 1 of the window fall in this tile: their
             // rows in the tile to shared memory, in order
             int n = 0;
+            bool seeded = false;  // a seed among them: its row keeps the cached K/V
             {
                 const int vv[4] = {v0, v1, v2, v3};
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int e = vbase + 32 * k + lane;
                     const bool in = e >= cur && vv[k] < tile_end;
+                    const bool is_seed = kSeeds && ((sflags >> k) & 1u);
                     const unsigned m = __ballot_sync(0xffffffffu, in);
+                    if constexpr (kSeeds) seeded |= __any_sync(0xffffffffu, in && is_seed);
                     if (in) {
                         const int rit = vv[k] - t * kBlockN;
-                        rows[e - cur] = rit >= 0 && rit < kBlockN ? static_cast<uint8_t>(rit) : uint8_t(255);
+                        rows[e - cur] = rit >= 0 && rit < kBlockN && !is_seed ? static_cast<uint8_t>(rit)
+                                                                              : uint8_t(255);
                     }
                     n += __popc(m);
                 }
             }
             __syncwarp();
             if (n > 0) {
-                if (n == kBlockN) {
+                if (n == kBlockN && !seeded) {
                     // a whole tile of fresh rows (128 distinct positions inside it,
                     // so 128 consecutive fresh rows): one TMA box per column block
                     if (lane == 0) {
@@ -565,7 +600,7 @@ __device__ __forceinline__ int share_rows(const Params &P, const Piece &w)
 // Nothing in this kernel reads a fresh row from the cache (each landed tile is
 // patched from the fresh tensor), so the copies need no ordering against the
 // loads.
-template <int D>
+template <int D, bool kSeeds>
 __device__ void write_back_share(const Params &P, int part, int n_parts)
 {
     constexpr int kChunks = D / 8;
@@ -590,6 +625,9 @@ __device__ void write_back_share(const Params &P, int part, int n_parts)
         if (j >= 0) {
             p = __ldg(P.idx + static_cast<int64_t>(w.b) * P.idx_stride + j);
             if (p < w.t0 * kBlockN || p >= min(w.t1 * kBlockN, P.L)) p = -1;
+            // a seed's position keeps the cached K/V (COVER's override)
+            if constexpr (kSeeds)
+                if (__ldg(P.seed + static_cast<int64_t>(w.b) * P.r_max + j)) p = -1;
         }
         if (p >= 0) {
             const int64_t src = (static_cast<int64_t>(w.b) * P.r_max + j) * row_elems + w.g * D;
@@ -615,7 +653,7 @@ __device__ void write_back_share(const Params &P, int part, int n_parts)
 // the whole warp patches the fresh K rows into it, and one thread issues
 // S = Q K^T into one of the two S buffers once the PV product of the tile two
 // back (which read its P from that buffer) completed.
-template <int D>
+template <int D, bool kSeeds>
 __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem, uint8_t *rows,
                           const CUtensorMap *tm_kn, const CUtensorMap *tm_k)
 {
@@ -623,7 +661,7 @@ __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
     constexpr uint32_t kIdescQK = idesc_bf16(kBlockM, kBlockN, false, false);
     const int lane = threadIdx.x & 31;
     const Range r = my_range(P);
-    Patch<D> pt;
+    Patch<D, kSeeds> pt;
     pt.init(B_KPATCH, rows, tm_kn, tm_k);
     uint32_t T = 0, it = 0;
     bool ok = true;
@@ -689,7 +727,7 @@ __device__ void qk_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
 // fresh V rows into it, and one thread issues O (+)= P V once the softmax warps
 // wrote P over its S buffer; the first tile of a piece overwrites O.  The
 // product's completion frees the V stage and the S buffer.
-template <int D>
+template <int D, bool kSeeds>
 __device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32_t tmem, uint8_t *rows,
                           const CUtensorMap *tm_vn, const CUtensorMap *tm_v)
 {
@@ -697,7 +735,7 @@ __device__ void pv_issuer(const Params &P, const Sync &S, uint32_t sbase, uint32
     constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, false, true);
     const int lane = threadIdx.x & 31;
     const Range r = my_range(P);
-    Patch<D> pt;
+    Patch<D, kSeeds> pt;
     pt.init(B_VPATCH, rows, tm_vn, tm_v);
     uint32_t T = 0;
     bool ok = true;
@@ -917,9 +955,11 @@ __device__ __forceinline__ int2 simsd_window(const Params &P, int b, int pos, bo
     return sec == 1 ? make_int2(0, t) : make_int2(t - kSlotBase, t - 1);
 }
 
-template <int D, bool kMasked>
+template <int D, int kMode>
 __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, float *xchg)
 {
+    constexpr bool kSimSD = kMode == MODE_SIMSD, kCover = kMode == MODE_COVER;
+    constexpr bool kMasked = kMode != MODE_PLAIN;  // some score may be hidden
     using C = Cfg<D>;
     constexpr int kOChunks = D / 64;  // 32-column chunks of O per half
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -943,17 +983,22 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, 
         float m_run = -INFINITY, l_run = 0.f;  // m in raw score units; l of this half
         int2 win = make_int2(INT_MIN, INT_MAX);  // rows past the unit's tokens see all
         bool bad_label = false;
+        int own = -1;  // COVER: a seed row's own position, whose cached key it must not see
         if constexpr (kMasked) {
             const int tok = w.mt * P.tok_per_tile + row / P.G;
-            if (row < P.tok_per_tile * P.G && tok < w.cnt)
-                win = simsd_window(P, w.b, __ldg(P.idx + w.b * P.idx_stride + tok), bad_label);
+            if (row < P.tok_per_tile * P.G && tok < w.cnt) {
+                const int pos = __ldg(P.idx + w.b * P.idx_stride + tok);
+                if constexpr (kSimSD) win = simsd_window(P, w.b, pos, bad_label);
+                if constexpr (kCover)
+                    if (__ldg(P.seed + static_cast<int64_t>(w.b) * P.r_max + tok)) own = pos;
+            }
         }
         for (int t = w.t0; t < w.t1; ++t, ++T) {
             const int sb = T & 1;
             // the labels of this half's 64 keys (two per lane) and their range,
             // loaded while the product runs
             int lab0 = 0, lab1 = 0, lab_lo = 0, lab_hi = 0;
-            if constexpr (kMasked) {
+            if constexpr (kSimSD) {
                 const int j0 = t * kBlockN + half * 64 + lane;
                 const bool in0 = j0 < P.L, in1 = j0 + 32 < P.L;
                 if (in0) lab0 = simsd_key_label(P, w.b, j0, bad_label);
@@ -979,7 +1024,19 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, 
                         for (int j = 0; j < 32; ++j)
                             if (cc * 32 + j >= live) sr[cc][j] = __float_as_uint(-INFINITY);
                 }
-                if constexpr (kMasked) {
+                if constexpr (kCover) {
+                    // a seed row hides the cached key at its own position (the
+                    // diagonal term is added from its masked-input K/V at the end)
+                    const int col = own - (t * kBlockN + half * 64);
+                    if (col >= 0 && col < 64) {
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (cc * 32 + j == col) sr[cc][j] = __float_as_uint(-INFINITY);
+                    }
+                }
+                if constexpr (kSimSD) {
                     // a row whose window misses part of the keys' label range
                     // hides those keys; the labels go round the warp
                     const bool all_in = win.x <= lab_lo && lab_hi <= win.y;
@@ -1060,7 +1117,7 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, 
             ok = __all_sync(0xffffffffu, S.wait(B_SFREE + (Tp & 1), (Tp >> 1) & 1));
         }
         tc_fence_after();
-        if constexpr (kMasked)
+        if constexpr (kSimSD)
             if (__any_sync(0xffffffffu, bad_label) && lane == 0) flag_status(P.status, EC_DEV_BAD_LABEL);
         // the row sum of both halves (same reference m)
         pair_sync(quarter);
@@ -1126,6 +1183,32 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, 
             const float ws = weight(s, M, ls);
             l = fmaf(ws, ls, l);
         }
+        // COVER: a seed row's diagonal term from its masked-input K/V, s = q . k_new
+        // (raw units, both halves alike): O and l are rescaled to M2 = max(M, s)
+        // and gain 2^{(s - M2) c} v_new and 2^{(s - M2) c}
+        float f_old = 1.f, p_new = 0.f;
+        const __nv_bfloat16 *vrow = nullptr;
+        if constexpr (kCover) {
+            if (valid && own >= 0) {
+                const int64_t kv = ((static_cast<int64_t>(w.b) * P.r_max + tok) * P.Hkv + w.g) * D;
+                const uint4 *qv = reinterpret_cast<const uint4 *>(P.q + ((static_cast<int64_t>(w.b) * P.r_max + tok) * P.H + h) * D);
+                const uint4 *kn = reinterpret_cast<const uint4 *>(P.k_new + kv);
+                float dot = 0.f;
+#pragma unroll 4
+                for (int u = 0; u < D / 8; ++u) {
+                    const uint4 a = __ldg(qv + u), b = __ldg(kn + u);
+                    dot = fmaf_bf16x2(a.x, b.x, dot);
+                    dot = fmaf_bf16x2(a.y, b.y, dot);
+                    dot = fmaf_bf16x2(a.z, b.z, dot);
+                    dot = fmaf_bf16x2(a.w, b.w, dot);
+                }
+                const float M2 = fmaxf(M, dot);
+                f_old = l > 0.f ? ex2((M - M2) * c) : 0.f;
+                p_new = ex2((dot - M2) * c);
+                l = fmaf(l, f_old, p_new);
+                vrow = P.v_new + kv;
+            }
+        }
         const float inv = kMasked ? (l > 0.f ? 1.f / l : 0.f) : 1.f / l;  // no visible key: zeros
 #pragma unroll 1
         for (int cc = half * kOChunks; cc < (half + 1) * kOChunks; ++cc) {
@@ -1150,6 +1233,22 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, 
                     }
                 }
             }
+            if constexpr (kCover) {
+                if (vrow) {
+                    const uint4 *vv = reinterpret_cast<const uint4 *>(vrow + cc * 32);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 x = __ldg(vv + q);
+                        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = bf16x2_to_f2(xs[e]);
+                            acc[8 * q + 2 * e] = fmaf(acc[8 * q + 2 * e], f_old, p_new * f.x);
+                            acc[8 * q + 2 * e + 1] = fmaf(acc[8 * q + 2 * e + 1], f_old, p_new * f.y);
+                        }
+                    }
+                }
+            }
             if (valid) {
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
 #pragma unroll
@@ -1167,7 +1266,7 @@ __device__ void softmax_epilogue(const Params &P, const Sync &S, uint32_t tmem, 
     }
 }
 
-template <int D, bool kMasked>
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_tc_kernel(const Params P, const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -1221,14 +1320,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        qk_issuer<D>(P, S, sbase, tmem, smem + C::kOffRows, &tm_kn, &tm_k);
+        qk_issuer<D, kMode == MODE_COVER>(P, S, sbase, tmem, smem + C::kOffRows, &tm_kn, &tm_k);
     } else if (warp == 7) {
-        pv_issuer<D>(P, S, sbase, tmem, smem + C::kOffRows + 128, &tm_vn, &tm_v);
+        pv_issuer<D, kMode == MODE_COVER>(P, S, sbase, tmem, smem + C::kOffRows + 128, &tm_vn, &tm_v);
     } else {
         // the eight softmax warps: the write-back share while the first scores are
         // being produced, then the softmax
-        write_back_share<D>(P, warp < 8 ? warp - 2 : warp - 4, 8);
-        softmax_epilogue<D, kMasked>(P, S, tmem, reinterpret_cast<float *>(smem + C::kOffXchg));
+        write_back_share<D, kMode == MODE_COVER>(P, warp < 8 ? warp - 2 : warp - 4, 8);
+        softmax_epilogue<D, kMode>(P, S, tmem, reinterpret_cast<float *>(smem + C::kOffXchg));
     }
     __syncthreads();
     if (warp == 1) {
@@ -1340,9 +1439,12 @@ cudaError_t launch_typed(const Params &p, const Plan &plan, const void *q, cudaS
         !encode_4d(&tvn, p.v_new, p.B, fresh_rows, p.r_max, p.Hkv, D, 1, kBlockN))
         return cudaErrorInvalidValue;
     if (p.section)
-        return launch(attention_tc_kernel<D, true>, dim3(plan.grid), dim3(kThreads), Cfg<D>::kBytes,
-                      stream, p, tq, tk, tv, tkn, tvn);
-    return launch(attention_tc_kernel<D, false>, dim3(plan.grid), dim3(kThreads), Cfg<D>::kBytes,
+        return launch(attention_tc_kernel<D, MODE_SIMSD>, dim3(plan.grid), dim3(kThreads),
+                      Cfg<D>::kBytes, stream, p, tq, tk, tv, tkn, tvn);
+    if (p.seed)
+        return launch(attention_tc_kernel<D, MODE_COVER>, dim3(plan.grid), dim3(kThreads),
+                      Cfg<D>::kBytes, stream, p, tq, tk, tv, tkn, tvn);
+    return launch(attention_tc_kernel<D, MODE_PLAIN>, dim3(plan.grid), dim3(kThreads), Cfg<D>::kBytes,
                   stream, p, tq, tk, tv, tkn, tvn);
 }
 
@@ -1372,7 +1474,7 @@ cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_
                                 int32_t seq_len, int32_t r_max, int32_t n_heads,
                                 int32_t n_kv_heads, int32_t head_dim, float scale,
                                 void *workspace, cudaStream_t stream, const uint8_t *section,
-                                const int32_t *tau)
+                                const int32_t *tau, const uint8_t *seed)
 {
     if (r_max == 0) return cudaSuccess;  // nothing to recompute, nothing to write back
     const Plan plan = make_plan(batch, seq_len, r_max, n_heads, n_kv_heads);
@@ -1411,6 +1513,8 @@ cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_
     p.part_o = reinterpret_cast<float4 *>(ws + o_o);
     p.section = section;
     p.tau = tau;
+    p.seed = seed;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
     return head_dim == 128 ? launch_typed<128>(p, plan, q, stream)
                            : launch_typed<64>(p, plan, q, stream);
 }

@@ -280,6 +280,37 @@ ec_status ec_selective_attention_simsd(const void *q, const void *k_new, const v
                                             reinterpret_cast<cudaStream_t>(stream), section, tau));
 }
 
+ec_status ec_selective_attention_cover(const void *q, const void *k_new, const void *v_new,
+                                       const int32_t *idx, int64_t idx_stride,
+                                       const int32_t *count, const uint8_t *seed, void *k_cache,
+                                       void *v_cache, void *out, ec_dtype dtype, int32_t batch,
+                                       int32_t seq_len, int32_t r_max, int32_t n_heads,
+                                       int32_t n_kv_heads, int32_t head_dim, float scale,
+                                       void *workspace, size_t workspace_bytes,
+                                       ec_stream_t stream)
+{
+    if (dtype != EC_F32 && dtype != EC_BF16) return EC_ERR_DTYPE;
+    if (batch < 1 || seq_len < 1 || r_max < 0 || n_heads < 1 || n_kv_heads < 1 ||
+        n_heads % n_kv_heads != 0 || (head_dim != 64 && head_dim != 128) || idx_stride < r_max ||
+        !isfinite(scale))
+        return EC_ERR_SHAPE;
+    if (!count || !k_cache || !v_cache || !workspace) return EC_ERR_NULL;
+    if (r_max > 0 && (!q || !k_new || !v_new || !idx || !out || !seed)) return EC_ERR_NULL;
+    if (!ec::attention_tc_supported(dtype, seq_len, head_dim)) return EC_ERR_UNSUPPORTED;
+    const void *ptrs[] = {q, k_new, v_new, k_cache, v_cache, out};
+    for (const void *p : ptrs)
+        if (p && !aligned(p, 16)) return EC_ERR_ALIGN;
+    if (!aligned(workspace, EC_WORKSPACE_ALIGN) ||
+        workspace_bytes <
+            ec::attention_workspace_bytes(batch, seq_len, r_max, n_heads, n_kv_heads, head_dim))
+        return EC_ERR_WORKSPACE;
+    return launched(ec::launch_attention_tc(q, k_new, v_new, idx, idx_stride, count, k_cache,
+                                            v_cache, out, batch, seq_len, r_max, n_heads,
+                                            n_kv_heads, head_dim, scale, workspace,
+                                            reinterpret_cast<cudaStream_t>(stream), nullptr,
+                                            nullptr, seed));
+}
+
 ec_status ec_qkv_projection(const void *x, const int32_t *count, int32_t batch, int32_t r_max,
                             int32_t hidden, const void *w_qkv, int32_t width, void *q, void *k,
                             void *v, void *workspace, size_t workspace_bytes, ec_stream_t stream)

@@ -143,7 +143,8 @@ cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_
                                 int32_t seq_len, int32_t r_max, int32_t n_heads,
                                 int32_t n_kv_heads, int32_t head_dim, float scale,
                                 void *workspace, cudaStream_t stream,
-                                const uint8_t *section = nullptr, const int32_t *tau = nullptr);
+                                const uint8_t *section = nullptr, const int32_t *tau = nullptr,
+                                const uint8_t *seed = nullptr);
 
 // qkv_gemm.cu
 bool qkv_shape_ok(int32_t hidden, int32_t width);

@@ -157,6 +157,21 @@ def make_simsd_layout(rng: np.random.Generator, batch: int, prompt_len: int,
     return section, tau, idx, count
 
 
+def cover_seeds(rng: np.random.Generator, is_masked: np.ndarray, idx: np.ndarray,
+                count: np.ndarray, r_max: int, n_seeds: int) -> np.ndarray:
+    """COVER's seed flags ``[batch, r_max]`` uint8: per sequence, ``n_seeds`` rows
+    (fewer if there are not enough) drawn at random among the recomputed rows whose
+    positions are already decoded (not masked), the tokens a verification pass
+    checks."""
+    seed = np.zeros((idx.shape[0], r_max), np.uint8)
+    for b in range(idx.shape[0]):
+        rows = [r for r in range(int(count[b])) if not is_masked[b, idx[b, r]]]
+        if rows:
+            pick = rng.choice(rows, size=min(n_seeds, len(rows)), replace=False)
+            seed[b, pick] = 1
+    return seed
+
+
 def scaled(w: Workload, **changes) -> Workload:
     """A copy of ``w`` with some fields replaced (smaller parity cases)."""
     return dataclasses.replace(w, **changes)

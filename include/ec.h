@@ -338,6 +338,38 @@ ec_status ec_selective_attention_simsd(const void *q, const void *k_new, const v
                                        int32_t head_dim, float scale, void *workspace,
                                        size_t workspace_bytes, ec_stream_t stream);
 
+/*
+ * ec_selective_attention with COVER's dual view: the KV-cache override and the
+ * diagonal correction ("Stop the Flip-Flop: Verifica Preservante il Contesto per
+ * una Decodifica di Diffusione Veloce e Revocabile", Italian technical summary,
+ * section "Metodologia: COVER", item 1).
+ *
+ * seed uint8, device, [batch, r_max]: seed[b*r_max + r] != 0 marks recomputed row
+ * r as a seed, a decoded token under verification whose input was [MASK], so its
+ * k_new / v_new rows are the masked-input K/V.  Then:
+ *   - only the non-seed rows are written back: a seed's position keeps the K/V
+ *     the cache held before the call (the previous step's), which every other
+ *     query attends to;
+ *   - a seed row's own column uses its masked-input k_new / v_new instead of the
+ *     cached K/V at its position (no self-leakage), and the softmax is taken over
+ *     the row so corrected:
+ *       out[b, r, h] = softmax_j(scale * q . K'_j) V'_j,  K'_j = cache after the
+ *       write-back, except K'_{idx[r]} = k_new[b, r] (and V') when r is a seed.
+ * No seeds: the same results as ec_selective_attention.  A fully recomputed
+ * sequence (count == seq_len) takes the general path.  Every other argument, the
+ * workspace (ec_attention_workspace_size bytes) and the errors are those of
+ * ec_selective_attention, but only bf16 with head_dim 64 or 128 is implemented
+ * (EC_ERR_UNSUPPORTED otherwise); one kernel launch.
+ */
+ec_status ec_selective_attention_cover(const void *q, const void *k_new, const void *v_new,
+                                       const int32_t *idx, int64_t idx_stride,
+                                       const int32_t *count, const uint8_t *seed, void *k_cache,
+                                       void *v_cache, void *out, ec_dtype dtype, int32_t batch,
+                                       int32_t seq_len, int32_t r_max, int32_t n_heads,
+                                       int32_t n_kv_heads, int32_t head_dim, float scale,
+                                       void *workspace, size_t workspace_bytes,
+                                       ec_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* the forward that produces the recomputed rows' queries, keys and values    */
 /* ------------------------------------------------------------------------- */

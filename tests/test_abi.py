@@ -130,6 +130,27 @@ def test_recompute_set_and_attention_reject_bad_arguments(L):
     assert call_m(q=0x1004) == -4
     assert call_m(wsb=8) == -5
 
+    # the COVER variant: its seed flags, and bf16 only
+    cv = L.ec_selective_attention_cover
+
+    def call_c(**kw):
+        args = list(base)
+        names = ["q", "kn", "vn", "idx", "stride", "count", "kc", "vc", "out", "dtype", "batch",
+                 "L", "r", "H", "Hkv", "d", "scale", "ws", "wsb", "stream"]
+        for k, v in kw.items():
+            if k in names:
+                args[names.index(k)] = v
+        return cv(*args[:6], kw.get("seed", 0x20000), *args[6:])
+
+    assert call_c(d=96) == -2
+    assert call_c(stride=40) == -2
+    assert call_c(dtype=3) == -3
+    assert call_c(seed=None) == -1
+    assert call_c(kc=None) == -1
+    assert call_c(dtype=0) == -7
+    assert call_c(out=0x8004) == -4
+    assert call_c(wsb=8) == -5
+
 
 def test_projection_and_gather_reject_bad_arguments(L):
     p = L.ec_qkv_projection
