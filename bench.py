@@ -1024,6 +1024,24 @@ def run_trajectory(args):
     value = aggregate(tbytes * K, world, t_max) / 1e9
     cpu = trajectory_cpu_baseline(w, args.seed, args.cpu_seconds, tbytes) \
         if rank == 0 and world == 1 else None
+    # the same trajectory under the sliding-window and multi-block decoding policies
+    policies = {}
+    for pol in (("sliding", 64), ("multiblock", 2)):
+        tp = Trajectory(w, seed=args.seed, device=device, stream=stream, policy=pol)
+        tp.warm_up()
+        tp.run()
+        torch.cuda.synchronize(device)
+        pw = []
+        for _ in range(max(1, min(K, 3))):
+            t0 = time.perf_counter()
+            pr = tp.run()
+            pw.append(time.perf_counter() - t0)
+        policies[f"{pol[0]}_{pol[1]}"] = {
+            "denoising_steps_per_s": w.n_steps / (sum(pw) / len(pw)),
+            "refresh_fraction": sum(r.refresh for r in pr) / len(pr),
+            "mean_rows": float(np.mean([r.rows for r in pr])),
+            "decode_and_sets_ms": float(np.mean([r.decode_ms for r in pr]))}
+        del tp
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": t_max / K * 1e3, "higher_is_better": True,
@@ -1051,6 +1069,7 @@ def run_trajectory(args):
             "projection_full_us": t_proj_full * 1e6, "projection_full_tflops": proj_tflops,
             "projection_partial_us": t_proj_sel * 1e6,
             "projection_partial_weight_gbs": wbytes / t_proj_sel / 1e9,
+            "policies": policies,
         },
         "roofline": {"bound": "tensor", "achieved": proj_tflops, "peak": tc, "unit": "TFLOP/s",
                      "frac": proj_tflops / tc, "traffic": None,

@@ -415,3 +415,9 @@ def trajectory_weights(seed: int, layer: int, hidden: int, width: int) -> np.nda
 def trajectory_logits(seed: int, step: int, n_rows: int, vocab: int) -> np.ndarray:
     """bf16 logits of one step's masked rows (the temperature + spike recipe)."""
     return make_logits(step_rng(seed, step), n_rows, vocab, BF16)
+
+
+def trajectory_window_logits(seed: int, step: int, width: int, vocab: int) -> np.ndarray:
+    """bf16 logits of ``width`` rows for one step of a window-policy trajectory; a
+    step whose window holds c masked positions uses the first c rows."""
+    return make_logits(step_rng(seed, step), width, vocab, BF16)

@@ -28,6 +28,19 @@ One step t, all on one CUDA stream:
              after the step, which picks the next forward's graph.
 Every arithmetic step runs in libec's kernels; this module only allocates,
 launches and reads the flag.
+
+Decoding policies (section 5 "Generalità" of the Italian summary: the skipping
+rule applies to sliding-window and block decoding).  A step may unmask only
+positions of its window [lo, hi), whose masked positions are also the "currently
+masked" part of the next recompute set:
+  ("block",)          the workload's block schedule, blocks left to right;
+  ("sliding", W)      lo = the first still-masked generated position, hi = lo + W;
+  ("multiblock", nb)  lo = the start of the block holding that position, nb blocks;
+hi clamped to L.  With the last two the window depends on the state: after each
+step the driver copies is_masked (one byte per position) to the host with the
+refresh flag, places the next window there, and builds the next recompute set
+before the next forward.  A step's logits are the first c rows of a W-row
+(nb-block) draw, c the masked positions in its window.
 """
 from __future__ import annotations
 
@@ -61,16 +74,25 @@ class Trajectory:
     """Device state and launch plan of one synthetic trajectory (batch 1)."""
 
     def __init__(self, w: synth.Workload, seed: int = 0, device=None, stream=None,
-                 use_graphs: bool = True, trace: bool = False):
+                 use_graphs: bool = True, trace: bool = False, policy=("block",)):
         if w.batch != 1 or w.n_kv_heads != w.n_heads:
             raise ValueError("the trajectory driver runs one sequence of a multi-head model")
+        if policy[0] not in ("block", "sliding", "multiblock") or (
+                policy[0] != "block" and (len(policy) != 2 or int(policy[1]) < 1)):
+            raise ValueError(f"unknown decoding policy {policy}")
+        self.policy = policy
+        self.windowed = policy[0] != "block"
         self.w, self.seed = w, seed
         self.dev = torch.device(device if device is not None else "cuda")
         self.stream = stream if stream is not None else torch.cuda.Stream(self.dev)
         L, V, H, d = w.seq_len, w.vocab, w.n_heads, w.head_dim
         self.hidden = H * d
         hid = self.hidden
-        self.r_sel = w.block + w.k  # largest partial recompute set
+        # rows of every step's logits draw (window policies) and the largest
+        # partial recompute set
+        self.win_rows = (policy[1] if policy[0] == "sliding" else policy[1] * w.block) \
+            if self.windowed else w.block
+        self.r_sel = min(self.win_rows + w.k, L)
         i32, u8, bf = torch.int32, torch.uint8, torch.bfloat16
         dev = self.dev
         with torch.cuda.stream(self.stream):
@@ -81,13 +103,17 @@ class Trajectory:
             self.k_cache = torch.zeros((w.n_layers, 1, L, w.n_kv_heads, d), dtype=bf, device=dev)
             self.v_cache = torch.zeros_like(self.k_cache)
             # every step's logits, resident: rows of step t start at row_off[t]
-            self.rows_per_step = synth.trajectory_rows_per_step(w)
+            if self.windowed:
+                self.rows_per_step = [self.win_rows] * w.n_steps  # rows drawn per step
+            else:
+                self.rows_per_step = synth.trajectory_rows_per_step(w)
             self.row_off = np.concatenate([[0], np.cumsum(self.rows_per_step)]).astype(np.int64)
             self.logits = torch.empty((int(self.row_off[-1]), V), dtype=bf, device=dev)
             for t, n in enumerate(self.rows_per_step):
                 if n:
-                    self.logits[self.row_off[t]:self.row_off[t + 1]].copy_(
-                        _up(synth.trajectory_logits(seed, t, n, V), dev))
+                    draw = (synth.trajectory_window_logits(seed, t, n, V) if self.windowed
+                            else synth.trajectory_logits(seed, t, n, V))
+                    self.logits[self.row_off[t]:self.row_off[t + 1]].copy_(_up(draw, dev))
             st = synth.trajectory_start(seed, w)
             self.start = st
             self.is_masked = _up(st.is_masked, dev)
@@ -108,8 +134,12 @@ class Trajectory:
             self.count_rows = torch.zeros(1, dtype=i32, device=dev)
             self.zero_flag = torch.zeros(1, dtype=u8, device=dev)
             # decode outputs
-            nb = w.block
-            self.offsets = _up(np.array([[0, n] for n in self.rows_per_step], np.int32), dev)
+            nb = self.win_rows
+            if self.windowed:  # offsets [0, c] for every possible row count c
+                self.offsets = _up(np.array([[0, c] for c in range(nb + 1)], np.int32), dev)
+            else:
+                self.offsets = _up(np.array([[0, n] for n in self.rows_per_step], np.int32), dev)
+            self.mask_host = torch.zeros((1, L), dtype=u8).pin_memory()
             self.token = torch.zeros(nb, dtype=i32, device=dev)
             self.conf = torch.zeros(nb, dtype=torch.float32, device=dev)
             self.entropy = torch.zeros(nb, dtype=torch.float32, device=dev)
@@ -138,6 +168,7 @@ class Trajectory:
         self.t = 0
         self.next_full = True
         self.next_rows = w.seq_len
+        self.win = None  # this step's window (window policies)
 
     # -- launch plan ---------------------------------------------------------
 
@@ -184,27 +215,59 @@ class Trajectory:
             self.logits_host.copy_(self.logits)
         self.copy_logits = on
 
+    def _window_of(self, mask: np.ndarray) -> tuple[int, int, int]:
+        """The window [lo, hi) placed on a host copy of is_masked, and the number of
+        masked positions in it."""
+        w, pol = self.w, self.policy
+        gen = np.flatnonzero(mask[w.prompt_len:])
+        first = w.prompt_len + int(gen[0]) if gen.size else w.seq_len
+        if pol[0] == "sliding":
+            lo = first
+        else:
+            lo = w.prompt_len + (first - w.prompt_len) // w.block * w.block
+        hi = min(lo + self.win_rows, w.seq_len)
+        return lo, hi, int(mask[lo:hi].sum())
+
     def _decode(self, t: int):
         """Unmask and gate with step t's logits, then build the next row set."""
         w = self.w
-        n_rows = self.rows_per_step[t]
+        if self.windowed:
+            lo, hi, n_rows = self.win
+        else:
+            lo, hi = synth.trajectory_block(w, t)
+            n_rows = self.rows_per_step[t]
         if self.copy_logits and n_rows:
-            a, b = int(self.row_off[t]), int(self.row_off[t + 1])
-            self.logits[a:b].copy_(self.logits_host[a:b], non_blocking=True)
-        lo, hi = synth.trajectory_block(w, t)
+            a = int(self.row_off[t])
+            self.logits[a:a + n_rows].copy_(self.logits_host[a:a + n_rows], non_blocking=True)
         nat.ec_build_recompute_set(self.is_masked, self.decode_step, self.zero_flag, lo, hi, 0,
                                    self.idx_rows, self.count_rows, stream=self.stream)
-        lg = self.logits[self.row_off[t]:self.row_off[t + 1]]
-        nat.ec_decode_step(lg, self.offsets[t], self.idx_rows[0, :n_rows], w.seq_len, w.n_unmask,
+        lg = self.logits[self.row_off[t]:self.row_off[t] + n_rows]
+        offs = self.offsets[n_rows] if self.windowed else self.offsets[t]
+        nat.ec_decode_step(lg, offs, self.idx_rows[0, :n_rows], w.seq_len, w.n_unmask,
                            w.tau, t, self.token[:n_rows], self.conf[:n_rows],
                            self.entropy[:n_rows], self.unmask, self.emax, self.refresh,
                            self.is_masked, self.tokens, self.decode_step, self.ws_dec,
                            stream=self.stream)
-        nlo, nhi = synth.trajectory_block(w, t + 1)
-        nat.ec_build_recompute_set(self.is_masked, self.decode_step, self.refresh, nlo, nhi,
-                                   w.k, self.idx_sel, self.count_sel, stream=self.stream)
+        if self.windowed:  # the next window is placed on the host after the step
+            self.mask_host.copy_(self.is_masked, non_blocking=True)
+        else:
+            nlo, nhi = synth.trajectory_block(w, t + 1)
+            nat.ec_build_recompute_set(self.is_masked, self.decode_step, self.refresh, nlo, nhi,
+                                       w.k, self.idx_sel, self.count_sel, stream=self.stream)
+            self.count_host.copy_(self.count_sel, non_blocking=True)
         self.refresh_host.copy_(self.refresh, non_blocking=True)
-        self.count_host.copy_(self.count_sel, non_blocking=True)
+
+    def _next_window(self):
+        """Window policies, after a step: the next window from the host copy of
+        is_masked, and the next recompute set for it (queued before the next
+        forward)."""
+        lo, hi, c = self._window_of(self.mask_host[0].numpy())
+        self.win = (lo, hi, c)
+        w = self.w
+        with torch.cuda.stream(self.stream):
+            nat.ec_build_recompute_set(self.is_masked, self.decode_step, self.refresh, lo, hi, w.k,
+                                       self.idx_sel, self.count_sel, stream=self.stream)
+            self.count_host.copy_(self.count_sel, non_blocking=True)
 
     # -- driving -------------------------------------------------------------
 
@@ -233,6 +296,8 @@ class Trajectory:
         self.next_rows = self.w.seq_len
         self.records = []
         self.traces = []
+        if self.windowed:
+            self.win = self._window_of(st.is_masked[0])
 
     def step(self):
         t = self.t
@@ -248,10 +313,13 @@ class Trajectory:
         refresh = int(self.refresh_host[0])
         self.records.append(StepRecord(t, full, rows, refresh, ev[0].elapsed_time(ev[1]),
                                        ev[1].elapsed_time(ev[2])))
+        n = self.win[2] if self.windowed else self.rows_per_step[t]
+        if self.windowed:
+            self._next_window()
+            self.stream.synchronize()  # the next set's size (for the records) has landed
         self.next_full = refresh != 0
         self.next_rows = self.w.seq_len if self.next_full else int(self.count_host[0])
         if self.trace:  # host copies of this step's decisions (outside any timing)
-            n = self.rows_per_step[t]
             self.traces.append(dict(
                 row_pos=self.idx_rows[0, :n].cpu().numpy(), token=self.token[:n].cpu().numpy(),
                 entropy=self.entropy[:n].cpu().numpy(), conf=self.conf[:n].cpu().numpy(),

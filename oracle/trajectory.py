@@ -15,6 +15,17 @@ The steps are the oracle's own functions (row_stats, unmask_gate,
 recompute_set; embed_rows, projection, scatter_kv, attention), composed in the
 pages' order.  The workload's block schedule, starting state, weights and
 logits come from the shared seeded generator.
+
+Decoding policies (EntropyCache, Italian summary, section 5 "Generalità": the
+entropy-based skipping applies to other decoding strategies, sliding windows and
+blocks).  The positions a step may unmask, and the "currently masked" part of the
+next recompute set, lie in the step's window [lo, hi):
+  ("block",)          the workload's block schedule (blocks left to right);
+  ("sliding", W)      lo = the first still-masked generated position, hi = lo + W;
+  ("multiblock", nb)  lo = the start of the block holding the first still-masked
+                      position, hi = lo + nb blocks;
+hi clamped to L.  With the last two, a step's logits rows are the first c rows of
+a W-row (nb-block) draw, c = the masked positions in its window.
 """
 from __future__ import annotations
 
@@ -31,8 +42,29 @@ def _widen(a):
     return synth.bf16_bits_to_f32(a).astype(np.float64) if a.dtype == np.uint16 else a
 
 
+def window(w: synth.Workload, policy, t: int, is_masked: np.ndarray) -> tuple[int, int]:
+    """The window [lo, hi) of step t under ``policy`` (see the module notes)."""
+    if policy[0] == "block":
+        return synth.trajectory_block(w, t)
+    gen = np.flatnonzero(is_masked[0, w.prompt_len:])
+    first = w.prompt_len + int(gen[0]) if gen.size else w.seq_len
+    if policy[0] == "sliding":
+        lo, width = first, policy[1]
+    elif policy[0] == "multiblock":
+        lo = w.prompt_len + (first - w.prompt_len) // w.block * w.block
+        width = policy[1] * w.block
+    else:
+        raise ValueError(f"unknown policy {policy}")
+    return lo, min(lo + width, w.seq_len)
+
+
+def window_rows(w: synth.Workload, policy) -> int:
+    """Rows of every step's logits draw under a window policy."""
+    return policy[1] if policy[0] == "sliding" else policy[1] * w.block
+
+
 def run(w: synth.Workload, seed: int, n_steps: int | None = None, logits_of_step=None,
-        layers: int = 0):
+        layers: int = 0, policy=("block",)):
     """Decisions (and, with ``layers`` > 0, the float64 forward of that many
     synthetic layers) of the first n_steps steps.  Returns a list of per-step
     dicts and the final state; with layers > 0 also the float64 K/V caches and
@@ -41,10 +73,15 @@ def run(w: synth.Workload, seed: int, n_steps: int | None = None, logits_of_step
     L, n, k, tau = w.seq_len, w.n_unmask, w.k, w.tau
     H, d = w.n_heads, w.head_dim
     hid = H * d
-    rows_per_step = synth.trajectory_rows_per_step(w)
     if logits_of_step is None:
-        def logits_of_step(t):
-            return synth.trajectory_logits(seed, t, rows_per_step[t], w.vocab)
+        if policy[0] == "block":
+            rows_per_step = synth.trajectory_rows_per_step(w)
+
+            def logits_of_step(t):
+                return synth.trajectory_logits(seed, t, rows_per_step[t], w.vocab)
+        else:
+            def logits_of_step(t):
+                return synth.trajectory_window_logits(seed, t, window_rows(w, policy), w.vocab)
     st = synth.trajectory_start(seed, w)
     im, tk, ds = st.is_masked.copy(), st.tokens.copy(), st.decode_step.copy()
     if layers:
@@ -73,18 +110,21 @@ def run(w: synth.Workload, seed: int, n_steps: int | None = None, logits_of_step
                 x = attention(q, kc[l], vc[l], cnt, 1.0 / math.sqrt(d)).reshape(r, hid)
             out = x
         # ---- decode and gate with step t's logits ----
-        lo, hi = synth.trajectory_block(w, t)
+        lo, hi = window(w, policy, t, im)
         pos_idx, pos_cnt = recompute_set(im, ds, np.zeros(1, np.uint8), lo, hi, 0)
         row_pos = pos_idx[0, :pos_cnt[0]]
         logits = logits_of_step(t)
+        if policy[0] != "block":
+            logits = logits[:row_pos.shape[0]]
         if logits.shape[0] != row_pos.shape[0]:
             raise ValueError("step logits do not match the masked rows of the block")
         h, c, tok = row_stats(logits)
         g = unmask_gate(c, h, tok, [0, len(row_pos)], row_pos, L, n, tau, t, im, tk, ds)
         im, tk, ds = g["is_masked"], g["tokens"], g["decode_step"]
-        nlo, nhi = synth.trajectory_block(w, t + 1)
+        nlo, nhi = window(w, policy, t + 1, im)
         idx_next, cnt_next = recompute_set(im, ds, g["refresh"], nlo, nhi, k)
-        records.append(dict(step=t, full=full_next, rows=int(cnt[0]), idx=idx[0, :cnt[0]].copy(),
+        records.append(dict(step=t, full=full_next, rows=int(cnt[0]), window=(lo, hi),
+                            idx=idx[0, :cnt[0]].copy(),
                             row_pos=row_pos.copy(), unmask_rows=g["unmask_rows"][0].copy(),
                             token=tok, entropy=h, conf=c, max_entropy=float(g["max_entropy"][0]),
                             refresh=int(g["refresh"][0]),

@@ -77,3 +77,61 @@ def test_always_refresh_forward_matches_dense_numpy():
         assert np.allclose(final["k_cache"][layer][0], kc, rtol=1e-12, atol=1e-12)
         x = np.concatenate(outs, axis=1)
     assert np.allclose(final["out"], x, rtol=1e-12, atol=1e-12)
+
+
+def _first_masked(is_masked, prompt_len, L):
+    gen = np.flatnonzero(is_masked[prompt_len:])
+    return prompt_len + int(gen[0]) if gen.size else L
+
+
+def _replay_masks(recs, w):
+    """is_masked before every step, rebuilt from the records' unmask decisions."""
+    im = np.zeros(w.seq_len, np.uint8)
+    im[w.prompt_len:] = 1
+    out = []
+    for r in recs:
+        out.append(im.copy())
+        for u in r["unmask_rows"]:
+            if u >= 0:
+                im[r["row_pos"][u]] = 0
+    return out
+
+
+def test_sliding_window_invariants():
+    # EntropyCache, section 5: the same skipping rule under a sliding window; the
+    # window starts at the first still-masked position and holds W positions
+    width = 12
+    recs, final = otraj.run(W, 5, policy=("sliding", width))
+    masks = _replay_masks(recs, W)
+    for t, (r, im) in enumerate(zip(recs, masks)):
+        lo = _first_masked(im, W.prompt_len, W.seq_len)
+        assert r["window"] == (lo, min(lo + width, W.seq_len))
+        want = np.flatnonzero(im[lo:lo + width]) + lo  # its masked positions, ascending
+        assert np.array_equal(r["row_pos"], want)
+        if t > 0 and not r["full"]:
+            # the partial forward recomputes the masked positions of this window
+            assert set(want.tolist()) <= set(r["idx"].tolist())
+    assert final["is_masked"].sum() == 0
+
+
+def test_multiblock_windows_are_whole_blocks():
+    recs, _ = otraj.run(W, 6, policy=("multiblock", 2))
+    masks = _replay_masks(recs, W)
+    for r, im in zip(recs, masks):
+        lo, hi = r["window"]
+        first = _first_masked(im, W.prompt_len, W.seq_len)
+        assert (lo - W.prompt_len) % W.block == 0 and lo <= first < lo + W.block
+        assert hi == min(lo + 2 * W.block, W.seq_len)
+        assert np.array_equal(r["row_pos"], np.flatnonzero(im[lo:hi]) + lo)
+
+
+def test_window_rules_agree_when_the_window_covers_the_response():
+    # a sliding window and a run of blocks as wide as the generated region see the
+    # same masked positions at every step, so the trajectories are identical
+    gen = W.seq_len - W.prompt_len
+    a, fa = otraj.run(W, 7, policy=("sliding", gen))
+    b, fb = otraj.run(W, 7, policy=("multiblock", gen // W.block))
+    for ra, rb in zip(a, b):
+        for key in ("full", "rows", "row_pos", "unmask_rows", "refresh", "idx_next"):
+            assert np.array_equal(ra[key], rb[key]), key
+    assert np.array_equal(fa["tokens"], fb["tokens"])
