@@ -1042,6 +1042,43 @@ def run_trajectory(args):
             "mean_rows": float(np.mean([r.rows for r in pr])),
             "decode_and_sets_ms": float(np.mean([r.decode_ms for r in pr]))}
         del tp
+    # the same trajectory with pre-norm layers (norms, rotary embedding, output
+    # projection, SwiGLU MLP of width 12288): its full forward, and the MLP's two
+    # contractions alone (launch indices in the layer's call list: 7 and 8)
+    wl = synth.scaled(w, ffn=12288)
+    tl = Trajectory(wl, seed=args.seed, device=device, stream=stream)
+    tl.warm_up()
+    tl.run()
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    lr = tl.run()
+    lwall = time.perf_counter() - t0
+    t_lfull = time_forward(tl, True, reps=3)
+
+    def time_call(call, reps=10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            call()
+            e0.record()
+            for _ in range(reps):
+                call()
+            e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / reps
+
+    t_gu = time_call(tl.forward_full[7])
+    t_down = time_call(tl.forward_full[8])
+    prenorm = {
+        "denoising_steps_per_s": wl.n_steps / lwall,
+        "refresh_fraction": sum(r.refresh for r in lr) / len(lr),
+        "full_forward_ms_replay": t_lfull * 1e3,
+        "mlp_gate_up_swiglu_us": t_gu * 1e6,
+        "mlp_gate_up_tflops": 2.0 * wl.seq_len * hid * 2 * wl.ffn / t_gu / 1e12,
+        "mlp_down_residual_us": t_down * 1e6,
+        "mlp_down_tflops": 2.0 * wl.seq_len * wl.ffn * hid / t_down / 1e12,
+        "layer": "rms_norm, qkv, rope, attention, o-proj + residual, rms_norm, SwiGLU, down + residual",
+        "weights": "drawn on the device (seeded), N(0, 1/fan_in)"}
+    del tl
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": t_max / K * 1e3, "higher_is_better": True,
@@ -1070,6 +1107,7 @@ def run_trajectory(args):
             "projection_partial_us": t_proj_sel * 1e6,
             "projection_partial_weight_gbs": wbytes / t_proj_sel / 1e9,
             "policies": policies,
+            "prenorm_layers": prenorm,
         },
         "roofline": {"bound": "tensor", "achieved": proj_tflops, "peak": tc, "unit": "TFLOP/s",
                      "frac": proj_tflops / tc, "traffic": None,

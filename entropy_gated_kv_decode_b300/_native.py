@@ -32,7 +32,8 @@ EXPORTED = ("ec_status_str", "ec_abi_version", "ec_debug_set_wait_limit", "ec_wo
             "ec_decode_noalloc_read_status", "ec_lmhead_workspace_size", "ec_lmhead_decode_step",
             "ec_build_recompute_set", "ec_attention_workspace_size", "ec_attention_kernel_count",
             "ec_selective_attention", "ec_selective_attention_simsd",
-            "ec_selective_attention_cover", "ec_embed_rows", "ec_qkv_projection")
+            "ec_selective_attention_cover", "ec_embed_rows", "ec_qkv_projection",
+            "ec_rms_norm", "ec_rope", "ec_linear")
 
 
 class NativeLibraryMissing(RuntimeError):
@@ -91,12 +92,17 @@ def lib() -> ctypes.CDLL:
         L.ec_embed_rows.argtypes = [vp, i64, i32, vp, i64, vp, vp, vp, i32, i32, i32, i32, vp, vp,
                                     sz, vp]
         L.ec_qkv_projection.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, sz, vp]
+        L.ec_rms_norm.argtypes = [vp, vp, i32, i32, i32, vp, f32, vp, vp, sz, vp]
+        L.ec_rope.argtypes = [vp, vp, vp, i64, vp, i32, i32, i32, i32, i32, i32, ctypes.c_double,
+                              vp, sz, vp]
+        L.ec_linear.argtypes = [vp, vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, sz, vp]
         for name in ("ec_debug_set_wait_limit", "ec_workspace_init", "ec_read_device_status",
                      "ec_decode_step",
                      "ec_decode_step_noalloc", "ec_decode_noalloc_read_status",
                      "ec_lmhead_decode_step", "ec_build_recompute_set",
                      "ec_selective_attention", "ec_selective_attention_simsd",
-                     "ec_selective_attention_cover", "ec_embed_rows", "ec_qkv_projection"):
+                     "ec_selective_attention_cover", "ec_embed_rows", "ec_qkv_projection",
+                     "ec_rms_norm", "ec_rope", "ec_linear"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -439,6 +445,72 @@ def ec_qkv_projection(x, count, w_qkv, q, k, v, workspace, stream=None):
     _check(lib().ec_qkv_projection(*args, _stream(stream)), "ec_qkv_projection")
 
 
+def _rms_norm_args(x, count, weight, eps, y, workspace):
+    for name, t in (("x", x), ("weight", weight), ("y", y)):
+        _cuda(name, t, torch.bfloat16)
+    _cuda("workspace", workspace, torch.uint8)
+    if count is not None:
+        _cuda("count", count, torch.int32)
+    if x.dim() != 3 or y.shape != x.shape or weight.numel() != x.shape[2]:
+        raise ValueError("x, y [batch, r_max, hidden]; weight [hidden]")
+    batch, r_max, hidden = x.shape
+    return [_p(x), _p(count), batch, r_max, hidden, _p(weight), float(eps), _p(y), _p(workspace),
+            workspace.numel()]
+
+
+def ec_rms_norm(x, count, weight, eps, y, workspace, stream=None):
+    """y = x / sqrt(mean(x^2) + eps) * weight over the rows < count (bf16)."""
+    _check(lib().ec_rms_norm(*_rms_norm_args(x, count, weight, eps, y, workspace),
+                             _stream(stream)), "ec_rms_norm")
+
+
+def _rope_args(q, k, idx, count, seq_len, theta, workspace):
+    for name, t in (("q", q), ("k", k)):
+        _cuda(name, t, torch.bfloat16)
+    _cuda("idx", idx, torch.int32)
+    _cuda("count", count, torch.int32)
+    _cuda("workspace", workspace, torch.uint8)
+    if q.dim() != 4 or k.dim() != 4 or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q [batch, r_max, heads, d], k [batch, r_max, kv_heads, d]")
+    batch, r_max, h, d = q.shape
+    return [_p(q), _p(k), _p(idx), idx.shape[1], _p(count), batch, int(seq_len), r_max, h,
+            k.shape[2], d, float(theta), _p(workspace), workspace.numel()]
+
+
+def ec_rope(q, k, idx, count, seq_len, theta, workspace, stream=None):
+    """Rotary embedding of q and k rows in place, row r of sequence b at idx[b, r]."""
+    _check(lib().ec_rope(*_rope_args(q, k, idx, count, seq_len, theta, workspace),
+                         _stream(stream)), "ec_rope")
+
+
+LINEAR_STORE, LINEAR_RESIDUAL, LINEAR_SWIGLU = 0, 1, 2
+
+
+def _linear_args(x, count, w, mode, residual, y, workspace):
+    for name, t in (("x", x), ("w", w), ("y", y)):
+        _cuda(name, t, torch.bfloat16)
+    if mode == LINEAR_RESIDUAL:
+        _cuda("residual", residual, torch.bfloat16)
+    _cuda("workspace", workspace, torch.uint8)
+    if count is not None:
+        _cuda("count", count, torch.int32)
+    if x.dim() != 3 or w.dim() != 2 or w.shape[1] != x.shape[2]:
+        raise ValueError("x [batch, r_max, in], w [out (x2 for SwiGLU), in]")
+    batch, r_max, n_in = x.shape
+    n_out = w.shape[0] // 2 if mode == LINEAR_SWIGLU else w.shape[0]
+    if y.shape != (batch, r_max, n_out) or (mode == LINEAR_RESIDUAL and residual.shape != y.shape):
+        raise ValueError("y (and residual) [batch, r_max, out]")
+    return [_p(x), _p(count), batch, r_max, n_in, _p(w), n_out, int(mode),
+            _p(residual) if mode == LINEAR_RESIDUAL else None, _p(y), _p(workspace),
+            workspace.numel()]
+
+
+def ec_linear(x, count, w, mode, residual, y, workspace, stream=None):
+    """y = x w^T (mode 0), residual + x w^T (1), silu(x w_g^T) * x w_u^T (2, w = [w_g; w_u])."""
+    _check(lib().ec_linear(*_linear_args(x, count, w, mode, residual, y, workspace),
+                           _stream(stream)), "ec_linear")
+
+
 # ---------------------------------------------------------------------------
 # Prepared calls: validate and marshal once, then invoke with almost no host
 # cost.  The tensors bound at preparation must stay alive and in place.
@@ -499,6 +571,18 @@ def prepare_selective_attention_simsd(*args, stream=None, **kwargs):
 def prepare_selective_attention_cover(*args, stream=None, **kwargs):
     return Prepared("ec_selective_attention_cover", _cover_args(*args, **kwargs), stream,
                     keep=(args, kwargs))
+
+
+def prepare_rms_norm(*args, stream=None, **kwargs):
+    return Prepared("ec_rms_norm", _rms_norm_args(*args, **kwargs), stream, keep=(args, kwargs))
+
+
+def prepare_rope(*args, stream=None, **kwargs):
+    return Prepared("ec_rope", _rope_args(*args, **kwargs), stream, keep=(args, kwargs))
+
+
+def prepare_linear(*args, stream=None, **kwargs):
+    return Prepared("ec_linear", _linear_args(*args, **kwargs), stream, keep=(args, kwargs))
 
 
 def prepare_embed_rows(*args, stream=None, **kwargs):

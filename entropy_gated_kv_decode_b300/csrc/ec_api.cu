@@ -348,4 +348,59 @@ ec_status ec_embed_rows(const void *table, int64_t table_rows, int32_t hidden, c
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+
+ec_status ec_rms_norm(const void *x, const int32_t *count, int32_t batch, int32_t r_max,
+                      int32_t hidden, const void *weight, float eps, void *y, void *workspace,
+                      size_t workspace_bytes, ec_stream_t stream)
+{
+    if (batch < 1 || r_max < 0 || !ec::rms_norm_shape_ok(hidden) || !(eps >= 0.f) || !isfinite(eps))
+        return EC_ERR_SHAPE;
+    if (!workspace) return EC_ERR_NULL;
+    if (r_max > 0 && (!x || !weight || !y)) return EC_ERR_NULL;
+    const void *ptrs[] = {x, weight, y};
+    for (const void *p : ptrs)
+        if (p && !aligned(p, 16)) return EC_ERR_ALIGN;
+    if (!aligned(workspace, EC_WORKSPACE_ALIGN) || workspace_bytes < ec::kWsHeader)
+        return EC_ERR_WORKSPACE;
+    return launched(ec::launch_rms_norm(x, count, batch, r_max, hidden, weight, eps, y,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ec_status ec_rope(void *q, void *k, const int32_t *idx, int64_t idx_stride, const int32_t *count,
+                  int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
+                  int32_t n_kv_heads, int32_t head_dim, double theta, void *workspace,
+                  size_t workspace_bytes, ec_stream_t stream)
+{
+    if (batch < 1 || seq_len < 1 || r_max < 0 || n_heads < 1 || n_kv_heads < 1 ||
+        !ec::rope_shape_ok(head_dim) || idx_stride < r_max || !(theta > 1.0) || !isfinite(theta))
+        return EC_ERR_SHAPE;
+    if (!count || !workspace) return EC_ERR_NULL;
+    if (r_max > 0 && (!q || !k || !idx)) return EC_ERR_NULL;
+    if (!aligned(workspace, EC_WORKSPACE_ALIGN) || workspace_bytes < ec::kWsHeader)
+        return EC_ERR_WORKSPACE;
+    return launched(ec::launch_rope(q, k, idx, idx_stride, count, batch, seq_len, r_max, n_heads,
+                                    n_kv_heads, head_dim, theta,
+                                    static_cast<uint32_t *>(workspace),
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ec_status ec_linear(const void *x, const int32_t *count, int32_t batch, int32_t r_max,
+                    int32_t in_features, const void *w, int32_t out_features, int32_t mode,
+                    const void *residual, void *y, void *workspace, size_t workspace_bytes,
+                    ec_stream_t stream)
+{
+    if (batch < 1 || r_max < 0 || !ec::linear_shape_ok(in_features, out_features, mode))
+        return EC_ERR_SHAPE;
+    if (!workspace) return EC_ERR_NULL;
+    if (r_max > 0 && (!x || !w || !y || (mode == 1 && !residual))) return EC_ERR_NULL;
+    const void *ptrs[] = {x, w, y, mode == 1 ? residual : nullptr};
+    for (const void *p : ptrs)
+        if (p && !aligned(p, 16)) return EC_ERR_ALIGN;
+    if (!aligned(workspace, EC_WORKSPACE_ALIGN) || workspace_bytes < ec::kWsHeader)
+        return EC_ERR_WORKSPACE;
+    return launched(ec::launch_linear(x, count, batch, r_max, in_features, w, out_features, mode,
+                                      residual, y, static_cast<uint32_t *>(workspace),
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -148,6 +148,21 @@ cudaError_t launch_attention_tc(const void *q, const void *k_new, const void *v_
 
 // qkv_gemm.cu
 bool qkv_shape_ok(int32_t hidden, int32_t width);
+bool linear_shape_ok(int32_t in_features, int32_t out_features, int32_t mode);
+cudaError_t launch_linear(const void *x, const int32_t *count, int32_t batch, int32_t r_max,
+                          int32_t in_features, const void *w, int32_t out_features, int32_t mode,
+                          const void *residual, void *out, uint32_t *status, cudaStream_t stream);
+
+// layer_ops.cu
+bool rms_norm_shape_ok(int32_t hidden);
+cudaError_t launch_rms_norm(const void *x, const int32_t *count, int32_t batch, int32_t r_max,
+                            int32_t hidden, const void *weight, float eps, void *out,
+                            cudaStream_t stream);
+bool rope_shape_ok(int32_t head_dim);
+cudaError_t launch_rope(void *q, void *k, const int32_t *idx, int64_t idx_stride, const int32_t *count,
+                        int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
+                        int32_t n_kv_heads, int32_t head_dim, double theta, uint32_t *status,
+                        cudaStream_t stream);
 cudaError_t launch_qkv_projection(const void *x, const int32_t *count, int32_t batch,
                                   int32_t r_max, int32_t hidden, const void *w_qkv, int32_t width,
                                   void *q, void *k, void *v, uint32_t *status, cudaStream_t stream);

@@ -20,6 +20,16 @@
 //               a time, rounded to bf16 and stored into Q, K or V.
 // Tiles are dealt round-robin with the (sequence, row-tile) index varying
 // fastest, so the CTAs running at one time share weight tiles through L2.
+//
+// The same kernel serves the other dense contractions of a transformer layer
+// (a pre-norm block: output projection and gated MLP), with one of four
+// epilogues:
+//   QKV       the three column segments of W into Q, K and V;
+//   STORE     Y = X W^T;
+//   RESIDUAL  Y = R + X W^T (R may be Y itself);
+//   SWIGLU    W = [W_gate; W_up] ([2F, hidden]); a tile's B operand holds BN/2
+//             gate rows and the BN/2 up rows of the same outputs (two TMA boxes),
+//             and Y[:, j] = silu(g_j) u_j, g and u the two halves of the tile.
 // Row tiles at or past count[b] are skipped by every role alike.  Every wait is
 // bounded (~2 s); a timeout sets EC_DEV_TIMEOUT and unwinds.
 #include <cuda_bf16.h>
@@ -63,10 +73,15 @@ enum : int {
     G_COUNT = 21
 };
 
+enum : int { EPI_QKV = 0, EPI_STORE = 1, EPI_RESIDUAL = 2, EPI_SWIGLU = 3 };
+
 struct GemmParams {
     const int32_t *count;  // [batch] rows present per sequence, or null (= r_max)
     __nv_bfloat16 *out[3];
+    const __nv_bfloat16 *res;  // RESIDUAL: R, [batch, r_max, width]
+    int mode;
     int batch, r_max, hidden, width, n_mt, n_nt, n_tiles;
+    int w_half;  // SWIGLU: F, the row where W_up starts
     uint32_t *status;
     long long wait_limit;  // cycles one in-kernel wait may take
 };
@@ -108,7 +123,13 @@ __device__ void gemm_producer(const GemmParams &P, const Sync &S, uint32_t sbase
             const uint32_t dst = sbase + s * C::kStage;
             mbar_expect_tx(S.bar(G_FULL + s), C::kStage);
             tma_load_3d(dst, tm_x, S.bar(G_FULL + s), kb * kBK, w.mt * kBM, w.b);
-            tma_load_2d(dst + C::kA, tm_w, S.bar(G_FULL + s), kb * kBK, w.nt * BN);
+            if (P.mode == EPI_SWIGLU) {  // BN/2 gate rows, then the same outputs' up rows
+                tma_load_2d(dst + C::kA, tm_w, S.bar(G_FULL + s), kb * kBK, w.nt * (BN / 2));
+                tma_load_2d(dst + C::kA + (BN / 2) * kBK * 2, tm_w, S.bar(G_FULL + s), kb * kBK,
+                            P.w_half + w.nt * (BN / 2));
+            } else {
+                tma_load_2d(dst + C::kA, tm_w, S.bar(G_FULL + s), kb * kBK, w.nt * BN);
+            }
         }
     }
     if (!ok)  // let every copy already started land before the CTA exits
@@ -172,15 +193,40 @@ __device__ void gemm_epilogue(const GemmParams &P, const Sync &S, uint32_t tmem)
         tc_fence_after();
         const int r = w.mt * kBM + row;
         const bool valid = r < w.rows;
-        const int n0 = w.nt * BN;
-        const int seg = n0 / P.width;
-        __nv_bfloat16 *dst = P.out[seg] +
-                             (static_cast<int64_t>(w.b) * P.r_max + r) * P.width + (n0 - seg * P.width);
+        const bool swiglu = P.mode == EPI_SWIGLU;
+        const int n0 = swiglu ? w.nt * (BN / 2) : w.nt * BN;  // first output column
+        const int seg = P.mode == EPI_QKV ? n0 / P.width : 0;
+        const int64_t off = (static_cast<int64_t>(w.b) * P.r_max + r) * P.width + (n0 - seg * P.width);
+        __nv_bfloat16 *dst = P.out[seg] + off;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < (swiglu ? BN / 64 : BN / 32); ++c) {
             uint32_t v[32];
             tmem_ld32(tmem + lane_off + a * BN + c * 32, v);
             tmem_wait_ld(v);
+            if (swiglu) {  // v = gate columns; the up columns sit BN/2 further
+                uint32_t u[32];
+                tmem_ld32(tmem + lane_off + a * BN + BN / 2 + c * 32, u);
+                tmem_wait_ld(u);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float g = __uint_as_float(v[j]);
+                    v[j] = __float_as_uint(g / (1.f + __expf(-g)) * __uint_as_float(u[j]));
+                }
+            } else if (P.mode == EPI_RESIDUAL && valid) {
+                const uint4 *r4 = reinterpret_cast<const uint4 *>(P.res + off + c * 32);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 x = r4[q];
+                    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        v[8 * q + 2 * e] = __float_as_uint(__uint_as_float(v[8 * q + 2 * e]) +
+                                                           __uint_as_float(xs[e] << 16));
+                        v[8 * q + 2 * e + 1] = __float_as_uint(__uint_as_float(v[8 * q + 2 * e + 1]) +
+                                                               __uint_as_float(xs[e] & 0xffff0000u));
+                    }
+                }
+            }
             if (valid) {
                 uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
 #pragma unroll
@@ -278,16 +324,17 @@ bool encode(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims
 }
 
 // Tile width: minimise (rounds of tiles per CTA) x (per-tile cost ~ BN + 64),
-// among the widths that divide `width`.
-int choose_bn(int batch, int r_max, int width)
+// among the widths that tile the output (`segs` segments of `width` columns;
+// SWIGLU: BN/2 must divide F).
+int choose_bn(int batch, int r_max, int width, int segs = 3, bool swiglu = false)
 {
     const int n_sm = device_sm_count();
     const int n_mt = (r_max + kBM - 1) / kBM;
     int best_bn = 0;
     double best = 1e30;
     for (int bn : {256, 128, 64}) {
-        if (width % bn) continue;
-        const int64_t tiles = static_cast<int64_t>(batch) * n_mt * (3 * width / bn);
+        if (swiglu ? width % (bn / 2) : width % bn) continue;
+        const int64_t tiles = static_cast<int64_t>(batch) * n_mt * (segs * width / bn);
         const double cost = static_cast<double>((tiles + n_sm - 1) / n_sm) * (bn + 64);
         if (cost < best - 1e-9) {
             best = cost;
@@ -301,7 +348,8 @@ template <int BN>
 cudaError_t launch_bn(GemmParams p, const void *x, const void *w, cudaStream_t stream)
 {
     using C = GemmCfg<BN>;
-    p.n_nt = 3 * p.width / BN;
+    const int w_rows = p.mode == EPI_QKV ? 3 * p.width : (p.mode == EPI_SWIGLU ? 2 * p.width : p.width);
+    p.n_nt = w_rows / BN;
     p.n_tiles = p.batch * p.n_mt * p.n_nt;
     CUtensorMap tx, tw;
     const cuuint64_t xd[3] = {static_cast<cuuint64_t>(p.hidden), static_cast<cuuint64_t>(p.r_max),
@@ -309,9 +357,9 @@ cudaError_t launch_bn(GemmParams p, const void *x, const void *w, cudaStream_t s
     const cuuint64_t xs[2] = {static_cast<cuuint64_t>(p.hidden) * 2,
                               static_cast<cuuint64_t>(p.r_max) * p.hidden * 2};
     const cuuint32_t xb[3] = {kBK, kBM, 1};
-    const cuuint64_t wd[2] = {static_cast<cuuint64_t>(p.hidden), static_cast<cuuint64_t>(3 * p.width)};
+    const cuuint64_t wd[2] = {static_cast<cuuint64_t>(p.hidden), static_cast<cuuint64_t>(w_rows)};
     const cuuint64_t ws[1] = {static_cast<cuuint64_t>(p.hidden) * 2};
-    const cuuint32_t wbx[2] = {kBK, BN};
+    const cuuint32_t wbx[2] = {kBK, static_cast<cuuint32_t>(p.mode == EPI_SWIGLU ? BN / 2 : BN)};
     if (!encode(&tx, x, 3, xd, xs, xb) || !encode(&tw, w, 2, wd, ws, wbx)) return cudaErrorInvalidValue;
     const int grid = std::min(p.n_tiles, device_sm_count());
     return launch(qkv_gemm_kernel<BN>, dim3(grid), dim3(kThreads), C::kBytes, stream, p, tx, tw);
@@ -373,10 +421,45 @@ cudaError_t launch_qkv_projection(const void *x, const int32_t *count, int32_t b
     p.n_mt = (r_max + kBM - 1) / kBM;
     p.status = status;
     p.wait_limit = wait_limit_cycles();
+    p.mode = EPI_QKV;
+    p.res = nullptr;
+    p.w_half = 0;
     switch (choose_bn(batch, r_max, width)) {
     case 256: return launch_bn<256>(p, x, w_qkv, stream);
     case 128: return launch_bn<128>(p, x, w_qkv, stream);
     default: return launch_bn<64>(p, x, w_qkv, stream);
+    }
+}
+
+bool linear_shape_ok(int32_t in_features, int32_t out_features, int32_t mode)
+{
+    return in_features >= kBK && in_features % kBK == 0 && out_features >= 64 &&
+           out_features % (mode == 2 ? 32 : 64) == 0 && mode >= 0 && mode <= 2;
+}
+
+cudaError_t launch_linear(const void *x, const int32_t *count, int32_t batch, int32_t r_max,
+                          int32_t in_features, const void *w, int32_t out_features, int32_t mode,
+                          const void *residual, void *out, uint32_t *status, cudaStream_t stream)
+{
+    if (r_max == 0) return cudaSuccess;
+    GemmParams p;
+    p.count = count;
+    p.out[0] = p.out[1] = p.out[2] = static_cast<__nv_bfloat16 *>(out);
+    p.res = static_cast<const __nv_bfloat16 *>(residual);
+    p.mode = mode == 0 ? EPI_STORE : (mode == 1 ? EPI_RESIDUAL : EPI_SWIGLU);
+    p.batch = batch;
+    p.r_max = r_max;
+    p.hidden = in_features;
+    p.width = out_features;
+    p.w_half = mode == 2 ? out_features : 0;
+    p.n_mt = (r_max + kBM - 1) / kBM;
+    p.status = status;
+    p.wait_limit = wait_limit_cycles();
+    const bool sw = p.mode == EPI_SWIGLU;
+    switch (choose_bn(batch, r_max, out_features, sw ? 2 : 1, sw)) {
+    case 256: return launch_bn<256>(p, x, w, stream);
+    case 128: return launch_bn<128>(p, x, w, stream);
+    default: return launch_bn<64>(p, x, w, stream);
     }
 }
 

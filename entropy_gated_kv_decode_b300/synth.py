@@ -70,6 +70,9 @@ class Workload:
     qkv_std: float
     n_layers: int = 0
     n_steps: int = 0
+    ffn: int = 0            # > 0: pre-norm layers with a SwiGLU MLP of this width
+    rope_theta: float = 500000.0
+    norm_eps: float = 1e-5
 
     @property
     def rows_per_seq(self) -> int:
@@ -396,6 +399,22 @@ def trajectory_start(seed: int, w: Workload) -> TrajectoryStart:
     is_masked = np.zeros((1, L), np.uint8)
     is_masked[0, w.prompt_len:] = 1
     return TrajectoryStart(is_masked, tokens, np.full((1, L), -1, np.int32))
+
+
+def trajectory_layer_weights(seed: int, layer: int, hidden: int, ffn: int) -> dict:
+    """bf16 weights of one pre-norm layer: w_qkv [3h, h], w_o [h, h], w_gu [2F, h]
+    (gate rows, then up rows), w_down [h, F], each N(0, 1/fan_in); the two RMS-norm
+    gains 1 + N(0, 0.1^2)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0x1A7, layer]))
+
+    def draw(rows, cols):
+        x = rng.standard_normal((rows, cols), dtype=np.float32)
+        x *= np.float32(1.0 / math.sqrt(cols))
+        return f32_to_bf16_bits(x)
+
+    gains = (1.0 + 0.1 * rng.standard_normal((2, hidden))).astype(np.float32)
+    return dict(w_qkv=draw(3 * hidden, hidden), w_o=draw(hidden, hidden), w_gu=draw(2 * ffn, hidden),
+                w_down=draw(hidden, ffn), g1=f32_to_bf16_bits(gains[0]), g2=f32_to_bf16_bits(gains[1]))
 
 
 def trajectory_embedding(seed: int, vocab: int, hidden: int) -> np.ndarray:

@@ -11,7 +11,11 @@ and the Arabic technical summary, "Algorithm workflow" phases 1-3.
 The model is synthetic: ``n_layers`` layers, each a Q/K/V projection of the
 recomputed rows followed by selective bidirectional attention over that
 layer's KV cache; a layer's attention output rows are the next layer's input
-rows, and layer 0 reads token embeddings.  The logits of every step are seeded
+rows, and layer 0 reads token embeddings.  With ``ffn`` > 0 the layers are
+pre-norm transformer blocks instead (the layer of the pages' models):
+    a = rms_norm(x, g1); [q|k|v] = a W_qkv^T; rope(q, k); o = attention;
+    x += o W_o^T; b = rms_norm(x, g2); x += (silu(b W_gate^T) * b W_up^T) W_down^T
+(ec_rms_norm, ec_qkv_projection, ec_rope, ec_selective_attention, ec_linear).  The logits of every step are seeded
 random numbers (no LM head), so the decision sequence does not depend on the
 layers' numerics.
 
@@ -95,11 +99,16 @@ class Trajectory:
         self.r_sel = min(self.win_rows + w.k, L)
         i32, u8, bf = torch.int32, torch.uint8, torch.bfloat16
         dev = self.dev
+        self.llama = w.ffn > 0
         with torch.cuda.stream(self.stream):
             self.table = _up(synth.trajectory_embedding(seed, V, hid), dev)
-            self.weights = torch.empty((w.n_layers, 3 * hid, hid), dtype=bf, device=dev)
-            for layer in range(w.n_layers):
-                self.weights[layer].copy_(_up(synth.trajectory_weights(seed, layer, hid, hid), dev))
+            if self.llama:
+                self.layers = [self._layer_weights(seed, layer) for layer in range(w.n_layers)]
+                self.weights = torch.stack([lw["w_qkv"] for lw in self.layers])
+            else:
+                self.weights = torch.empty((w.n_layers, 3 * hid, hid), dtype=bf, device=dev)
+                for layer in range(w.n_layers):
+                    self.weights[layer].copy_(_up(synth.trajectory_weights(seed, layer, hid, hid), dev))
             self.k_cache = torch.zeros((w.n_layers, 1, L, w.n_kv_heads, d), dtype=bf, device=dev)
             self.v_cache = torch.zeros_like(self.k_cache)
             # every step's logits, resident: rows of step t start at row_off[t]
@@ -122,6 +131,9 @@ class Trajectory:
             # activations: two hidden-state buffers and q / k / v
             self.xa = torch.zeros((1, L, hid), dtype=bf, device=dev)
             self.xb = torch.zeros_like(self.xa)
+            if self.llama:
+                self.o = torch.zeros_like(self.xa)
+                self.m = torch.zeros((1, L, w.ffn), dtype=bf, device=dev)
             self.q = torch.zeros_like(self.xa)
             self.k = torch.zeros_like(self.xa)
             self.v = torch.zeros_like(self.xa)
@@ -170,10 +182,31 @@ class Trajectory:
         self.next_rows = w.seq_len
         self.win = None  # this step's window (window policies)
 
+    def _layer_weights(self, seed: int, layer: int) -> dict:
+        """One pre-norm layer's weights on the device: from the shared generator
+        for models up to hidden 1024, else drawn on the device (seeded) with the
+        same scales, since the host would take minutes for billions of values."""
+        w, dev, hid = self.w, self.dev, self.hidden
+        if hid <= 1024:
+            return {k: _up(v, dev) for k, v in
+                    synth.trajectory_layer_weights(seed, layer, hid, w.ffn).items()}
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed * 1000003 + layer)
+
+        def draw(rows, cols):
+            return (torch.randn((rows, cols), generator=g, device=dev) / math.sqrt(cols)).to(torch.bfloat16)
+
+        gains = 1.0 + 0.1 * torch.randn((2, hid), generator=g, device=dev)
+        return dict(w_qkv=draw(3 * hid, hid), w_o=draw(hid, hid), w_gu=draw(2 * w.ffn, hid),
+                    w_down=draw(hid, w.ffn), g1=gains[0].to(torch.bfloat16).contiguous(),
+                    g2=gains[1].to(torch.bfloat16).contiguous())
+
     # -- launch plan ---------------------------------------------------------
 
     def _forward_calls(self, idx, count, r):
         """Prepared calls of one forward over `r` row slots (count[0] of them used)."""
+        if self.llama:
+            return self._llama_calls(idx, count, r)
         w, s = self.w, self.stream
         x = [self.xa[:, :r], self.xb[:, :r]]
         q, k, v = self.q[:, :r], self.k[:, :r], self.v[:, :r]
@@ -188,6 +221,33 @@ class Trajectory:
                 q.view(1, r, H, d), k.view(1, r, Hkv, d), v.view(1, r, Hkv, d), idx, count,
                 self.k_cache[layer], self.v_cache[layer], xout.view(1, r, H, d), self.scale,
                 self.ws_att, stream=s))
+        return calls
+
+    def _llama_calls(self, idx, count, r):
+        """The pre-norm layers: the residual stream stays in xa, xb holds the
+        normalised rows."""
+        w, s = self.w, self.stream
+        H, Hkv, d = w.n_heads, w.n_kv_heads, w.head_dim
+        x, a, o, m = self.xa[:, :r], self.xb[:, :r], self.o[:, :r], self.m[:, :r]
+        q, k, v = self.q[:, :r], self.k[:, :r], self.v[:, :r]
+        ws = self.ws_fwd
+        calls = [nat.prepare_embed_rows(self.table, idx, count, self.tokens, self.is_masked,
+                                        w.vocab, x, ws, stream=s)]
+        for layer, lw in enumerate(self.layers):
+            calls += [
+                nat.prepare_rms_norm(x, count, lw["g1"], w.norm_eps, a, ws, stream=s),
+                nat.prepare_qkv_projection(a, count, lw["w_qkv"], q, k, v, ws, stream=s),
+                nat.prepare_rope(q.view(1, r, H, d), k.view(1, r, Hkv, d), idx, count, w.seq_len,
+                                 w.rope_theta, ws, stream=s),
+                nat.prepare_selective_attention(
+                    q.view(1, r, H, d), k.view(1, r, Hkv, d), v.view(1, r, Hkv, d), idx, count,
+                    self.k_cache[layer], self.v_cache[layer], o.view(1, r, H, d), self.scale,
+                    self.ws_att, stream=s),
+                nat.prepare_linear(o, count, lw["w_o"], nat.LINEAR_RESIDUAL, x, x, ws, stream=s),
+                nat.prepare_rms_norm(x, count, lw["g2"], w.norm_eps, a, ws, stream=s),
+                nat.prepare_linear(a, count, lw["w_gu"], nat.LINEAR_SWIGLU, None, m, ws, stream=s),
+                nat.prepare_linear(m, count, lw["w_down"], nat.LINEAR_RESIDUAL, x, x, ws, stream=s),
+            ]
         return calls
 
     def _forward(self, full: bool):

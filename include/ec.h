@@ -421,6 +421,54 @@ ec_status ec_qkv_projection(const void *x, const int32_t *count, int32_t batch, 
                             int32_t hidden, const void *w_qkv, int32_t width, void *q, void *k,
                             void *v, void *workspace, size_t workspace_bytes, ec_stream_t stream);
 
+/* ------------------------------------------------------------------------- */
+/* the rest of a pre-norm transformer layer over the recomputed rows          */
+/* ------------------------------------------------------------------------- */
+/*
+ * The models the pages run (LLaDA-8B, Dream-7B) stack pre-norm layers:
+ *   a = rms_norm(x, g1);  [q|k|v] = a W_qkv^T;  rope(q, k);  o = attention;
+ *   h = x + o W_o^T;  b = rms_norm(h, g2);  y = h + W_down (silu(b W_gate^T) * b W_up^T)
+ * and a partial forward ([EC-it] step 2) runs them on the recomputed rows only.
+ * These three calls, with ec_qkv_projection and ec_selective_attention, make that
+ * layer; each works on rows r < count[b] of [batch, r_max, ...] bf16 tensors and
+ * leaves the others unchanged.  Workspace: at least EC_WORKSPACE_ALIGN bytes (the
+ * status word), aligned, zeroed once.
+ */
+
+/* y = x / sqrt(mean_j x_j^2 + eps) * weight, float32 arithmetic, bf16 out.  x, y
+ * [batch, r_max, hidden] (may alias), weight [hidden]; hidden a multiple of 8;
+ * count may be NULL (all r_max rows); 16-byte aligned pointers. */
+ec_status ec_rms_norm(const void *x, const int32_t *count, int32_t batch, int32_t r_max,
+                      int32_t hidden, const void *weight, float eps, void *y, void *workspace,
+                      size_t workspace_bytes, ec_stream_t stream);
+
+/* Rotary position embedding in place: for row r of sequence b at position
+ * p = idx[b*idx_stride + r] and every head of q ([batch, r_max, n_heads,
+ * head_dim]) and k ([batch, r_max, n_kv_heads, head_dim]), the pairs
+ * (x_i, x_{i + head_dim/2}), i < head_dim/2, turn by the angle
+ * p * theta^(-2 i / head_dim) (computed in double precision):
+ *   x_i' = x_i cos - x_{i+d/2} sin,   x_{i+d/2}' = x_{i+d/2} cos + x_i sin.
+ * head_dim even, at most 128; a position outside [0, seq_len) leaves its row
+ * unchanged and sets EC_DEV_BAD_INDEX. */
+ec_status ec_rope(void *q, void *k, const int32_t *idx, int64_t idx_stride, const int32_t *count,
+                  int32_t batch, int32_t seq_len, int32_t r_max, int32_t n_heads,
+                  int32_t n_kv_heads, int32_t head_dim, double theta, void *workspace,
+                  size_t workspace_bytes, ec_stream_t stream);
+
+/* Linear layer of the recomputed rows on the tensor cores (bf16 operands, float32
+ * accumulation, bf16 out), x [batch, r_max, in_features]:
+ *   mode 0  y = x W^T,               W [out_features, in_features]
+ *   mode 1  y = residual + x W^T     (residual may be y itself)
+ *   mode 2  y = silu(x W_g^T) * (x W_u^T), W = [W_g; W_u] [2 out_features, in_features],
+ *           silu(z) = z / (1 + e^-z)
+ * y and residual [batch, r_max, out_features].  in_features a multiple of 64;
+ * out_features a multiple of 64 (mode 2: of 32, at least 64); count may be NULL;
+ * 16-byte aligned pointers. */
+ec_status ec_linear(const void *x, const int32_t *count, int32_t batch, int32_t r_max,
+                    int32_t in_features, const void *w, int32_t out_features, int32_t mode,
+                    const void *residual, void *y, void *workspace, size_t workspace_bytes,
+                    ec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,6 +36,7 @@ import numpy as np
 from entropy_gated_kv_decode_b300 import synth
 
 from . import attention, embed_rows, projection, recompute_set, row_stats, scatter_kv, unmask_gate
+from . import layer as olayer
 
 
 def _widen(a):
@@ -86,7 +87,10 @@ def run(w: synth.Workload, seed: int, n_steps: int | None = None, logits_of_step
     im, tk, ds = st.is_masked.copy(), st.tokens.copy(), st.decode_step.copy()
     if layers:
         table = synth.trajectory_embedding(seed, w.vocab, hid)
-        weights = [_widen(synth.trajectory_weights(seed, l, hid, hid)) for l in range(layers)]
+        if w.ffn:
+            weights = [synth.trajectory_layer_weights(seed, l, hid, w.ffn) for l in range(layers)]
+        else:
+            weights = [_widen(synth.trajectory_weights(seed, l, hid, hid)) for l in range(layers)]
         kc = [np.zeros((1, L, H, d)) for _ in range(layers)]
         vc = [np.zeros((1, L, H, d)) for _ in range(layers)]
     full_next, idx_next, cnt_next = True, None, None
@@ -102,6 +106,21 @@ def run(w: synth.Workload, seed: int, n_steps: int | None = None, logits_of_step
             r = int(cnt[0])
             x = _widen(embed_rows(table, idx, cnt, tk, im, w.vocab, r)).reshape(r, hid)
             for l in range(layers):
+                if w.ffn:  # a pre-norm block (oracle/layer.py)
+                    lw = weights[l]
+                    a = olayer.rms_norm(x, lw["g1"], w.norm_eps)
+                    y = olayer.linear(a, lw["w_qkv"])
+                    pos = idx[0, :r]
+                    q = olayer.rope(y[:, :hid].reshape(r, H, d), pos, w.rope_theta).reshape(1, r, H, d)
+                    kn = olayer.rope(y[:, hid:2 * hid].reshape(r, H, d), pos,
+                                     w.rope_theta).reshape(1, r, H, d)
+                    vn = y[:, 2 * hid:].reshape(1, r, H, d)
+                    kc[l], vc[l] = scatter_kv(kn, vn, idx, cnt, kc[l], vc[l])
+                    o = attention(q, kc[l], vc[l], cnt, 1.0 / math.sqrt(d)).reshape(r, hid)
+                    x = olayer.linear(o, lw["w_o"], 1, x)
+                    b = olayer.rms_norm(x, lw["g2"], w.norm_eps)
+                    x = olayer.linear(olayer.linear(b, lw["w_gu"], 2), lw["w_down"], 1, x)
+                    continue
                 y = projection(x, weights[l])
                 q = y[:, :hid].reshape(1, r, H, d)
                 kn = y[:, hid:2 * hid].reshape(1, r, H, d)
