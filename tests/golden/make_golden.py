@@ -25,6 +25,35 @@ import oracle  # noqa: E402
 from entropy_gated_kv_decode_b300 import synth  # noqa: E402
 
 
+def variant_inputs():
+    """Seeded inputs of the attention variants and the layer pieces (shared with
+    tests/test_golden.py)."""
+    rng = np.random.default_rng(2025)
+    sec, tau, idx, cnt = synth.make_simsd_layout(rng, 1, 3, 2)  # L = 7
+    q = rng.standard_normal((1, 4, 2, 4))
+    kc = rng.standard_normal((1, 7, 1, 4))
+    vc = rng.standard_normal((1, 7, 1, 4))
+    kn = rng.standard_normal((1, 4, 1, 4))
+    vn = rng.standard_normal((1, 4, 1, 4))
+    seed = np.array([[0, 1, 0, 1]], np.uint8)
+    x = rng.standard_normal((3, 8))
+    g = rng.standard_normal(8)
+    return dict(sec=sec, tau=tau, idx=idx, cnt=cnt, q=q, kc=kc, vc=vc, kn=kn, vn=vn, seed=seed,
+                x=x, g=g)
+
+
+def variant_record():
+    from oracle import layer
+    v = variant_inputs()
+    simsd = oracle.attention_simsd(v["q"], v["kc"], v["vc"], v["idx"], v["cnt"], v["sec"],
+                                   v["tau"], 0.5)
+    _, _, cover = oracle.attention_cover(v["q"], v["kn"], v["vn"], v["kc"], v["vc"], v["idx"],
+                                         v["cnt"], v["seed"], 0.5)
+    return {"simsd": simsd.tolist(), "cover": cover.tolist(),
+            "rms_norm": layer.rms_norm(v["x"], v["g"], 1e-5).tolist(),
+            "rope": layer.rope(v["x"].reshape(3, 1, 8), [0, 5, 900], 10000.0).tolist()}
+
+
 def main():
     rng = np.random.default_rng(2024)
     x = rng.standard_normal((6, 37)) * np.array([[0.3], [1.0], [3.0], [0.1], [8.0], [1.5]])
@@ -49,6 +78,7 @@ def main():
                         "refresh": np.asarray(g["refresh"]).tolist(),
                         "idx": idx[:, :int(cnt.max())].tolist(), "count": cnt.tolist()},
     }
+    out["variants"] = variant_record()
     with open(os.path.join(HERE, "oracle_regression.json"), "w") as f:
         json.dump(out, f, indent=1)
         f.write("\n")

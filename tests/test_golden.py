@@ -36,3 +36,16 @@ def test_oracle_matches_its_regression_record(orc):
                                  st.block_lo, st.block_hi, w.k)
     assert cnt.tolist() == d["count"]
     assert idx[:, :int(cnt.max())].tolist() == d["idx"]
+
+
+def test_variants_match_their_regression_record(orc):
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "make_golden", os.path.join(os.path.dirname(GOLDEN), "make_golden.py"))
+    mg = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mg)
+    with open(GOLDEN) as f:
+        g = json.load(f)["variants"]
+    now = mg.variant_record()
+    for key in ("simsd", "cover", "rms_norm", "rope"):
+        assert np.allclose(np.array(now[key]), np.array(g[key]), rtol=1e-12, atol=1e-14), key
