@@ -497,6 +497,8 @@ def _linear_args(x, count, w, mode, residual, y, workspace):
     if x.dim() != 3 or w.dim() != 2 or w.shape[1] != x.shape[2]:
         raise ValueError("x [batch, r_max, in], w [out (x2 for SwiGLU), in]")
     batch, r_max, n_in = x.shape
+    if mode == LINEAR_SWIGLU and w.shape[0] % 2:
+        raise ValueError("a SwiGLU weight stacks gate and up rows: [2 * out, in]")
     n_out = w.shape[0] // 2 if mode == LINEAR_SWIGLU else w.shape[0]
     if y.shape != (batch, r_max, n_out) or (mode == LINEAR_RESIDUAL and residual.shape != y.shape):
         raise ValueError("y (and residual) [batch, r_max, out]")
