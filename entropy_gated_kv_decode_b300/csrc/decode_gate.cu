@@ -648,6 +648,12 @@ __global__ void __launch_bounds__(kFinishThreads) decode_finish_kernel(const Arg
     const int pos_first = first_live ? __ldg(A.g.row_pos + lo + r_first) : 0;
     pdl_wait();  // the stream kernel's slots are complete and visible
     pdl_launch_dependents();
+    // this lane's first slot of its first row travels with the status word (one
+    // round trip for both); it is used only if no wait timed out
+    const float4 *slots_first =
+        reinterpret_cast<const float4 *>(A.parts + static_cast<int64_t>(lo + r_first) * kMaxSplits);
+    float4 slot_first = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (seq_ok && first_live && j < n_first) slot_first = __ldcg(slots_first + j);
     if (ld_status(A.status) & EC_DEV_TIMEOUT) return;  // the whole block alike
     if (!seq_ok) {
         if (tid == 0) flag_status(A.status, EC_DEV_BAD_OFFSETS);
@@ -664,7 +670,8 @@ __global__ void __launch_bounds__(kFinishThreads) decode_finish_kernel(const Arg
                 reinterpret_cast<const float4 *>(A.parts + static_cast<int64_t>(i) * kMaxSplits);
             const int n = r0 == 0 ? n_first : row_slots(A, i);
             pos = r0 == 0 ? pos_first : __ldg(A.g.row_pos + i);
-            for (int k = j; k < n; k += g) merge(p, gate::from_f4(__ldcg(slots + k)));
+            for (int k = j; k < n; k += g)
+                merge(p, gate::from_f4(r0 == 0 && k == j ? slot_first : __ldcg(slots + k)));
         }
         for (int off = g >> 1; off; off >>= 1) merge(p, shfl_xor(p, off));
         if (live && j == 0) {
