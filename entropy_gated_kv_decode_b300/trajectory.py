@@ -41,7 +41,7 @@ masked" part of the next recompute set:
   ("sliding", W)      lo = the first still-masked generated position, hi = lo + W;
   ("multiblock", nb)  lo = the start of the block holding that position, nb blocks;
 hi clamped to L.  With the last two the window depends on the state: after each
-step the driver copies is_masked (one byte per position) to the host with the
+step this module copies is_masked (one byte per position) to the host with the
 refresh flag, places the next window there, and builds the next recompute set
 before the next forward.  A step's logits are the first c rows of a W-row
 (nb-block) draw, c the masked positions in its window.

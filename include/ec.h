@@ -49,7 +49,7 @@ typedef enum {
     EC_ERR_ALIGN = -4,       /* a pointer or row stride breaks the 16-byte rule */
     EC_ERR_WORKSPACE = -5,   /* workspace missing, misaligned or too small */
     EC_ERR_CUDA = -6,        /* a CUDA runtime call or launch failed */
-    EC_ERR_UNSUPPORTED = -7, /* valid request this build does not implement */
+    EC_ERR_UNSUPPORTED = -7, /* valid request this library does not implement */
     EC_ERR_SCRATCH_LIMIT = -8 /* request needs more than the fixed built-in scratch */
 } ec_status;
 
