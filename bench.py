@@ -100,7 +100,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                   choices=sorted(synth.WORKLOADS) + ["all"])
+                   choices=sorted(synth.WORKLOADS) + ["all", "lmhead"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=200,
@@ -1127,12 +1127,35 @@ def run_trajectory(args):
         print(json.dumps(line), flush=True)
 
 
+def run_lmhead(args):
+    """The LM-head fused decode-and-gate call alone on the batched workload's rows
+    (the default line's lmhead_gate part), for profiling that kernel by itself."""
+    import torch
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    from entropy_gated_kv_decode_b300 import _native as nat
+    nat.lib()
+    w = synth.WORKLOADS[DEFAULT_WORKLOAD]
+    st = synth.make_state(np.random.default_rng(args.seed), w)
+    stream = torch.cuda.Stream(device)
+    torch.cuda.set_stream(stream)
+    peaks, _ = load_peaks()
+    part = lmhead_part(nat, w, st, device, stream, L2Flush(device), max(1, args.steps),
+                       float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+                       float(peaks["hbm_gbs"]), args.seed)
+    print(json.dumps({"workload": "lmhead", "config": {"rows": w.n_rows, "vocab": w.vocab,
+                                                        "hidden": LMHEAD_HIDDEN},
+                      "lmhead_gate": part}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "trajectory":
         run_trajectory(args)
+    elif args.workload == "lmhead":
+        run_lmhead(args)
     elif args.workload == "all":
         for name in ("tiny", "single_seq", "batched", "long_ctx"):
             run_ours(args, name)
