@@ -237,3 +237,60 @@ def test_lmhead_rejects_bad_arguments(L):
     assert call(1, 0x2004) == -4      # w_lm not 16-byte aligned
     assert call(22, 64) == -5         # workspace too small
     assert call(21, 0x10010) == -5    # workspace misaligned
+
+
+def test_layer_calls_reject_bad_arguments(L):
+    # ec_rms_norm(x, count, B, R, hidden, weight, eps, y, ws, wsb, stream)
+    n = L.ec_rms_norm
+    base = [0x1000, None, 1, 4, 4096, 0x2000, 1e-5, 0x3000, 0x10000, 256, None]
+
+    def norm(**kw):
+        names = ["x", "count", "B", "R", "hidden", "g", "eps", "y", "ws", "wsb", "stream"]
+        a = list(base)
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return n(*a)
+
+    assert norm(hidden=12) == -2
+    assert norm(eps=-1.0) == -2
+    assert norm(eps=float("nan")) == -2
+    assert norm(x=None) == -1
+    assert norm(g=0x2004) == -4
+    assert norm(wsb=4) == -5
+    # ec_rope(q, k, idx, stride, count, B, L, R, H, Hkv, d, theta, ws, wsb, stream)
+    r = L.ec_rope
+    rb = [0x1000, 0x2000, 0x3000, 8, 0x4000, 1, 1024, 8, 4, 2, 128, 10000.0, 0x10000, 256, None]
+
+    def rope(**kw):
+        names = ["q", "k", "idx", "stride", "count", "B", "L", "R", "H", "Hkv", "d", "theta", "ws",
+                 "wsb", "stream"]
+        a = list(rb)
+        for key, v in kw.items():
+            a[names.index(key)] = v
+        return r(*a)
+
+    assert rope(d=129) == -2
+    assert rope(d=256) == -2
+    assert rope(theta=1.0) == -2
+    assert rope(stride=4) == -2
+    assert rope(count=None) == -1
+    assert rope(q=None) == -1
+    # ec_linear(x, count, B, R, in, w, out, mode, residual, y, ws, wsb, stream)
+    f = L.ec_linear
+    lb = [0x1000, None, 1, 4, 4096, 0x2000, 4096, 0, None, 0x3000, 0x10000, 256, None]
+
+    def lin(**kw):
+        names = ["x", "count", "B", "R", "in", "w", "out", "mode", "res", "y", "ws", "wsb", "stream"]
+        a = list(lb)
+        for key, v in kw.items():
+            a[names.index(key)] = v
+        return f(*a)
+
+    assert lin(mode=3) == -2
+    assert lin(**{"in": 100}) == -2
+    assert lin(out=96) == -2             # a plain output is a multiple of 64
+    assert lin(mode=2, out=96, w=0x2008) == -4  # SwiGLU: a multiple of 32 passes the shape check ...
+    assert lin(mode=2, out=48) == -2      # ... and at least 64
+    assert lin(mode=1) == -1              # the residual form needs its residual
+    assert lin(w=0x2008) == -4
+    assert lin(wsb=4) == -5
