@@ -155,3 +155,50 @@ def test_lmhead_timeout_unwinds_and_recovers(orc):
     nat.ec_workspace_init(ws)
     again = run_lmhead_gpu(nat, x, wl, st, w.n_unmask, w.tau, st.step, workspace=ws)
     check_decode(again, ref, st, w.n_unmask, w.tau, st.step)
+
+
+@pytest.mark.parametrize("mode", ["simsd", "cover"])
+def test_masked_attention_modes_timeout_unwinds_and_recovers(orc, mode):
+    # the SimSD and COVER instances of the attention kernel take the same bounded
+    # waits; a timeout raises the bit and the next call (workspace re-initialised)
+    # is correct
+    nat = native()
+    w = synth.scaled(synth.SIMSD, batch=2, seq_len=600, prompt_len=560, block=20, n_heads=8,
+                     n_kv_heads=2)
+    rng = np.random.default_rng(41)
+    section, tau, idx, cnt = synth.make_simsd_layout(rng, 2, 560, 20)
+    r = 40
+    seed = (rng.random((2, r)) < 0.25).astype(np.uint8)
+    a = synth.make_attention(rng, w, r)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    ws = nat.new_workspace(nat.ec_attention_workspace_size(2, 600, r, 8, 2, w.head_dim))
+
+    def call():
+        q, kn, vn, kc, vc = (dev(x) for x in (a.q, a.k_new, a.v_new, a.k_cache, a.v_cache))
+        out = torch.full(q.shape, float("nan"), dtype=q.dtype, device=q.device)
+        if mode == "simsd":
+            nat.ec_selective_attention_simsd(q, kn, vn, dev(idx), dev(cnt), dev(section), dev(tau),
+                                             kc, vc, out, scale, ws)
+        else:
+            nat.ec_selective_attention_cover(q, kn, vn, dev(idx), dev(cnt), dev(seed), kc, vc, out,
+                                             scale, ws)
+        return out, kc, vc
+
+    with short_waits(nat):
+        call()
+        torch.cuda.synchronize()
+    bits = nat.ec_read_device_status(ws)
+    assert bits & nat.DEV_TIMEOUT, f"status {bits:#x}"
+    nat.ec_workspace_init(ws)
+    out, kc, vc = call()
+    assert nat.ec_read_device_status(ws) == 0
+    if mode == "simsd":
+        kc_ref, vc_ref = orc.scatter_kv(a.k_new, a.v_new, idx, cnt, a.k_cache, a.v_cache)
+        ref = orc.attention_simsd(a.q, kc_ref, vc_ref, idx, cnt, section, tau, scale)
+    else:
+        kc_ref, vc_ref, ref = orc.attention_cover(a.q, a.k_new, a.v_new, a.k_cache, a.v_cache, idx,
+                                                  cnt, seed, scale)
+    assert np.array_equal(host(kc), kc_ref) and np.array_equal(host(vc), vc_ref)
+    got = synth.bf16_bits_to_f32(host(out)).astype(np.float64)
+    for b in range(2):
+        attention_close(got[b, :cnt[b]], ref[b, :cnt[b]], True)
