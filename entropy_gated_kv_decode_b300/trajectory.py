@@ -393,3 +393,40 @@ class Trajectory:
         for _ in range(self.w.n_steps if n_steps is None else n_steps):
             self.step()
         return self.records
+
+    # -- checkpoint / resume ---------------------------------------------------
+
+    _STATE_TENSORS = ("is_masked", "tokens", "decode_step", "k_cache", "v_cache", "idx_sel",
+                      "count_sel", "refresh")
+
+    def state_dict(self) -> dict:
+        """The state after the last completed step, copied to the host: the decode
+        state, every layer's K/V cache, the next forward's row set, the gate flag, the
+        step counter and (window policies) the next window.  With the same workload,
+        seed and policy, load_state_dict then continues the trajectory exactly as it
+        would have gone on."""
+        torch.cuda.synchronize(self.dev)
+        sd = {name: getattr(self, name).detach().cpu().clone() for name in self._STATE_TENSORS}
+        sd.update(t=self.t, next_full=self.next_full, next_rows=self.next_rows, win=self.win,
+                  policy=tuple(self.policy), seed=self.seed,
+                  workload=dataclasses.asdict(self.w))
+        return sd
+
+    def load_state_dict(self, sd: dict):
+        """Resume from state_dict(): the next step() is step sd['t']."""
+        if (sd["workload"] != dataclasses.asdict(self.w) or sd["seed"] != self.seed
+                or tuple(sd["policy"]) != tuple(self.policy)):
+            raise ValueError("the checkpoint belongs to another workload, seed or policy")
+        with torch.cuda.stream(self.stream):
+            for name in self._STATE_TENSORS:
+                getattr(self, name).copy_(sd[name].to(self.dev))
+        torch.cuda.synchronize(self.dev)
+        self.t, self.next_full, self.next_rows = sd["t"], sd["next_full"], sd["next_rows"]
+        self.win = sd["win"]
+        self.records, self.traces = [], []
+
+    def save(self, path: str):
+        torch.save(self.state_dict(), path)
+
+    def load(self, path: str):
+        self.load_state_dict(torch.load(path, weights_only=False))
