@@ -442,8 +442,10 @@ ec_status ec_rms_norm(const void *x, const int32_t *count, int32_t batch, int32_
                       int32_t hidden, const void *weight, float eps, void *y, void *workspace,
                       size_t workspace_bytes, ec_stream_t stream);
 
-/* Rotary position embedding in place: for row r of sequence b at position
- * p = idx[b*idx_stride + r] and every head of q ([batch, r_max, n_heads,
+/* Rotary position embedding in place: for row r of sequence b at rotary position
+ * p = idx[b*idx_stride + r] (normally the row's sequence position, the recompute
+ * set itself; SimSD's prediction slots take their data token's position, see
+ * entropy_gated_kv_decode_b300/simsd.py) and every head of q ([batch, r_max, n_heads,
  * head_dim]) and k ([batch, r_max, n_kv_heads, head_dim]), the pairs
  * (x_i, x_{i + head_dim/2}), i < head_dim/2, turn by the angle
  * p * theta^(-2 i / head_dim) (computed in double precision):

@@ -158,3 +158,38 @@ def test_bad_labels_raise_the_status_bit_and_hide_keys(orc):
     sec_ref[0, bad_key], tau_ref[0, bad_key] = 1, 10**6
     ref = orc.attention_simsd(a.q, kc_ref, vc_ref, idx, cnt, sec_ref, np.maximum(tau_ref, 1), scale)
     attention_close(got[0], ref[0], True)
+
+
+def test_rope_copy_gives_a_slot_its_data_tokens_rotation(orc):
+    # item 3 (RoPE copy): the oracle side pairs each slot with the data token of the
+    # same step label and takes that token's position; the product maps positions
+    # by the layout (slot P + B + k -> P + k)
+    from entropy_gated_kv_decode_b300 import simsd
+    from oracle import layer as olayer
+    nat = native()
+    rng = np.random.default_rng(12)
+    P, blk, H, Hkv, d = 1000, 8, 4, 2, 128
+    section, tau, idx, cnt = synth.make_simsd_layout(rng, 3, P, blk)
+    want = idx.copy()
+    for b in range(3):
+        for r in range(cnt[b]):
+            p = idx[b, r]
+            if section[b, p] == 2:
+                data = [j for j in range(P, P + blk) if section[b, j] == 1 and tau[b, j] == tau[b, p]]
+                want[b, r] = data[0]
+    rope_pos = simsd.rope_positions(idx, cnt, P, blk)
+    assert np.array_equal(rope_pos, want)
+    q = synth.f32_to_bf16_bits(rng.standard_normal((3, 2 * blk, H, d), dtype=np.float32))
+    k = synth.f32_to_bf16_bits(rng.standard_normal((3, 2 * blk, Hkv, d), dtype=np.float32))
+    q[:, blk:] = q[:, :blk]  # each slot row the same vectors as its section-order data row
+    k[:, blk:] = k[:, :blk]
+    qd, kd = dev(q), dev(k)
+    ws = nat.new_workspace(256)
+    nat.ec_rope(qd, kd, dev(rope_pos), dev(cnt), P + 2 * blk, 500000.0, ws)
+    got_q = synth.bf16_bits_to_f32(host(qd)).astype(np.float64)
+    for b in range(3):
+        ref = olayer.rope(q[b], want[b], 500000.0)
+        assert np.all(np.abs(got_q[b] - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5)
+    # slot row k and data row k were equal and now sit at one rotary position
+    assert np.array_equal(host(qd)[:, blk:], host(qd)[:, :blk])
+    assert np.array_equal(host(kd)[:, blk:], host(kd)[:, :blk])
