@@ -56,8 +56,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 MEASURED_TRAFFIC = {
     # `bench.py --steps 20 --warmup 3 --e2e-steps 100 --cpu-seconds 0.1 --no-lmhead
     # --no-simsd --no-cover`, mean of two launches; the decode call is both of its kernels
-    ("batched", "attention"): {"bytes": 39192192, "sources": "958c1e7b14af8eac"},
-    ("batched", "decode"): {"bytes": 156046336, "sources": "958c1e7b14af8eac"},
+    ("batched", "attention"): {"bytes": 39193728, "sources": "2b16f06ea4df9189"},
+    ("batched", "decode"): {"bytes": 156080896, "sources": "2b16f06ea4df9189"},
 }
 
 

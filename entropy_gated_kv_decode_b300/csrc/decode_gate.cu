@@ -12,7 +12,7 @@
 // a = the first index of m.  States merge associatively (rescaling by
 // 2^{difference of the references}; on equal maxima the earlier index wins).
 //
-// Work split.  A row's 16-byte vectors form a head (about 80 %) and, for rows
+// Work split.  A row's 16-byte vectors form a head (about 95 %) and, for rows
 // of 64 KB or more, a few tail chunks of at most 32 KB.  The heads of all rows,
 // laid end to end, are cut into one equal contiguous range per CTA of a
 // persistent grid (3 CTAs per SM); the tail chunks form a pool that CTAs claim
@@ -79,7 +79,7 @@ constexpr int kVecPerStage = kStageBytes / 16;   // 1024 vectors
 constexpr int kPieceSlots = 4;               // finished pieces queued for the finisher
 constexpr int kMaxSplits = 64;               // partial slots per row
 constexpr int kTailMinBytes = 65536;         // rows this long get a tail pool
-constexpr int kTailPercent = 20;             // share of such a row in the pool
+constexpr int kTailPercent = 5;              // share of such a row in the pool
 constexpr int kTailChunkVecs = 2048;         // 32 KB per pool chunk at most
 constexpr int kMaxUnmask = gate::kMaxUnmask;
 constexpr int kFinishThreads = 512;          // threads of a finishing block (one per sequence)
