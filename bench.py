@@ -56,19 +56,45 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 MEASURED_TRAFFIC = {
     # `bench.py --steps 20 --warmup 3 --e2e-steps 100 --cpu-seconds 0.1 --no-lmhead
     # --no-simsd --no-cover`, mean of two launches; the decode call is both of its kernels
-    ("batched", "attention"): {"bytes": 39193728, "sources": "2b16f06ea4df9189"},
-    ("batched", "decode"): {"bytes": 156080896, "sources": "2b16f06ea4df9189"},
+    ("batched", "attention"): {"bytes": 39193728, "sources": "c658b83728938fd0"},
+    ("batched", "decode"): {"bytes": 156080896, "sources": "c658b83728938fd0"},
 }
 
 
-def kernel_sources_hash() -> str:
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments and with whitespace runs collapsed:
+    what the compiler sees, so that editing a comment keeps the hash."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # a string or character literal, escapes included
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def kernel_sources_hash(csrc: str | None = None) -> str:
+    """Hash of the kernels' code (csrc/*.cu, *.cuh; comments and layout ignored)."""
     import hashlib
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "entropy_gated_kv_decode_b300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "entropy_gated_kv_decode_b300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

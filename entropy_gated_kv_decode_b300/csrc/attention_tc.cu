@@ -22,26 +22,31 @@
 //            (the first piece a group runs) is done long before its owner (the
 //            last piece of the next group) needs it.
 // Write-back: the fresh K/V rows of a tile are patched into the tile in shared
-// memory after its TMA load lands (so no CTA depends on another's global write),
-// and the group whose range holds the tile writes them to the cache from its
-// mt = 0 CTA.  A sequence that recomputes all L rows (count = L, so the index
+// memory after its TMA load lands (so no CTA depends on another's global write);
+// the cache is written from the fresh tensors by each CTA's softmax warps before
+// their first tile, the CTA mt of a group taking every n_mt-th fresh row of the
+// group's tiles.  A sequence that recomputes all L rows (count = L, so the index
 // set is 0 .. L-1) loads its tiles from the fresh K/V directly, and its mt = 0
 // CTAs store every tile to the cache with a TMA store.
+// Instances: MODE_PLAIN; MODE_SIMSD (SimSD's temporal causal mask, label windows
+// applied in the softmax); MODE_COVER (COVER's dual view: seed rows neither
+// written back nor patched, a seed row's own column hidden and its masked-input
+// term added in the epilogue).
 //
 // Warp roles (384 threads):
 //   warp 0     TMA producer of Q (one tile per piece) and K tiles; warp 6 of V
 //              tiles (128-byte swizzle, rings of stages);
-//   warp 1     TMEM allocation; at the start its share of the K write-back;
-//              Q into TMEM (tcgen05.cp); per K tile the whole warp patches the
-//              fresh rows into it (a TMA box for a tile of fresh rows, else
-//              cp.async), or stores the tile for a full refresh; then one thread
+//   warp 1     TMEM allocation; Q into TMEM (tcgen05.cp); per K tile the whole
+//              warp patches the fresh rows into it (a TMA box for a tile of fresh
+//              rows, else cp.async), or stores the tile for a full refresh; then one thread
 //              issues S = Q K^T (tcgen05.mma) into one of two TMEM S buffers once
 //              the PV product that read that buffer's P has completed;
-//   warp 7     the same for V (write-back share, patching), then O += P V into the TMEM O
+//   warp 7     the same for V (patching), then O += P V into the TMEM O
 //              accumulator: a second issuing thread, so the next tile's QK never
 //              queues behind this tile's PV;
-//   warps 2-5, 8-11  softmax, two warps per quarter of the TMEM lanes: one row per
-//              thread and half a tile's score columns per warp (the two halves
+//   warps 2-5, 8-11  the write-back share, then the softmax, two warps per quarter
+//              of the TMEM lanes: one row per thread and half a tile's score
+//              columns per warp (the two halves
 //              agree on the row maximum through shared memory); online softmax in
 //              the log2 domain on S read by tcgen05.ld (the reference maximum moves
 //              only when it grows by more than 8 in log2 units, rescaling O in

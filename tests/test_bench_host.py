@@ -43,3 +43,19 @@ def test_traffic_is_reported_only_for_the_captured_sources():
     finally:
         bench.MEASURED_TRAFFIC.clear()
         bench.MEASURED_TRAFFIC.update(saved)
+
+
+def test_sources_hash_ignores_comments_but_not_code(tmp_path):
+    src = tmp_path / "k.cu"
+    src.write_text('// a kernel\n__global__ void k(int *p) { p[0] = 1; /* one */ }\n'
+                   'const char *s = "// not a comment";\n')
+    h0 = bench.kernel_sources_hash(str(tmp_path))
+    src.write_text('// the kernel, reworded\n__global__ void k(int *p)\n{\n    p[0] = 1;\n}\n'
+                   'const char *s = "// not a comment";\n')
+    assert bench.kernel_sources_hash(str(tmp_path)) == h0
+    src.write_text('// a kernel\n__global__ void k(int *p) { p[0] = 2; }\n'
+                   'const char *s = "// not a comment";\n')
+    assert bench.kernel_sources_hash(str(tmp_path)) != h0
+    src.write_text('// a kernel\n__global__ void k(int *p) { p[0] = 1; }\n'
+                   'const char *s = "// not a comment!";\n')
+    assert bench.kernel_sources_hash(str(tmp_path)) != h0  # string contents are code
