@@ -56,6 +56,8 @@ def lib():
                                           i32, i32, i32, i32, f64, vp, i64, vp]
         L.orc_attention_cover.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp, i64, vp, vp, i32,
                                           i32, i32, i32, i32, i32, f64, vp]
+        L.orc_cover_seed_score.argtypes = [vp, vp, ctypes.c_int, vp, i64, vp, vp, vp, vp, i32, i32,
+                                           i32, i32, i32, i32, f64, i32, vp, vp, vp, vp]
         L.orc_embed_rows.argtypes = [vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, i32, i32,
                                      i32, i32, vp]
         L.orc_projection.argtypes = [vp, vp, ctypes.c_int, i64, i32, i32, vp, i64, vp]
@@ -243,6 +245,33 @@ def attention_cover(q, k_new, v_new, k_cache, v_cache, idx, count, seed, scale):
                                      ix.shape[-1], _p(cnt), _p(sd), batch, seq_len, r_max, h, hkv,
                                      d, float(scale), _p(out)), "attention_cover")
     return kc, vc, out
+
+
+def cover_seed_score(q, k_cache, idx, count, role, drafted, u, scale, n_seed):
+    """COVER's seed score (``oracle.c``, ``orc_cover_seed_score``): returns
+    ``(d_in, d_out, score, seeds)``; the first three float64 ``[B, r_max]``, NaN
+    except at candidate rows, ``seeds`` int32 ``[B, n_seed]`` positions (-1 pad).
+    ``role`` uint8 ``[B, r_max]`` (bit 0 still masked, bit 1 candidate),
+    ``drafted`` uint8 ``[B, L]``, ``u`` ``[B, r_max]`` (widened to float64)."""
+    qq = np.ascontiguousarray(q)
+    kc = np.ascontiguousarray(k_cache)
+    ix = np.ascontiguousarray(idx, np.int32)
+    cnt = np.ascontiguousarray(count, np.int32)
+    rl = np.ascontiguousarray(role, np.uint8)
+    dr = np.ascontiguousarray(drafted, np.uint8)
+    uu = np.ascontiguousarray(u, np.float64)
+    batch, r_max, h, d = qq.shape
+    seq_len, hkv = kc.shape[1], kc.shape[2]
+    assert rl.shape == (batch, r_max) and uu.shape == (batch, r_max)
+    assert dr.shape == (batch, seq_len) and kc.dtype == qq.dtype
+    dt = _dtype_of(qq)
+    d_in, d_out, score = (np.empty((batch, r_max), np.float64) for _ in range(3))
+    seeds = np.empty((batch, n_seed), np.int32)
+    _check(lib().orc_cover_seed_score(_p(qq), _p(kc), dt, _p(ix), ix.shape[-1], _p(cnt), _p(rl),
+                                      _p(dr), _p(uu), batch, seq_len, r_max, h, hkv, d,
+                                      float(scale), n_seed, _p(d_in), _p(d_out), _p(score),
+                                      _p(seeds)), "cover_seed_score")
+    return d_in, d_out, score, seeds
 
 
 def embed_rows(table, idx, count, tokens, is_masked, mask_id, r_max):

@@ -787,3 +787,121 @@ int orc_attention_cover(const void *q, const void *k_new, const void *v_new, voi
     }
     return status;
 }
+
+/*
+ * COVER's stability-aware seed score ("Stop the Flip-Flop: Verifica Preservante
+ * il Contesto per una Decodifica di Diffusione Veloce e Revocabile", Italian
+ * technical summary (gist.science/it/paper/2602.06161), section "Metodologia:
+ * COVER", item 2 "Selezione dei Seed Sensibile alla Stabilità").
+ *
+ * The page scores a decoded token by Score = u (1 + d_in) / (1 + d_out): u the
+ * entropy of its current assignment, d_in how much the still-masked positions
+ * rely on it as context, d_out how strongly it attends to the positions drafted
+ * at this step.  It gives no formula for the two attention terms; the plain one
+ * is taken, over one layer's attention probabilities averaged over the heads:
+ *   a^h_{r,j} = softmax_j(scale * q_{r,h} . k_{j,g(h)}), j < seq_len: recomputed
+ *               row r's bidirectional attention on every key of the cache as it
+ *               stands (g(h) = h / (n_heads / n_kv_heads));
+ *   d_in(c)   = (1/H) sum_h sum_{r < count[b], role_r & 1} a^h_{r, p_c};
+ *   d_out(c)  = (1/H) sum_h sum_{j : drafted[b, j] != 0} a^h_{c, j};
+ *   score(c)  = u_c (1 + d_in(c)) / (1 + d_out(c)).
+ * role[b*r_max + r]: bit 0 = the row's position is still masked after this step
+ * (its query counts toward d_in), bit 1 = the row is a candidate (a decoded token
+ * that may be verified); p_c = idx[b*idx_stride + c].  u[b*r_max + r] is the
+ * candidate row's entropy.  The seed set is the n_seed candidates of highest
+ * score, ties to the lower position (a NaN score ranks last), written as
+ * positions to seeds[b*n_seed ...] and padded with -1.
+ * Outputs d_in, d_out, score: [batch, r_max] float64, NaN except at the
+ * candidate rows r < count[b].
+ */
+int orc_cover_seed_score(const void *q, const void *k_cache, int dtype, const int32_t *idx,
+                         int64_t idx_stride, const int32_t *count, const uint8_t *role,
+                         const uint8_t *drafted, const double *u, int32_t batch,
+                         int32_t seq_len, int32_t r_max, int32_t n_heads, int32_t n_kv_heads,
+                         int32_t head_dim, double scale, int32_t n_seed, double *d_in,
+                         double *d_out, double *score, int32_t *seeds)
+{
+    if (!dtype_ok(dtype))
+        return ORC_BAD_DTYPE;
+    if (batch < 0 || seq_len <= 0 || r_max < 0 || idx_stride < r_max || n_heads <= 0 ||
+        n_kv_heads <= 0 || head_dim <= 0 || n_heads % n_kv_heads != 0 || n_seed < 0)
+        return ORC_BAD_ARG;
+    for (int32_t b = 0; b < batch; ++b) {
+        if (count[b] < 0 || count[b] > r_max)
+            return ORC_BAD_ARG;
+        for (int32_t r = 0; r < count[b]; ++r) {
+            const int32_t p = idx[b * idx_stride + r];
+            if (p < 0 || p >= seq_len)
+                return ORC_BAD_ARG;
+        }
+    }
+    int status = ORC_OK;
+#pragma omp parallel for num_threads(g_threads) schedule(dynamic, 1)
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t row0 = (int64_t)b * r_max;
+        for (int32_t r = 0; r < r_max; ++r)
+            d_in[row0 + r] = d_out[row0 + r] = score[row0 + r] = NAN;
+        double *a = (double *)malloc((size_t)seq_len * sizeof(double));
+        double *in_sum = (double *)calloc((size_t)r_max + 1, sizeof(double));
+        double *out_sum = (double *)calloc((size_t)r_max + 1, sizeof(double));
+        ranked_row *cand = (ranked_row *)malloc(((size_t)r_max + 1) * sizeof(ranked_row));
+        if (!a || !in_sum || !out_sum || !cand) {
+#pragma omp atomic write
+            status = ORC_NOMEM;
+            free(a), free(in_sum), free(out_sum), free(cand);
+            continue;
+        }
+        for (int32_t h = 0; h < n_heads; ++h) {
+            const int32_t g = h / (n_heads / n_kv_heads);
+            for (int32_t r = 0; r < count[b]; ++r) {
+                const uint8_t rr = role[row0 + r];
+                if (!(rr & 3))
+                    continue;
+                /* a^h_{r, j} for every key j */
+                const int64_t qoff = ((row0 + r) * n_heads + h) * head_dim;
+                double m = -INFINITY;
+                for (int32_t j = 0; j < seq_len; ++j) {
+                    const int64_t koff = (((int64_t)b * seq_len + j) * n_kv_heads + g) * head_dim;
+                    double dot = 0.0;
+                    for (int32_t e = 0; e < head_dim; ++e)
+                        dot += load(q, dtype, qoff + e) * load(k_cache, dtype, koff + e);
+                    a[j] = scale * dot;
+                    if (a[j] > m)
+                        m = a[j];
+                }
+                double z = 0.0;
+                for (int32_t j = 0; j < seq_len; ++j) {
+                    a[j] = exp(a[j] - m);
+                    z += a[j];
+                }
+                for (int32_t j = 0; j < seq_len; ++j)
+                    a[j] /= z;
+                if (rr & 1) /* a still-masked query: the weight it puts on every candidate */
+                    for (int32_t c = 0; c < count[b]; ++c)
+                        if (role[row0 + c] & 2)
+                            in_sum[c] += a[idx[b * idx_stride + c]];
+                if (rr & 2) /* a candidate: its weight on the drafted positions */
+                    for (int32_t j = 0; j < seq_len; ++j)
+                        if (drafted[(int64_t)b * seq_len + j])
+                            out_sum[r] += a[j];
+            }
+        }
+        int32_t nc = 0;
+        for (int32_t c = 0; c < count[b]; ++c) {
+            if (!(role[row0 + c] & 2))
+                continue;
+            d_in[row0 + c] = in_sum[c] / n_heads;
+            d_out[row0 + c] = out_sum[c] / n_heads;
+            score[row0 + c] = u[row0 + c] * (1.0 + d_in[row0 + c]) / (1.0 + d_out[row0 + c]);
+            cand[nc].conf = isnan(score[row0 + c]) ? -INFINITY : score[row0 + c];
+            cand[nc].pos = idx[b * idx_stride + c];
+            cand[nc].row = c;
+            ++nc;
+        }
+        qsort(cand, (size_t)nc, sizeof(ranked_row), by_conf_then_pos);
+        for (int32_t s = 0; s < n_seed; ++s)
+            seeds[(int64_t)b * n_seed + s] = s < nc ? cand[s].pos : -1;
+        free(a), free(in_sum), free(out_sum), free(cand);
+    }
+    return status;
+}
