@@ -51,13 +51,23 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) per call of the dominant call, from one ncu capture of
 # the same bench command (dram__bytes_read.sum + dram__bytes_write.sum summed over
-# the call's kernels, per launch).  Used only while the kernel sources hash to the
-# value they had when the counters were taken.
+# the call's kernels, per launch).  Used only while the files the call is built
+# from (CALL_SOURCES) hash to the value they had when the counters were taken.
 MEASURED_TRAFFIC = {
     # `bench.py --steps 20 --warmup 3 --e2e-steps 100 --cpu-seconds 0.1 --no-lmhead
     # --no-simsd --no-cover`, mean of two launches; the decode call is both of its kernels
-    ("batched", "attention"): {"bytes": 39193728, "sources": "c658b83728938fd0"},
-    ("batched", "decode"): {"bytes": 156080896, "sources": "c658b83728938fd0"},
+    ("batched", "attention"): {"bytes": 39193728, "sources": "bfc20f966a175408"},
+    ("batched", "decode"): {"bytes": 156080896, "sources": "514662fb16117650"},
+}
+
+# The files a measured call's kernels are compiled from: the kernels' own source,
+# the device headers it includes, the C ABI entry that validates and launches it
+# (kernel attributes are set there) and the public header.
+CALL_SOURCES = {
+    "decode": ("csrc/decode_gate.cu", "csrc/gate_common.cuh", "csrc/tc_ptx.cuh",
+               "csrc/ec_internal.cuh", "csrc/ec_api.cu", "../include/ec.h"),
+    "attention": ("csrc/attention_tc.cu", "csrc/tc_ptx.cuh", "csrc/ec_internal.cuh",
+                  "csrc/ec_api.cu", "../include/ec.h"),
 }
 
 
@@ -86,21 +96,26 @@ def _code_only(text: str) -> str:
     return " ".join("".join(out).split())
 
 
-def kernel_sources_hash(csrc: str | None = None) -> str:
-    """Hash of the kernels' code (csrc/*.cu, *.cuh; comments and layout ignored)."""
+def kernel_sources_hash(csrc: str | None = None, files=None) -> str:
+    """Hash of kernel code, comments and layout ignored: the named files (paths
+    relative to the package), else every csrc/*.cu and *.cuh of ``csrc``."""
     import hashlib
     h = hashlib.sha256()
-    csrc = csrc or os.path.join(ROOT, "entropy_gated_kv_decode_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), encoding="utf-8") as f:
-                h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
+    if files is not None:
+        pkg = os.path.join(ROOT, "entropy_gated_kv_decode_b300")
+        paths = [os.path.normpath(os.path.join(pkg, f)) for f in files]
+    else:
+        csrc = csrc or os.path.join(ROOT, "entropy_gated_kv_decode_b300", "csrc")
+        paths = [os.path.join(csrc, n) for n in sorted(os.listdir(csrc)) if n.endswith((".cu", ".cuh"))]
+    for path in paths:
+        with open(path, encoding="utf-8") as f:
+            h.update(os.path.basename(path).encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
 def measured_traffic(workload: str, call: str):
     t = MEASURED_TRAFFIC.get((workload, call))
-    if t is None or t["sources"] != kernel_sources_hash():
+    if t is None or t["sources"] != kernel_sources_hash(files=CALL_SOURCES[call]):
         return None
     return t["bytes"]
 

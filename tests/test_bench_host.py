@@ -30,7 +30,7 @@ def test_packed_views_are_aligned_disjoint_and_contiguous():
 
 
 def test_traffic_is_reported_only_for_the_captured_sources():
-    h = bench.kernel_sources_hash()
+    h = bench.kernel_sources_hash(files=bench.CALL_SOURCES["attention"])
     assert len(h) == 16 and int(h, 16) >= 0
     saved = dict(bench.MEASURED_TRAFFIC)
     try:
@@ -43,6 +43,19 @@ def test_traffic_is_reported_only_for_the_captured_sources():
     finally:
         bench.MEASURED_TRAFFIC.clear()
         bench.MEASURED_TRAFFIC.update(saved)
+
+
+def test_call_hash_covers_its_own_files_only(tmp_path):
+    a, b = tmp_path / "a.cu", tmp_path / "b.cu"
+    a.write_text("__global__ void ka(int *p) { p[0] = 1; }\n")
+    b.write_text("__global__ void kb(int *p) { p[0] = 1; }\n")
+    h0 = bench.kernel_sources_hash(files=[str(a)])
+    b.write_text("__global__ void kb(int *p) { p[0] = 2; }\n")
+    assert bench.kernel_sources_hash(files=[str(a)]) == h0  # another call's kernel changed
+    a.write_text("__global__ void ka(int *p) { p[0] = 3; }\n")
+    assert bench.kernel_sources_hash(files=[str(a)]) != h0
+    for call, files in bench.CALL_SOURCES.items():  # every listed file exists
+        assert bench.kernel_sources_hash(files=files)
 
 
 def test_sources_hash_ignores_comments_but_not_code(tmp_path):
