@@ -835,24 +835,30 @@ int orc_cover_seed_score(const void *q, const void *k_cache, int dtype, const in
                 return ORC_BAD_ARG;
         }
     }
+    /* per (sequence, head): that head's sums, in_h[(b*H + h)*r_max + c] and
+       out_h[...]; then the head means, in head order */
+    const int64_t n_items = (int64_t)batch * n_heads;
+    double *in_h = (double *)calloc((size_t)(n_items * r_max + 1), sizeof(double));
+    double *out_h = (double *)calloc((size_t)(n_items * r_max + 1), sizeof(double));
+    if (!in_h || !out_h) {
+        free(in_h), free(out_h);
+        return ORC_NOMEM;
+    }
     int status = ORC_OK;
-#pragma omp parallel for num_threads(g_threads) schedule(dynamic, 1)
-    for (int32_t b = 0; b < batch; ++b) {
-        const int64_t row0 = (int64_t)b * r_max;
-        for (int32_t r = 0; r < r_max; ++r)
-            d_in[row0 + r] = d_out[row0 + r] = score[row0 + r] = NAN;
+#pragma omp parallel num_threads(g_threads)
+    {
         double *a = (double *)malloc((size_t)seq_len * sizeof(double));
-        double *in_sum = (double *)calloc((size_t)r_max + 1, sizeof(double));
-        double *out_sum = (double *)calloc((size_t)r_max + 1, sizeof(double));
-        ranked_row *cand = (ranked_row *)malloc(((size_t)r_max + 1) * sizeof(ranked_row));
-        if (!a || !in_sum || !out_sum || !cand) {
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < n_items; ++t) {
+            if (!a) {
 #pragma omp atomic write
-            status = ORC_NOMEM;
-            free(a), free(in_sum), free(out_sum), free(cand);
-            continue;
-        }
-        for (int32_t h = 0; h < n_heads; ++h) {
+                status = ORC_NOMEM;
+                continue;
+            }
+            const int32_t b = (int32_t)(t / n_heads), h = (int32_t)(t % n_heads);
             const int32_t g = h / (n_heads / n_kv_heads);
+            const int64_t row0 = (int64_t)b * r_max;
+            double *in_sum = in_h + t * r_max, *out_sum = out_h + t * r_max;
             for (int32_t r = 0; r < count[b]; ++r) {
                 const uint8_t rr = role[row0 + r];
                 if (!(rr & 3))
@@ -886,12 +892,26 @@ int orc_cover_seed_score(const void *q, const void *k_cache, int dtype, const in
                             out_sum[r] += a[j];
             }
         }
+        free(a);
+    }
+    ranked_row *cand = (ranked_row *)malloc(((size_t)r_max + 1) * sizeof(ranked_row));
+    if (!cand)
+        status = ORC_NOMEM;
+    for (int32_t b = 0; b < batch && cand; ++b) {
+        const int64_t row0 = (int64_t)b * r_max;
+        for (int32_t r = 0; r < r_max; ++r)
+            d_in[row0 + r] = d_out[row0 + r] = score[row0 + r] = NAN;
         int32_t nc = 0;
         for (int32_t c = 0; c < count[b]; ++c) {
             if (!(role[row0 + c] & 2))
                 continue;
-            d_in[row0 + c] = in_sum[c] / n_heads;
-            d_out[row0 + c] = out_sum[c] / n_heads;
+            double din = 0.0, dout = 0.0;
+            for (int32_t h = 0; h < n_heads; ++h) {
+                din += in_h[((int64_t)b * n_heads + h) * r_max + c];
+                dout += out_h[((int64_t)b * n_heads + h) * r_max + c];
+            }
+            d_in[row0 + c] = din / n_heads;
+            d_out[row0 + c] = dout / n_heads;
             score[row0 + c] = u[row0 + c] * (1.0 + d_in[row0 + c]) / (1.0 + d_out[row0 + c]);
             cand[nc].conf = isnan(score[row0 + c]) ? -INFINITY : score[row0 + c];
             cand[nc].pos = idx[b * idx_stride + c];
@@ -901,7 +921,7 @@ int orc_cover_seed_score(const void *q, const void *k_cache, int dtype, const in
         qsort(cand, (size_t)nc, sizeof(ranked_row), by_conf_then_pos);
         for (int32_t s = 0; s < n_seed; ++s)
             seeds[(int64_t)b * n_seed + s] = s < nc ? cand[s].pos : -1;
-        free(a), free(in_sum), free(out_sum), free(cand);
     }
+    free(cand), free(in_h), free(out_h);
     return status;
 }
