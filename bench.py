@@ -155,6 +155,8 @@ def parse_args(argv=None):
                    help="leave out the COVER dual-view attention part")
     p.add_argument("--no-simsd", action="store_true",
                    help="leave out the SimSD masked-attention part")
+    p.add_argument("--cover-score", action="store_true",
+                   help="add the COVER seed-score part (off by default)")
     p.add_argument("--cpu-seconds", type=float, default=8.0,
                    help="CPU time budget of each oracle baseline sample (one core, all cores)")
     return p.parse_args(argv)
@@ -540,6 +542,9 @@ def run_ours(args, workload=None):
     if w.attn_dtype == synth.BF16 and not args.no_cover:
         out_parts["cover_attention"] = cover_part(nat, step, st, w, flush, min(K, 200), hbm, tc,
                                                   args.seed)
+    if w.attn_dtype == synth.BF16 and args.cover_score:
+        out_parts["cover_seed_score"] = cover_score_part(nat, step, st, w, flush, min(K, 200),
+                                                         args.seed)
     if w.attn_dtype == synth.BF16 and not args.no_simsd:
         out_parts["simsd_attention"] = simsd_part(nat, device, stream, flush, min(K, 200), tc, hbm,
                                                   args.seed)
@@ -746,6 +751,60 @@ def cover_part(nat, step, st, w, flush, K, hbm_peak, tc_peak, seed, n_seeds=8):
     return {"us": t_c, "tflops": tflops, "frac_tensor_peak": tflops / tc_peak,
             "gbs": geo["attn_bytes"] / t_c / 1e3, "frac_hbm": geo["attn_bytes"] / t_c / 1e3 / hbm_peak,
             "plain_us": t_p, "seeds_per_sequence": n_seeds, "launches": 1,
+            "device_status": nat.ec_read_device_status(ws)}
+
+
+# float32 FMA peak of the SIMT pipes: 148 SMs x 128 lanes x 2 flops x 2.032 GHz
+FP32_SIMT_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
+def cover_score_part(nat, step, st, w, flush, K, seed, n_drafted=4, n_seed=8):
+    """COVER's seed score on this workload's recompute set after the step's
+    attention: ``n_drafted`` masked rows per sequence drafted at this step, the
+    rest still masked, the decoded rows candidates.  float32 SIMT work: one
+    q . k per (active row, head, key) and per (candidate, head, masked row)."""
+    import torch
+    torch.cuda.synchronize()
+    idx_h, cnt_h = step.idx.cpu().numpy(), step.count.cpu().numpy()
+    r = w.r_max
+    role, drafted, u = synth.cover_score_inputs(np.random.default_rng(seed + 404), st.is_masked,
+                                                idx_h, cnt_h, r, n_drafted)
+    dev = step.dev
+    role_d, drafted_d, u_d = (torch.from_numpy(a).to(dev) for a in (role, drafted, u))
+    outs = [torch.empty((w.batch, r), dtype=torch.float32, device=dev) for _ in range(3)]
+    seeds = torch.empty((w.batch, n_seed), dtype=torch.int32, device=dev)
+    ws = nat.new_workspace(nat.ec_cover_score_workspace_size(w.batch, w.seq_len, r, w.n_heads), dev)
+    call = nat.prepare_cover_seed_score(step.q, step.k_cache, step.idx, step.count, role_d,
+                                        drafted_d, u_d, 1.0 / math.sqrt(w.head_dim), n_seed,
+                                        outs[0], outs[1], outs[2], seeds, ws, stream=step.stream)
+    e0 = torch.cuda.Event(enable_timing=True, external=True)
+    e1 = torch.cuda.Event(enable_timing=True, external=True)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=step.stream):
+        e0.record()
+        call()
+        e1.record()
+    for _ in range(3):
+        flush()
+        g.replay()
+    tot = 0.0
+    for _ in range(K):
+        flush()
+        g.replay()
+        e1.synchronize()
+        tot += e0.elapsed_time(e1) / 1e3
+    us = tot / K * 1e6
+    flops = 0.0
+    for b in range(w.batch):
+        rows = role[b, :int(cnt_h[b])]
+        active, cand, masked = (int(np.count_nonzero(rows & 3)), int(np.count_nonzero(rows & 2)),
+                                int(np.count_nonzero(rows & 1)))
+        flops += 2.0 * w.head_dim * w.n_heads * (active * w.seq_len + cand * masked)
+    tflops = flops / us / 1e6
+    return {"us": us, "tflops_fp32": tflops, "frac_fp32_simt_peak": tflops / FP32_SIMT_TFLOPS,
+            "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 x 2.032 GHz",
+            "drafted_per_sequence": n_drafted, "n_seed": n_seed,
+            "launches": nat.ec_cover_score_kernel_count(w.batch, r, n_seed),
             "device_status": nat.ec_read_device_status(ws)}
 
 

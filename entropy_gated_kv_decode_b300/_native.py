@@ -33,7 +33,8 @@ EXPORTED = ("ec_status_str", "ec_abi_version", "ec_debug_set_wait_limit", "ec_wo
             "ec_build_recompute_set", "ec_attention_workspace_size", "ec_attention_kernel_count",
             "ec_selective_attention", "ec_selective_attention_simsd",
             "ec_selective_attention_cover", "ec_embed_rows", "ec_qkv_projection",
-            "ec_rms_norm", "ec_rope", "ec_linear")
+            "ec_rms_norm", "ec_rope", "ec_linear",
+            "ec_cover_score_workspace_size", "ec_cover_seed_score", "ec_cover_score_kernel_count")
 
 
 class NativeLibraryMissing(RuntimeError):
@@ -96,13 +97,19 @@ def lib() -> ctypes.CDLL:
         L.ec_rope.argtypes = [vp, vp, vp, i64, vp, i32, i32, i32, i32, i32, i32, ctypes.c_double,
                               vp, sz, vp]
         L.ec_linear.argtypes = [vp, vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, sz, vp]
+        L.ec_cover_score_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.ec_cover_score_workspace_size.restype = sz
+        L.ec_cover_seed_score.argtypes = [vp, vp, vp, i64, vp, vp, vp, vp, ctypes.c_int, i32, i32,
+                                          i32, i32, i32, i32, f32, i32, vp, vp, vp, vp, vp, sz, vp]
+        L.ec_cover_score_kernel_count.argtypes = [i32, i32, i32]
+        L.ec_cover_score_kernel_count.restype = i32
         for name in ("ec_debug_set_wait_limit", "ec_workspace_init", "ec_read_device_status",
                      "ec_decode_step",
                      "ec_decode_step_noalloc", "ec_decode_noalloc_read_status",
                      "ec_lmhead_decode_step", "ec_build_recompute_set",
                      "ec_selective_attention", "ec_selective_attention_simsd",
                      "ec_selective_attention_cover", "ec_embed_rows", "ec_qkv_projection",
-                     "ec_rms_norm", "ec_rope", "ec_linear"):
+                     "ec_rms_norm", "ec_rope", "ec_linear", "ec_cover_seed_score"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -394,6 +401,55 @@ def ec_selective_attention_cover(q, k_new, v_new, idx, count, seed, k_cache, v_c
            "ec_selective_attention_cover")
 
 
+def ec_cover_score_workspace_size(batch, seq_len, r_max, n_heads) -> int:
+    return int(lib().ec_cover_score_workspace_size(batch, seq_len, r_max, n_heads))
+
+
+def ec_cover_score_kernel_count(batch, r_max, n_seed) -> int:
+    return int(lib().ec_cover_score_kernel_count(batch, r_max, n_seed))
+
+
+def _cover_score_args(q, k_cache, idx, count, role, drafted, u, scale, n_seed, d_in, d_out, score,
+                      seeds, workspace):
+    _cuda("q", q, torch.bfloat16)
+    _cuda("k_cache", k_cache, torch.bfloat16)
+    _cuda("idx", idx, torch.int32)
+    _cuda("count", count, torch.int32)
+    _cuda("role", role, torch.uint8)
+    _cuda("drafted", drafted, torch.uint8)
+    for name, t in (("u", u), ("d_in", d_in), ("d_out", d_out), ("score", score)):
+        _cuda(name, t, torch.float32)
+    _cuda("workspace", workspace, torch.uint8)
+    if q.dim() != 4 or k_cache.dim() != 4:
+        raise ValueError("q must be [B, R, H, d] and k_cache [B, L, Hkv, d]")
+    batch, r_max, n_heads, head_dim = q.shape
+    seq_len, n_kv_heads = k_cache.shape[1], k_cache.shape[2]
+    n_seed = int(n_seed)
+    if (k_cache.shape[0] != batch or k_cache.shape[3] != head_dim or idx.dim() != 2
+            or idx.shape[0] != batch or count.numel() != batch
+            or tuple(role.shape) != (batch, r_max) or tuple(u.shape) != (batch, r_max)
+            or tuple(drafted.shape) != (batch, seq_len)
+            or any(tuple(t.shape) != (batch, r_max) for t in (d_in, d_out, score))):
+        raise ValueError("inconsistent seed-score shapes")
+    if n_seed > 0:
+        _cuda("seeds", seeds, torch.int32)
+        if tuple(seeds.shape) != (batch, n_seed):
+            raise ValueError("seeds must be [B, n_seed]")
+    return [_p(q), _p(k_cache), _p(idx), idx.shape[1], _p(count), _p(role), _p(drafted), _p(u),
+            EC_BF16, batch, seq_len, r_max, n_heads, n_kv_heads, head_dim, float(scale), n_seed,
+            _p(d_in), _p(d_out), _p(score), _p(seeds) if n_seed > 0 else None, _p(workspace),
+            workspace.numel()]
+
+
+def ec_cover_seed_score(q, k_cache, idx, count, role, drafted, u, scale, n_seed, d_in, d_out, score,
+                        seeds, workspace, stream=None):
+    """COVER's seed score: d_in, d_out, score [B, R] float32 at the candidate rows
+    (role bit 1; bit 0 marks still-masked queries), seeds [B, n_seed] int32 positions."""
+    args = _cover_score_args(q, k_cache, idx, count, role, drafted, u, scale, n_seed, d_in, d_out,
+                             score, seeds, workspace)
+    _check(lib().ec_cover_seed_score(*args, _stream(stream)), "ec_cover_seed_score")
+
+
 def _embed_args(table, idx, count, seq_tokens, is_masked, mask_id, x, workspace):
     _cuda("table", table, torch.bfloat16)
     _cuda("idx", idx, torch.int32)
@@ -562,6 +618,11 @@ def prepare_build_recompute_set(*args, stream=None, **kwargs):
 
 def prepare_selective_attention(*args, stream=None, **kwargs):
     return Prepared("ec_selective_attention", _attention_args(*args, **kwargs), stream,
+                    keep=(args, kwargs))
+
+
+def prepare_cover_seed_score(*args, stream=None, **kwargs):
+    return Prepared("ec_cover_seed_score", _cover_score_args(*args, **kwargs), stream,
                     keep=(args, kwargs))
 
 

@@ -175,6 +175,27 @@ def cover_seeds(rng: np.random.Generator, is_masked: np.ndarray, idx: np.ndarray
     return seed
 
 
+def cover_score_inputs(rng: np.random.Generator, is_masked: np.ndarray, idx: np.ndarray,
+                       count: np.ndarray, r_max: int, n_drafted: int):
+    """Flags and entropies for COVER's seed score: per sequence, ``n_drafted`` of
+    the recomputed masked rows are drafted at this step (``drafted`` [batch,
+    seq_len] uint8 at their positions); the other masked rows stay masked (role
+    bit 0) and the decoded rows are candidates (role bit 1).  ``u`` [batch, r_max]
+    float32 is drawn uniform in [0, 5) nats."""
+    batch, seq_len = is_masked.shape
+    role = np.zeros((batch, r_max), np.uint8)
+    drafted = np.zeros((batch, seq_len), np.uint8)
+    for b in range(batch):
+        rows = np.arange(int(count[b]))
+        masked = rows[is_masked[b, idx[b, rows]] != 0]
+        pick = rng.choice(masked, size=min(n_drafted, len(masked)), replace=False)
+        drafted[b, idx[b, pick]] = 1
+        role[b, np.setdiff1d(masked, pick)] = 1
+        role[b, rows[is_masked[b, idx[b, rows]] == 0]] = 2
+    u = rng.uniform(0.0, 5.0, (batch, r_max)).astype(np.float32)
+    return role, drafted, u
+
+
 def scaled(w: Workload, **changes) -> Workload:
     """A copy of ``w`` with some fields replaced (smaller parity cases)."""
     return dataclasses.replace(w, **changes)

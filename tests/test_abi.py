@@ -1,5 +1,5 @@
 """The C ABI library loads without a GPU, exports every entry point declared in
-include/ec.h, and rejects bad arguments on the host before launching anything."""
+include/*.h, and rejects bad arguments on the host before launching anything."""
 import ctypes
 import os
 import re
@@ -17,9 +17,13 @@ def L():
 
 
 def declared_functions():
-    text = open(os.path.join(ROOT, "include", "ec.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(ec_[a-z_]+)\s*\(", text)))
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for h in sorted(os.listdir(inc)):
+        if h.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, h)).read(), flags=re.S)
+            names |= set(re.findall(r"\b(ec_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_every_declared_symbol_is_exported(L):
@@ -294,3 +298,49 @@ def test_layer_calls_reject_bad_arguments(L):
     assert lin(mode=1) == -1              # the residual form needs its residual
     assert lin(w=0x2008) == -4
     assert lin(wsb=4) == -5
+
+
+def test_cover_seed_score_rejects_bad_arguments_on_the_host(L):
+    # every case below fails validation, so the fake device addresses are never used
+    f = L.ec_cover_seed_score
+    names = ["q", "k", "idx", "stride", "count", "role", "drafted", "u", "dtype", "B", "L", "R", "H",
+             "Hkv", "d", "scale", "n_seed", "d_in", "d_out", "score", "seeds", "ws", "wsb", "stream"]
+    base = [0x1000, 0x2000, 0x3000, 96, 0x4000, 0x5000, 0x6000, 0x7000, 1, 8, 2048, 96, 28, 4, 128,
+            0.088, 8, 0x8000, 0x9000, 0xa000, 0xb000, 0x10000, 1 << 40, None]
+
+    def call(**kw):
+        a = list(base)
+        for key, v in kw.items():
+            a[names.index(key)] = v
+        return f(*a)
+
+    assert call(dtype=7) == -3
+    assert call(dtype=0) == -7             # float32 is not implemented
+    assert call(d=96) == -7
+    assert call(B=0) == -2
+    assert call(Hkv=5) == -2
+    assert call(stride=95) == -2
+    assert call(n_seed=-1) == -2
+    assert call(scale=float("nan")) == -2
+    assert call(count=None) == -1
+    assert call(q=None) == -1
+    assert call(drafted=None) == -1
+    assert call(seeds=None) == -1          # seeds asked for
+    assert call(ws=None) == -1
+    assert call(q=0x1008) == -4
+    assert call(k=0x2004) == -4
+    assert call(ws=0x10010) == -5
+    assert call(wsb=L.ec_cover_score_workspace_size(8, 2048, 96, 28) - 1) == -5
+    # no rows and no seed slots: nothing to launch
+    assert call(R=0, stride=0, n_seed=0, seeds=None, wsb=256) == 0
+
+
+def test_cover_score_sizes_and_launches(L):
+    small = L.ec_cover_score_workspace_size(1, 1024, 48, 32)
+    big = L.ec_cover_score_workspace_size(8, 2048, 96, 28)
+    assert small >= 256 and big > small and big % 256 == 0
+    assert L.ec_cover_score_workspace_size(1, 8192, 0, 32) == 256  # the status word only
+    assert L.ec_cover_score_kernel_count(8, 96, 8) == 5
+    assert L.ec_cover_score_kernel_count(8, 96, 0) == 4
+    assert L.ec_cover_score_kernel_count(8, 0, 4) == 1
+    assert L.ec_cover_score_kernel_count(8, 0, 0) == 0
