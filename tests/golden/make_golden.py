@@ -38,8 +38,11 @@ def variant_inputs():
     seed = np.array([[0, 1, 0, 1]], np.uint8)
     x = rng.standard_normal((3, 8))
     g = rng.standard_normal(8)
+    role = np.array([[1, 2, 3, 2]], np.uint8)       # COVER seed score: masked / candidate rows
+    drafted = np.array([[0, 0, 0, 1, 0, 1, 0]], np.uint8)
+    u = np.array([[0.5, 1.25, 2.0, 0.75]])
     return dict(sec=sec, tau=tau, idx=idx, cnt=cnt, q=q, kc=kc, vc=vc, kn=kn, vn=vn, seed=seed,
-                x=x, g=g)
+                x=x, g=g, role=role, drafted=drafted, u=u)
 
 
 def variant_record():
@@ -49,7 +52,11 @@ def variant_record():
                                    v["tau"], 0.5)
     _, _, cover = oracle.attention_cover(v["q"], v["kn"], v["vn"], v["kc"], v["vc"], v["idx"],
                                          v["cnt"], v["seed"], 0.5)
+    d_in, d_out, score, seeds = oracle.cover_seed_score(v["q"], v["kc"], v["idx"], v["cnt"],
+                                                        v["role"], v["drafted"], v["u"], 0.5, 3)
     return {"simsd": simsd.tolist(), "cover": cover.tolist(),
+            "cover_score": [d_in.tolist(), d_out.tolist(), score.tolist()],
+            "cover_seeds": seeds.tolist(),
             "rms_norm": layer.rms_norm(v["x"], v["g"], 1e-5).tolist(),
             "rope": layer.rope(v["x"].reshape(3, 1, 8), [0, 5, 900], 10000.0).tolist()}
 

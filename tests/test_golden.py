@@ -47,5 +47,7 @@ def test_variants_match_their_regression_record(orc):
     with open(GOLDEN) as f:
         g = json.load(f)["variants"]
     now = mg.variant_record()
-    for key in ("simsd", "cover", "rms_norm", "rope"):
-        assert np.allclose(np.array(now[key]), np.array(g[key]), rtol=1e-12, atol=1e-14), key
+    for key in ("simsd", "cover", "rms_norm", "rope", "cover_score"):
+        assert np.allclose(np.array(now[key]), np.array(g[key]), rtol=1e-12, atol=1e-14,
+                           equal_nan=True), key
+    assert now["cover_seeds"] == g["cover_seeds"]
