@@ -24,7 +24,10 @@ extern "C" {
 #endif
 
 /* Bytes of device workspace ec_cover_seed_score needs (EC_WORKSPACE_ALIGN-
- * aligned, status word first). */
+ * aligned, status word first): the status header, one 16-byte running softmax
+ * state per (row, head, key range) and four floats per (row, head).  Sizes out
+ * of range (batch or seq_len or n_heads below 1, r_max below 0) give the header's
+ * 256 bytes; the call itself rejects them. */
 size_t ec_cover_score_workspace_size(int32_t batch, int32_t seq_len, int32_t r_max,
                                      int32_t n_heads);
 
