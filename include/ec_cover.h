@@ -53,7 +53,10 @@ size_t ec_cover_score_workspace_size(int32_t batch, int32_t seq_len, int32_t r_m
  * 16-byte aligned.  role uint8 device [batch, r_max]: bit 0 = the row's
  * position is still masked after this step's unmasking (its query counts toward
  * d_in), bit 1 = the row is a candidate (a decoded token that may be verified);
- * a row may carry both.  drafted uint8 device [batch, seq_len]: nonzero at the
+ * a row may carry both; other bits are ignored.  Positions are distinct within a
+ * sequence (as ec_build_recompute_set produces them); two candidate rows at one
+ * position tie on both keys and share a seed slot, so the list then ends early
+ * (-1).  drafted uint8 device [batch, seq_len]: nonzero at the
  * positions unmasked at this step.  u float32 device [batch, r_max]: a
  * candidate row's entropy (the entropy output of ec_decode_step for the logits
  * row of that position).  Outputs float32 device [batch, r_max]: d_in, d_out,
